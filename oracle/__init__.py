@@ -1,0 +1,14 @@
+"""fp64 CPU oracle for paged varlen attention (test infrastructure only).
+
+Only tests, the smoke check and the benchmark's CPU-baseline leg use this
+package; the CUDA library never imports or links it.
+"""
+from .paged_attention import (  # noqa: F401
+    reshape_and_cache,
+    gather_kv,
+    attend_dense,
+    varlen_attention,
+    merge_attn_states,
+    cascade_attention,
+    cascade_attention_steps,
+)

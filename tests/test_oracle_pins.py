@@ -1,0 +1,480 @@
+"""Pins for the fp64 oracle: every function is checked against something other
+than itself (hand-derived fixtures, brute-force loops, closed forms, a torch
+library routine, invariants). CPU only.
+
+Sources: "FlashAttention 在 vLLM 中的实现分析" (§1.1 online softmax target,
+§4.2 scatter, §5 paged addressing, §6.3 cascade and merge) and
+"AttentionBackend:アテンションバックエンド抽象レイヤー" (境界と失敗: natural-log
+LSE).
+"""
+import json
+import math
+import os
+
+import pytest
+import torch
+
+import oracle
+from oracle import paged_attention as P
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")
+F64 = torch.float64
+
+
+def golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def _ln(expr):
+    return {"0": 0.0, "ln(3)": math.log(3.0), "ln(4)": math.log(4.0)}[expr]
+
+
+# ----------------------------------------------------------------------------
+# Pin checks, written as functions so the mutation tests below can run them
+# against an oracle with a planted mistake.
+# ----------------------------------------------------------------------------
+def check_golden_merge():
+    g = golden()["merge"]
+    oa = torch.tensor(g["prefix_out"], dtype=F64).view(1, 1, -1)
+    ob = torch.tensor(g["suffix_out"], dtype=F64).view(1, 1, -1)
+    a = torch.tensor([[_ln(g["prefix_lse"])]], dtype=F64)
+    b = torch.tensor([[_ln(g["suffix_lse"])]], dtype=F64)
+    o, l = oracle.merge_attn_states(oa, a, ob, b)
+    assert torch.allclose(o.view(-1), torch.tensor(g["expected_out"], dtype=F64), atol=1e-14)
+    assert abs(float(l) - _ln(g["expected_lse"])) < 1e-14
+
+
+def check_golden_two_key():
+    g = golden()["two_key_attention"]
+    q = torch.tensor(g["q"], dtype=F64).view(1, 1, 2)
+    k = torch.tensor(g["k"], dtype=F64).view(2, 1, 2)
+    v = torch.tensor(g["v"], dtype=F64).view(2, 1, 2)
+    o, l = oracle.attend_dense(q, k, v, g["softmax_scale"], False, 1, 2)
+    e4 = math.exp(4.0)
+    exp_o = [(1 - e4) / (1 + e4), (3 + 5 * e4) / (1 + e4)]
+    assert torch.allclose(o.view(-1), torch.tensor(exp_o, dtype=F64), atol=1e-14)
+    assert abs(float(l) - math.log(1 + e4)) < 1e-13
+
+
+def visible_matrix(q_len, kv_len, causal=True):
+    """Which keys each row sees, read off the oracle: with Q = 0 every visible
+    key gets the same weight, and V = one-hot key indicators."""
+    D = max(kv_len, 1)
+    q = torch.zeros((q_len, 1, D), dtype=F64)
+    k = torch.randn((kv_len, 1, D), dtype=F64)
+    v = torch.eye(kv_len, D, dtype=F64).view(kv_len, 1, D)
+    o, _ = oracle.attend_dense(q, k, v, 1.0, causal, q_len, kv_len)
+    return (o[:, 0, :kv_len] > 0).to(torch.int64)
+
+
+def check_golden_causal():
+    g = golden()["bottom_right_causal"]
+    vis = visible_matrix(g["q_len"], g["kv_len"])
+    assert vis.tolist() == g["visible"]
+
+
+def check_golden_paged_address():
+    g = golden()["paged_address"]
+    bt = torch.tensor(g["block_table_row"], dtype=torch.int32)
+    pages, rows = P.logical_to_physical(bt, g["positions"], g["block_size"])
+    assert [[int(p), int(r)] for p, r in zip(pages, rows)] == g["expected_page_row"]
+
+
+def check_lse_fsum(seed=0):
+    """LSE against a direct ln(sum exp) with math.fsum on tiny inputs."""
+    torch.manual_seed(seed)
+    q_len, kv_len, H, D = 3, 7, 2, 5
+    q = torch.randn(q_len, H, D, dtype=F64)
+    k = torch.randn(kv_len, 1, D, dtype=F64)
+    v = torch.randn(kv_len, 1, D, dtype=F64)
+    scale = 0.37
+    _, lse = oracle.attend_dense(q, k, v, scale, True, q_len, kv_len)
+    for h in range(H):
+        for i in range(q_len):
+            last = kv_len - q_len + i
+            logits = [scale * math.fsum(float(q[i, h, d]) * float(k[j, 0, d]) for d in range(D))
+                      for j in range(last + 1)]
+            ref = math.log(math.fsum(math.exp(x) for x in logits))
+            assert abs(float(lse[h, i]) - ref) < 1e-12, (h, i, float(lse[h, i]), ref)
+
+
+def brute_attention(q, k, v, scale, causal):
+    """Explicit loops over (i, j): the textbook definition, float64."""
+    q_len, H, D = q.shape
+    kv_len, H_kv, _ = k.shape
+    G = H // H_kv
+    out = [[[0.0] * D for _ in range(H)] for _ in range(q_len)]
+    lse = [[float("-inf")] * q_len for _ in range(H)]
+    for i in range(q_len):
+        for h in range(H):
+            hk = h // G
+            js = [j for j in range(kv_len) if (not causal) or j <= kv_len - q_len + i]
+            if not js:
+                continue
+            logits = {j: scale * math.fsum(float(q[i, h, d]) * float(k[j, hk, d])
+                                           for d in range(D)) for j in js}
+            m = max(logits.values())
+            w = {j: math.exp(logits[j] - m) for j in js}
+            den = math.fsum(w.values())
+            for d in range(D):
+                out[i][h][d] = math.fsum(w[j] * float(v[j, hk, d]) for j in js) / den
+            lse[h][i] = m + math.log(den)
+    return torch.tensor(out, dtype=F64), torch.tensor(lse, dtype=F64)
+
+
+def check_brute_force(max_len=6, seed=1, H=4, H_kv=2, D=3):
+    g = torch.Generator().manual_seed(seed)
+    for causal in (True, False):
+        for kv_len in range(1, max_len + 1):
+            for q_len in range(1, max_len + 1):
+                q = torch.randn(q_len, H, D, generator=g, dtype=F64)
+                k = torch.randn(kv_len, H_kv, D, generator=g, dtype=F64)
+                v = torch.randn(kv_len, H_kv, D, generator=g, dtype=F64)
+                o, l = oracle.attend_dense(q, k, v, 0.8, causal, q_len, kv_len)
+                bo, bl = brute_attention(q, k, v, 0.8, causal)
+                assert torch.allclose(o, bo, atol=1e-12, rtol=0), (causal, q_len, kv_len)
+                fin = torch.isfinite(bl)
+                assert torch.equal(fin, torch.isfinite(l))
+                assert torch.allclose(l[fin], bl[fin], atol=1e-12, rtol=0)
+
+
+def contiguous_copy(wl, kc, vc):
+    """The same batch laid out with sequence s's pages consecutive (identity
+    block table). Returns (block_table, key_cache, value_cache)."""
+    bs = wl.block_size
+    pages = [wl.pages_of(s) for s in range(wl.num_seqs)]
+    total = sum(len(p) for p in pages)
+    kc2 = torch.zeros((max(total, 1),) + tuple(kc.shape[1:]), dtype=kc.dtype)
+    vc2 = torch.zeros_like(kc2)
+    bt2 = torch.full_like(wl.block_table, W.INT32_MAX)
+    cur = 0
+    for s, ps in enumerate(pages):
+        for i, p in enumerate(ps):
+            kc2[cur] = kc[p]
+            vc2[cur] = vc[p]
+            bt2[s, i] = cur
+            cur += 1
+    return bt2, kc2, vc2
+
+
+def scattered_pools(wl):
+    kc, vc = wl.pool(0, threads=1), wl.pool(1, threads=1)
+    oracle.reshape_and_cache(wl.k_new, wl.v_new, wl.slot_mapping, kc, vc)
+    return kc, vc
+
+
+def check_sdpa(seed=5, causal=True):
+    """Contiguous layout vs torch scaled_dot_product_attention (fp64, GQA via
+    the library's enable_gqa, explicit bottom-right boolean mask)."""
+    wl = W.random_case(seed, num_seqs=4, num_heads=8, num_kv_heads=2, head_size=32,
+                       block_size=16, max_q=20, max_kv=70, causal=causal)
+    kc, vc = scattered_pools(wl)
+    out, lse = oracle.varlen_attention(wl.q, kc, vc, wl.cu_seqlens_q, wl.seqused_k,
+                                       wl.block_table, wl.softmax_scale, causal)
+    cu = wl.cu_seqlens_q.tolist()
+    for s in range(wl.num_seqs):
+        q_len, kv_len = wl.q_lens[s], wl.kv_lens[s]
+        if q_len == 0 or kv_len == 0:
+            continue
+        k = P.gather_kv(kc, wl.block_table[s], kv_len).to(F64)
+        v = P.gather_kv(vc, wl.block_table[s], kv_len).to(F64)
+        qs = wl.q[cu[s]:cu[s + 1]].to(F64)
+        mask = torch.ones(q_len, kv_len, dtype=torch.bool)
+        if causal:
+            mask = torch.ones(q_len, kv_len, dtype=torch.bool).tril(kv_len - q_len)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qs.transpose(0, 1)[None], k.transpose(0, 1)[None], v.transpose(0, 1)[None],
+            attn_mask=mask, scale=wl.softmax_scale, enable_gqa=True)[0].transpose(0, 1)
+        assert torch.allclose(out[cu[s]:cu[s + 1]], ref, atol=1e-12, rtol=0), s
+        # LSE: logsumexp of the masked logits through torch's own routine
+        kk = k.repeat_interleave(wl.num_heads // wl.num_kv_heads, dim=1)
+        logits = wl.softmax_scale * torch.einsum("ihd,jhd->hij", qs, kk)
+        logits = logits.masked_fill(~mask[None], float("-inf"))
+        assert torch.allclose(lse[:, cu[s]:cu[s + 1]], torch.logsumexp(logits, dim=-1),
+                              atol=1e-12, rtol=0)
+
+
+def check_permutation_invariance(seed=7):
+    wl = W.random_case(seed, num_seqs=5, num_heads=4, num_kv_heads=2, head_size=16,
+                       block_size=16, max_q=30, max_kv=90)
+    kc, vc = scattered_pools(wl)
+    o1, l1 = oracle.varlen_attention(wl.q, kc, vc, wl.cu_seqlens_q, wl.seqused_k,
+                                     wl.block_table, wl.softmax_scale, True)
+    bt2, kc2, vc2 = contiguous_copy(wl, kc, vc)
+    o2, l2 = oracle.varlen_attention(wl.q, kc2, vc2, wl.cu_seqlens_q, wl.seqused_k,
+                                     bt2, wl.softmax_scale, True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ----------------------------------------------------------------------------
+# The pins as tests.
+# ----------------------------------------------------------------------------
+def test_golden_merge():
+    check_golden_merge()
+
+
+def test_golden_two_key_attention():
+    check_golden_two_key()
+
+
+def test_golden_bottom_right_causal():
+    check_golden_causal()
+
+
+def test_golden_paged_address():
+    check_golden_paged_address()
+
+
+def test_golden_scatter_slots():
+    g = golden()["scatter_slot"]
+    bs = g["block_size"]
+    kc = torch.zeros(4, bs, 1, 2)
+    vc = torch.zeros(4, bs, 1, 2)
+    n = len(g["slots"])
+    key = torch.arange(1, n + 1, dtype=torch.float32).view(n, 1, 1).expand(n, 1, 2).clone()
+    val = -key
+    oracle.reshape_and_cache(key, val, torch.tensor(g["slots"]), kc, vc)
+    for t, pr in enumerate(g["expected_page_row"]):
+        if pr is None:
+            assert not (kc == key[t, 0, 0]).any()
+            continue
+        assert torch.equal(kc[pr[0], pr[1]], key[t]) and torch.equal(vc[pr[0], pr[1]], val[t])
+    assert int((kc != 0).any(dim=-1).sum()) == 3
+
+
+def test_scatter_brute_force_and_canary():
+    """Element-by-element Python reference over nested lists; every slot that no
+    token targets keeps its canary value."""
+    wl = W.random_case(11, num_seqs=4, num_heads=4, num_kv_heads=2, head_size=8,
+                       block_size=16, max_q=20, max_kv=60)
+    slots = wl.slot_mapping.clone()
+    slots[::5] = -1                                     # padding tokens
+    NB, bs, Hk, D = wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_size
+    canary = torch.full((NB, bs, Hk, D), 7.25, dtype=torch.bfloat16)
+    kc, vc = canary.clone(), canary.clone()
+    oracle.reshape_and_cache(wl.k_new, wl.v_new, slots, kc, vc)
+    ref = [[[[7.25] * D for _ in range(Hk)] for _ in range(bs)] for _ in range(NB)]
+    written = set()
+    for t, slot in enumerate(slots.tolist()):
+        if slot < 0:
+            continue
+        b, r = divmod(slot, bs)
+        written.add((b, r))
+        for h in range(Hk):
+            for d in range(D):
+                ref[b][r][h][d] = float(wl.k_new[t, h, d])
+    assert torch.equal(kc.float(), torch.tensor(ref))
+    for b in range(NB):
+        for r in range(bs):
+            if (b, r) not in written:
+                assert bool((kc[b, r] == 7.25).all()) and bool((vc[b, r] == 7.25).all())
+
+
+def test_brute_force_tiny_all_lengths():
+    check_brute_force()
+
+
+def test_lse_fsum():
+    check_lse_fsum()
+
+
+def test_matches_torch_sdpa_causal():
+    check_sdpa(causal=True)
+
+
+def test_matches_torch_sdpa_noncausal():
+    check_sdpa(seed=6, causal=False)
+
+
+def test_page_permutation_invariance():
+    check_permutation_invariance()
+
+
+def test_closed_form_single_visible_key():
+    """Causal with q_len == kv_len: row 0 sees only key 0, so O = V[0] and
+    LSE = scale * q.k0."""
+    torch.manual_seed(3)
+    q = torch.randn(4, 2, 8, dtype=F64)
+    k = torch.randn(4, 1, 8, dtype=F64)
+    v = torch.randn(4, 1, 8, dtype=F64)
+    o, l = oracle.attend_dense(q, k, v, 0.3, True, 4, 4)
+    for h in range(2):
+        assert torch.equal(o[0, h], v[0, 0])
+        dot = math.fsum(float(q[0, h, d]) * float(k[0, 0, d]) for d in range(8))
+        assert abs(float(l[h, 0]) - 0.3 * dot) < 1e-13
+
+
+def test_closed_form_constant_v():
+    torch.manual_seed(4)
+    q = torch.randn(5, 4, 8, dtype=F64)
+    k = torch.randn(9, 2, 8, dtype=F64)
+    c = torch.randn(1, 2, 8, dtype=F64)
+    v = c.expand(9, 2, 8).clone()
+    o, _ = oracle.attend_dense(q, k, v, 0.5, True, 5, 9)
+    for h in range(4):
+        assert torch.allclose(o[:, h], c[0, h // 2].expand(5, 8), atol=1e-14, rtol=0)
+
+
+def test_closed_form_zero_q():
+    """Q = 0: uniform weights over the visible keys -> mean of V, LSE = ln(n)."""
+    torch.manual_seed(5)
+    q_len, kv_len = 3, 10
+    q = torch.zeros(q_len, 2, 4, dtype=F64)
+    k = torch.randn(kv_len, 2, 4, dtype=F64)
+    v = torch.randn(kv_len, 2, 4, dtype=F64)
+    o, l = oracle.attend_dense(q, k, v, 0.9, True, q_len, kv_len)
+    for i in range(q_len):
+        n = kv_len - q_len + i + 1
+        for h in range(2):
+            mean = [math.fsum(float(v[j, h, d]) for j in range(n)) / n for d in range(4)]
+            assert torch.allclose(o[i, h], torch.tensor(mean, dtype=F64), atol=1e-14)
+            assert abs(float(l[h, i]) - math.log(n)) < 1e-14
+
+
+def test_closed_form_shift_invariance():
+    """Adding a vector w to every key adds scale*q.w to a row's logits: O is
+    unchanged and the LSE moves by exactly that amount."""
+    torch.manual_seed(6)
+    q = torch.randn(4, 2, 8, dtype=F64)
+    k = torch.randn(11, 1, 8, dtype=F64)
+    v = torch.randn(11, 1, 8, dtype=F64)
+    w = torch.randn(1, 1, 8, dtype=F64)
+    o1, l1 = oracle.attend_dense(q, k, v, 0.4, True, 4, 11)
+    o2, l2 = oracle.attend_dense(q, k + w, v, 0.4, True, 4, 11)
+    assert torch.allclose(o1, o2, atol=1e-12, rtol=0)
+    shift = 0.4 * torch.einsum("ihd,d->hi", q, w[0, 0])
+    assert torch.allclose(l2 - l1, shift, atol=1e-12, rtol=0)
+
+
+def test_rows_without_visible_key():
+    """Causal with q_len > kv_len: the first q_len - kv_len rows see nothing."""
+    q = torch.randn(5, 2, 4, dtype=F64)
+    k = torch.randn(2, 1, 4, dtype=F64)
+    v = torch.randn(2, 1, 4, dtype=F64)
+    o, l = oracle.attend_dense(q, k, v, 1.0, True, 5, 2)
+    assert torch.equal(o[:3], torch.zeros(3, 2, 4, dtype=F64))
+    assert bool(torch.isinf(l[:, :3]).all()) and bool((l[:, :3] < 0).all())
+    assert bool(torch.isfinite(l[:, 3:]).all())
+
+
+def test_empty_sequences():
+    """q_len = 0 rows produce nothing; kv_len = 0 rows see nothing."""
+    q = torch.randn(2, 2, 4, dtype=torch.bfloat16)
+    kc = torch.randn(3, 16, 1, 4, dtype=torch.bfloat16)
+    vc = torch.randn(3, 16, 1, 4, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 0, 2], dtype=torch.int32)
+    lk = torch.tensor([5, 0], dtype=torch.int32)
+    bt = torch.tensor([[0], [1]], dtype=torch.int32)
+    o, l = oracle.varlen_attention(q, kc, vc, cu, lk, bt, 0.5, False)
+    assert torch.equal(o, torch.zeros_like(o)) and bool(torch.isinf(l).all())
+
+
+def test_merge_split_invariance():
+    """Attention over keys [0, c) merged with attention over [c, n) equals
+    attention over all n keys, for every split point c."""
+    torch.manual_seed(8)
+    q = torch.randn(3, 4, 8, dtype=F64)
+    k = torch.randn(13, 2, 8, dtype=F64)
+    v = torch.randn(13, 2, 8, dtype=F64)
+    full_o, full_l = oracle.attend_dense(q, k, v, 0.6, False, 3, 13)
+    for c in range(1, 13):
+        oa, la = oracle.attend_dense(q, k[:c], v[:c], 0.6, False, 3, c)
+        ob, lb = oracle.attend_dense(q, k[c:], v[c:], 0.6, False, 3, 13 - c)
+        o, l = oracle.merge_attn_states(oa, la, ob, lb)
+        assert torch.allclose(o, full_o, atol=1e-12, rtol=0), c
+        assert torch.allclose(l, full_l, atol=1e-12, rtol=0), c
+
+
+def test_merge_identity_commutative_and_empty():
+    torch.manual_seed(9)
+    oa = torch.randn(4, 3, 5, dtype=F64)
+    ob = torch.randn(4, 3, 5, dtype=F64)
+    a = torch.randn(3, 4, dtype=F64)
+    b = torch.randn(3, 4, dtype=F64)
+    ninf = torch.full((3, 4), float("-inf"), dtype=F64)
+    o, l = oracle.merge_attn_states(oa, a, ob, ninf)
+    assert torch.equal(o, oa) and torch.equal(l, a)
+    o1, l1 = oracle.merge_attn_states(oa, a, ob, b)
+    o2, l2 = oracle.merge_attn_states(ob, b, oa, a)
+    assert torch.allclose(o1, o2, atol=1e-15) and torch.allclose(l1, l2, atol=1e-15)
+    o3, l3 = oracle.merge_attn_states(oa, ninf, ob, ninf)
+    assert torch.equal(o3, torch.zeros_like(o3)) and bool(torch.isinf(l3).all())
+
+
+def test_cascade_steps_equal_flat():
+    """The pages' three cascade steps reproduce flat causal attention."""
+    g = torch.Generator().manual_seed(12)
+    S, P, bs = 5, 48, 16
+    suffix = [int(x) for x in torch.randint(3, 40, (S,), generator=g)]
+    q_lens = [min(int(x), s) for x, s in zip(torch.randint(1, 6, (S,), generator=g), suffix)]
+    wl = W._build("cascade_small", 12, 4, 2, 16, bs, q_lens, [P + s for s in suffix], g,
+                  shared_prefix_pages=P // bs)
+    kc, vc = scattered_pools(wl)
+    args = (wl.q, kc, vc, wl.cu_seqlens_q, wl.seqused_k, wl.block_table, wl.softmax_scale)
+    flat_o, flat_l = oracle.cascade_attention(*args, P)
+    steps_o, steps_l = oracle.cascade_attention_steps(*args, P)
+    assert torch.allclose(flat_o, steps_o, atol=1e-12, rtol=0)
+    assert torch.allclose(flat_l, steps_l, atol=1e-12, rtol=0)
+
+
+def test_workload_recipe_is_deterministic():
+    a, b = W.tiny_mixed(), W.tiny_mixed()
+    assert torch.equal(a.q, b.q) and torch.equal(a.block_table, b.block_table)
+    assert torch.equal(a.pool(0, threads=1), b.pool(0, threads=4))
+    pages = a.pages_of(3)
+    got = a.pool_pages(1, pages)
+    full = a.pool(1)
+    for p in pages:
+        assert torch.equal(got[p], full[p])
+    # the tiny config: 166 query tokens, 16 of 64 pages in use
+    assert a.total_q == 166 and a.num_blocks == 64
+    used = sum(len(a.pages_of(s)) for s in range(a.num_seqs))
+    assert used == 16
+
+
+# ----------------------------------------------------------------------------
+# Planted mistakes: each plausible slip in the oracle must fail some pin.
+# ----------------------------------------------------------------------------
+def _fails(check):
+    try:
+        check()
+    except AssertionError:
+        return True
+    return False
+
+
+def test_planted_top_left_causal_is_caught(monkeypatch):
+    monkeypatch.setattr(P, "causal_last_visible", lambda q_len, kv_len, i: i)
+    assert _fails(check_golden_causal)
+    assert _fails(lambda: check_sdpa(causal=True))
+
+
+def test_planted_gqa_modulo_mapping_is_caught(monkeypatch):
+    monkeypatch.setattr(P, "kv_head_of", lambda h, H, H_kv: h % H_kv)
+    assert _fails(lambda: check_sdpa(causal=True))
+    assert _fails(check_brute_force)
+
+
+def test_planted_log2_lse_is_caught(monkeypatch):
+    monkeypatch.setattr(P, "log_sum_exp_from", lambda m, l: m + torch.log2(l))
+    assert _fails(check_lse_fsum)
+    assert _fails(check_golden_two_key)
+
+
+def test_planted_swapped_page_index_is_caught(monkeypatch):
+    def swapped(bt_row, positions, bs):
+        positions = torch.as_tensor(positions, dtype=torch.long)
+        return bt_row[positions % bs % bt_row.numel()].long(), positions // bs
+    monkeypatch.setattr(P, "logical_to_physical", swapped)
+    assert _fails(check_golden_paged_address)
+
+
+def test_planted_dropped_scale_is_caught(monkeypatch):
+    real = P.attend_dense
+
+    def no_scale(q, k, v, softmax_scale, *a, **kw):
+        return real(q, k, v, 1.0, *a, **kw)
+    monkeypatch.setattr(oracle, "attend_dense", no_scale)
+    assert _fails(check_golden_two_key)

@@ -1,0 +1,296 @@
+"""Seeded synthetic inputs for paged varlen attention, shared by the tests, the
+benchmark and the smoke check.
+
+This module only draws random numbers and lays out metadata the way a serving
+engine's scheduler would hand it to the attention backend (FlashAttention in
+vLLM analysis page, section 5 "PagedAttention integration": a K/V page pool
+[num_blocks, block_size, num_kv_heads, head_size], an int32 block_table
+[num_seqs, max_blocks], seqused_k and cu_seqlens_q). It holds none of the
+attention arithmetic: no softmax, no gather, no scatter.
+
+Recipe (every workload):
+  * one torch CPU generator seeded with ``seed``; draw order is lengths,
+    page permutation, Q, new K, new V;
+  * pool contents (the prior context) are N(0,1) drawn per chunk of pages from
+    a generator whose seed is a splitmix64 mix of (seed, K|V, chunk index), so
+    any page can be regenerated on its own and chunks can be drawn in parallel;
+  * pages are handed to sequences in order from a random permutation of the
+    pool; unused block_table entries hold INT32_MAX;
+  * the new tokens of sequence s are its last q_len[s] positions, and their
+    slot is (physical page) * block_size + (position % block_size);
+  * all values are drawn in fp32 and rounded to bf16; both the oracle and the
+    GPU path consume the same bf16 values.
+"""
+from __future__ import annotations
+
+import math
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import torch
+
+INT32_MAX = 2**31 - 1
+PAGES_PER_CHUNK = 64
+_MASK64 = (1 << 64) - 1
+
+
+def _splitmix64(x: int) -> int:
+    x = (x + 0x9E3779B97F4A7C15) & _MASK64
+    x = ((x ^ (x >> 30)) * 0xBF58476D1CE4E5B9) & _MASK64
+    x = ((x ^ (x >> 27)) * 0x94D049BB133111EB) & _MASK64
+    return x ^ (x >> 31)
+
+
+def derived_seed(seed: int, stream: int, index: int) -> int:
+    return _splitmix64(_splitmix64(_splitmix64(seed) ^ stream) ^ index) & ((1 << 63) - 1)
+
+
+@dataclass
+class Workload:
+    """One synthetic batch. Host (CPU) tensors except where noted."""
+
+    name: str
+    seed: int
+    num_heads: int
+    num_kv_heads: int
+    head_size: int
+    block_size: int
+    num_blocks: int
+    softmax_scale: float
+    causal: bool
+    q_lens: list
+    kv_lens: list
+    block_table: torch.Tensor          # int32 [S, max_blocks]
+    slot_mapping: torch.Tensor         # int64 [T_new]
+    q: torch.Tensor                    # bf16 [T, H, D]
+    k_new: torch.Tensor                # bf16 [T_new, H_kv, D]
+    v_new: torch.Tensor                # bf16 [T_new, H_kv, D]
+    common_prefix_len: int = 0
+    meta: dict = field(default_factory=dict)
+
+    # ---- derived metadata -------------------------------------------------
+    @property
+    def num_seqs(self) -> int:
+        return len(self.q_lens)
+
+    @property
+    def total_q(self) -> int:
+        return int(sum(self.q_lens))
+
+    @property
+    def cu_seqlens_q(self) -> torch.Tensor:
+        cu = [0]
+        for n in self.q_lens:
+            cu.append(cu[-1] + n)
+        return torch.tensor(cu, dtype=torch.int32)
+
+    @property
+    def seqused_k(self) -> torch.Tensor:
+        return torch.tensor(self.kv_lens, dtype=torch.int32)
+
+    @property
+    def max_seqlen_q(self) -> int:
+        return max(self.q_lens) if self.q_lens else 0
+
+    @property
+    def max_seqlen_k(self) -> int:
+        return max(self.kv_lens) if self.kv_lens else 0
+
+    @property
+    def page_shape(self):
+        return (self.block_size, self.num_kv_heads, self.head_size)
+
+    # ---- pool contents (prior context) ------------------------------------
+    def num_chunks(self) -> int:
+        return (self.num_blocks + PAGES_PER_CHUNK - 1) // PAGES_PER_CHUNK
+
+    def pool_chunk(self, which: int, chunk: int) -> torch.Tensor:
+        """bf16 pages [chunk*64, chunk*64+64) of the K (which=0) or V (which=1) pool."""
+        first = chunk * PAGES_PER_CHUNK
+        n = min(PAGES_PER_CHUNK, self.num_blocks - first)
+        g = torch.Generator().manual_seed(derived_seed(self.seed, 1 + which, chunk))
+        x = torch.randn((n,) + self.page_shape, generator=g, dtype=torch.float32)
+        return x.to(torch.bfloat16)
+
+    def pool(self, which: int, device="cpu", threads: int = 8) -> torch.Tensor:
+        """The whole K or V pool [num_blocks, block_size, H_kv, D] before the scatter."""
+        out = torch.empty((self.num_blocks,) + self.page_shape, dtype=torch.bfloat16,
+                          device=device)
+
+        def fill(c):
+            first = c * PAGES_PER_CHUNK
+            chunk = self.pool_chunk(which, c)
+            out[first:first + chunk.shape[0]].copy_(chunk)
+
+        if threads > 1 and self.num_chunks() > 1:
+            with ThreadPoolExecutor(threads) as ex:
+                list(ex.map(fill, range(self.num_chunks())))
+        else:
+            for c in range(self.num_chunks()):
+                fill(c)
+        return out
+
+    def pool_pages(self, which: int, pages) -> dict:
+        """{page id: bf16 [bs, H_kv, D]} for the given page ids (pre-scatter contents)."""
+        by_chunk = {}
+        for p in sorted(set(int(p) for p in pages)):
+            by_chunk.setdefault(p // PAGES_PER_CHUNK, []).append(p)
+        res = {}
+        for c, ps in by_chunk.items():
+            chunk = self.pool_chunk(which, c)
+            for p in ps:
+                res[p] = chunk[p - c * PAGES_PER_CHUNK].clone()
+        return res
+
+    def pages_of(self, s: int):
+        nb = (self.kv_lens[s] + self.block_size - 1) // self.block_size
+        return [int(x) for x in self.block_table[s, :nb]]
+
+    def sub_batch(self, seqs) -> "Workload":
+        """A batch made of the given sequences only, sharing the same pool.
+
+        The page table rows, lengths, queries and new K/V of the chosen sequences
+        are kept unchanged; the pool (num_blocks, seeds) is the same, so pages
+        regenerate identically.
+        """
+        seqs = list(seqs)
+        cu = self.cu_seqlens_q.tolist()
+        q_rows = torch.cat([torch.arange(cu[s], cu[s + 1]) for s in seqs]) if seqs else \
+            torch.zeros(0, dtype=torch.long)
+        return Workload(
+            name=f"{self.name}[sub]", seed=self.seed, num_heads=self.num_heads,
+            num_kv_heads=self.num_kv_heads, head_size=self.head_size,
+            block_size=self.block_size, num_blocks=self.num_blocks,
+            softmax_scale=self.softmax_scale, causal=self.causal,
+            q_lens=[self.q_lens[s] for s in seqs], kv_lens=[self.kv_lens[s] for s in seqs],
+            block_table=self.block_table[seqs].clone(),
+            slot_mapping=self.slot_mapping[q_rows].clone(),
+            q=self.q[q_rows].clone(), k_new=self.k_new[q_rows].clone(),
+            v_new=self.v_new[q_rows].clone(),
+            common_prefix_len=self.common_prefix_len, meta=dict(self.meta))
+
+
+def _build(name, seed, H, H_kv, D, bs, q_lens, kv_lens, g, causal=True, scale=None,
+           num_blocks=None, shared_prefix_pages=0, pool_slack=1.1, meta=None):
+    """Lay out pages, draw Q and new K/V. ``g`` has already drawn the lengths."""
+    S = len(q_lens)
+    assert all(0 <= q <= k for q, k in zip(q_lens, kv_lens)), "new tokens lie inside the KV"
+    pages_needed = [(k + bs - 1) // bs for k in kv_lens]
+    private = [max(0, p - shared_prefix_pages) for p in pages_needed]
+    used = shared_prefix_pages + sum(private)
+    if num_blocks is None:
+        num_blocks = max(1, math.ceil(pool_slack * used))
+    assert num_blocks >= used, (num_blocks, used)
+    perm = torch.randperm(num_blocks, generator=g).to(torch.int32)
+    max_blocks = max(pages_needed) if pages_needed else 1
+    bt = torch.full((S, max(1, max_blocks)), INT32_MAX, dtype=torch.int32)
+    cursor = 0
+    shared = perm[:shared_prefix_pages]
+    cursor = shared_prefix_pages
+    for s in range(S):
+        n_sh = min(shared_prefix_pages, pages_needed[s])
+        bt[s, :n_sh] = shared[:n_sh]
+        n_pr = private[s]
+        bt[s, n_sh:n_sh + n_pr] = perm[cursor:cursor + n_pr]
+        cursor += n_pr
+    T = sum(q_lens)
+    q = torch.randn((T, H, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k_new = torch.randn((T, H_kv, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v_new = torch.randn((T, H_kv, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    slots = []
+    for s in range(S):
+        for pos in range(kv_lens[s] - q_lens[s], kv_lens[s]):
+            slots.append(int(bt[s, pos // bs]) * bs + pos % bs)
+    slot_mapping = torch.tensor(slots, dtype=torch.int64)
+    return Workload(name=name, seed=seed, num_heads=H, num_kv_heads=H_kv, head_size=D,
+                    block_size=bs, num_blocks=num_blocks,
+                    softmax_scale=(1.0 / math.sqrt(D)) if scale is None else scale,
+                    causal=causal, q_lens=list(q_lens), kv_lens=list(kv_lens),
+                    block_table=bt, slot_mapping=slot_mapping, q=q, k_new=k_new,
+                    v_new=v_new, common_prefix_len=shared_prefix_pages * bs,
+                    meta=meta or {})
+
+
+def _uniform_int(g, lo, hi, n):
+    """n integers uniform on {lo..hi} (inclusive)."""
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
+
+
+def tiny_mixed(seed=1001):
+    """4 seqs, 4 query / 2 KV heads, head_size 64, block_size 16, pool of 64 pages.
+    KV lens {17, 33, 64, 100}; seqs 0-1 decode (one query), seqs 2-3 causal
+    prefill with query length equal to KV length."""
+    g = torch.Generator().manual_seed(seed)
+    kv = [17, 33, 64, 100]
+    ql = [1, 1, 64, 100]
+    return _build("tiny_mixed", seed, 4, 2, 64, 16, ql, kv, g, num_blocks=64,
+                  scale=1.0 / 8.0)
+
+
+def decode_llama8b(seed=1002, num_seqs=64):
+    """64 decode seqs x 1 query token, 32/8 heads, head_size 128, block_size 16,
+    KV lens uniform on [512, 8192], pool = total pages + 10%."""
+    g = torch.Generator().manual_seed(seed)
+    kv = _uniform_int(g, 512, 8192, num_seqs)
+    return _build("decode_llama8b", seed, 32, 8, 128, 16, [1] * num_seqs, kv, g)
+
+
+def chunked_prefill_mix(seed=1003, n_prefill=8, chunk=2048, n_decode=56):
+    """8 causal prefill chunks of 2048 tokens with prior context uniform on
+    [0, 4096], then 56 decode seqs with KV uniform on [1024, 8192]; 32/8 heads,
+    head_size 128, block_size 16."""
+    g = torch.Generator().manual_seed(seed)
+    ctx = _uniform_int(g, 0, 4096, n_prefill)
+    dec = _uniform_int(g, 1024, 8192, n_decode)
+    ql = [chunk] * n_prefill + [1] * n_decode
+    kv = [c + chunk for c in ctx] + dec
+    return _build("chunked_prefill_mix", seed, 32, 8, 128, 16, ql, kv, g)
+
+
+def cascade_shared_prefix(seed=1004, num_seqs=64, prefix=2048):
+    """64 requests sharing a 2048-token prefix (128 pages of 16, the same first
+    128 block_table entries in every row), each with one query token and a
+    private suffix uniform on [64, 512] tokens; 32/8 heads, head_size 128."""
+    g = torch.Generator().manual_seed(seed)
+    suf = _uniform_int(g, 64, 512, num_seqs)
+    kv = [prefix + s for s in suf]
+    return _build("cascade_shared_prefix", seed, 32, 8, 128, 16, [1] * num_seqs, kv, g,
+                  shared_prefix_pages=prefix // 16)
+
+
+def long_context_70b(seed=1005, n_decode=32, kv_len=32768, n_prefill=4, q_len=4096):
+    """64/8 heads (GQA 8), head_size 128, block_size 128: 32 decode seqs at KV
+    32768, then 4 causal prefill seqs of 4096 tokens on 28672 prior tokens."""
+    g = torch.Generator().manual_seed(seed)
+    ql = [1] * n_decode + [q_len] * n_prefill
+    kv = [kv_len] * (n_decode + n_prefill)
+    return _build("long_context_70b", seed, 64, 8, 128, 128, ql, kv, g)
+
+
+CONFIGS = {
+    "tiny_mixed": tiny_mixed,
+    "decode_llama8b": decode_llama8b,
+    "chunked_prefill_mix": chunked_prefill_mix,
+    "cascade_shared_prefix": cascade_shared_prefix,
+    "long_context_70b": long_context_70b,
+}
+
+
+def random_case(seed, num_seqs=3, num_heads=4, num_kv_heads=2, head_size=64,
+                block_size=16, max_q=40, max_kv=120, causal=True, decode_frac=0.3,
+                empty_ok=False, slack=1.5):
+    """A small random batch: lengths, pages and values all from ``seed``."""
+    g = torch.Generator().manual_seed(seed)
+    ql, kv = [], []
+    for _ in range(num_seqs):
+        lo = 0 if empty_ok else 1
+        k = int(torch.randint(lo, max_kv + 1, (1,), generator=g))
+        if float(torch.rand((1,), generator=g)) < decode_frac:
+            q = min(1, k) if not empty_ok else int(torch.randint(0, 2, (1,), generator=g))
+        else:
+            q = int(torch.randint(lo, max_q + 1, (1,), generator=g))
+        q = min(q, k)
+        ql.append(q)
+        kv.append(k)
+    return _build(f"random_{seed}", seed, num_heads, num_kv_heads, head_size, block_size,
+                  ql, kv, g, causal=causal, pool_slack=slack)
