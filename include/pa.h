@@ -1,0 +1,200 @@
+/*
+ * pa.h -- C ABI of the paged varlen attention library (libpa.so), sm_103a.
+ *
+ * The operations follow the web pages that describe vLLM's attention
+ * backends:
+ *   [FA-vLLM] "FlashAttention 在 vLLM 中的实现分析" (blog.chen3feng.top,
+ *             vllm-analysis/07): §1.1 tiled online softmax, §4 forward() and the
+ *             flash_attn_varlen_func call, §4.2 KV-cache update, §5 PagedAttention
+ *             integration (block_table addressing), §6.3 cascade execution,
+ *             §8.2 reshape_and_cache_flash / merge_attn_states.
+ *   [FA/FI]   "FlashAttention と FlashInfer:2 大 GPU アテンションバックエンド":
+ *             データフロー (KV cache shape, block size multiple of 16),
+ *             境界と失敗 (head-size and dtype limits).
+ *   [Backend] "AttentionBackend:アテンションバックエンド抽象レイヤー": 境界と失敗
+ *             (head size, block size ValueError, natural-log LSE).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *     never allocates device memory: temporaries live in a caller-provided
+ *     workspace whose size the *_workspace_size functions return.
+ *   - Work is enqueued on the caller's stream (`stream` is a cudaStream_t; NULL
+ *     means the legacy default stream). Calls are asynchronous, make no
+ *     host<->device copies, never synchronize, and keep no state between calls,
+ *     so they can be recorded into a CUDA graph and called from several host
+ *     threads on different streams with different workspaces.
+ *   - Element type: PA_BF16 (bfloat16) for Q, K, V and outputs; LSE is float32.
+ *     Arithmetic accumulates in float32.
+ *   - Strides are in ELEMENTS. Every tensor pointer must be 16-byte aligned and
+ *     every stride a multiple of 8 elements (16 bytes).
+ *   - Return value: PA_OK, or an error code. On any host-side error nothing is
+ *     launched and nothing is written. PA_ERR_CUDA reports a failed launch.
+ *   - dev_status (nullable): a device int32 the kernels OR error bits into
+ *     (PA_DEV_*) when they meet metadata they cannot use (a page id outside the
+ *     pool, a slot outside the pool, a sequence longer than its page-table row,
+ *     a bounded wait that gave up). The offending access is skipped, never
+ *     performed: bad metadata cannot make a kernel read or write out of bounds.
+ *     The caller clears the word; the library only ORs bits into it.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int pa_status;
+
+#define PA_OK 0
+#define PA_ERR_INVALID_ARG 1 /* null pointer, negative size, bad stride/alignment, H % H_kv != 0 */
+#define PA_ERR_BLOCK_SIZE 2  /* block_size not a positive multiple of 16, or > 1024 */
+#define PA_ERR_UNSUPPORTED 3 /* head_size not 64/128, dtype not bf16, H/H_kv not 1,2,4,8,16 */
+#define PA_ERR_WORKSPACE 4   /* workspace NULL, misaligned or smaller than required */
+#define PA_ERR_CUDA 5        /* a kernel launch or a CUDA runtime query failed */
+
+/* bits OR-ed into *dev_status by the kernels */
+#define PA_DEV_BAD_PAGE 1    /* a block_table entry outside [0, num_blocks): its keys read as 0 */
+#define PA_DEV_BAD_SLOT 2    /* a slot_mapping entry >= num_blocks * block_size: token skipped */
+#define PA_DEV_BAD_SEQLEN 4  /* cu_seqlens_q / seqused_k inconsistent with the stated bounds */
+#define PA_DEV_TIMEOUT 8     /* a bounded wait on a pipeline barrier gave up */
+#define PA_DEV_CASCADE 16    /* cascade precondition violated (see pa_cascade_fwd) */
+
+#define PA_BF16 0
+
+/* Human-readable name of a pa_status value (static string). */
+const char* pa_status_string(pa_status status);
+
+/* ABI version of this header (increments on any signature change). */
+int pa_abi_version(void);
+
+/*
+ * pa_reshape_and_cache -- the slot_mapping scatter that writes new K/V rows
+ * into their pages before attention ([FA-vLLM] §4.2 and §8.2
+ * reshape_and_cache_flash; [FA/FI] 役割: the cache write is its own op).
+ *
+ *   key[t], value[t]  : [num_kv_heads, head_size] rows, token t at
+ *                       key + t * key_token_stride (likewise value).
+ *   key_cache, value_cache : page pools; page b starts at b * cache_block_stride
+ *                       and holds [block_size, num_kv_heads, head_size]
+ *                       contiguous (the NHD layout of [FA-vLLM] §5). Passing
+ *                       cache_block_stride = 2*block_size*H_kv*D with value_cache
+ *                       = key_cache + block_size*H_kv*D addresses a combined
+ *                       [num_blocks, 2, block_size, H_kv, D] tensor ([FA/FI]
+ *                       データフロー); the [2, num_blocks, ...] layout is two
+ *                       plain pools.
+ *   slot_mapping[t]   : int64 flat slot; the token goes to page slot / block_size,
+ *                       row slot % block_size. slot < 0 skips the token (padding).
+ *                       Slots must be distinct (duplicates: unspecified winner).
+ * Bit-exact copy; no arithmetic on values.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value, int64_t key_token_stride,
+                               int64_t value_token_stride, void* key_cache, void* value_cache,
+                               int64_t cache_block_stride, const int64_t* slot_mapping,
+                               int num_tokens, int num_kv_heads, int head_size, int block_size,
+                               int num_blocks, int dtype, int32_t* dev_status, void* stream);
+
+/*
+ * Workspace bytes pa_varlen_fwd needs for these bounds. sm_count is the
+ * multiprocessor count of the device the call will run on (0: query the
+ * current device). Returns 0 if the arguments are invalid.
+ */
+size_t pa_varlen_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q, int max_seqlen_k,
+                                    int num_heads, int num_kv_heads, int head_size, int block_size,
+                                    int sm_count);
+
+/*
+ * pa_varlen_fwd -- varlen attention over a paged KV cache ([FA-vLLM] §4 call
+ * flash_attn_varlen_func(q, k_cache, v_cache, cu_seqlens_q, seqused_k,
+ * block_table, ...), §5 addressing, §1.1 tiled online softmax).
+ *
+ *   q            : [total_q, num_heads, head_size]; token t at q + t*q_token_stride,
+ *                  heads contiguous.
+ *   key_cache, value_cache, cache_block_stride : as in pa_reshape_and_cache.
+ *   cu_seqlens_q : int32 [num_seqs + 1], nondecreasing prefix sums of query
+ *                  lengths, cu_seqlens_q[0] = 0, cu_seqlens_q[num_seqs] = total_q.
+ *   seqused_k    : int32 [num_seqs], number of keys of each sequence (>= 0).
+ *   block_table  : int32 [num_seqs, bt_stride]; logical key j of sequence s is
+ *                  row j % block_size of page block_table[s * bt_stride + j / block_size].
+ *                  Only entries j / block_size < ceil(seqused_k[s] / block_size)
+ *                  are read.
+ *   max_seqlen_q, max_seqlen_k : host upper bounds of the query / key lengths
+ *                  (used to size launches; no device value is read on the host).
+ *   softmax_scale: multiplies q.k (commonly 1/sqrt(head_size)).
+ *   causal       : 0 or 1. Causal masking is bottom-right aligned: query i of a
+ *                  sequence with q_len queries and kv_len keys sees keys
+ *                  j <= kv_len - q_len + i (a decode query sees all keys).
+ *   GQA          : query head h reads KV head h / (num_heads / num_kv_heads).
+ *   out          : [total_q, num_heads, head_size] bf16, contiguous.
+ *   lse          : float32 [num_heads, total_q] natural-log log-sum-exp of the
+ *                  scaled logits each row saw, or NULL. A row that sees no key
+ *                  gets out = 0 and lse = -inf.
+ *   workspace    : >= pa_varlen_fwd_workspace_size(...) bytes, 256-byte aligned;
+ *                  its contents need no initialisation and are scratch after the
+ *                  call. One workspace must not be used by two calls in flight.
+ */
+pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_cache,
+                        const void* value_cache, int64_t cache_block_stride,
+                        const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                        const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
+                        int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                        int head_size, int block_size, int num_blocks, float softmax_scale,
+                        int causal, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream);
+
+/*
+ * pa_merge_attn_states -- LSE-weighted combine of two partial attention
+ * results over disjoint key sets ([FA-vLLM] §6.3 step 3 and §8.2
+ * merge_attn_states(prefix_out, suffix_out, prefix_lse, suffix_lse)).
+ *
+ *   prefix_out, suffix_out, out : [num_tokens, num_heads, head_size] bf16, contiguous.
+ *   prefix_lse, suffix_lse      : float32 [num_heads, num_tokens], natural log.
+ *   out_lse                     : float32 [num_heads, num_tokens] or NULL.
+ * With m = max(a, b), wa = e^(a-m), wb = e^(b-m):
+ *   out = (wa*prefix_out + wb*suffix_out) / (wa + wb), out_lse = m + ln(wa + wb);
+ * a row whose two LSEs are both -inf gets out = 0, out_lse = -inf.
+ * out may alias prefix_out or suffix_out.
+ */
+pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
+                               const float* prefix_lse, const void* suffix_out,
+                               const float* suffix_lse, int num_tokens, int num_heads,
+                               int head_size, int dtype, void* stream);
+
+/* Workspace bytes pa_cascade_fwd needs (same arguments as the varlen query). */
+size_t pa_cascade_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
+                                     int max_seqlen_k, int num_heads, int num_kv_heads,
+                                     int head_size, int block_size, int sm_count);
+
+/*
+ * pa_cascade_fwd -- shared-prefix (cascade) attention ([FA-vLLM] §6.3):
+ *   1. prefix pass: all total_q query tokens, as one non-causal segment,
+ *      against the first common_prefix_len keys of block_table row 0;
+ *   2. suffix pass: each sequence, causal, against its own keys from position
+ *      common_prefix_len on (block_table[s, common_prefix_len/block_size:]);
+ *   3. the two states merged by LSE as in pa_merge_attn_states.
+ * The result equals pa_varlen_fwd(causal = 1) over the whole KV. Arguments as
+ * pa_varlen_fwd plus common_prefix_len. Preconditions: common_prefix_len is a
+ * multiple of block_size (else PA_ERR_INVALID_ARG); every row's first
+ * common_prefix_len / block_size block_table entries equal row 0's; and
+ * seqused_k[s] - q_len(s) >= common_prefix_len for every sequence, so every
+ * query lies in its private suffix. A sequence that breaks the last rule sets
+ * PA_DEV_CASCADE; its rows still follow the three steps literally (every
+ * prefix key, then the causal suffix), which then differs from flat attention.
+ * The shared-entries rule is not checked (row 0's pages are used).
+ */
+pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_cache,
+                         const void* value_cache, int64_t cache_block_stride,
+                         const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                         const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
+                         int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                         int head_size, int block_size, int num_blocks, float softmax_scale,
+                         int common_prefix_len, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,242 @@
+"""Python binding of libpa.so: paged varlen attention for GB300 (sm_103a).
+
+Thin ctypes marshalling over the C ABI in include/pa.h. Torch is used for
+device memory (outputs and workspaces are allocated here, on the caller's
+side of the ABI) and for the current CUDA stream; every step of the
+computation runs in the library's CUDA kernels. There is no CPU fallback: the
+functions raise if the library or a GPU is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpa.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_BLOCK_SIZE = 2
+PA_ERR_UNSUPPORTED = 3
+PA_ERR_WORKSPACE = 4
+PA_ERR_CUDA = 5
+PA_DEV_BAD_PAGE = 1
+PA_DEV_BAD_SLOT = 2
+PA_DEV_BAD_SEQLEN = 4
+PA_DEV_TIMEOUT = 8
+PA_DEV_CASCADE = 16
+PA_BF16 = 0
+
+EXPORTS = (
+    "pa_status_string",
+    "pa_abi_version",
+    "pa_reshape_and_cache",
+    "pa_varlen_fwd_workspace_size",
+    "pa_varlen_fwd",
+    "pa_merge_attn_states",
+    "pa_cascade_fwd_workspace_size",
+    "pa_cascade_fwd",
+)
+
+_lib = None
+
+_c = ctypes
+_vp, _i64, _i32, _f32, _sz = _c.c_void_p, _c.c_int64, _c.c_int, _c.c_float, _c.c_size_t
+
+_SIGS = {
+    "pa_status_string": ([_i32], _c.c_char_p),
+    "pa_abi_version": ([], _i32),
+    "pa_reshape_and_cache": ([_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _i32, _i32, _i32, _i32,
+                              _i32, _i32, _vp, _vp], _i32),
+    "pa_varlen_fwd_workspace_size": ([_i32] * 9, _sz),
+    "pa_varlen_fwd": ([_vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                       _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _i32, _vp,
+                       _vp], _i32),
+    "pa_merge_attn_states": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
+    "pa_cascade_fwd_workspace_size": ([_i32] * 9, _sz),
+    "pa_cascade_fwd": ([_vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                        _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _i32, _vp,
+                        _vp], _i32),
+}
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libpa.so (built by ``_build.build()``) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libpa.so not built ({path}); run __graft_entry__.build() "
+                           "or python paged_kv_varlen_attn_gb300/_build.py")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+class PAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = load_library().pa_status_string(code).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def _check(code: int, where: str):
+    if code != PA_OK:
+        raise PAError(code, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (no CPU fallback)")
+
+
+def _sm_count(device) -> int:
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
+def _row_stride(t):
+    """Token stride of a [T, heads, D] tensor whose [heads, D] rows are contiguous."""
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError("tensor must be [tokens, heads, head_size] with contiguous rows")
+    return t.stride(0)
+
+
+def _cache_stride(c):
+    if c.dim() != 4 or c.stride(3) != 1 or c.stride(2) != c.shape[3] or \
+            c.stride(1) != c.shape[2] * c.shape[3]:
+        raise ValueError("cache must be [num_blocks, block_size, num_kv_heads, head_size] with "
+                         "contiguous pages")
+    return c.stride(0)
+
+
+# ---------------------------------------------------------------------------
+def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, dev_status=None):
+    """Scatter new K/V rows into their pages (in place on the caches)."""
+    lib = load_library()
+    _need_cuda(key, value, key_cache, value_cache, slot_mapping, dev_status)
+    if key_cache.stride(0) != value_cache.stride(0):
+        raise ValueError("key and value caches must share the page stride")
+    nb, bs, hk, d = key_cache.shape
+    code = lib.pa_reshape_and_cache(
+        _ptr(key), _ptr(value), _row_stride(key), _row_stride(value), _ptr(key_cache),
+        _ptr(value_cache), _cache_stride(key_cache), _ptr(slot_mapping), key.shape[0], hk, d, bs,
+        nb, PA_BF16, _ptr(dev_status), _stream(key.device))
+    _check(code, "pa_reshape_and_cache")
+
+
+def varlen_fwd_workspace_size(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                              num_kv_heads, head_size, block_size, sm_count):
+    return load_library().pa_varlen_fwd_workspace_size(
+        num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size,
+        block_size, sm_count)
+
+
+def cascade_fwd_workspace_size(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                               num_kv_heads, head_size, block_size, sm_count):
+    return load_library().pa_cascade_fwd_workspace_size(
+        num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size,
+        block_size, sm_count)
+
+
+def alloc_workspace(nbytes, device):
+    # 256-byte aligned (the caching allocator aligns to 512 bytes).
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table):
+    _need_cuda(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table)
+    if key_cache.stride(0) != value_cache.stride(0) or key_cache.shape != value_cache.shape:
+        raise ValueError("key and value caches must have the same shape and page stride")
+    for t, name in ((cu_seqlens_q, "cu_seqlens_q"), (seqused_k, "seqused_k"),
+                    (block_table, "block_table")):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [num_seqs, max_blocks] with unit column stride")
+
+
+def varlen_fwd(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
+               max_seqlen_k, softmax_scale, causal, out=None, lse=None, return_lse=True,
+               workspace=None, dev_status=None):
+    """Varlen attention over a paged KV cache. Returns (out, lse or None)."""
+    lib = load_library()
+    _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table)
+    T, H, D = q.shape
+    nb, bs, hk, _ = key_cache.shape
+    S = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(varlen_fwd_workspace_size(
+            S, T, max_seqlen_q, max_seqlen_k, H, hk, D, bs, _sm_count(q.device)), q.device)
+    code = lib.pa_varlen_fwd(
+        _ptr(q), _row_stride(q), _ptr(key_cache), _ptr(value_cache), _cache_stride(key_cache),
+        _ptr(cu_seqlens_q), _ptr(seqused_k), _ptr(block_table), block_table.stride(0), S, T,
+        int(max_seqlen_q), int(max_seqlen_k), H, hk, D, bs, nb, float(softmax_scale),
+        int(bool(causal)), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
+        _ptr(dev_status), _stream(q.device))
+    _check(code, "pa_varlen_fwd")
+    return out, lse
+
+
+def merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse, out=None, out_lse=None,
+                      return_lse=True):
+    """LSE-weighted combine of two partial attention states. Returns (out, lse or None)."""
+    lib = load_library()
+    _need_cuda(prefix_out, prefix_lse, suffix_out, suffix_lse)
+    T, H, D = prefix_out.shape
+    for t in (prefix_out, suffix_out):
+        if not t.is_contiguous():
+            raise ValueError("outputs must be contiguous [tokens, heads, head_size]")
+    if out is None:
+        out = torch.empty_like(prefix_out)
+    if out_lse is None and return_lse:
+        out_lse = torch.empty((H, T), dtype=torch.float32, device=prefix_out.device)
+    code = lib.pa_merge_attn_states(
+        _ptr(out), _ptr(out_lse), _ptr(prefix_out), _ptr(prefix_lse), _ptr(suffix_out),
+        _ptr(suffix_lse), T, H, D, PA_BF16, _stream(prefix_out.device))
+    _check(code, "pa_merge_attn_states")
+    return out, out_lse
+
+
+def cascade_fwd(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
+                max_seqlen_k, softmax_scale, common_prefix_len, out=None, lse=None,
+                return_lse=True, workspace=None, dev_status=None):
+    """Shared-prefix (cascade) attention. Returns (out, lse or None)."""
+    lib = load_library()
+    _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table)
+    T, H, D = q.shape
+    nb, bs, hk, _ = key_cache.shape
+    S = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(cascade_fwd_workspace_size(
+            S, T, max_seqlen_q, max_seqlen_k, H, hk, D, bs, _sm_count(q.device)), q.device)
+    code = lib.pa_cascade_fwd(
+        _ptr(q), _row_stride(q), _ptr(key_cache), _ptr(value_cache), _cache_stride(key_cache),
+        _ptr(cu_seqlens_q), _ptr(seqused_k), _ptr(block_table), block_table.stride(0), S, T,
+        int(max_seqlen_q), int(max_seqlen_k), H, hk, D, bs, nb, float(softmax_scale),
+        int(common_prefix_len), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
+        _ptr(dev_status), _stream(q.device))
+    _check(code, "pa_cascade_fwd")
+    return out, lse

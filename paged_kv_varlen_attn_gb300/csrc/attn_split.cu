@@ -1,0 +1,533 @@
+// Split-KV attention kernel for decode and short-query segments.
+//
+// What it computes is the paged varlen attention of "FlashAttention 在 vLLM 中的
+// 实现分析" §4 / §5 (block_table[seq][logical block] -> physical page, offset in
+// page) with the tiled online softmax of §1.1, split over the keys as in the
+// num_splits decode of §1.3, the splits recombined with the LSE-weighted merge
+// of §6.3.
+//
+// Design (GB300):
+//  * One CTA per work item (segment, row tile of <= 64 packed query rows,
+//    key chunk) and KV head. Packed rows are (query token, head of the GQA
+//    group), so the K/V tile read from HBM serves all G heads at once.
+//  * Warp 4 is the producer: one lane walks the block table and issues TMA
+//    tile loads (128-byte swizzled boxes of 16-64 page rows x 64 dims) into a
+//    multi-stage shared-memory ring guarded by full/empty mbarriers. Every wait
+//    is bounded; a timeout sets PA_DEV_TIMEOUT and the CTA drains and returns.
+//  * Warps 0-3 are consumers. With R packed rows, ceil(R/16) warps (rounded to
+//    1, 2 or 4) take 16 rows each and the remaining factor splits every 64-key
+//    tile between warps, so a decode item (R <= 16) keeps all four warps busy
+//    on different keys. Q.K^T and P.V use the warp-level bf16 MMA
+//    (m16n8k16, fp32 accumulate) on ldmatrix fragments; row max/sum use quad
+//    shuffles; the warps' partial states are merged through shared memory.
+//  * A split item writes its normalised fp32 partial (O, LSE) to the
+//    workspace; the last CTA of a (row tile, KV head) group -- found with one
+//    atomic counter, no spinning -- merges all splits in a fixed order, so the
+//    result is deterministic.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace pa {
+
+template <int D>
+struct SplitCfg {
+  static constexpr int BN = kKeyTile;                  // keys per stage
+  static constexpr int HALVES = D / 64;                // 64-dim swizzled halves
+  static constexpr int HALF_BYTES = BN * 128;          // [64 rows x 128 B]
+  static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K and V
+  static constexpr int STAGES = D == 128 ? 3 : 6;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int SMEM_BYTES = RING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int THREADS = 160;
+};
+
+struct SplitShared {
+  uint64_t* full;
+  uint64_t* empty;
+  volatile int* flags;   // [0] abort, [1] last-CTA, [2] tiles issued, [4..7] consumed per warp
+};
+
+// ---------------------------------------------------------------------------
+// Producer: one lane issues the page-table walk and the TMA loads.
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void split_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                               const AttnArgs& a, uint8_t* ring, SplitShared sh,
+                                               const int32_t* bt_row, int hk, int kb, int kv_len,
+                                               int ntiles) {
+  using C = SplitCfg<D>;
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % C::STAGES;
+    if (t >= C::STAGES) {
+      if (!mbar_wait(&sh.empty[s], ((t / C::STAGES) - 1) & 1)) {
+        flag_status(a.status, PA_DEV_TIMEOUT);
+        sh.flags[0] = 1;
+        break;
+      }
+    }
+    if (sh.flags[0]) break;
+    uint8_t* kdst = ring + s * C::STAGE_BYTES;
+    uint8_t* vdst = kdst + C::TILE_BYTES;
+    mbar_arrive_expect_tx(&sh.full[s], C::STAGE_BYTES);
+    const int key0 = kb + t * C::BN;
+    for (int r = 0; r < C::BN; r += a.box_rows) {
+      const int k = key0 + r;
+      int page = a.num_blocks;  // out of range: TMA fills zeros
+      int prow = 0;
+      if (k < kv_len) {
+        const int lp = k / a.bs;
+        prow = k - lp * a.bs;
+        const int pg = __ldg(bt_row + lp);
+        if (pg >= 0 && pg < a.num_blocks) page = pg;
+        else flag_status(a.status, PA_DEV_BAD_PAGE);
+      }
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) {
+        tma_load_4d(kdst + h * C::HALF_BYTES + r * 128, tmK, &sh.full[s], h * 64, hk, prow, page);
+        tma_load_4d(vdst + h * C::HALF_BYTES + r * 128, tmV, &sh.full[s], h * 64, hk, prow, page);
+      }
+    }
+    sh.flags[2] = t + 1;
+  }
+}
+
+// Final write of one 8-wide column pair set of a row: out = o (already
+// normalised), optionally merged with a prefix state (cascade).
+__device__ __forceinline__ void merge_prefix(const AttnArgs& a, int64_t obase, int h, int tok,
+                                             float& lse_nat, float* o, int n) {
+  // o[0..n) are the values of consecutive columns starting at obase.
+  const float la = a.merge_lse[static_cast<int64_t>(h) * a.lse_stride + tok];
+  const float lb = lse_nat;
+  const float m = fmaxf(la, lb);
+  if (m == -INFINITY) {
+    for (int i = 0; i < n; ++i) o[i] = 0.f;
+    return;
+  }
+  const float wa = fast_exp2((la - m) * kLog2e), wb = fast_exp2((lb - m) * kLog2e);
+  const float inv = 1.f / (wa + wb);
+  for (int i = 0; i < n; ++i) o[i] = (wa * __ldcg(a.merge_o + obase + i) + wb * o[i]) * inv;
+  lse_nat = m + fast_log2(wa + wb) * kLn2;
+}
+
+// ---------------------------------------------------------------------------
+// Consumers. RGN = number of 16-row groups (1, 2 or 4); 4 / RGN warps share
+// each group and split every key tile between them.
+// ---------------------------------------------------------------------------
+template <int D, int RGN>
+__device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring, SplitShared sh,
+                                               int hk, int seg, int rt, int j, int q_start,
+                                               int q_len, int kv_len, int kb, int ke, int ntiles,
+                                               int nsplit, int slot_base) {
+  using C = SplitCfg<D>;
+  constexpr int KS = 4 / RGN;       // warps per row group
+  constexpr int KW = C::BN / KS;    // keys per warp per tile
+  constexpr int NT = KW / 8;        // 8-key n-tiles per warp per tile
+  constexpr int DK = D / 16;        // 16-dim k-steps
+  constexpr int DN = D / 8;         // 8-dim n-tiles of O
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rg = warp % RGN, ks = warp / RGN;
+  const int G = a.G;
+  const int row0 = rt * kRowsSplit;
+  const int R = min(kRowsSplit, q_len * G - row0);
+  const int gq = lane >> 2, cq = lane & 3;
+
+  // Rows owned by this thread: local rows rg*16 + gq and +8.
+  int lim[2];
+  bool rvalid[2];
+  int tok[2], head[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int rl = rg * 16 + gq + 8 * r;
+    rvalid[r] = rl < R;
+    const int pr = row0 + (rvalid[r] ? rl : 0);
+    const int i = pr / G;
+    tok[r] = q_start + i;
+    head[r] = hk * G + (pr - i * G);
+    lim[r] = !rvalid[r] ? -1 : (a.causal ? kv_len - q_len + i : 0x7fffffff);
+  }
+  int lim_max = max(lim[0], lim[1]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lim_max = max(lim_max, __shfl_xor_sync(0xffffffffu, lim_max, o));
+
+  // Q fragments (A operand, 16 x D), loaded once from global memory.
+  uint32_t qf[DK][4];
+#pragma unroll
+  for (int kk = 0; kk < DK; ++kk) {
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int r = x & 1;                    // a0,a2: row gq; a1,a3: row gq+8
+      const int col = kk * 16 + 2 * cq + (x >> 1) * 8;
+      uint32_t v = 0;
+      if (rvalid[r]) {
+        const __nv_bfloat16* p = a.q + static_cast<int64_t>(tok[r]) * a.q_stride +
+                                 static_cast<int64_t>(head[r]) * D + col;
+        v = __ldg(reinterpret_cast<const uint32_t*>(p));
+      }
+      qf[kk][x] = v;
+    }
+  }
+
+  float o[DN][4];
+#pragma unroll
+  for (int n = 0; n < DN; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  const float sl2 = a.scale_log2;
+  const int slice0 = ks * KW;
+  int consumed = 0;
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % C::STAGES;
+    if (!mbar_wait(&sh.full[s], (t / C::STAGES) & 1)) {
+      flag_status(a.status, PA_DEV_TIMEOUT);
+      sh.flags[0] = 1;
+      break;
+    }
+    consumed = t + 1;
+    uint8_t* ktile = ring + s * C::STAGE_BYTES;
+    uint8_t* vtile = ktile + C::TILE_BYTES;
+    const int tile_key0 = kb + t * C::BN;
+    const int key_base = tile_key0 + slice0;
+    if (key_base < ke && key_base <= lim_max) {
+      // Keys past the sequence end inside a loaded page hold arbitrary bytes;
+      // zero those V rows so 0 * garbage cannot produce NaN.
+      if (tile_key0 + slice0 + KW > kv_len) {
+        const int first = max(kv_len - tile_key0, slice0);
+        const int nrow = slice0 + KW - first;
+        for (int idx = lane; idx < nrow * C::HALVES * 8; idx += 32) {
+          const int rr = first + idx / (C::HALVES * 8);
+          const int rem = idx % (C::HALVES * 8);
+          *reinterpret_cast<uint4*>(vtile + (rem >> 3) * C::HALF_BYTES + rr * 128 + (rem & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        // These generic-proxy stores precede the next TMA write of the stage.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+      float sacc[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+      const uint32_t kbase = smem_u32(ktile);
+      const int mat = lane >> 3, rr = lane & 7;
+#pragma unroll
+      for (int kk = 0; kk < DK; ++kk) {
+        const int half = kk >> 2, col = (kk & 3) * 16;
+#pragma unroll
+        for (int np = 0; np < NT / 2; ++np) {
+          const int key = slice0 + np * 16 + rr + ((mat >> 1) << 3);
+          const int c = col + ((mat & 1) << 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kbase + half * C::HALF_BYTES + sw128(key, c), b0, b1, b2, b3);
+          mma_16816(sacc[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+          mma_16816(sacc[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+        }
+      }
+      // Mask, scale into the log2 domain, running max.
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = key_base + n * 8 + 2 * cq + (e & 1);
+          const int r = e >> 1;
+          const bool ok = key < ke && key <= lim[r];
+          const float v = ok ? sacc[n][e] * sl2 : -INFINITY;
+          sacc[n][e] = v;
+          mx[r] = fmaxf(mx[r], v);
+        }
+      }
+      float alpha[2], muse[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        const float mn = fmaxf(m[r], mx[r]);
+        muse[r] = mn == -INFINITY ? 0.f : mn;
+        alpha[r] = fast_exp2(m[r] - muse[r]);
+        m[r] = mn;
+        l[r] *= alpha[r];
+      }
+#pragma unroll
+      for (int n = 0; n < DN; ++n) {
+        o[n][0] *= alpha[0];
+        o[n][1] *= alpha[0];
+        o[n][2] *= alpha[1];
+        o[n][3] *= alpha[1];
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p = fast_exp2(sacc[n][e] - muse[e >> 1]);
+          sacc[n][e] = p;
+          l[e >> 1] += p;
+        }
+      }
+      // O += P V.
+      const uint32_t vbase = smem_u32(vtile);
+#pragma unroll
+      for (int kk = 0; kk < NT / 2; ++kk) {
+        const uint32_t pa0 = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
+        const uint32_t pa1 = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
+        const uint32_t pa2 = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+        const uint32_t pa3 = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          const int half = dp >> 2, col = (dp & 3) * 16;
+          const int key = slice0 + kk * 16 + rr + ((mat & 1) << 3);
+          const int c = col + ((mat >> 1) << 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vbase + half * C::HALF_BYTES + sw128(key, c), b0, b1, b2, b3);
+          mma_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
+          mma_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[s]);
+    if (sh.flags[0]) break;
+  }
+  if (lane == 0) sh.flags[4 + warp] = consumed;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+  }
+
+  // All consumers are done with the ring: drain any load still in flight
+  // (only after an abort), then reuse the ring as merge scratch.
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  if (threadIdx.x == 0) {
+    int cmin = sh.flags[4];
+    for (int w = 1; w < 4; ++w) cmin = min(cmin, sh.flags[4 + w]);
+    const int issued = sh.flags[2];
+    for (int t = cmin; t < issued; ++t)
+      if (!mbar_wait(&sh.full[t % C::STAGES], (t / C::STAGES) & 1)) break;
+  }
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+
+  if constexpr (KS > 1) {
+    float* scratch = reinterpret_cast<float*>(ring);
+    constexpr int PER_WARP = DN * 4 * 32 + 64;   // O fragments + (m, l) of 16 rows
+    if (ks > 0) {
+      float* w = scratch + warp * PER_WARP;
+#pragma unroll
+      for (int n = 0; n < DN; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[(n * 4 + e) * 32 + lane] = o[n][e];
+      if (cq == 0) {
+        w[DN * 128 + gq] = m[0];
+        w[DN * 128 + gq + 8] = m[1];
+        w[DN * 128 + 16 + gq] = l[0];
+        w[DN * 128 + 16 + gq + 8] = l[1];
+      }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (ks > 0) return;
+#pragma unroll
+    for (int k2 = 1; k2 < KS; ++k2) {
+      const float* w = scratch + (rg + k2 * RGN) * PER_WARP;
+      float alpha_a[2], alpha_b[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float mb = w[DN * 128 + gq + 8 * r];
+        const float lb = w[DN * 128 + 16 + gq + 8 * r];
+        const float mn = fmaxf(m[r], mb);
+        const float mu = mn == -INFINITY ? 0.f : mn;
+        alpha_a[r] = fast_exp2(m[r] - mu);
+        alpha_b[r] = fast_exp2(mb - mu);
+        l[r] = l[r] * alpha_a[r] + lb * alpha_b[r];
+        m[r] = mn;
+      }
+#pragma unroll
+      for (int n = 0; n < DN; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o[n][e] = o[n][e] * alpha_a[e >> 1] + w[(n * 4 + e) * 32 + lane] * alpha_b[e >> 1];
+    }
+  }
+
+  // Epilogue (warps 0 .. RGN-1 hold the merged rows of their group).
+  float inv_l[2], lse_nat[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const bool any = l[r] > 0.f;
+    inv_l[r] = any ? 1.f / l[r] : 0.f;
+    lse_nat[r] = any ? (m[r] + fast_log2(l[r])) * kLn2 : -INFINITY;
+  }
+  const int H = a.H;
+  if (nsplit == 1) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (!rvalid[r]) continue;
+      const int64_t obase = (static_cast<int64_t>(tok[r]) * H + head[r]) * D;
+      float lse_r = lse_nat[r];
+#pragma unroll
+      for (int n = 0; n < DN; ++n) {
+        float v[2] = {o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]};
+        const int col = n * 8 + 2 * cq;
+        if (a.merge_o) {
+          float lse_tmp = lse_nat[r];
+          merge_prefix(a, obase + col, head[r], tok[r], lse_tmp, v, 2);
+          lse_r = lse_tmp;
+        }
+        if (a.out_f32) {
+          *reinterpret_cast<float2*>(a.out_f32 + obase + col) = make_float2(v[0], v[1]);
+        } else {
+          *reinterpret_cast<uint32_t*>(a.out + obase + col) = pack_bf16(v[0], v[1]);
+        }
+      }
+      if (a.lse && cq == 0) a.lse[static_cast<int64_t>(head[r]) * a.lse_stride + tok[r]] = lse_r;
+    }
+    return;
+  }
+
+  // Split item: publish the normalised partial, then the last CTA merges.
+  const int slot = slot_base + rt * nsplit + j;
+  const int64_t slot_row0 = (static_cast<int64_t>(slot) * a.H_kv + hk) * kSlotRows;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int rl = rg * 16 + gq + 8 * r;
+    if (!rvalid[r]) continue;
+    float* po = a.part_o + (slot_row0 + rl) * D;
+#pragma unroll
+    for (int n = 0; n < DN; ++n)
+      __stcg(reinterpret_cast<float2*>(po + n * 8 + 2 * cq),
+             make_float2(o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]));
+    if (cq == 0) __stcg(a.part_lse + slot_row0 + rl, lse_nat[r]);
+  }
+  __threadfence();
+  asm volatile("bar.sync 2, %0;" ::"r"(32 * RGN) : "memory");
+  const int grp = slot_base + rt * nsplit;
+  int* counter = a.counters + static_cast<int64_t>(grp) * a.H_kv + hk;
+  if (threadIdx.x == 0) sh.flags[1] = (atomicAdd(counter, 1) == nsplit - 1) ? 1 : 0;
+  asm volatile("bar.sync 2, %0;" ::"r"(32 * RGN) : "memory");
+  if (!sh.flags[1]) return;
+  __threadfence();
+  constexpr int C4 = D / 4;
+  for (int idx = threadIdx.x; idx < R * C4; idx += 32 * RGN) {
+    const int rl = idx / C4, c4 = idx - rl * C4;
+    const int pr = row0 + rl;
+    const int i = pr / G;
+    const int tk = q_start + i, hh = hk * G + (pr - i * G);
+    float mx = -INFINITY;
+    for (int jj = 0; jj < nsplit; ++jj) {
+      const int64_t sr = (static_cast<int64_t>(grp + jj) * a.H_kv + hk) * kSlotRows + rl;
+      mx = fmaxf(mx, __ldcg(a.part_lse + sr));
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float lse_r = -INFINITY;
+    if (mx != -INFINITY) {
+      float sw = 0.f;
+      for (int jj = 0; jj < nsplit; ++jj) {
+        const int64_t sr = (static_cast<int64_t>(grp + jj) * a.H_kv + hk) * kSlotRows + rl;
+        const float w = fast_exp2((__ldcg(a.part_lse + sr) - mx) * kLog2e);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + sr * D) + c4);
+        sw += w;
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2] += w * v.z;
+        acc[3] += w * v.w;
+      }
+      const float inv = 1.f / sw;
+#pragma unroll
+      for (int x = 0; x < 4; ++x) acc[x] *= inv;
+      lse_r = mx + fast_log2(sw) * kLn2;
+    }
+    const int64_t obase = (static_cast<int64_t>(tk) * H + hh) * D + c4 * 4;
+    if (a.merge_o) merge_prefix(a, obase, hh, tk, lse_r, acc, 4);
+    if (a.out_f32) {
+      *reinterpret_cast<float4*>(a.out_f32 + obase) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    } else {
+      uint2 pk = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+      *reinterpret_cast<uint2*>(a.out + obase) = pk;
+    }
+    if (a.lse && c4 == 0) a.lse[static_cast<int64_t>(hh) * a.lse_stride + tk] = lse_r;
+  }
+  if (threadIdx.x == 0) *counter = 0;   // ready for the next call
+}
+
+template <int D>
+__global__ void __launch_bounds__(SplitCfg<D>::THREADS, 2)
+attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ AttnArgs a) {
+  using C = SplitCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  SplitShared sh;
+  sh.full = reinterpret_cast<uint64_t*>(ring + C::RING_BYTES);
+  sh.empty = sh.full + C::STAGES;
+  sh.flags = reinterpret_cast<volatile int*>(sh.empty + C::STAGES);
+
+  if (static_cast<int>(blockIdx.x) >= a.header[0]) return;
+  const int hk = blockIdx.y;
+  const int4 it = a.items[blockIdx.x];
+  const int seg = it.x, rt = it.y, j = it.z;
+  const int4 sg = a.seg[seg];
+  const int4 sp = a.segsplit[seg];
+  const int q_start = sg.x, q_len = sg.y, kv_len = sg.z;
+  const int nsplit = sp.x, slot_base = sp.y, chunk = sp.z;
+  const int G = a.G;
+  const int row0 = rt * kRowsSplit;
+  const int R = min(kRowsSplit, q_len * G - row0);
+  const int kb = j * chunk;
+  int ke = min(kv_len, kb + chunk);
+  if (a.causal) {
+    const int i_last = (row0 + R - 1) / G;
+    ke = min(ke, kv_len - q_len + i_last + 1);
+  }
+  const int ntiles = ke > kb ? (ke - kb + C::BN - 1) / C::BN : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 4);
+    }
+    for (int f = 0; f < 8; ++f) sh.flags[f] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5;
+  if (warp == 4) {
+    if ((threadIdx.x & 31) == 0 && ntiles > 0) {
+      const int32_t* bt_row = a.bt + static_cast<int64_t>(seg) * a.bt_row_stride + a.bt_col_offset;
+      split_producer<D>(&tmK, &tmV, a, ring, sh, bt_row, hk, kb, kv_len, ntiles);
+    }
+    return;
+  }
+  if (R <= 16)
+    split_consumer<D, 1>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke, ntiles,
+                         nsplit, slot_base);
+  else if (R <= 32)
+    split_consumer<D, 2>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke, ntiles,
+                         nsplit, slot_base);
+  else
+    split_consumer<D, 4>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke, ntiles,
+                         nsplit, slot_base);
+}
+
+template <int D>
+static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                  const AttnArgs& a, int items_bound, cudaStream_t st) {
+  using C = SplitCfg<D>;
+  // Per-device attribute; cheap, so it is set on every launch.
+  cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(items_bound, a.H_kv);
+  attn_split_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmK, tmV, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
+                              int items_bound, cudaStream_t st) {
+  if (items_bound <= 0) return cudaSuccess;
+  if (a.D == 128) return launch_split_d<128>(tmK, tmV, a, items_bound, st);
+  return launch_split_d<64>(tmK, tmV, a, items_bound, st);
+}
+
+}  // namespace pa

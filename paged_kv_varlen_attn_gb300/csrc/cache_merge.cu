@@ -1,0 +1,155 @@
+// reshape_and_cache (slot_mapping scatter) and merge_attn_states (LSE-weighted
+// combine): the two memory-bound helper kernels of the attention path.
+//
+// Sources: "FlashAttention 在 vLLM 中的实现分析" §4.2 (do_kv_cache_update ->
+// reshape_and_cache_flash writes new K/V into the paged cache by slot_mapping),
+// §6.3 step 3 and §8.2 (merge_attn_states combines two (out, lse) states).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// Scatter. Every thread moves 16-byte vectors; consecutive threads move
+// consecutive vectors of one token's [H_kv, D] row, so both the read of the
+// new token and the write into its page row are fully coalesced. The grid is
+// a multiple of the SM count and strides over all vectors.
+// ---------------------------------------------------------------------------
+constexpr int kScatterThreads = 256;
+constexpr int kScatterUnroll = 4;
+
+__global__ void __launch_bounds__(kScatterThreads)
+reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                         int64_t kstride_v, int64_t vstride_v, uint4* __restrict__ kc,
+                         uint4* __restrict__ vc, int64_t block_stride_v,
+                         const int64_t* __restrict__ slots, int num_tokens, int vpt, int bs,
+                         int64_t num_slots, int32_t* status) {
+  // vpt = 16-byte vectors per token row (H_kv * D / 8); each token has a K and
+  // a V row, so the flat index space is num_tokens * 2 * vpt.
+  const int64_t total = static_cast<int64_t>(num_tokens) * 2 * vpt;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+       base += step * kScatterUnroll) {
+    uint4 v[kScatterUnroll];
+    uint4* dst[kScatterUnroll];
+#pragma unroll
+    for (int u = 0; u < kScatterUnroll; ++u) {
+      dst[u] = nullptr;
+      const int64_t idx = base + u * step;
+      if (idx >= total) continue;
+      const int64_t t = idx / (2 * vpt);
+      const int rem = static_cast<int>(idx - t * 2 * vpt);
+      const int which = rem >= vpt;            // 0: key, 1: value
+      const int vi = rem - which * vpt;
+      const int64_t slot = __ldg(slots + t);
+      if (slot < 0) continue;                  // padding token
+      if (slot >= num_slots) {
+        flag_status(status, PA_DEV_BAD_SLOT);
+        continue;
+      }
+      const int64_t page = slot / bs;
+      const int64_t row = slot - page * bs;
+      const uint4* src = which ? value + t * vstride_v : key + t * kstride_v;
+      v[u] = __ldcs(src + vi);
+      uint4* pool = which ? vc : kc;
+      dst[u] = pool + page * block_stride_v + row * vpt + vi;
+    }
+#pragma unroll
+    for (int u = 0; u < kScatterUnroll; ++u)
+      if (dst[u]) *dst[u] = v[u];
+  }
+}
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t kstride,
+                                     int64_t vstride, void* kc, void* vc, int64_t block_stride,
+                                     const int64_t* slots, int num_tokens, int H_kv, int D, int bs,
+                                     int num_blocks, int32_t* status, cudaStream_t st, int sms) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int vpt = H_kv * D / 8;
+  const int64_t total = static_cast<int64_t>(num_tokens) * 2 * vpt;
+  const int64_t want = (total + kScatterThreads * kScatterUnroll - 1) /
+                       (kScatterThreads * kScatterUnroll);
+  const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 CTAs of 256 threads per SM
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  reshape_and_cache_kernel<<<grid, kScatterThreads, 0, st>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value), kstride / 8, vstride / 8,
+      static_cast<uint4*>(kc), static_cast<uint4*>(vc), block_stride / 8, slots, num_tokens, vpt,
+      bs, static_cast<int64_t>(num_blocks) * bs, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// merge_attn_states. One thread per 8 output elements (one 16-byte vector) of
+// a (token, head) row; the two LSEs of the row are read per thread (they hit
+// L1). With m = max(a, b): out = (e^(a-m) oa + e^(b-m) ob) / (e^(a-m) + e^(b-m)),
+// lse = m + ln(e^(a-m) + e^(b-m)); both -inf gives out 0, lse -inf.
+// ---------------------------------------------------------------------------
+constexpr int kMergeThreads = 256;
+
+__device__ __forceinline__ void bf16x8_to_float(const uint4& v, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 x = __bfloat1622float2(h[i]);
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
+}
+
+__global__ void __launch_bounds__(kMergeThreads)
+merge_attn_states_kernel(uint4* out, float* out_lse, const uint4* __restrict__ a,
+                         const float* __restrict__ alse, const uint4* __restrict__ b,
+                         const float* __restrict__ blse, int T, int H, int vpr) {
+  const int64_t total = static_cast<int64_t>(T) * H * vpr;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += step) {
+    const int64_t row = idx / vpr;            // row = t * H + h
+    const int vi = static_cast<int>(idx - row * vpr);
+    const int t = static_cast<int>(row / H);
+    const int h = static_cast<int>(row - static_cast<int64_t>(t) * H);
+    const float la = __ldg(alse + static_cast<int64_t>(h) * T + t);
+    const float lb = __ldg(blse + static_cast<int64_t>(h) * T + t);
+    const float m = fmaxf(la, lb);
+    uint4 res;
+    float lse_out;
+    if (m == -INFINITY) {
+      res = make_uint4(0, 0, 0, 0);
+      lse_out = -INFINITY;
+    } else {
+      const float wa = fast_exp2((la - m) * kLog2e);
+      const float wb = fast_exp2((lb - m) * kLog2e);
+      const float inv = 1.0f / (wa + wb);
+      const float ca = wa * inv, cb = wb * inv;
+      float fa[8], fb[8];
+      bf16x8_to_float(__ldcs(a + idx), fa);
+      bf16x8_to_float(__ldcs(b + idx), fb);
+      uint32_t* r = reinterpret_cast<uint32_t*>(&res);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        r[i] = pack_bf16(ca * fa[2 * i] + cb * fb[2 * i], ca * fa[2 * i + 1] + cb * fb[2 * i + 1]);
+      lse_out = m + fast_log2(wa + wb) * kLn2;
+    }
+    out[idx] = res;
+    if (out_lse && vi == 0) out_lse[static_cast<int64_t>(h) * T + t] = lse_out;
+  }
+}
+
+cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* alse,
+                         const void* b, const float* blse, int T, int H, int D, cudaStream_t st,
+                         int sms) {
+  if (T == 0) return cudaSuccess;
+  const int vpr = D / 8;
+  const int64_t total = static_cast<int64_t>(T) * H * vpr;
+  const int64_t want = (total + kMergeThreads - 1) / kMergeThreads;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  merge_attn_states_kernel<<<grid, kMergeThreads, 0, st>>>(
+      static_cast<uint4*>(out), out_lse, static_cast<const uint4*>(a), alse,
+      static_cast<const uint4*>(b), blse, T, H, vpr);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,458 @@
+// C-ABI entry points (include/pa.h): argument validation, workspace layout,
+// TMA descriptor encoding and kernel launches. Host code only; every step of
+// the computation runs in the kernels of the other translation units.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Split targets (work items per KV head) per kernel class, from the SM count:
+// the split-KV kernel runs 2 CTAs per SM and aims at ~2 waves; the prefill
+// kernel runs 1 CTA per SM.
+inline int target_split(int sms, int H_kv) { return cdiv(4LL * sms, H_kv); }
+inline int target_tc(int sms, int H_kv) { return cdiv(1LL * sms, H_kv); }
+
+struct PassDims {
+  int num_segs;   // segments planned
+  int total_q;
+  int G, H, H_kv, D;
+  int sms;
+  bool tc;
+};
+
+// Workspace layout of one pass starting at byte offset `base`.
+PassLayout layout_pass(const PassDims& d, size_t base) {
+  PassLayout L{};
+  L.target[0] = target_split(d.sms, d.H_kv);
+  L.target[1] = d.tc ? target_tc(d.sms, d.H_kv) : 0;
+  const long long rows = static_cast<long long>(d.total_q) * d.G;
+  L.items_bound[0] = L.target[0] + d.num_segs + cdiv(rows, kRowsSplit) + 1;
+  L.items_bound[1] = d.tc ? L.target[1] + d.num_segs + cdiv(rows, kRowsTc) + 1 : 0;
+  L.slots_bound = 2 * (L.target[0] + L.target[1]) + 2;
+  size_t off = align_up(base);
+  L.header = off;                 off = align_up(off + 64 * sizeof(int));
+  L.seg = off;                    off = align_up(off + static_cast<size_t>(d.num_segs) * 16);
+  L.segsplit = off;               off = align_up(off + static_cast<size_t>(d.num_segs) * 16);
+  L.items[0] = off;               off = align_up(off + static_cast<size_t>(L.items_bound[0]) * 16);
+  L.items[1] = off;               off = align_up(off + static_cast<size_t>(L.items_bound[1]) * 16);
+  const size_t slot_rows = static_cast<size_t>(L.slots_bound) * d.H_kv * kSlotRows;
+  L.counters = off;               off = align_up(off + static_cast<size_t>(L.slots_bound) * d.H_kv * 4);
+  L.part_lse = off;               off = align_up(off + slot_rows * 4);
+  L.part_o = off;                 off = align_up(off + slot_rows * d.D * 4);
+  L.end = off;
+  return L;
+}
+
+// The tensor-core prefill kernel is not in this build yet; every segment is
+// planned for the split-KV kernel.
+constexpr bool kTcAvailable = false;
+
+struct CascadeLayout {
+  PassLayout prefix, suffix;
+  size_t prefix_o, prefix_lse, end;
+};
+
+CascadeLayout layout_cascade(int num_seqs, int total_q, int G, int H, int H_kv, int D, int sms) {
+  CascadeLayout C{};
+  PassDims pd{1, total_q, G, H, H_kv, D, sms, kTcAvailable};
+  C.prefix = layout_pass(pd, 0);
+  PassDims sd{num_seqs, total_q, G, H, H_kv, D, sms, kTcAvailable};
+  C.suffix = layout_pass(sd, C.prefix.end);
+  size_t off = C.suffix.end;
+  C.prefix_o = off;   off = align_up(off + static_cast<size_t>(total_q) * H * D * 4);
+  C.prefix_lse = off; off = align_up(off + static_cast<size_t>(total_q) * H * 4);
+  C.end = off;
+  return C;
+}
+
+int query_sms(int sm_count) {
+  if (sm_count > 0) return sm_count;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool pow2_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
+
+// Checks shared by the attention entry points that need no device pointer.
+pa_status check_shape(int num_seqs, int total_q, int max_seqlen_q, int max_seqlen_k, int H,
+                      int H_kv, int D, int bs, int dtype) {
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return PA_ERR_INVALID_ARG;
+  if (H <= 0 || H_kv <= 0 || H % H_kv != 0) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (!pow2_group(H / H_kv)) return PA_ERR_UNSUPPORTED;
+  if (bs <= 0 || bs % 16 != 0 || bs > 1024) return PA_ERR_BLOCK_SIZE;
+  return PA_OK;
+}
+
+pa_status check_attn_ptrs(const void* q, int64_t q_stride, const void* kc, const void* vc,
+                          int64_t block_stride, const int32_t* cu, const int32_t* lens,
+                          const int32_t* bt, int bt_stride, int num_seqs, int total_q,
+                          int num_blocks, int H, int H_kv, int D, int bs, float scale, int causal,
+                          const void* out, const float* lse) {
+  if (num_seqs > 0 && (!cu || !lens || !bt)) return PA_ERR_INVALID_ARG;
+  if (total_q > 0 && (!q || !out)) return PA_ERR_INVALID_ARG;
+  if (!kc || !vc) return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(out)) return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return PA_ERR_INVALID_ARG;
+  if (q_stride < static_cast<int64_t>(H) * D || q_stride % 8 != 0) return PA_ERR_INVALID_ARG;
+  if (block_stride < static_cast<int64_t>(bs) * H_kv * D || block_stride % 8 != 0)
+    return PA_ERR_INVALID_ARG;
+  if (bt_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4-D view of a page pool: (dim, kv head, row in page, page), 128-byte
+// swizzled boxes of 64 dims x 1 head x box_rows rows x 1 page. Coordinates
+// past the pool (a page id == num_blocks) read as zeros.
+bool encode_pool_map(CUtensorMap* map, const void* base, int D, int H_kv, int bs, int num_blocks,
+                     int64_t block_stride, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_kv),
+                        static_cast<cuuint64_t>(bs),
+                        static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H_kv) * D * 2,
+                           static_cast<cuuint64_t>(block_stride) * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int gcd_int(int a, int b) {
+  while (b) {
+    int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+struct CommonAttn {
+  const void* q;
+  int64_t q_stride;
+  const void* kc;
+  const void* vc;
+  int64_t block_stride;
+  const int32_t* cu;
+  const int32_t* lens;
+  const int32_t* bt;
+  int bt_stride, num_seqs, total_q, max_q, max_k, H, H_kv, D, bs, num_blocks;
+  float scale;
+  int32_t* status;
+  cudaStream_t st;
+};
+
+PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int single, int single_kv,
+                   int kv_off, int kv_cap, int causal, int check_cascade) {
+  PlanArgs p{};
+  p.cu_seqlens_q = c.cu;
+  p.seqused_k = c.lens;
+  p.num_segs = c.num_seqs;
+  p.single_segment = single;
+  p.total_q = c.total_q;
+  p.single_kv_len = single_kv;
+  p.kv_len_offset = kv_off;
+  p.kv_len_cap = kv_cap;
+  p.max_q = c.max_q;
+  p.max_k = c.max_k;
+  p.G = c.H / c.H_kv;
+  p.H_kv = c.H_kv;
+  p.tc_enabled = kTcAvailable ? 1 : 0;
+  p.causal = causal;
+  p.target0 = L.target[0];
+  p.target1 = L.target[1];
+  p.items_bound0 = L.items_bound[0];
+  p.items_bound1 = L.items_bound[1];
+  p.slots_bound = L.slots_bound;
+  p.ws = ws;
+  p.L = L;
+  p.status = c.status;
+  p.check_cascade = check_cascade;
+  return p;
+}
+
+AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt_row_stride,
+                   int bt_col_offset, int causal, void* out, float* out_f32, float* lse,
+                   const float* merge_o, const float* merge_lse) {
+  AttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(c.q);
+  a.q_stride = c.q_stride;
+  a.bt = c.bt;
+  a.bt_row_stride = bt_row_stride;
+  a.bt_col_offset = bt_col_offset;
+  a.H = c.H;
+  a.H_kv = c.H_kv;
+  a.G = c.H / c.H_kv;
+  a.D = c.D;
+  a.bs = c.bs;
+  a.num_blocks = c.num_blocks;
+  a.scale_log2 = c.scale * 1.4426950408889634f;
+  a.causal = causal;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.out_f32 = out_f32;
+  a.lse = lse;
+  a.lse_stride = c.total_q;
+  a.merge_o = merge_o;
+  a.merge_lse = merge_lse;
+  a.header = reinterpret_cast<const int*>(ws + L.header);
+  a.seg = reinterpret_cast<const int4*>(ws + L.seg);
+  a.segsplit = reinterpret_cast<const int4*>(ws + L.segsplit);
+  a.items = reinterpret_cast<const int4*>(ws + L.items[0]);
+  a.counters = reinterpret_cast<int*>(ws + L.counters);
+  a.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  a.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  a.status = c.status;
+  a.box_rows = gcd_int(c.bs, kKeyTile);
+  return a;
+}
+
+pa_status launch_pass(const CommonAttn& c, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                      const AttnArgs& a, const PassLayout& L) {
+  if (launch_attn_split(tmK, tmV, a, L.items_bound[0], c.st) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: invalid argument";
+    case PA_ERR_BLOCK_SIZE: return "PA_ERR_BLOCK_SIZE: block size must be a multiple of 16 (<= 1024)";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: head size, dtype or GQA ratio not supported";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA launch or query failed";
+    default: return "PA_ERR_UNKNOWN";
+  }
+}
+
+int pa_abi_version(void) { return kAbiVersion; }
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, int64_t key_token_stride,
+                               int64_t value_token_stride, void* key_cache, void* value_cache,
+                               int64_t cache_block_stride, const int64_t* slot_mapping,
+                               int num_tokens, int num_kv_heads, int head_size, int block_size,
+                               int num_blocks, int dtype, int32_t* dev_status, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (head_size != 64 && head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size <= 0 || block_size % 16 != 0 || block_size > 1024) return PA_ERR_BLOCK_SIZE;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+    return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0) return PA_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_size;
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 ||
+      value_token_stride % 8)
+    return PA_ERR_INVALID_ARG;
+  if (cache_block_stride < row * block_size || cache_block_stride % 8) return PA_ERR_INVALID_ARG;
+  const int sms = query_sms(0);
+  if (sms <= 0) return PA_ERR_CUDA;
+  cudaError_t e = launch_reshape_and_cache(key, value, key_token_stride, value_token_stride,
+                                           key_cache, value_cache, cache_block_stride,
+                                           slot_mapping, num_tokens, num_kv_heads, head_size,
+                                           block_size, num_blocks, dev_status,
+                                           static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_varlen_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q, int max_seqlen_k,
+                                    int num_heads, int num_kv_heads, int head_size, int block_size,
+                                    int sm_count) {
+  if (check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
+                  head_size, block_size, PA_BF16) != PA_OK)
+    return 0;
+  const int sms = query_sms(sm_count);
+  if (sms <= 0) return 0;
+  PassDims d{num_seqs, total_q, num_heads / num_kv_heads, num_heads, num_kv_heads, head_size, sms,
+             kTcAvailable};
+  return layout_pass(d, 0).end;
+}
+
+size_t pa_cascade_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
+                                     int max_seqlen_k, int num_heads, int num_kv_heads,
+                                     int head_size, int block_size, int sm_count) {
+  if (check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
+                  head_size, block_size, PA_BF16) != PA_OK)
+    return 0;
+  const int sms = query_sms(sm_count);
+  if (sms <= 0) return 0;
+  return layout_cascade(num_seqs, total_q, num_heads / num_kv_heads, num_heads, num_kv_heads,
+                        head_size, sms)
+      .end;
+}
+
+pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_cache,
+                        const void* value_cache, int64_t cache_block_stride,
+                        const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                        const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
+                        int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                        int head_size, int block_size, int num_blocks, float softmax_scale,
+                        int causal, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream) {
+  pa_status st = check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                             num_kv_heads, head_size, block_size, dtype);
+  if (st != PA_OK) return st;
+  st = check_attn_ptrs(q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
+                       seqused_k, block_table, bt_stride, num_seqs, total_q, num_blocks, num_heads,
+                       num_kv_heads, head_size, block_size, softmax_scale, causal, out, lse);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0 || total_q == 0) return PA_OK;
+  const int sms = query_sms(0);
+  if (sms <= 0) return PA_ERR_CUDA;
+  PassDims d{num_seqs, total_q, num_heads / num_kv_heads, num_heads, num_kv_heads, head_size, sms,
+             kTcAvailable};
+  const PassLayout L = layout_pass(d, 0);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      workspace_bytes < L.end)
+    return PA_ERR_WORKSPACE;
+  CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
+               seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+               num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
+               dev_status, static_cast<cudaStream_t>(stream)};
+  const int box_rows = gcd_int(block_size, kKeyTile);
+  CUtensorMap tmK, tmV;
+  if (!encode_pool_map(&tmK, key_cache, head_size, num_kv_heads, block_size, num_blocks,
+                       cache_block_stride, box_rows) ||
+      !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
+                       cache_block_stride, box_rows))
+    return PA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const long long cap = static_cast<long long>(bt_stride) * block_size;
+  PlanPasses pp{};
+  pp.p[0] = make_plan(c, ws, L, 0, 0, 0, cap > 0x7fffffff ? 0x7fffffff : static_cast<int>(cap),
+                      causal, 0);
+  if (launch_plan(pp, 1, c.st) != cudaSuccess) return PA_ERR_CUDA;
+  AttnArgs a = make_attn(c, ws, L, bt_stride, 0, causal, out, nullptr, lse, nullptr, nullptr);
+  return launch_pass(c, tmK, tmV, a, L);
+}
+
+pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
+                               const float* prefix_lse, const void* suffix_out,
+                               const float* suffix_lse, int num_tokens, int num_heads,
+                               int head_size, int dtype, void* stream) {
+  if (num_tokens < 0 || num_heads <= 0) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (head_size <= 0 || head_size % 8 != 0 || head_size > 256) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!out || !prefix_out || !suffix_out || !prefix_lse || !suffix_lse) return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(prefix_out) || !aligned16(suffix_out)) return PA_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(prefix_lse) | reinterpret_cast<uintptr_t>(suffix_lse) |
+        reinterpret_cast<uintptr_t>(out_lse)) & 3u) != 0)
+    return PA_ERR_INVALID_ARG;
+  if (out_lse && (out_lse == prefix_lse || out_lse == suffix_lse)) return PA_ERR_INVALID_ARG;
+  const int sms = query_sms(0);
+  if (sms <= 0) return PA_ERR_CUDA;
+  cudaError_t e = launch_merge(out, out_lse, prefix_out, prefix_lse, suffix_out, suffix_lse,
+                               num_tokens, num_heads, head_size,
+                               static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_cache,
+                         const void* value_cache, int64_t cache_block_stride,
+                         const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                         const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
+                         int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                         int head_size, int block_size, int num_blocks, float softmax_scale,
+                         int common_prefix_len, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream) {
+  pa_status st = check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                             num_kv_heads, head_size, block_size, dtype);
+  if (st != PA_OK) return st;
+  st = check_attn_ptrs(q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
+                       seqused_k, block_table, bt_stride, num_seqs, total_q, num_blocks, num_heads,
+                       num_kv_heads, head_size, block_size, softmax_scale, 1, out, lse);
+  if (st != PA_OK) return st;
+  if (common_prefix_len < 0 || common_prefix_len % block_size != 0) return PA_ERR_INVALID_ARG;
+  if (static_cast<long long>(common_prefix_len) > static_cast<long long>(bt_stride) * block_size)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) return PA_OK;
+  const int sms = query_sms(0);
+  if (sms <= 0) return PA_ERR_CUDA;
+  const int G = num_heads / num_kv_heads;
+  const CascadeLayout CL = layout_cascade(num_seqs, total_q, G, num_heads, num_kv_heads,
+                                          head_size, sms);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      workspace_bytes < CL.end)
+    return PA_ERR_WORKSPACE;
+  CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
+               seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+               num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
+               dev_status, static_cast<cudaStream_t>(stream)};
+  const int box_rows = gcd_int(block_size, kKeyTile);
+  CUtensorMap tmK, tmV;
+  if (!encode_pool_map(&tmK, key_cache, head_size, num_kv_heads, block_size, num_blocks,
+                       cache_block_stride, box_rows) ||
+      !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
+                       cache_block_stride, box_rows))
+    return PA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* prefix_o = reinterpret_cast<float*>(ws + CL.prefix_o);
+  float* prefix_lse = reinterpret_cast<float*>(ws + CL.prefix_lse);
+  const int P = common_prefix_len;
+  const int pages = P / block_size;
+  const long long cap = (static_cast<long long>(bt_stride) - pages) * block_size;
+  PlanPasses pp{};
+  // Pass A: all queries, one non-causal segment, row 0's first P keys.
+  pp.p[0] = make_plan(c, ws, CL.prefix, 1, P, 0, P, 0, 0);
+  // Pass B: each sequence, causal, its own keys from position P on.
+  pp.p[1] = make_plan(c, ws, CL.suffix, 0, 0, P,
+                      cap > 0x7fffffff ? 0x7fffffff : static_cast<int>(cap), 1, 1);
+  if (launch_plan(pp, 2, c.st) != cudaSuccess) return PA_ERR_CUDA;
+  AttnArgs pa_ = make_attn(c, ws, CL.prefix, 0, 0, 0, nullptr, prefix_o, prefix_lse, nullptr,
+                           nullptr);
+  st = launch_pass(c, tmK, tmV, pa_, CL.prefix);
+  if (st != PA_OK) return st;
+  AttnArgs pb = make_attn(c, ws, CL.suffix, bt_stride, pages, 1, out, nullptr, lse, prefix_o,
+                          prefix_lse);
+  return launch_pass(c, tmK, tmV, pb, CL.suffix);
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+// Internal structures shared by the host entry points and the kernels.
+// Not part of the public ABI (include/pa.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Query rows handled by one work item of each attention kernel. A "row" is
+// one (query token, query head) pair of a KV-head group: packed row r of a
+// segment is token r / G, head-in-group r % G (GQA heads share the K/V tile).
+constexpr int kRowsSplit = 64;     // split-KV kernel (decode and short queries)
+constexpr int kRowsTc = 128;       // tcgen05 prefill kernel (one MMA M tile)
+constexpr int kSlotRows = 128;     // rows reserved per partial-result slot
+constexpr int kKeyTile = 64;       // keys per pipeline stage / split granularity
+constexpr int kMinChunk = 256;     // smallest KV split (keys)
+
+// Work planned for one pass (one attention launch pair) lives in the
+// workspace. Device-side layout, all offsets 256-byte aligned.
+struct PassLayout {
+  size_t header;      // int[64]: [0] items class 0, [1] items class 1
+  size_t seg;         // int4[num_segs]: q_start, q_len, kv_len, class
+  size_t segsplit;    // int4[num_segs]: nsplit, slot_base, chunk, item_base
+  size_t items[2];    // int4[items_bound[c]]: seg, row tile, split index, 0
+  size_t counters;    // int[slots_bound * H_kv]
+  size_t part_lse;    // float[slots_bound * H_kv * kSlotRows]
+  size_t part_o;      // float[slots_bound * H_kv * kSlotRows * D]
+  size_t end;
+  int items_bound[2];
+  int slots_bound;
+  int target[2];      // split target (work items per KV head) per class
+};
+
+// Everything the planner kernel needs for one pass.
+struct PlanArgs {
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqused_k;
+  int num_segs;          // sequences (or 1 for the cascade prefix pass)
+  int single_segment;    // 1: one segment of total_q queries with kv_len = single_kv_len
+  int total_q;
+  int single_kv_len;
+  int kv_len_offset;     // subtracted from seqused_k (cascade suffix pass)
+  int kv_len_cap;        // keys addressable through a block_table row
+  int max_q, max_k;      // host bounds (for the BAD_SEQLEN check)
+  int G, H_kv;
+  int tc_enabled;
+  int causal;
+  int target0, target1;
+  int items_bound0, items_bound1, slots_bound;
+  uint8_t* ws;           // pass base
+  PassLayout L;
+  int32_t* status;
+  int check_cascade;     // flag q_len > kv_len (suffix pass of cascade)
+};
+
+struct PlanPasses {
+  PlanArgs p[2];
+};
+
+// Arguments of the attention kernels (both classes).
+struct AttnArgs {
+  const __nv_bfloat16* q;
+  int64_t q_stride;          // elements between tokens
+  const int32_t* bt;         // block_table
+  int bt_row_stride;         // 0 for the cascade prefix pass (row 0 only)
+  int bt_col_offset;         // first page column (cascade suffix pass)
+  int H, H_kv, G, D, bs, num_blocks;
+  float scale_log2;          // softmax_scale * log2(e)
+  int causal;
+  __nv_bfloat16* out;        // [T, H, D] bf16 (final) or NULL
+  float* out_f32;            // [T, H, D] fp32 (final, cascade prefix) or NULL
+  float* lse;                // [H, lse_stride] natural log or NULL
+  int lse_stride;            // = total_q
+  const float* merge_o;      // cascade: prefix state to merge with ([T,H,D] fp32)
+  const float* merge_lse;    // [H, lse_stride]
+  // plan of this pass
+  const int* header;
+  const int4* seg;
+  const int4* segsplit;
+  const int4* items;
+  int* counters;
+  float* part_lse;
+  float* part_o;
+  int32_t* status;
+  int box_rows;              // rows per TMA box (divides block_size and 64)
+};
+
+// Host launchers (defined in the kernel translation units).
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t kstride,
+                                     int64_t vstride, void* kc, void* vc, int64_t block_stride,
+                                     const int64_t* slots, int num_tokens, int H_kv, int D, int bs,
+                                     int num_blocks, int32_t* status, cudaStream_t st, int sms);
+cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* alse,
+                         const void* b, const float* blse, int T, int H, int D, cudaStream_t st,
+                         int sms);
+cudaError_t launch_plan(const PlanPasses& passes, int npasses, cudaStream_t st);
+cudaError_t launch_attn_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
+                              int items_bound, cudaStream_t st);
+cudaError_t launch_attn_tc(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
+                           const AttnArgs& a, int items_bound, cudaStream_t st);
+
+}  // namespace pa

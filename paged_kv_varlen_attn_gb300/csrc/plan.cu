@@ -1,0 +1,206 @@
+// Device-side work planner for one attention call.
+//
+// The idea follows the ahead-of-time scheduling of "FlashAttention 在 vLLM 中的
+// 实现分析" §7 (a plan computed before the kernels run makes execution
+// deterministic and CUDA-graph capturable) and the num_splits split-KV of §1.3,
+// but it runs ON THE DEVICE from cu_seqlens_q / seqused_k, so the host never
+// reads a device value and the call needs no synchronisation.
+//
+// For each segment (a sequence, or the whole batch in the cascade prefix pass)
+// the planner picks a class -- 0: the split-KV kernel (<= 64 packed query rows,
+// i.e. decode and short queries), 1: the tensor-core prefill kernel -- cuts the
+// packed rows into row tiles, and splits the keys into equal chunks so that
+// each class has about `target` work items per KV head. Chunk length
+//   L = max(kMinChunk, ceil(W / target)) rounded up to kKeyTile,
+// where W = sum over segments of (row tiles x keys). Then
+//   sum of items <= target + sum of row tiles, and
+//   slots (items of segments split more than once) <= 2 * target,
+// which is what the host reserves in the workspace.
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace pa {
+
+constexpr int kPlanThreads = 1024;
+
+// Block-wide exclusive scan of three counters; returns the block totals.
+__device__ __forceinline__ int3 block_scan3(int3 v, int3& excl, int* sh /* [3 * 32] */) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int3 x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int a = __shfl_up_sync(0xffffffffu, x.x, o);
+    int b = __shfl_up_sync(0xffffffffu, x.y, o);
+    int c = __shfl_up_sync(0xffffffffu, x.z, o);
+    if (lane >= o) { x.x += a; x.y += b; x.z += c; }
+  }
+  if (lane == 31) { sh[warp] = x.x; sh[32 + warp] = x.y; sh[64 + warp] = x.z; }
+  __syncthreads();
+  if (warp == 0) {
+    int a = sh[lane], b = sh[32 + lane], c = sh[64 + lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int a2 = __shfl_up_sync(0xffffffffu, a, o);
+      int b2 = __shfl_up_sync(0xffffffffu, b, o);
+      int c2 = __shfl_up_sync(0xffffffffu, c, o);
+      if (lane >= o) { a += a2; b += b2; c += c2; }
+    }
+    sh[lane] = a; sh[32 + lane] = b; sh[64 + lane] = c;
+  }
+  __syncthreads();
+  int3 before = make_int3(0, 0, 0);
+  if (warp > 0) before = make_int3(sh[warp - 1], sh[32 + warp - 1], sh[64 + warp - 1]);
+  excl = make_int3(before.x + x.x - v.x, before.y + x.y - v.y, before.z + x.z - v.z);
+  int3 tot = make_int3(sh[31], sh[63], sh[95]);
+  __syncthreads();
+  return tot;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanPasses pp) {
+  const PlanArgs& P = pp.p[blockIdx.x];
+  __shared__ int sh[96];
+  __shared__ unsigned long long shW[2];
+  uint8_t* ws = P.ws;
+  int* header = reinterpret_cast<int*>(ws + P.L.header);
+  int4* seg = reinterpret_cast<int4*>(ws + P.L.seg);
+  int4* segsplit = reinterpret_cast<int4*>(ws + P.L.segsplit);
+  int4* items0 = reinterpret_cast<int4*>(ws + P.L.items[0]);
+  int4* items1 = reinterpret_cast<int4*>(ws + P.L.items[1]);
+  int* counters = reinterpret_cast<int*>(ws + P.L.counters);
+  const int nseg = P.single_segment ? 1 : P.num_segs;
+  const int G = P.G;
+
+  if (threadIdx.x < 2) shW[threadIdx.x] = 0ull;
+  __syncthreads();
+
+  // Pass 1: segment geometry, validation, class, and total work per class.
+  unsigned long long w0 = 0, w1 = 0;
+  for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
+    int q_start, q_len, kv;
+    int bad = 0;
+    if (P.single_segment) {
+      q_start = 0;
+      q_len = P.total_q;
+      kv = P.single_kv_len;
+    } else {
+      const int q0 = P.cu_seqlens_q[s], q1 = P.cu_seqlens_q[s + 1];
+      q_start = q0;
+      q_len = q1 - q0;
+      if (q0 < 0 || q1 > P.total_q || q_len < 0 || q_len > P.max_q) {
+        bad |= PA_DEV_BAD_SEQLEN;
+        q_len = 0;
+        q_start = 0;
+      }
+      const int used = P.seqused_k[s];
+      if (used < 0 || used > P.max_k) bad |= PA_DEV_BAD_SEQLEN;
+      kv = used - P.kv_len_offset;
+    }
+    if (kv < 0) {
+      bad |= P.check_cascade ? PA_DEV_CASCADE : PA_DEV_BAD_SEQLEN;
+      kv = 0;
+    }
+    if (kv > P.kv_len_cap) {
+      bad |= PA_DEV_BAD_SEQLEN;
+      kv = P.kv_len_cap;
+    }
+    if (P.check_cascade && q_len > kv) bad |= PA_DEV_CASCADE;
+    if (bad) flag_status(P.status, bad);
+    const int rows = q_len * G;
+    const int cls = (P.tc_enabled && rows > kRowsSplit) ? 1 : 0;
+    const int nrt = (rows + (cls ? kRowsTc : kRowsSplit) - 1) / (cls ? kRowsTc : kRowsSplit);
+    const unsigned long long w = static_cast<unsigned long long>(nrt) * static_cast<unsigned>(kv);
+    if (cls) w1 += w; else w0 += w;
+    seg[s] = make_int4(q_start, q_len, kv, cls);
+  }
+  atomicAdd(&shW[0], w0);
+  atomicAdd(&shW[1], w1);
+  __syncthreads();
+  const int target[2] = {P.target0, P.target1};
+  int chunk_max[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const unsigned long long W = shW[c];
+    unsigned long long L = (W + target[c] - 1) / (target[c] > 0 ? target[c] : 1);
+    if (L < static_cast<unsigned long long>(kMinChunk)) L = kMinChunk;
+    L = (L + kKeyTile - 1) / kKeyTile * kKeyTile;
+    if (L > 0x40000000ull) L = 0x40000000ull;
+    chunk_max[c] = static_cast<int>(L);
+  }
+
+  // Pass 2: splits, item and slot offsets (block scans in chunks of the
+  // block size, carried across chunks), then the item lists.
+  int3 carry = make_int3(0, 0, 0);
+  for (int base = 0; base < nseg; base += blockDim.x) {
+    const int s = base + threadIdx.x;
+    int nsplit = 1, chunk = 0, nrt = 0, cls = 0;
+    int3 v = make_int3(0, 0, 0);
+    if (s < nseg) {
+      const int4 g = seg[s];
+      cls = g.w;
+      const int rows = g.y * G;
+      const int R = cls ? kRowsTc : kRowsSplit;
+      nrt = (rows + R - 1) / R;
+      const int kv = g.z;
+      const int L = chunk_max[cls];
+      if (kv > 0) {
+        nsplit = (kv + L - 1) / L;
+        chunk = (kv + nsplit - 1) / nsplit;
+        chunk = (chunk + kKeyTile - 1) / kKeyTile * kKeyTile;
+        nsplit = (kv + chunk - 1) / chunk;
+      } else {
+        nsplit = 1;
+        chunk = kKeyTile;
+      }
+      const int n_items = nrt * nsplit;
+      v = make_int3(cls ? 0 : n_items, cls ? n_items : 0, nsplit > 1 ? n_items : 0);
+    }
+    int3 ex;
+    const int3 tot = block_scan3(v, ex, sh);
+    if (s < nseg) {
+      const int item_base = (cls ? carry.y + ex.y : carry.x + ex.x);
+      const int slot_base = carry.z + ex.z;
+      segsplit[s] = make_int4(nsplit, slot_base, chunk, item_base);
+      int4* items = cls ? items1 : items0;
+      const int bound = cls ? P.items_bound1 : P.items_bound0;
+      // Row tiles in reverse order: under the causal mask later tiles see more
+      // keys, so the longest items are dispatched first.
+      for (int rt = 0; rt < nrt; ++rt) {
+        for (int j = 0; j < nsplit; ++j) {
+          const int idx = item_base + (nrt - 1 - rt) * nsplit + j;
+          if (idx < bound) items[idx] = make_int4(s, rt, j, 0);
+        }
+      }
+      if (nsplit > 1) {
+        for (int rt = 0; rt < nrt; ++rt) {
+          const int grp = slot_base + rt * nsplit;
+          if (grp + nsplit <= P.slots_bound)
+            for (int hk = 0; hk < P.H_kv; ++hk) counters[grp * P.H_kv + hk] = 0;
+        }
+      }
+    }
+    carry.x += tot.x;
+    carry.y += tot.y;
+    carry.z += tot.z;
+  }
+  if (threadIdx.x == 0) {
+    int n0 = carry.x, n1 = carry.y;
+    if (n0 > P.items_bound0 || n1 > P.items_bound1 || carry.z > P.slots_bound) {
+      // Cannot happen for inputs within the stated bounds; refuse the work
+      // rather than run past the reserved workspace.
+      flag_status(P.status, PA_DEV_BAD_SEQLEN);
+      n0 = n0 > P.items_bound0 ? 0 : n0;
+      n1 = n1 > P.items_bound1 ? 0 : n1;
+      if (carry.z > P.slots_bound) n0 = n1 = 0;
+    }
+    header[0] = n0;
+    header[1] = n1;
+  }
+}
+
+cudaError_t launch_plan(const PlanPasses& pp, int npasses, cudaStream_t st) {
+  plan_kernel<<<npasses, kPlanThreads, 0, st>>>(pp);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,148 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/pa.h declares, and rejects invalid arguments on the host before any
+CUDA call (the pages' ValueError for a block size that is not a multiple of
+16, head-size and dtype limits -- "FlashAttention と FlashInfer" 境界と失敗,
+"AttentionBackend" 境界と失敗)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_varlen_attn_gb300 as pa
+from paged_kv_varlen_attn_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pa.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for op in ("pa_reshape_and_cache", "pa_varlen_fwd", "pa_merge_attn_states", "pa_cascade_fwd"):
+        assert op in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(pa.EXPORTS) | set(names)
+    assert set(pa.EXPORTS) == set(names)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.pa_abi_version() == 1
+    assert lib.pa_status_string(0) == b"PA_OK"
+    assert b"multiple of 16" in lib.pa_status_string(pa.PA_ERR_BLOCK_SIZE)
+    assert lib.pa_status_string(99) == b"PA_ERR_UNKNOWN"
+
+
+def test_workspace_size_pure_host(lib):
+    n = lib.pa_varlen_fwd_workspace_size(64, 64, 1, 8192, 32, 8, 128, 16, 152)
+    assert n > 0 and n % 256 == 0
+    # grows with the batch, and cascade needs more than plain varlen
+    assert lib.pa_varlen_fwd_workspace_size(128, 128, 1, 8192, 32, 8, 128, 16, 152) > n
+    assert lib.pa_cascade_fwd_workspace_size(64, 64, 1, 8192, 32, 8, 128, 16, 152) > n
+    # invalid shapes give 0
+    assert lib.pa_varlen_fwd_workspace_size(64, 64, 1, 8192, 32, 7, 128, 16, 152) == 0
+    assert lib.pa_varlen_fwd_workspace_size(64, 64, 1, 8192, 32, 8, 96, 16, 152) == 0
+    assert lib.pa_varlen_fwd_workspace_size(64, 64, 1, 8192, 32, 8, 128, 24, 152) == 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _varlen(lib, **kw):
+    a = dict(q=FAKE, qs=32 * 128, kc=FAKE, vc=FAKE, cbs=16 * 8 * 128, cu=FAKE, lens=FAKE,
+             bt=FAKE, bts=4, S=2, T=2, mq=1, mk=64, H=32, Hk=8, D=128, bs=16, nb=10,
+             scale=0.088, causal=1, out=FAKE, lse=None, ws=FAKE, wsb=1 << 20, dtype=0)
+    a.update(kw)
+    return lib.pa_varlen_fwd(a["q"], a["qs"], a["kc"], a["vc"], a["cbs"], a["cu"], a["lens"],
+                             a["bt"], a["bts"], a["S"], a["T"], a["mq"], a["mk"], a["H"], a["Hk"],
+                             a["D"], a["bs"], a["nb"], a["scale"], a["causal"], a["out"], a["lse"],
+                             a["ws"], a["wsb"], a["dtype"], None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bs=24), pa.PA_ERR_BLOCK_SIZE),
+    (dict(bs=0), pa.PA_ERR_BLOCK_SIZE),
+    (dict(bs=2048), pa.PA_ERR_BLOCK_SIZE),
+    (dict(D=96), pa.PA_ERR_UNSUPPORTED),
+    (dict(D=256), pa.PA_ERR_UNSUPPORTED),
+    (dict(dtype=1), pa.PA_ERR_UNSUPPORTED),
+    (dict(H=24, Hk=8), pa.PA_ERR_UNSUPPORTED),          # GQA ratio 3
+    (dict(H=32, Hk=6), pa.PA_ERR_INVALID_ARG),          # H % H_kv != 0
+    (dict(q=None), pa.PA_ERR_INVALID_ARG),
+    (dict(out=None), pa.PA_ERR_INVALID_ARG),
+    (dict(kc=FAKE + 2), pa.PA_ERR_INVALID_ARG),         # misaligned
+    (dict(qs=32 * 128 + 4), pa.PA_ERR_INVALID_ARG),     # stride not 16-byte multiple
+    (dict(qs=16), pa.PA_ERR_INVALID_ARG),               # stride shorter than a row
+    (dict(cbs=100), pa.PA_ERR_INVALID_ARG),
+    (dict(causal=2), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), pa.PA_ERR_INVALID_ARG),
+    (dict(S=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(S=0, T=0), pa.PA_OK),                         # empty batch: nothing to do
+])
+def test_varlen_host_validation(lib, kw, code):
+    assert _varlen(lib, **kw) == code
+
+
+def test_cascade_prefix_must_be_page_multiple(lib):
+    args = [FAKE, 32 * 128, FAKE, FAKE, 16 * 8 * 128, FAKE, FAKE, FAKE, 200, 2, 2, 1, 64, 32, 8,
+            128, 16, 10, 0.088]
+    tail = [FAKE, None, FAKE, 1 << 20, 0, None, None]
+    assert lib.pa_cascade_fwd(*args, 24, *tail) == pa.PA_ERR_INVALID_ARG   # 24 % 16 != 0
+    assert lib.pa_cascade_fwd(*args, -16, *tail) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_cascade_fwd(*args, 16 * 201, *tail) == pa.PA_ERR_INVALID_ARG  # past the row
+
+
+def test_reshape_and_cache_host_validation(lib):
+    f = lib.pa_reshape_and_cache
+    ok = [FAKE, FAKE, 1024, 1024, FAKE, FAKE, 16 * 1024, FAKE, 4, 8, 128, 16, 10, 0, None, None]
+
+    def call(i, v):
+        a = list(ok)
+        a[i] = v
+        return f(*a)
+    assert call(11, 24) == pa.PA_ERR_BLOCK_SIZE      # the pages' "multiple of 16" rule
+    assert call(10, 80) == pa.PA_ERR_UNSUPPORTED     # head size
+    assert call(13, 1) == pa.PA_ERR_UNSUPPORTED      # dtype
+    assert call(0, None) == pa.PA_ERR_INVALID_ARG
+    assert call(7, FAKE + 4) == pa.PA_ERR_INVALID_ARG   # int64 slots misaligned
+    assert call(2, 512) == pa.PA_ERR_INVALID_ARG     # token stride shorter than a row
+    assert call(8, 0) == pa.PA_OK                    # no tokens: nothing to do
+
+
+def test_merge_host_validation(lib):
+    f = lib.pa_merge_attn_states
+    base = [FAKE, FAKE + 0x1000, FAKE, FAKE + 0x2000, FAKE, FAKE + 0x3000, 4, 8, 128, 0, None]
+
+    def call(i, v):
+        a = list(base)
+        a[i] = v
+        return f(*a)
+    assert call(9, 1) == pa.PA_ERR_UNSUPPORTED
+    assert call(2, None) == pa.PA_ERR_INVALID_ARG
+    assert call(1, FAKE + 0x2000) == pa.PA_ERR_INVALID_ARG   # out_lse aliases prefix_lse
+    assert call(6, 0) == pa.PA_OK
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(2, 8, 128, dtype=torch.bfloat16)
+    c = torch.zeros(4, 16, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pa.reshape_and_cache(x, x, c, c, torch.zeros(2, dtype=torch.int64))
