@@ -1,0 +1,506 @@
+"""Benchmark of the paged varlen attention hot path on GB300.
+
+One step = the whole hot path over one synthetic batch: the slot_mapping
+scatter of the batch's new K/V tokens into the page pool, the device-side
+work plan, the paged attention (split-KV decode kernel; tensor-core prefill
+kernel for long queries) and the split combine.
+
+Default workload: the Llama-3-8B-shaped decode batch (64 sequences x 1 query,
+32/8 heads, head_size 128, block_size 16, KV lengths uniform on [512, 8192],
+pages randomly permuted). Metric: algorithmic HBM bytes per step / step time
+(GB/s). Algorithmic bytes count each visible K/V byte once per step plus Q, O,
+LSE, the block-table rows read and the scatter's read+write of the new tokens;
+workspace (split partial) traffic is not counted.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME]
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak
+scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged-attn decode HBM GB/s + prefill TFLOPS on 1 GB300, % of roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+SPLIT_KERNEL_SRC = os.path.join(ROOT, "paged_kv_varlen_attn_gb300", "csrc", "attn_split.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ---------------------------------------------------------------------------
+def is_prefill(wl, s):
+    """Segments with more than 64 packed query rows run on the tensor-core kernel."""
+    return wl.q_lens[s] * (wl.num_heads // wl.num_kv_heads) > 64
+
+
+def algorithmic_counts(wl: W.Workload, seqs=None, cascade=False):
+    """Bytes and FLOPs of one step by the counting rule in the module docstring.
+
+    Each visible K/V byte counts once per step (for cascade, the shared prefix
+    counts once for the whole batch), plus Q, O, LSE and the block-table rows;
+    FLOPs are 4 * D * H per visible (query, key) pair.
+    """
+    H, Hk, D = wl.num_heads, wl.num_kv_heads, wl.head_size
+    seqs = range(wl.num_seqs) if seqs is None else seqs
+    kv_bytes = {"decode": 0, "prefill": 0}
+    flops = {"decode": 0, "prefill": 0}
+    T = 0
+    bt = 0
+    per_key = Hk * D * 2 * 2
+    for s in seqs:
+        ql, kl = wl.q_lens[s], wl.kv_lens[s]
+        kind = "prefill" if is_prefill(wl, s) else "decode"
+        keys = kl - wl.common_prefix_len if cascade else kl
+        kv_bytes[kind] += keys * per_key
+        if wl.causal:
+            pairs = ql * (kl - ql) + ql * (ql + 1) // 2
+        else:
+            pairs = ql * kl
+        flops[kind] += 4 * D * H * pairs
+        T += ql
+        bt += (kl + wl.block_size - 1) // wl.block_size * 4
+    if cascade:
+        kv_bytes["decode"] += wl.common_prefix_len * per_key
+    qo = 2 * T * H * D * 2
+    lse = H * T * 4
+    scatter = 2 * 2 * T * Hk * D * 2
+    attn_bytes = kv_bytes["decode"] + kv_bytes["prefill"] + qo + lse + bt
+    return {"attn_bytes": attn_bytes, "scatter_bytes": scatter,
+            "step_bytes": attn_bytes + scatter, "flops": flops["decode"] + flops["prefill"],
+            "kv_bytes": kv_bytes, "flops_by_kind": flops, "qo_lse_bt": qo + lse + bt}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        hbm = p.get("hbm_gbs") or p.get("hbm_GBs")
+        bf16 = p.get("bf16_tflops")
+        return {"hbm_gbs": float(hbm) if hbm else FALLBACK_HBM_GBS,
+                "bf16_tflops": float(bf16) if bf16 else FALLBACK_BF16_TFLOPS,
+                "source": "measured" if hbm else "fallback"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "source": "fallback"}
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(kernel, workload):
+    """Per-launch DRAM bytes of `kernel` from a committed ncu summary, or None
+    when the kernel source changed since the counters were taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        t = json.load(f)
+    e = t.get(kernel, {}).get(workload)
+    if not e or e.get("source_sha") != file_sha(SPLIT_KERNEL_SRC):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_oracle_sample(wl, max_seconds=12.0, max_seqs=None):
+    """Returns (algorithmic bytes covered, flops covered, seconds, description)."""
+    import oracle
+    torch.set_num_threads(os.cpu_count() or 1)
+    cu = wl.cu_seqlens_q.tolist()
+    covered_bytes, covered_flops, secs, n = 0, 0, 0.0, 0
+    Hk, D, H = wl.num_kv_heads, wl.head_size, wl.num_heads
+    order = list(range(wl.num_seqs))
+    for s in order:
+        if secs >= max_seconds or (max_seqs is not None and n >= max_seqs):
+            break
+        sub = wl.sub_batch([s])
+        pages = sub.pages_of(0)
+        kp, vp = sub.pool_pages(0, pages), sub.pool_pages(1, pages)
+        kc = torch.stack([kp[p] for p in pages])
+        vc = torch.stack([vp[p] for p in pages])
+        bt = torch.arange(len(pages), dtype=torch.int32)[None]
+        bs = wl.block_size
+        remap = {p: i for i, p in enumerate(pages)}
+        slots = torch.tensor([remap[int(x) // bs] * bs + int(x) % bs for x in sub.slot_mapping],
+                             dtype=torch.int64)
+        ql, kl = sub.q_lens[0], sub.kv_lens[0]
+        rows = None
+        if ql > 64:
+            g = torch.Generator().manual_seed(s)
+            rows = {0: sorted(set(int(x) for x in torch.randint(0, ql, (64,), generator=g)))}
+        t0 = time.perf_counter()
+        oracle.reshape_and_cache(sub.k_new, sub.v_new, slots, kc, vc)
+        oracle.varlen_attention(sub.q, kc, vc, sub.cu_seqlens_q, sub.seqused_k, bt,
+                                wl.softmax_scale, wl.causal, rows=rows)
+        secs += time.perf_counter() - t0
+        nrows = ql if rows is None else len(rows[0])
+        covered_bytes += kl * Hk * D * 2 * 2 + 2 * ql * H * D * 2 + H * ql * 4 + 2 * 2 * ql * Hk * D * 2
+        covered_flops += 4 * D * H * nrows * kl
+        n += 1
+    desc = f"{n} of {wl.num_seqs} sequences of {wl.name} (all query rows of decode sequences, " \
+           f"64 seeded rows of longer ones), scatter + attention, fp64 torch CPU"
+    return covered_bytes, covered_flops, secs, desc
+
+
+# ---------------------------------------------------------------------------
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = W.CONFIGS[args.workload]()
+    times = []
+    total_bytes = 0
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        b, f, s, desc = run_oracle_sample(wl, max_seconds=3.0, max_seqs=4)
+        if i >= args.warmup:
+            times.append(s)
+            total_bytes += b
+    secs = sum(times)
+    value = total_bytes / secs / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": torch.get_num_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+class DeviceBatch:
+    """Device copies of one batch's per-step inputs, plus its outputs."""
+
+    def __init__(self, wl, dev):
+        self.wl = wl
+        self.host = {
+            "q": wl.q.pin_memory(), "k_new": wl.k_new.pin_memory(),
+            "v_new": wl.v_new.pin_memory(), "slot_mapping": wl.slot_mapping.pin_memory(),
+            "cu_seqlens_q": wl.cu_seqlens_q.pin_memory(),
+            "seqused_k": wl.seqused_k.pin_memory(), "block_table": wl.block_table.pin_memory(),
+        }
+        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        T, H, D = wl.q.shape
+        self.out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+        self.out_h = torch.empty_like(self.out, device="cpu").pin_memory()
+        self.lse_h = torch.empty_like(self.lse, device="cpu").pin_memory()
+
+
+def bench_ours(args, rank, world, local):
+    import paged_kv_varlen_attn_gb300 as pa
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        from paged_kv_varlen_attn_gb300 import _build
+        _build.build()
+    barrier(world)
+    pa.load_library()
+
+    wl = W.CONFIGS[args.workload]()
+    cascade = wl.common_prefix_len > 0
+    counts = algorithmic_counts(wl, cascade=cascade)
+    kc0 = wl.pool(0, device=dev)
+    vc0 = wl.pool(1, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    T, H, D = wl.q.shape
+    size_fn = pa.cascade_fwd_workspace_size if cascade else pa.varlen_fwd_workspace_size
+    ws = pa.alloc_workspace(size_fn(wl.num_seqs, T, wl.max_seqlen_q, wl.max_seqlen_k, H,
+                                    wl.num_kv_heads, D, wl.block_size, sms), dev)
+    main = DeviceBatch(wl, dev)
+
+    def attention(b, dd=None):
+        dd = dd or b.d
+        w = b.wl
+        args_ = (dd["q"], kc0, vc0, dd["cu_seqlens_q"], dd["seqused_k"], dd["block_table"],
+                 w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale)
+        if cascade:
+            pa.cascade_fwd(*args_, w.common_prefix_len, out=b.out, lse=b.lse, workspace=ws,
+                           dev_status=status)
+        else:
+            pa.varlen_fwd(*args_, w.causal, out=b.out, lse=b.lse, workspace=ws,
+                          dev_status=status)
+
+    def step(b, dd=None, ev_a=None, ev_b=None):
+        dd = dd or b.d
+        pa.reshape_and_cache(dd["k_new"], dd["v_new"], kc0, vc0, dd["slot_mapping"],
+                             dev_status=status)
+        if ev_a is not None:
+            ev_a.record(stream)
+        attention(b, dd)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step(main)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timing -------------------------------------------
+    # The K/V pages read per step exceed the 129 MB L2 for the decode and
+    # mixed workloads, so no flush is needed between steps; the cascade
+    # workload flushes L2 (a 256 MB write) before every step, outside the
+    # per-step attention events.
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if cascade else None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    step_ms = 0.0
+    if flush is None:
+        t_begin.record(stream)
+        for i in range(args.steps):
+            step(main, None, *ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        step_ms = t_begin.elapsed_time(t_end)
+    else:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            starts[i].record(stream)
+            step(main, None, *ev[i])
+        torch.cuda.synchronize()
+        step_ms = sum(st.elapsed_time(e[1]) for st, e in zip(starts, ev))
+    barrier(world)
+    clocks = sampler.stop()
+    attn_ms = sum(x.elapsed_time(y) for x, y in ev)
+    total_ms = max_over_ranks(step_ms, world, dev)
+    ms_per_step = total_ms / args.steps
+    value = world * counts["step_bytes"] / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end-to-end through the API with host buffers ------------------------
+    h2d = sum(t.numel() * t.element_size() for t in main.host.values())
+    d2h = main.out_h.numel() * main.out_h.element_size() + \
+        main.lse_h.numel() * main.lse_h.element_size()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        dd = {k: v.to(dev, non_blocking=True) for k, v in main.host.items()}
+        step(main, dd)
+        main.out_h.copy_(main.out, non_blocking=True)
+        main.lse_h.copy_(main.lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    e2e_value = world * counts["step_bytes"] / (e2e_ms * 1e-3) / 1e9
+
+    # ---- sub-launches of a mixed batch: decode-only and prefill-only ----------
+    sub = {}
+    kinds = {"prefill": [s for s in range(wl.num_seqs) if is_prefill(wl, s)],
+             "decode": [s for s in range(wl.num_seqs) if not is_prefill(wl, s)]}
+    if not cascade and kinds["prefill"] and kinds["decode"]:
+        for kind, seqs in kinds.items():
+            b = DeviceBatch(wl.sub_batch(seqs), dev)
+            c = algorithmic_counts(wl, seqs)
+            for _ in range(3):
+                attention(b)
+            torch.cuda.synchronize()
+            x0 = torch.cuda.Event(enable_timing=True)
+            x1 = torch.cuda.Event(enable_timing=True)
+            n = max(3, args.steps // 2)
+            x0.record(stream)
+            for _ in range(n):
+                attention(b)
+            x1.record(stream)
+            torch.cuda.synchronize()
+            ms = x0.elapsed_time(x1) / n
+            sub[kind] = {"ms": ms, "gbs": c["attn_bytes"] / (ms * 1e-3) / 1e9,
+                         "tflops": c["flops"] / (ms * 1e-3) / 1e12, "seqs": len(seqs)}
+    assert int(status.item()) == 0, f"device status bits {int(status.item())}"
+
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    attn_ms_avg = attn_ms / args.steps
+    config = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": H,
+              "num_kv_heads": wl.num_kv_heads, "head_size": D, "block_size": wl.block_size,
+              "kv_tokens": int(sum(wl.kv_lens)), "query_tokens": T,
+              "step_bytes": counts["step_bytes"], "step_flops": counts["flops"],
+              "l2": ("L2 flushed (256 MB write) before every step" if cascade else
+                     "inputs larger than L2: %.2f GB of K/V pages read per step vs 129 MB L2"
+                     % (counts["attn_bytes"] / 1e9)),
+              "parallelism": f"replicas x{world}"}
+    if cascade:
+        config["common_prefix_len"] = wl.common_prefix_len
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config}
+    prefill_heavy = counts["flops_by_kind"]["prefill"] > 0
+    if prefill_heavy:
+        # Mixed batch: one figure of merit = t_ideal / t_measured, where
+        # t_ideal = decode-side bytes / HBM peak + prefill FLOPs / bf16 peak.
+        t_ideal = ((counts["step_bytes"] - counts["kv_bytes"]["prefill"]) / (peaks["hbm_gbs"] * 1e9)
+                   + counts["flops_by_kind"]["prefill"] / (peaks["bf16_tflops"] * 1e12))
+        line["value"] = 100.0 * t_ideal / (ms_per_step * 1e-3)
+        line["unit"] = "% of roofline"
+        line["e2e"] = {"value": 100.0 * t_ideal / (e2e_ms * 1e-3), "unit": "% of roofline",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        ach = counts["flops"] / (attn_ms_avg * 1e-3) / 1e12
+        line["roofline"] = {"bound": "tensor", "kernel": "plan + attn_tc_kernel<128> + attn_split_kernel<128>",
+                            "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                            "peak_source": peaks["source"], "attn_ms_per_launch": attn_ms_avg}
+    else:
+        achieved = counts["attn_bytes"] / (attn_ms_avg * 1e-3) / 1e9
+        line["e2e"] = {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        line["roofline"] = {"bound": "hbm",
+                            "kernel": "plan + attn_split_kernel<128> (+ split combine)",
+                            "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": achieved / peaks["hbm_gbs"],
+                            "traffic": load_traffic("attn_split_kernel<128>", wl.name),
+                            "peak_source": peaks["source"], "attn_ms_per_launch": attn_ms_avg}
+    if sub:
+        for kind, r in sub.items():
+            r["frac_hbm"] = r["gbs"] / peaks["hbm_gbs"]
+            r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
+        line["sub_launches"] = sub
+    line["gpu_launches"] = (3 if not cascade else 4) * args.steps + \
+        (args.steps if flush is not None else 0) * 0
+    line["clocks"] = clocks
+    if not args.no_cpu_baseline:
+        b, f, sec, desc = run_oracle_sample(wl, max_seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": b / sec / 1e9, "unit": "GB/s",
+                                "cores": torch.get_num_threads(), "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_llama8b", choices=sorted(W.CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        bench_reference(args, rank, world)
+    else:
+        bench_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

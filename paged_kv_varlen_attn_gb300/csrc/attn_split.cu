@@ -10,10 +10,11 @@
 //  * One CTA per work item (segment, row tile of <= 64 packed query rows,
 //    key chunk) and KV head. Packed rows are (query token, head of the GQA
 //    group), so the K/V tile read from HBM serves all G heads at once.
-//  * Warp 4 is the producer: one lane walks the block table and issues TMA
-//    tile loads (128-byte swizzled boxes of 16-64 page rows x 64 dims) into a
-//    multi-stage shared-memory ring guarded by full/empty mbarriers. Every wait
-//    is bounded; a timeout sets PA_DEV_TIMEOUT and the CTA drains and returns.
+//  * Warp 4 is the producer: it prefetches block-table entries a group of
+//    boxes ahead and issues TMA tile loads (128-byte swizzled boxes of 16-64
+//    page rows x 64 dims) into a multi-stage shared-memory ring guarded by
+//    full/empty mbarriers. Every wait is bounded; a timeout sets
+//    PA_DEV_TIMEOUT and the call's abort word, and the CTA drains and returns.
 //  * Warps 0-3 are consumers. With R packed rows, ceil(R/16) warps (rounded to
 //    1, 2 or 4) take 16 rows each and the remaining factor splits every 64-key
 //    tile between warps, so a decode item (R <= 16) keeps all four warps busy
@@ -28,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
+#include "epilogue.cuh"
 
 namespace pa {
 
@@ -49,68 +51,6 @@ struct SplitShared {
   uint64_t* empty;
   volatile int* flags;   // [0] abort, [1] last-CTA, [2] tiles issued, [4..7] consumed per warp
 };
-
-// ---------------------------------------------------------------------------
-// Producer: one lane issues the page-table walk and the TMA loads.
-// ---------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ void split_producer(const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                               const AttnArgs& a, uint8_t* ring, SplitShared sh,
-                                               const int32_t* bt_row, int hk, int kb, int kv_len,
-                                               int ntiles) {
-  using C = SplitCfg<D>;
-  for (int t = 0; t < ntiles; ++t) {
-    const int s = t % C::STAGES;
-    if (t >= C::STAGES) {
-      if (!mbar_wait(&sh.empty[s], ((t / C::STAGES) - 1) & 1)) {
-        flag_status(a.status, PA_DEV_TIMEOUT);
-        sh.flags[0] = 1;
-        break;
-      }
-    }
-    if (sh.flags[0]) break;
-    uint8_t* kdst = ring + s * C::STAGE_BYTES;
-    uint8_t* vdst = kdst + C::TILE_BYTES;
-    mbar_arrive_expect_tx(&sh.full[s], C::STAGE_BYTES);
-    const int key0 = kb + t * C::BN;
-    for (int r = 0; r < C::BN; r += a.box_rows) {
-      const int k = key0 + r;
-      int page = a.num_blocks;  // out of range: TMA fills zeros
-      int prow = 0;
-      if (k < kv_len) {
-        const int lp = k / a.bs;
-        prow = k - lp * a.bs;
-        const int pg = __ldg(bt_row + lp);
-        if (pg >= 0 && pg < a.num_blocks) page = pg;
-        else flag_status(a.status, PA_DEV_BAD_PAGE);
-      }
-#pragma unroll
-      for (int h = 0; h < C::HALVES; ++h) {
-        tma_load_4d(kdst + h * C::HALF_BYTES + r * 128, tmK, &sh.full[s], h * 64, hk, prow, page);
-        tma_load_4d(vdst + h * C::HALF_BYTES + r * 128, tmV, &sh.full[s], h * 64, hk, prow, page);
-      }
-    }
-    sh.flags[2] = t + 1;
-  }
-}
-
-// Final write of one 8-wide column pair set of a row: out = o (already
-// normalised), optionally merged with a prefix state (cascade).
-__device__ __forceinline__ void merge_prefix(const AttnArgs& a, int64_t obase, int h, int tok,
-                                             float& lse_nat, float* o, int n) {
-  // o[0..n) are the values of consecutive columns starting at obase.
-  const float la = a.merge_lse[static_cast<int64_t>(h) * a.lse_stride + tok];
-  const float lb = lse_nat;
-  const float m = fmaxf(la, lb);
-  if (m == -INFINITY) {
-    for (int i = 0; i < n; ++i) o[i] = 0.f;
-    return;
-  }
-  const float wa = fast_exp2((la - m) * kLog2e), wb = fast_exp2((lb - m) * kLog2e);
-  const float inv = 1.f / (wa + wb);
-  for (int i = 0; i < n; ++i) o[i] = (wa * __ldcg(a.merge_o + obase + i) + wb * o[i]) * inv;
-  lse_nat = m + fast_log2(wa + wb) * kLn2;
-}
 
 // ---------------------------------------------------------------------------
 // Consumers. RGN = number of 16-row groups (1, 2 or 4); 4 / RGN warps share
@@ -181,7 +121,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % C::STAGES;
     if (!mbar_wait(&sh.full[s], (t / C::STAGES) & 1)) {
-      flag_status(a.status, PA_DEV_TIMEOUT);
+      abort_call(a);
       sh.flags[0] = 1;
       break;
     }
@@ -406,46 +346,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
   asm volatile("bar.sync 2, %0;" ::"r"(32 * RGN) : "memory");
   if (!sh.flags[1]) return;
   __threadfence();
-  constexpr int C4 = D / 4;
-  for (int idx = threadIdx.x; idx < R * C4; idx += 32 * RGN) {
-    const int rl = idx / C4, c4 = idx - rl * C4;
-    const int pr = row0 + rl;
-    const int i = pr / G;
-    const int tk = q_start + i, hh = hk * G + (pr - i * G);
-    float mx = -INFINITY;
-    for (int jj = 0; jj < nsplit; ++jj) {
-      const int64_t sr = (static_cast<int64_t>(grp + jj) * a.H_kv + hk) * kSlotRows + rl;
-      mx = fmaxf(mx, __ldcg(a.part_lse + sr));
-    }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float lse_r = -INFINITY;
-    if (mx != -INFINITY) {
-      float sw = 0.f;
-      for (int jj = 0; jj < nsplit; ++jj) {
-        const int64_t sr = (static_cast<int64_t>(grp + jj) * a.H_kv + hk) * kSlotRows + rl;
-        const float w = fast_exp2((__ldcg(a.part_lse + sr) - mx) * kLog2e);
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + sr * D) + c4);
-        sw += w;
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2] += w * v.z;
-        acc[3] += w * v.w;
-      }
-      const float inv = 1.f / sw;
-#pragma unroll
-      for (int x = 0; x < 4; ++x) acc[x] *= inv;
-      lse_r = mx + fast_log2(sw) * kLn2;
-    }
-    const int64_t obase = (static_cast<int64_t>(tk) * H + hh) * D + c4 * 4;
-    if (a.merge_o) merge_prefix(a, obase, hh, tk, lse_r, acc, 4);
-    if (a.out_f32) {
-      *reinterpret_cast<float4*>(a.out_f32 + obase) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    } else {
-      uint2 pk = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
-      *reinterpret_cast<uint2*>(a.out + obase) = pk;
-    }
-    if (a.lse && c4 == 0) a.lse[static_cast<int64_t>(hh) * a.lse_stride + tk] = lse_r;
-  }
+  combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, threadIdx.x, 32 * RGN);
   if (threadIdx.x == 0) *counter = 0;   // ready for the next call
 }
 
@@ -462,7 +363,7 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   sh.empty = sh.full + C::STAGES;
   sh.flags = reinterpret_cast<volatile int*>(sh.empty + C::STAGES);
 
-  if (static_cast<int>(blockIdx.x) >= a.header[0]) return;
+  if (static_cast<int>(blockIdx.x) >= a.header[0] || call_aborted(a)) return;
   const int hk = blockIdx.y;
   const int4 it = a.items[blockIdx.x];
   const int seg = it.x, rt = it.y, j = it.z;
@@ -493,9 +394,11 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   if (warp == 4) {
-    if ((threadIdx.x & 31) == 0 && ntiles > 0) {
+    if (ntiles > 0) {
       const int32_t* bt_row = a.bt + static_cast<int64_t>(seg) * a.bt_row_stride + a.bt_col_offset;
-      split_producer<D>(&tmK, &tmV, a, ring, sh, bt_row, hk, kb, kv_len, ntiles);
+      produce_kv<C::BN, C::HALVES, C::STAGES>(&tmK, &tmV, a, ring, sh.full, sh.empty,
+                                              &sh.flags[0], &sh.flags[2], bt_row, hk, kb, kv_len,
+                                              ntiles, threadIdx.x & 31);
     }
     return;
   }

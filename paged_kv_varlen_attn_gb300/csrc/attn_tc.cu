@@ -1,0 +1,428 @@
+// Tensor-core (tcgen05) prefill / chunked-prefill attention kernel.
+//
+// Computes the paged varlen attention of "FlashAttention 在 vLLM 中的实现分析"
+// §4 / §5 with the tiled online softmax of §1.1 for segments with more than
+// 64 packed query rows (prefill, chunked prefill with prior context, the
+// cascade prefix pass of §6.3).
+//
+// One CTA per work item: 128 packed query rows (128/G tokens x the G query
+// heads of one KV head, so each K/V byte loaded serves G heads) against a key
+// range, in 128-key tiles. Warp roles:
+//   warp 0  TMA producer: the Q tile once, then K and V page boxes (128-byte
+//           swizzle) into a 2-stage ring (full/empty mbarriers), block-table
+//           entries prefetched a group of boxes ahead by the whole warp;
+//   warp 1  MMA issuer (one lane): S = Q K^T into TMEM (double-buffered,
+//           128 fp32 columns each), then O += P V into TMEM (D columns), with
+//           tcgen05.commit arriving on the barriers that free each resource;
+//   warps 2-5  softmax: thread r owns row r (TMEM lane r). It reads its S row
+//           from TMEM, masks (bottom-right causal, key range), keeps a running
+//           max, writes P = exp2(S - m) as bf16 into a swizzled shared-memory
+//           tile that is the A operand of the P V MMA, and at the end reads O
+//           from TMEM, divides by the row sum and writes the output and LSE.
+// The O rescale is lazy: the reference max only moves when a row's max grows
+// by more than 2^8, so most tiles need no TMEM round trip for O (exact, since
+// O and the row sum always share the same reference).
+// Causal tile skipping: the key range of an item is clamped to the last key
+// its last row may see, so tiles above the diagonal are never loaded.
+// Every mbarrier wait is bounded; on a timeout the CTA records
+// PA_DEV_TIMEOUT, drains its MMAs and copies, frees TMEM and returns.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "epilogue.cuh"
+
+namespace pa {
+
+template <int D>
+struct TcCfg {
+  static constexpr int BM = kRowsTc;   // 128 query rows
+  static constexpr int BN = 128;       // keys per tile
+  static constexpr int HALVES = D / 64;
+  static constexpr int Q_HALF = BM * 128;
+  static constexpr int Q_BYTES = HALVES * Q_HALF;
+  static constexpr int KV_HALF = BN * 128;
+  static constexpr int KV_TILE = HALVES * KV_HALF;
+  static constexpr int STAGE = 2 * KV_TILE;
+  static constexpr int STAGES = D == 128 ? 2 : 4;
+  static constexpr int P_HALF = BM * 128;   // 64 keys x 128 rows
+  static constexpr int P_BYTES = 2 * P_HALF;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = Q_BYTES;
+  static constexpr int OFF_P = OFF_KV + STAGES * STAGE;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int O_COL = 256;
+  static constexpr float RESCALE_LOG2 = 8.0f;
+};
+
+struct TcBars {
+  uint64_t q_full;
+  uint64_t kv_full[4];
+  uint64_t kv_empty[4];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t p_free[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort;
+  volatile int last;
+  volatile int issued;
+  volatile int consumed;
+};
+
+template <int D>
+__global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ AttnArgs a) {
+  using C = TcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  TcBars* bars = reinterpret_cast<TcBars*>(smem + C::OFF_BAR);
+
+  if (static_cast<int>(blockIdx.x) >= a.header[1] || call_aborted(a)) return;
+  const int hk = blockIdx.y;
+  const int4 it = a.items[blockIdx.x];
+  const int seg = it.x, rt = it.y, j = it.z;
+  const int4 sg = a.seg[seg];
+  const int4 sp = a.segsplit[seg];
+  const int q_start = sg.x, q_len = sg.y, kv_len = sg.z;
+  const int nsplit = sp.x, slot_base = sp.y, chunk = sp.z;
+  const int G = a.G;
+  const int row0 = rt * C::BM;
+  const int R = min(C::BM, q_len * G - row0);
+  const int kb = j * chunk;
+  int ke = min(kv_len, kb + chunk);
+  if (a.causal) ke = min(ke, kv_len - q_len + (row0 + R - 1) / G + 1);
+  const int ntiles = ke > kb ? (ke - kb + C::BN - 1) / C::BN : 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], 128);
+      mbar_init(&bars->p_full[b], 128);
+      mbar_init(&bars->p_free[b], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    bars->last = 0;
+    bars->issued = 0;
+    bars->consumed = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+  const uint32_t sKV = smem_u32(smem + C::OFF_KV);
+  const uint32_t sP = smem_u32(smem + C::OFF_P);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (ntiles > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        const int token0 = q_start + row0 / G;
+        mbar_arrive_expect_tx(&bars->q_full, C::Q_BYTES);
+        for (int h = 0; h < C::HALVES; ++h)
+          tma_load_3d(smem + C::OFF_Q + h * C::Q_HALF, &tmQ, &bars->q_full, h * 64, hk * G,
+                      token0);
+      }
+      const int32_t* bt_row =
+          a.bt + static_cast<int64_t>(seg) * a.bt_row_stride + a.bt_col_offset;
+      produce_kv<C::BN, C::HALVES, C::STAGES>(&tmK, &tmV, a, smem + C::OFF_KV, bars->kv_full,
+                                              bars->kv_empty, &bars->abort, &bars->issued,
+                                              bt_row, hk, kb, kv_len, ntiles, lane);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc_s = mma_idesc_bf16(C::BM, C::BN, false);
+      constexpr uint32_t idesc_o = mma_idesc_bf16(C::BM, D, true);
+      bool ok = mbar_wait(&bars->q_full, 0);
+      int t = 0;
+      for (; ok && t <= ntiles; ++t) {
+        if (bars->abort) { ok = false; break; }
+        if (t < ntiles) {
+          const int s = t % C::STAGES, b = t & 1;
+          ok = mbar_wait(&bars->kv_full[s], (t / C::STAGES) & 1);
+          if (ok && t >= 2) ok = mbar_wait(&bars->s_free[b], ((t >> 1) - 1) & 1);
+          if (!ok) break;
+          bars->consumed = t + 1;
+          tc_fence_after();
+          const uint32_t kbase = sKV + s * C::STAGE;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(sQ + (kk >> 2) * C::Q_HALF + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * C::KV_HALF + (kk & 3) * 32, 16, 1024);
+            tc_mma(tmem + b * 128, ad, bd, idesc_s, kk > 0);
+          }
+          tc_commit(&bars->s_full[b]);
+        }
+        if (t >= 1) {
+          const int u = t - 1, bu = u & 1, su = u % C::STAGES;
+          ok = mbar_wait(&bars->p_full[bu], (u >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vbase = sKV + su * C::STAGE + C::KV_TILE;
+          const uint32_t pbase = sP + bu * C::P_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(pbase + (kk >> 2) * C::P_HALF + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(vbase + kk * 16 * 128, C::KV_HALF, 1024);
+            tc_mma(tmem + C::O_COL, ad, bd, idesc_o, (u > 0 || kk > 0) ? 1 : 0);
+          }
+          tc_commit(&bars->kv_empty[su]);
+          tc_commit(&bars->p_free[bu]);
+        }
+      }
+      if (!ok) {
+        abort_call(a);
+        bars->abort = 1;
+      }
+      // Drain: arrive once every MMA issued above has completed.
+      tc_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t tm_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool rvalid = r < R;
+    const int pr = row0 + (rvalid ? r : 0);
+    const int ti = pr / G;
+    const int tok = q_start + ti;
+    const int head = hk * G + (pr - ti * G);
+    // Last key this row may see (bottom-right causal), or the last key.
+    const int lim = !rvalid ? -1 : (a.causal ? kv_len - q_len + ti : kv_len - 1);
+    const float sl2 = a.scale_log2;
+    float m_use = -INFINITY, l = 0.f;
+    const int tid = threadIdx.x - 64;   // 0..127
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int b = t & 1;
+      if (!mbar_wait(&bars->s_full[b], (t >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      float x[C::BN];
+#pragma unroll
+      for (int c = 0; c < C::BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tm_row + b * 128 + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[b]);
+      const int key0 = kb + t * C::BN;
+      const int vis_end = min(ke, lim + 1);   // keys [key0, vis_end) are visible
+      float tmax = -INFINITY;
+      if (key0 + C::BN <= vis_end) {
+#pragma unroll
+        for (int e = 0; e < C::BN; ++e) {
+          x[e] *= sl2;
+          tmax = fmaxf(tmax, x[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < C::BN; ++e) {
+          x[e] = (key0 + e < vis_end) ? x[e] * sl2 : -INFINITY;
+          tmax = fmaxf(tmax, x[e]);
+        }
+      }
+      // Lazy rescale of the reference max.
+      float m_new = m_use;
+      bool need = false;
+      if (tmax > m_use) {
+        if (m_use == -INFINITY) m_new = tmax;                 // O holds only zeros so far
+        else if (tmax - m_use > C::RESCALE_LOG2) { need = true; m_new = tmax; }
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        // O must hold P(t-1) V(t-1) before it is rescaled. p_free[(t-1) & 1]
+        // completes when that MMA does (one barrier per parity, so a wait
+        // can never alias a phase two steps away).
+        if (t > 0 && !mbar_wait(&bars->p_free[(t - 1) & 1], ((t - 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float alpha = need ? fast_exp2(m_use - m_new) : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tm_row + C::O_COL + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st32(tm_row + C::O_COL + c * 32, v);
+        }
+        tmem_wait_st();
+        l *= alpha;
+      }
+      m_use = m_new;
+      const float mu = m_use == -INFINITY ? 0.f : m_use;
+      // P = exp2(x - mu) as bf16 into the swizzled P tile (row r).
+      if (t >= 2 && !mbar_wait(&bars->p_free[b], ((t >> 1) - 1) & 1)) { ok = false; break; }
+      uint8_t* prow = smem + C::OFF_P + b * C::P_BYTES + r * 128;
+#pragma unroll
+      for (int c = 0; c < C::BN / 8; ++c) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = fast_exp2(x[c * 8 + e] - mu);
+          l += p[e];
+        }
+        uint4 v = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
+                             pack_bf16(p[6], p[7]));
+        const int half = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(prow + half * C::P_HALF + ((cc ^ (r & 7)) << 4)) = v;
+      }
+      // V rows past the sequence end hold arbitrary bytes: zero them so the
+      // P V product (P = 0 there) cannot pick up NaN.
+      if (key0 + C::BN > kv_len) {
+        const int first = max(0, kv_len - key0);
+        uint8_t* vt = smem + C::OFF_KV + (t % C::STAGES) * C::STAGE + C::KV_TILE;
+        const int n16 = (C::BN - first) * C::HALVES * 8;
+        for (int idx = tid; idx < n16; idx += 128) {
+          const int rr = first + idx / (C::HALVES * 8);
+          const int rem = idx % (C::HALVES * 8);
+          *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::KV_HALF + rr * 128 + (rem & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[b]);
+    }
+    if (!ok) {
+      abort_call(a);
+      bars->abort = 1;
+    }
+    // ---------------------------------------------------------- epilogue
+    ok = __all_sync(0xffffffffu, ok);   // TMEM loads below are warp-collective
+    if (ok && ntiles > 0) {
+      if (!mbar_wait(&bars->p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
+        abort_call(a);
+        bars->abort = 1;
+        ok = false;
+      }
+      tc_fence_after();
+    }
+    const bool any = ok && l > 0.f;
+    const float inv_l = any ? 1.f / l : 0.f;
+    float lse_nat = any ? (m_use + fast_log2(l)) * kLn2 : -INFINITY;
+    const int H = a.H;
+    const int64_t obase = (static_cast<int64_t>(tok) * H + head) * D;
+    const int slot = slot_base + rt * nsplit + j;
+    const int64_t srow = slot_row(a, slot, hk, r);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[32];
+      if (ntiles > 0 && ok) {
+        tmem_ld32(tm_row + C::O_COL + c * 32, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
+      }
+      if (!rvalid) continue;
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        float o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o4[e] = __uint_as_float(v[q4 * 4 + e]) * inv_l;
+        const int col = c * 32 + q4 * 4;
+        if (nsplit > 1) {
+          __stcg(reinterpret_cast<float4*>(a.part_o + srow * D + col),
+                 make_float4(o4[0], o4[1], o4[2], o4[3]));
+        } else {
+          float lse_tmp = lse_nat;
+          if (a.merge_o) merge_prefix(a, obase + col, head, tok, lse_tmp, o4, 4);
+          store4(a, obase + col, o4);
+        }
+      }
+    }
+    if (rvalid) {
+      if (nsplit > 1) {
+        __stcg(a.part_lse + srow, lse_nat);
+      } else if (a.lse) {
+        if (a.merge_o) {
+          const float la = a.merge_lse[static_cast<int64_t>(head) * a.lse_stride + tok];
+          const float m = fmaxf(la, lse_nat);
+          lse_nat = m == -INFINITY ? -INFINITY
+                                   : m + fast_log2(fast_exp2((la - m) * kLog2e) +
+                                                   fast_exp2((lse_nat - m) * kLog2e)) * kLn2;
+        }
+        a.lse[static_cast<int64_t>(head) * a.lse_stride + tok] = lse_nat;
+      }
+    }
+    if (nsplit > 1) {
+      __threadfence();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      const int grp = slot_base + rt * nsplit;
+      int* counter = a.counters + static_cast<int64_t>(grp) * a.H_kv + hk;
+      if (tid == 0) bars->last = (atomicAdd(counter, 1) == nsplit - 1) ? 1 : 0;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (bars->last) {
+        __threadfence();
+        combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, tid, 128);
+        if (tid == 0) *counter = 0;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && bars->abort) {
+    // After an abort, wait (bounded) for the copies still in flight.
+    if (ntiles > 0) mbar_wait(&bars->q_full, 0);
+    for (int t = bars->consumed; t < bars->issued; ++t)
+      if (!mbar_wait(&bars->kv_full[t % C::STAGES], (t / C::STAGES) & 1)) break;
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               const CUtensorMap& tmQ, const AttnArgs& a, int items_bound,
+                               cudaStream_t st) {
+  using C = TcCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(items_bound, a.H_kv);
+  attn_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmK, tmV, tmQ, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_tc(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
+                           const AttnArgs& a, int items_bound, cudaStream_t st) {
+  if (items_bound <= 0) return cudaSuccess;
+  if (a.D == 128) return launch_tc_d<128>(tmK, tmV, tmQ, a, items_bound, st);
+  return launch_tc_d<64>(tmK, tmV, tmQ, a, items_bound, st);
+}
+
+}  // namespace pa

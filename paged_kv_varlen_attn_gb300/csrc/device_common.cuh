@@ -10,9 +10,10 @@
 
 namespace pa {
 
-// A wait that has not completed after this many SM clocks (~1 s at 2 GHz)
-// gives up, records PA_DEV_TIMEOUT and lets the kernel return.
-constexpr long long kWaitBudget = 2000000000LL;
+// A wait that has not completed after this many SM clocks (~0.2 s at 2 GHz;
+// legitimate waits last microseconds) gives up, records PA_DEV_TIMEOUT and
+// lets the kernel return.
+constexpr long long kWaitBudget = 400000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -131,5 +132,189 @@ constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLog2e = 1.442695040888963407f;
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace pa
+
+namespace pa {
+
+// ---------------------------------------------------------------- tcgen05
+// Tensor memory (TMEM) allocation, MMA issue/commit, and TMEM<->register
+// moves. A warp may only touch TMEM lanes 32*(warp%4) .. +31.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, int ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, int ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 in, fp32 accumulate).
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+#define PA_R32(X) \
+  X(0) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(16) \
+  X(17) X(18) X(19) X(20) X(21) X(22) X(23) X(24) X(25) X(26) X(27) X(28) X(29) X(30) X(31)
+
+// Thread i of the warp receives 32 consecutive 32-bit columns of lane
+// (lane base + i), starting at column (taddr & 0xffff).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for tcgen05.mma: start address, leading
+// and stride byte offsets (all >> 4), descriptor version 1 (bits 46-47) and
+// the 128-byte swizzle layout (value 2 in bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D: D format
+// (bits 4-5) = 1, A format (7-9) = 1, B format (10-12) = 1, A K-major, B
+// K-major or MN-major (bit 16), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t mma_idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+}  // namespace pa
+
+namespace pa {
+
+// A timeout anywhere in a launch sets the call's abort word; CTAs that start
+// later see it and return at once, so a failing launch ends quickly.
+__device__ __forceinline__ bool call_aborted(const AttnArgs& a) {
+  return *reinterpret_cast<volatile const int*>(a.abort_all) != 0;
+}
+__device__ __forceinline__ void abort_call(const AttnArgs& a) {
+  flag_status(a.status, PA_DEV_TIMEOUT);
+  atomicExch(a.abort_all, 1);
+}
+
+// K/V producer shared by the attention kernels, run by one whole warp. Keys
+// [kb, kb + ntiles*BN) of one KV head are loaded tile by tile into a ring of
+// STAGES stages, each [K tile | V tile], each tile HALVES x [BN rows x 128 B]
+// (128-byte swizzle). A tile is BN / box_rows TMA boxes per half; every box
+// lies inside one page. The warp loads the page ids of the next 32 boxes
+// (one per lane, coalesced) while lane 0 issues the current ones, so the
+// block-table reads stay off the issue path. A page id outside the pool, or
+// a box past the sequence end, becomes the out-of-range coordinate
+// num_blocks, which TMA fills with zeros. Returns false on timeout/abort.
+template <int BN, int HALVES, int STAGES>
+__device__ bool produce_kv(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnArgs& a,
+                           uint8_t* ring, uint64_t* full, uint64_t* empty,
+                           volatile int* cta_abort, volatile int* issued,
+                           const int32_t* bt_row, int hk, int kb, int kv_len, int ntiles,
+                           int lane) {
+  constexpr int HALF = BN * 128;
+  constexpr int TILE = HALVES * HALF;
+  constexpr int STAGE = 2 * TILE;
+  const int box_rows = a.box_rows;
+  const int bpt = BN / box_rows;         // boxes per tile
+  const int tpg = 32 / bpt;              // tiles per group of 32 boxes
+  const int ngroups = (ntiles + tpg - 1) / tpg;
+  auto load_page = [&](int g) -> int {
+    const int k = kb + g * tpg * BN + lane * box_rows;
+    int page = a.num_blocks;
+    if (k < kv_len) {
+      const int pg = __ldg(bt_row + k / a.bs);
+      if (pg >= 0 && pg < a.num_blocks) page = pg;
+      else flag_status(a.status, PA_DEV_BAD_PAGE);
+    }
+    return page;
+  };
+  int next = ngroups > 0 ? load_page(0) : 0;
+  for (int g = 0; g < ngroups; ++g) {
+    const int cur = next;
+    if (g + 1 < ngroups) next = load_page(g + 1);
+    for (int tt = 0; tt < tpg; ++tt) {
+      const int t = g * tpg + tt;
+      if (t >= ntiles) break;
+      const int s = t % STAGES;
+      int ok = 1;
+      if (lane == 0) {
+        if (t >= STAGES && !mbar_wait(&empty[s], ((t / STAGES) - 1) & 1)) {
+          abort_call(a);
+          *cta_abort = 1;
+        }
+        if (*cta_abort) ok = 0;
+        if (ok) mbar_arrive_expect_tx(&full[s], STAGE);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) return false;
+      uint8_t* kdst = ring + s * STAGE;
+      for (int b = 0; b < bpt; ++b) {
+        const int page = __shfl_sync(0xffffffffu, cur, tt * bpt + b);
+        if (lane == 0) {
+          const int k = kb + t * BN + b * box_rows;
+          const int prow = k % a.bs;
+#pragma unroll
+          for (int h = 0; h < HALVES; ++h) {
+            tma_load_4d(kdst + h * HALF + b * box_rows * 128, tmK, &full[s], h * 64, hk, prow,
+                        page);
+            tma_load_4d(kdst + TILE + h * HALF + b * box_rows * 128, tmV, &full[s], h * 64, hk,
+                        prow, page);
+          }
+        }
+      }
+      if (lane == 0) *issued = t + 1;
+    }
+  }
+  return true;
+}
 
 }  // namespace pa

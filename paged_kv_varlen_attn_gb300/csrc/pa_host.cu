@@ -28,22 +28,35 @@ inline int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) 
 inline int target_split(int sms, int H_kv) { return cdiv(4LL * sms, H_kv); }
 inline int target_tc(int sms, int H_kv) { return cdiv(1LL * sms, H_kv); }
 
+// Segments with more than kRowsSplit packed query rows go to the tcgen05
+// prefill kernel; the rest to the split-KV kernel.
+constexpr bool kTcAvailable = true;
+
 struct PassDims {
   int num_segs;   // segments planned
   int total_q;
+  int max_q;      // host bound of a segment's query length
+  bool single;    // one segment of total_q queries (cascade prefix pass)
   int G, H, H_kv, D;
   int sms;
-  bool tc;
 };
+
+// Which kernels a pass can need, from host-known bounds only.
+bool pass_has_tc(const PassDims& d) {
+  const long long rows = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
+  return kTcAvailable && rows > kRowsSplit;
+}
+bool pass_has_split(const PassDims& d) { return !d.single || !pass_has_tc(d); }
 
 // Workspace layout of one pass starting at byte offset `base`.
 PassLayout layout_pass(const PassDims& d, size_t base) {
   PassLayout L{};
-  L.target[0] = target_split(d.sms, d.H_kv);
-  L.target[1] = d.tc ? target_tc(d.sms, d.H_kv) : 0;
+  const bool tc = pass_has_tc(d), sp = pass_has_split(d);
+  L.target[0] = sp ? target_split(d.sms, d.H_kv) : 0;
+  L.target[1] = tc ? target_tc(d.sms, d.H_kv) : 0;
   const long long rows = static_cast<long long>(d.total_q) * d.G;
-  L.items_bound[0] = L.target[0] + d.num_segs + cdiv(rows, kRowsSplit) + 1;
-  L.items_bound[1] = d.tc ? L.target[1] + d.num_segs + cdiv(rows, kRowsTc) + 1 : 0;
+  L.items_bound[0] = sp ? L.target[0] + d.num_segs + cdiv(rows, kRowsSplit) + 1 : 0;
+  L.items_bound[1] = tc ? L.target[1] + d.num_segs + cdiv(rows, kRowsTc) + 1 : 0;
   L.slots_bound = 2 * (L.target[0] + L.target[1]) + 2;
   size_t off = align_up(base);
   L.header = off;                 off = align_up(off + 64 * sizeof(int));
@@ -59,20 +72,17 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
   return L;
 }
 
-// The tensor-core prefill kernel is not in this build yet; every segment is
-// planned for the split-KV kernel.
-constexpr bool kTcAvailable = false;
-
 struct CascadeLayout {
   PassLayout prefix, suffix;
   size_t prefix_o, prefix_lse, end;
 };
 
-CascadeLayout layout_cascade(int num_seqs, int total_q, int G, int H, int H_kv, int D, int sms) {
+CascadeLayout layout_cascade(int num_seqs, int total_q, int max_q, int G, int H, int H_kv, int D,
+                             int sms) {
   CascadeLayout C{};
-  PassDims pd{1, total_q, G, H, H_kv, D, sms, kTcAvailable};
+  PassDims pd{1, total_q, total_q, true, G, H, H_kv, D, sms};
   C.prefix = layout_pass(pd, 0);
-  PassDims sd{num_seqs, total_q, G, H, H_kv, D, sms, kTcAvailable};
+  PassDims sd{num_seqs, total_q, max_q, false, G, H, H_kv, D, sms};
   C.suffix = layout_pass(sd, C.prefix.end);
   size_t off = C.suffix.end;
   C.prefix_o = off;   off = align_up(off + static_cast<size_t>(total_q) * H * D * 4);
@@ -197,7 +207,7 @@ PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int si
   p.max_k = c.max_k;
   p.G = c.H / c.H_kv;
   p.H_kv = c.H_kv;
-  p.tc_enabled = kTcAvailable ? 1 : 0;
+  p.tc_enabled = L.items_bound[1] > 0 ? 1 : 0;
   p.causal = causal;
   p.target0 = L.target[0];
   p.target1 = L.target[1];
@@ -235,6 +245,7 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
   a.merge_o = merge_o;
   a.merge_lse = merge_lse;
   a.header = reinterpret_cast<const int*>(ws + L.header);
+  a.abort_all = reinterpret_cast<int*>(ws + L.header) + 2;
   a.seg = reinterpret_cast<const int4*>(ws + L.seg);
   a.segsplit = reinterpret_cast<const int4*>(ws + L.segsplit);
   a.items = reinterpret_cast<const int4*>(ws + L.items[0]);
@@ -246,9 +257,38 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
   return a;
 }
 
+// Q viewed as (dim, head, token), boxes of 64 dims x G heads x 128/G tokens:
+// exactly the 128 packed rows of one prefill work item, 128-byte swizzled.
+bool encode_q_map(CUtensorMap* map, const void* q, int D, int H, int total_q, int64_t q_stride,
+                  int G) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(total_q > 0 ? total_q : 1)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(q_stride) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kRowsTc / G)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 pa_status launch_pass(const CommonAttn& c, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                      const AttnArgs& a, const PassLayout& L) {
-  if (launch_attn_split(tmK, tmV, a, L.items_bound[0], c.st) != cudaSuccess) return PA_ERR_CUDA;
+                      const CUtensorMap& tmQ, const AttnArgs& a, uint8_t* ws,
+                      const PassLayout& L) {
+  if (L.items_bound[1] > 0) {
+    AttnArgs a1 = a;
+    a1.items = reinterpret_cast<const int4*>(ws + L.items[1]);
+    if (launch_attn_tc(tmK, tmV, tmQ, a1, L.items_bound[1], c.st) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  if (L.items_bound[0] > 0) {
+    AttnArgs a0 = a;
+    a0.items = reinterpret_cast<const int4*>(ws + L.items[0]);
+    if (launch_attn_split(tmK, tmV, a0, L.items_bound[0], c.st) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
   return PA_OK;
 }
 
@@ -310,8 +350,8 @@ size_t pa_varlen_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
     return 0;
   const int sms = query_sms(sm_count);
   if (sms <= 0) return 0;
-  PassDims d{num_seqs, total_q, num_heads / num_kv_heads, num_heads, num_kv_heads, head_size, sms,
-             kTcAvailable};
+  PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
+             num_kv_heads, head_size, sms};
   return layout_pass(d, 0).end;
 }
 
@@ -323,8 +363,8 @@ size_t pa_cascade_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q
     return 0;
   const int sms = query_sms(sm_count);
   if (sms <= 0) return 0;
-  return layout_cascade(num_seqs, total_q, num_heads / num_kv_heads, num_heads, num_kv_heads,
-                        head_size, sms)
+  return layout_cascade(num_seqs, total_q, max_seqlen_q, num_heads / num_kv_heads, num_heads,
+                        num_kv_heads, head_size, sms)
       .end;
 }
 
@@ -346,8 +386,8 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
   if (num_seqs == 0 || total_q == 0) return PA_OK;
   const int sms = query_sms(0);
   if (sms <= 0) return PA_ERR_CUDA;
-  PassDims d{num_seqs, total_q, num_heads / num_kv_heads, num_heads, num_kv_heads, head_size, sms,
-             kTcAvailable};
+  PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
+             num_kv_heads, head_size, sms};
   const PassLayout L = layout_pass(d, 0);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < L.end)
@@ -363,6 +403,10 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
       !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
                        cache_block_stride, box_rows))
     return PA_ERR_CUDA;
+  CUtensorMap tmQ;
+  if (!encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride,
+                    num_heads / num_kv_heads))
+    return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const long long cap = static_cast<long long>(bt_stride) * block_size;
   PlanPasses pp{};
@@ -370,7 +414,7 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
                       causal, 0);
   if (launch_plan(pp, 1, c.st) != cudaSuccess) return PA_ERR_CUDA;
   AttnArgs a = make_attn(c, ws, L, bt_stride, 0, causal, out, nullptr, lse, nullptr, nullptr);
-  return launch_pass(c, tmK, tmV, a, L);
+  return launch_pass(c, tmK, tmV, tmQ, a, ws, L);
 }
 
 pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
@@ -417,8 +461,8 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
   const int sms = query_sms(0);
   if (sms <= 0) return PA_ERR_CUDA;
   const int G = num_heads / num_kv_heads;
-  const CascadeLayout CL = layout_cascade(num_seqs, total_q, G, num_heads, num_kv_heads,
-                                          head_size, sms);
+  const CascadeLayout CL = layout_cascade(num_seqs, total_q, max_seqlen_q, G, num_heads,
+                                          num_kv_heads, head_size, sms);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < CL.end)
     return PA_ERR_WORKSPACE;
@@ -432,6 +476,9 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
                        cache_block_stride, box_rows) ||
       !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
                        cache_block_stride, box_rows))
+    return PA_ERR_CUDA;
+  CUtensorMap tmQ;
+  if (!encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride, G))
     return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* prefix_o = reinterpret_cast<float*>(ws + CL.prefix_o);
@@ -448,11 +495,11 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
   if (launch_plan(pp, 2, c.st) != cudaSuccess) return PA_ERR_CUDA;
   AttnArgs pa_ = make_attn(c, ws, CL.prefix, 0, 0, 0, nullptr, prefix_o, prefix_lse, nullptr,
                            nullptr);
-  st = launch_pass(c, tmK, tmV, pa_, CL.prefix);
+  st = launch_pass(c, tmK, tmV, tmQ, pa_, ws, CL.prefix);
   if (st != PA_OK) return st;
   AttnArgs pb = make_attn(c, ws, CL.suffix, bt_stride, pages, 1, out, nullptr, lse, prefix_o,
                           prefix_lse);
-  return launch_pass(c, tmK, tmV, pb, CL.suffix);
+  return launch_pass(c, tmK, tmV, tmQ, pb, ws, CL.suffix);
 }
 
 }  // extern "C"

@@ -23,7 +23,7 @@ constexpr int kMinChunk = 256;     // smallest KV split (keys)
 // Work planned for one pass (one attention launch pair) lives in the
 // workspace. Device-side layout, all offsets 256-byte aligned.
 struct PassLayout {
-  size_t header;      // int[64]: [0] items class 0, [1] items class 1
+  size_t header;      // int[64]: [0] items class 0, [1] items class 1, [2] abort word
   size_t seg;         // int4[num_segs]: q_start, q_len, kv_len, class
   size_t segsplit;    // int4[num_segs]: nsplit, slot_base, chunk, item_base
   size_t items[2];    // int4[items_bound[c]]: seg, row tile, split index, 0
@@ -79,7 +79,8 @@ struct AttnArgs {
   const float* merge_o;      // cascade: prefix state to merge with ([T,H,D] fp32)
   const float* merge_lse;    // [H, lse_stride]
   // plan of this pass
-  const int* header;
+  const int* header;         // [0], [1]: item counts of the two kernels
+  int* abort_all;            // header[2]: set by any CTA whose wait timed out
   const int4* seg;
   const int4* segsplit;
   const int4* items;

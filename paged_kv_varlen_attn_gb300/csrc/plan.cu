@@ -113,8 +113,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (cls) w1 += w; else w0 += w;
     seg[s] = make_int4(q_start, q_len, kv, cls);
   }
-  atomicAdd(&shW[0], w0);
-  atomicAdd(&shW[1], w1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    w0 += __shfl_xor_sync(0xffffffffu, w0, o);
+    w1 += __shfl_xor_sync(0xffffffffu, w1, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&shW[0], w0);
+    atomicAdd(&shW[1], w1);
+  }
   __syncthreads();
   const int target[2] = {P.target0, P.target1};
   int chunk_max[2];
@@ -195,6 +202,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     }
     header[0] = n0;
     header[1] = n1;
+    header[2] = 0;   // abort word of this call
   }
 }
 

@@ -138,6 +138,9 @@ CASES = [
     (106, 3, 16, 1, 128, 48, 17, 260, True, 0.0),     # MQA-like group of 16, bs 48
     (107, 5, 8, 4, 64, 16, 130, 260, False, 0.2),
     (108, 4, 4, 4, 128, 80, 65, 500, True, 0.25),     # G = 1, bs 80
+    (109, 2, 8, 2, 128, 16, 300, 1100, True, 0.0),    # multi-tile causal prefill, prior context
+    (110, 2, 16, 2, 64, 32, 260, 700, False, 0.0),    # multi-tile non-causal, D = 64
+    (111, 3, 32, 8, 128, 128, 200, 900, True, 0.0),   # GQA 4, block 128
 ]
 
 
