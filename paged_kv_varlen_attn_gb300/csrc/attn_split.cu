@@ -326,7 +326,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
 
   // Split item: publish the normalised partial, then the last CTA merges.
   const int slot = slot_base + rt * nsplit + j;
-  const int64_t slot_row0 = (static_cast<int64_t>(slot) * a.H_kv + hk) * kSlotRows;
+  const int64_t slot_row0 = slot_row(a, slot, hk, 0);
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int rl = rg * 16 + gq + 8 * r;

@@ -36,7 +36,7 @@ __device__ __forceinline__ void store4(const AttnArgs& a, int64_t obase, const f
 
 // Partial-state slot of (group slot `slot`, KV head hk, row rl).
 __device__ __forceinline__ int64_t slot_row(const AttnArgs& a, int slot, int hk, int rl) {
-  return (static_cast<int64_t>(slot) * a.H_kv + hk) * kSlotRows + rl;
+  return (static_cast<int64_t>(slot) * a.H_kv + hk) * a.slot_rows + rl;
 }
 
 // The last CTA of a split group merges the nsplit partial states of its R

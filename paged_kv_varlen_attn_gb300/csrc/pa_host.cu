@@ -57,17 +57,26 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
   const long long rows = static_cast<long long>(d.total_q) * d.G;
   L.items_bound[0] = sp ? L.target[0] + d.num_segs + cdiv(rows, kRowsSplit) + 1 : 0;
   L.items_bound[1] = tc ? L.target[1] + d.num_segs + cdiv(rows, kRowsTc) + 1 : 0;
-  L.slots_bound = 2 * (L.target[0] + L.target[1]) + 2;
+  L.slots_bound[0] = sp ? 2 * L.target[0] + 2 : 0;
+  L.slots_bound[1] = tc ? 2 * L.target[1] + 2 : 0;
+  // A split-kernel item holds at most min(64, q_len * G) rows; prefill items
+  // hold one 128-row tile.
+  const long long rows_bound = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
+  L.slot_rows[0] = static_cast<int>(rows_bound < kRowsSplit ? (rows_bound > 0 ? rows_bound : 1)
+                                                            : kRowsSplit);
+  L.slot_rows[1] = kRowsTc;
   size_t off = align_up(base);
   L.header = off;                 off = align_up(off + 64 * sizeof(int));
   L.seg = off;                    off = align_up(off + static_cast<size_t>(d.num_segs) * 16);
   L.segsplit = off;               off = align_up(off + static_cast<size_t>(d.num_segs) * 16);
   L.items[0] = off;               off = align_up(off + static_cast<size_t>(L.items_bound[0]) * 16);
   L.items[1] = off;               off = align_up(off + static_cast<size_t>(L.items_bound[1]) * 16);
-  const size_t slot_rows = static_cast<size_t>(L.slots_bound) * d.H_kv * kSlotRows;
-  L.counters = off;               off = align_up(off + static_cast<size_t>(L.slots_bound) * d.H_kv * 4);
-  L.part_lse = off;               off = align_up(off + slot_rows * 4);
-  L.part_o = off;                 off = align_up(off + slot_rows * d.D * 4);
+  for (int c = 0; c < 2; ++c) {
+    const size_t slot_rows = static_cast<size_t>(L.slots_bound[c]) * d.H_kv * L.slot_rows[c];
+    L.counters[c] = off;          off = align_up(off + static_cast<size_t>(L.slots_bound[c]) * d.H_kv * 4);
+    L.part_lse[c] = off;          off = align_up(off + slot_rows * 4);
+    L.part_o[c] = off;            off = align_up(off + slot_rows * d.D * 4);
+  }
   L.end = off;
   return L;
 }
@@ -213,7 +222,8 @@ PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int si
   p.target1 = L.target[1];
   p.items_bound0 = L.items_bound[0];
   p.items_bound1 = L.items_bound[1];
-  p.slots_bound = L.slots_bound;
+  p.slots_bound0 = L.slots_bound[0];
+  p.slots_bound1 = L.slots_bound[1];
   p.ws = ws;
   p.L = L;
   p.status = c.status;
@@ -249,9 +259,6 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
   a.seg = reinterpret_cast<const int4*>(ws + L.seg);
   a.segsplit = reinterpret_cast<const int4*>(ws + L.segsplit);
   a.items = reinterpret_cast<const int4*>(ws + L.items[0]);
-  a.counters = reinterpret_cast<int*>(ws + L.counters);
-  a.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
-  a.part_o = reinterpret_cast<float*>(ws + L.part_o);
   a.status = c.status;
   a.box_rows = gcd_int(c.bs, kKeyTile);
   return a;
@@ -274,18 +281,27 @@ bool encode_q_map(CUtensorMap* map, const void* q, int D, int H, int total_q, in
   return r == CUDA_SUCCESS;
 }
 
+// Point a kernel's arguments at its class's work list and partial-slot pool.
+void set_class(AttnArgs& a, uint8_t* ws, const PassLayout& L, int c) {
+  a.items = reinterpret_cast<const int4*>(ws + L.items[c]);
+  a.counters = reinterpret_cast<int*>(ws + L.counters[c]);
+  a.part_lse = reinterpret_cast<float*>(ws + L.part_lse[c]);
+  a.part_o = reinterpret_cast<float*>(ws + L.part_o[c]);
+  a.slot_rows = L.slot_rows[c];
+}
+
 pa_status launch_pass(const CommonAttn& c, const CUtensorMap& tmK, const CUtensorMap& tmV,
                       const CUtensorMap& tmQ, const AttnArgs& a, uint8_t* ws,
                       const PassLayout& L) {
   if (L.items_bound[1] > 0) {
     AttnArgs a1 = a;
-    a1.items = reinterpret_cast<const int4*>(ws + L.items[1]);
+    set_class(a1, ws, L, 1);
     if (launch_attn_tc(tmK, tmV, tmQ, a1, L.items_bound[1], c.st) != cudaSuccess)
       return PA_ERR_CUDA;
   }
   if (L.items_bound[0] > 0) {
     AttnArgs a0 = a;
-    a0.items = reinterpret_cast<const int4*>(ws + L.items[0]);
+    set_class(a0, ws, L, 0);
     if (launch_attn_split(tmK, tmV, a0, L.items_bound[0], c.st) != cudaSuccess)
       return PA_ERR_CUDA;
   }

@@ -16,24 +16,24 @@ namespace pa {
 // segment is token r / G, head-in-group r % G (GQA heads share the K/V tile).
 constexpr int kRowsSplit = 64;     // split-KV kernel (decode and short queries)
 constexpr int kRowsTc = 128;       // tcgen05 prefill kernel (one MMA M tile)
-constexpr int kSlotRows = 128;     // rows reserved per partial-result slot
 constexpr int kKeyTile = 64;       // keys per pipeline stage / split granularity
 constexpr int kMinChunk = 256;     // smallest KV split (keys)
 
 // Work planned for one pass (one attention launch pair) lives in the
 // workspace. Device-side layout, all offsets 256-byte aligned.
 struct PassLayout {
-  size_t header;      // int[64]: [0] items class 0, [1] items class 1, [2] abort word
-  size_t seg;         // int4[num_segs]: q_start, q_len, kv_len, class
-  size_t segsplit;    // int4[num_segs]: nsplit, slot_base, chunk, item_base
-  size_t items[2];    // int4[items_bound[c]]: seg, row tile, split index, 0
-  size_t counters;    // int[slots_bound * H_kv]
-  size_t part_lse;    // float[slots_bound * H_kv * kSlotRows]
-  size_t part_o;      // float[slots_bound * H_kv * kSlotRows * D]
+  size_t header;       // int[64]: [0] items class 0, [1] items class 1, [2] abort word
+  size_t seg;          // int4[num_segs]: q_start, q_len, kv_len, class
+  size_t segsplit;     // int4[num_segs]: nsplit, slot_base (in its class pool), chunk, item_base
+  size_t items[2];     // int4[items_bound[c]]: seg, row tile, split index, 0
+  size_t counters[2];  // int[slots_bound[c] * H_kv]
+  size_t part_lse[2];  // float[slots_bound[c] * H_kv * slot_rows[c]]
+  size_t part_o[2];    // float[slots_bound[c] * H_kv * slot_rows[c] * D]
   size_t end;
   int items_bound[2];
-  int slots_bound;
-  int target[2];      // split target (work items per KV head) per class
+  int slots_bound[2];
+  int slot_rows[2];    // rows a partial slot holds: a bound on rows per work item
+  int target[2];       // split target (work items per KV head) per class
 };
 
 // Everything the planner kernel needs for one pass.
@@ -51,7 +51,7 @@ struct PlanArgs {
   int tc_enabled;
   int causal;
   int target0, target1;
-  int items_bound0, items_bound1, slots_bound;
+  int items_bound0, items_bound1, slots_bound0, slots_bound1;
   uint8_t* ws;           // pass base
   PassLayout L;
   int32_t* status;
@@ -84,9 +84,10 @@ struct AttnArgs {
   const int4* seg;
   const int4* segsplit;
   const int4* items;
-  int* counters;
+  int* counters;             // this kernel's class pool
   float* part_lse;
   float* part_o;
+  int slot_rows;
   int32_t* status;
   int box_rows;              // rows per TMA box (divides block_size and 64)
 };

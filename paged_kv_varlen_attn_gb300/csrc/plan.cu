@@ -15,7 +15,8 @@
 // where W = sum over segments of (row tiles x keys). Then
 //   sum of items <= target + sum of row tiles, and
 //   slots (items of segments split more than once) <= 2 * target,
-// which is what the host reserves in the workspace.
+// which is what the host reserves in the workspace (one slot pool per class;
+// a slot holds as many rows as one work item of its class can have).
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -24,42 +25,45 @@ namespace pa {
 
 constexpr int kPlanThreads = 1024;
 
-// Block-wide exclusive scan of three counters; returns the block totals.
-__device__ __forceinline__ int3 block_scan3(int3 v, int3& excl, int* sh /* [3 * 32] */) {
+// Block-wide exclusive scan of four counters; returns the block totals.
+__device__ __forceinline__ int4 block_scan4(int4 v, int4& excl, int* sh /* [4 * 32] */) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int3 x = v;
+  int4 x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int a = __shfl_up_sync(0xffffffffu, x.x, o);
-    int b = __shfl_up_sync(0xffffffffu, x.y, o);
-    int c = __shfl_up_sync(0xffffffffu, x.z, o);
-    if (lane >= o) { x.x += a; x.y += b; x.z += c; }
+    const int a = __shfl_up_sync(0xffffffffu, x.x, o);
+    const int b = __shfl_up_sync(0xffffffffu, x.y, o);
+    const int c = __shfl_up_sync(0xffffffffu, x.z, o);
+    const int d = __shfl_up_sync(0xffffffffu, x.w, o);
+    if (lane >= o) { x.x += a; x.y += b; x.z += c; x.w += d; }
   }
-  if (lane == 31) { sh[warp] = x.x; sh[32 + warp] = x.y; sh[64 + warp] = x.z; }
+  if (lane == 31) { sh[warp] = x.x; sh[32 + warp] = x.y; sh[64 + warp] = x.z; sh[96 + warp] = x.w; }
   __syncthreads();
   if (warp == 0) {
-    int a = sh[lane], b = sh[32 + lane], c = sh[64 + lane];
+    int a = sh[lane], b = sh[32 + lane], c = sh[64 + lane], d = sh[96 + lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int a2 = __shfl_up_sync(0xffffffffu, a, o);
-      int b2 = __shfl_up_sync(0xffffffffu, b, o);
-      int c2 = __shfl_up_sync(0xffffffffu, c, o);
-      if (lane >= o) { a += a2; b += b2; c += c2; }
+      const int a2 = __shfl_up_sync(0xffffffffu, a, o);
+      const int b2 = __shfl_up_sync(0xffffffffu, b, o);
+      const int c2 = __shfl_up_sync(0xffffffffu, c, o);
+      const int d2 = __shfl_up_sync(0xffffffffu, d, o);
+      if (lane >= o) { a += a2; b += b2; c += c2; d += d2; }
     }
-    sh[lane] = a; sh[32 + lane] = b; sh[64 + lane] = c;
+    sh[lane] = a; sh[32 + lane] = b; sh[64 + lane] = c; sh[96 + lane] = d;
   }
   __syncthreads();
-  int3 before = make_int3(0, 0, 0);
-  if (warp > 0) before = make_int3(sh[warp - 1], sh[32 + warp - 1], sh[64 + warp - 1]);
-  excl = make_int3(before.x + x.x - v.x, before.y + x.y - v.y, before.z + x.z - v.z);
-  int3 tot = make_int3(sh[31], sh[63], sh[95]);
+  int4 before = make_int4(0, 0, 0, 0);
+  if (warp > 0) before = make_int4(sh[warp - 1], sh[32 + warp - 1], sh[64 + warp - 1], sh[96 + warp - 1]);
+  excl = make_int4(before.x + x.x - v.x, before.y + x.y - v.y, before.z + x.z - v.z,
+                   before.w + x.w - v.w);
+  const int4 tot = make_int4(sh[31], sh[63], sh[95], sh[127]);
   __syncthreads();
   return tot;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanPasses pp) {
   const PlanArgs& P = pp.p[blockIdx.x];
-  __shared__ int sh[96];
+  __shared__ int sh[128];
   __shared__ unsigned long long shW[2];
   uint8_t* ws = P.ws;
   int* header = reinterpret_cast<int*>(ws + P.L.header);
@@ -67,7 +71,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   int4* segsplit = reinterpret_cast<int4*>(ws + P.L.segsplit);
   int4* items0 = reinterpret_cast<int4*>(ws + P.L.items[0]);
   int4* items1 = reinterpret_cast<int4*>(ws + P.L.items[1]);
-  int* counters = reinterpret_cast<int*>(ws + P.L.counters);
+  int* counters0 = reinterpret_cast<int*>(ws + P.L.counters[0]);
+  int* counters1 = reinterpret_cast<int*>(ws + P.L.counters[1]);
   const int nseg = P.single_segment ? 1 : P.num_segs;
   const int G = P.G;
 
@@ -137,11 +142,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 
   // Pass 2: splits, item and slot offsets (block scans in chunks of the
   // block size, carried across chunks), then the item lists.
-  int3 carry = make_int3(0, 0, 0);
+  int4 carry = make_int4(0, 0, 0, 0);
   for (int base = 0; base < nseg; base += blockDim.x) {
     const int s = base + threadIdx.x;
     int nsplit = 1, chunk = 0, nrt = 0, cls = 0;
-    int3 v = make_int3(0, 0, 0);
+    int4 v = make_int4(0, 0, 0, 0);
     if (s < nseg) {
       const int4 g = seg[s];
       cls = g.w;
@@ -160,13 +165,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         chunk = kKeyTile;
       }
       const int n_items = nrt * nsplit;
-      v = make_int3(cls ? 0 : n_items, cls ? n_items : 0, nsplit > 1 ? n_items : 0);
+      const int n_slots = nsplit > 1 ? n_items : 0;
+      v = cls ? make_int4(0, n_items, 0, n_slots) : make_int4(n_items, 0, n_slots, 0);
     }
-    int3 ex;
-    const int3 tot = block_scan3(v, ex, sh);
+    int4 ex;
+    const int4 tot = block_scan4(v, ex, sh);
     if (s < nseg) {
-      const int item_base = (cls ? carry.y + ex.y : carry.x + ex.x);
-      const int slot_base = carry.z + ex.z;
+      const int item_base = cls ? carry.y + ex.y : carry.x + ex.x;
+      const int slot_base = cls ? carry.w + ex.w : carry.z + ex.z;
       segsplit[s] = make_int4(nsplit, slot_base, chunk, item_base);
       int4* items = cls ? items1 : items0;
       const int bound = cls ? P.items_bound1 : P.items_bound0;
@@ -179,9 +185,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         }
       }
       if (nsplit > 1) {
+        int* counters = cls ? counters1 : counters0;
+        const int sbound = cls ? P.slots_bound1 : P.slots_bound0;
         for (int rt = 0; rt < nrt; ++rt) {
           const int grp = slot_base + rt * nsplit;
-          if (grp + nsplit <= P.slots_bound)
+          if (grp + nsplit <= sbound)
             for (int hk = 0; hk < P.H_kv; ++hk) counters[grp * P.H_kv + hk] = 0;
         }
       }
@@ -189,16 +197,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     carry.x += tot.x;
     carry.y += tot.y;
     carry.z += tot.z;
+    carry.w += tot.w;
   }
   if (threadIdx.x == 0) {
     int n0 = carry.x, n1 = carry.y;
-    if (n0 > P.items_bound0 || n1 > P.items_bound1 || carry.z > P.slots_bound) {
-      // Cannot happen for inputs within the stated bounds; refuse the work
-      // rather than run past the reserved workspace.
+    // Cannot happen for inputs within the stated bounds; refuse the work
+    // rather than run past the reserved workspace.
+    if (n0 > P.items_bound0 || carry.z > P.slots_bound0) {
       flag_status(P.status, PA_DEV_BAD_SEQLEN);
-      n0 = n0 > P.items_bound0 ? 0 : n0;
-      n1 = n1 > P.items_bound1 ? 0 : n1;
-      if (carry.z > P.slots_bound) n0 = n1 = 0;
+      n0 = 0;
+    }
+    if (n1 > P.items_bound1 || carry.w > P.slots_bound1) {
+      flag_status(P.status, PA_DEV_BAD_SEQLEN);
+      n1 = 0;
     }
     header[0] = n0;
     header[1] = n1;
