@@ -122,7 +122,8 @@ size_t pa_varlen_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
  *                  are read.
  *   max_seqlen_q, max_seqlen_k : host upper bounds of the query / key lengths
  *                  (used to size launches; no device value is read on the host).
- *   softmax_scale: multiplies q.k (commonly 1/sqrt(head_size)).
+ *   softmax_scale: multiplies q.k (commonly 1/sqrt(head_size)); must be finite
+ *                  and > 0 (PA_ERR_INVALID_ARG otherwise).
  *   causal       : 0 or 1. Causal masking is bottom-right aligned: query i of a
  *                  sequence with q_len queries and kv_len keys sees keys
  *                  j <= kv_len - q_len + i (a decode query sees all keys).

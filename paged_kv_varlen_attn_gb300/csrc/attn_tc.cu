@@ -221,33 +221,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       const int b = t & 1;
       if (!mbar_wait(&bars->s_full[b], (t >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
+      // Raw scores of this row: four TMEM loads in flight, one wait.
       float x[C::BN];
+      {
+        uint32_t v[C::BN / 32][32];
 #pragma unroll
-      for (int c = 0; c < C::BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tm_row + b * 128 + c * 32, v);
+        for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(tm_row + b * 128 + c * 32, v[c]);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
+        for (int c = 0; c < C::BN / 32; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
       }
       tc_fence_before();
       mbar_arrive(&bars->s_free[b]);
       const int key0 = kb + t * C::BN;
       const int vis_end = min(ke, lim + 1);   // keys [key0, vis_end) are visible
-      float tmax = -INFINITY;
-      if (key0 + C::BN <= vis_end) {
+      if (key0 + C::BN > vis_end) {
 #pragma unroll
-        for (int e = 0; e < C::BN; ++e) {
-          x[e] *= sl2;
-          tmax = fmaxf(tmax, x[e]);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < C::BN; ++e) {
-          x[e] = (key0 + e < vis_end) ? x[e] * sl2 : -INFINITY;
-          tmax = fmaxf(tmax, x[e]);
-        }
+        for (int e = 0; e < C::BN; ++e) x[e] = (key0 + e < vis_end) ? x[e] : -INFINITY;
       }
+      // Row max of the raw scores (the scale is positive) as a tree of eight
+      // independent chains, then into the log2 domain.
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = x[e];
+#pragma unroll
+      for (int e = 8; e < C::BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
+      const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
       // Lazy rescale of the reference max.
       float m_new = m_use;
       bool need = false;
@@ -282,19 +284,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       // P = exp2(x - mu) as bf16 into the swizzled P tile (row r).
       if (t >= 2 && !mbar_wait(&bars->p_free[b], ((t >> 1) - 1) & 1)) { ok = false; break; }
       uint8_t* prow = smem + C::OFF_P + b * C::P_BYTES + r * 128;
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < C::BN / 8; ++c) {
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          p[e] = fast_exp2(x[c * 8 + e] - mu);
-          l += p[e];
+          p[e] = fast_exp2(fmaf(x[c * 8 + e], sl2, -mu));   // masked scores are -inf -> 0
+          ls[e] += p[e];
         }
         uint4 v = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
                              pack_bf16(p[6], p[7]));
         const int half = c >> 3, cc = c & 7;
         *reinterpret_cast<uint4*>(prow + half * C::P_HALF + ((cc ^ (r & 7)) << 4)) = v;
       }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       // V rows past the sequence end hold arbitrary bytes: zero them so the
       // P V product (P = 0 there) cannot pick up NaN.
       if (key0 + C::BN > kv_len) {

@@ -136,7 +136,7 @@ pa_status check_attn_ptrs(const void* q, int64_t q_stride, const void* kc, const
   if (block_stride < static_cast<int64_t>(bs) * H_kv * D || block_stride % 8 != 0)
     return PA_ERR_INVALID_ARG;
   if (bt_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return PA_ERR_INVALID_ARG;
   return PA_OK;
 }

@@ -93,6 +93,8 @@ def _varlen(lib, **kw):
     (dict(cbs=100), pa.PA_ERR_INVALID_ARG),
     (dict(causal=2), pa.PA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=0.0), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=-0.1), pa.PA_ERR_INVALID_ARG),
     (dict(S=-1), pa.PA_ERR_INVALID_ARG),
     (dict(S=0, T=0), pa.PA_OK),                         # empty batch: nothing to do
 ])

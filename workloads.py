@@ -267,12 +267,22 @@ def long_context_70b(seed=1005, n_decode=32, kv_len=32768, n_prefill=4, q_len=40
     return _build("long_context_70b", seed, 64, 8, 128, 128, ql, kv, g)
 
 
+def prefill_profile(seed=1006, n_prefill=4, q_len=2048, kv_len=12288):
+    """A small case of the long-context prefill shape for profiler captures:
+    64/8 heads, head_size 128, block_size 128, 4 causal prefill sequences of
+    2048 queries on 10240 prior tokens (pool ~220 MB, larger than L2)."""
+    g = torch.Generator().manual_seed(seed)
+    return _build("prefill_profile", seed, 64, 8, 128, 128, [q_len] * n_prefill,
+                  [kv_len] * n_prefill, g)
+
+
 CONFIGS = {
     "tiny_mixed": tiny_mixed,
     "decode_llama8b": decode_llama8b,
     "chunked_prefill_mix": chunked_prefill_mix,
     "cascade_shared_prefix": cascade_shared_prefix,
     "long_context_70b": long_context_70b,
+    "prefill_profile": prefill_profile,
 }
 
 
