@@ -54,6 +54,7 @@ typedef int pa_status;
 #define PA_ERR_UNSUPPORTED 3 /* head_size not 64/128, dtype not bf16, H/H_kv not 1,2,4,8,16 */
 #define PA_ERR_WORKSPACE 4   /* workspace NULL, misaligned or smaller than required */
 #define PA_ERR_CUDA 5        /* a kernel launch or a CUDA runtime query failed */
+#define PA_ERR_NOALLOC_LIMIT 6 /* problem needs more scratch than pa_varlen_fwd_noalloc's fixed buffer */
 
 /* bits OR-ed into *dev_status by the kernels */
 #define PA_DEV_BAD_PAGE 1    /* a block_table entry outside [0, num_blocks): its keys read as 0 */
@@ -193,6 +194,41 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
                          int head_size, int block_size, int num_blocks, float softmax_scale,
                          int common_prefix_len, void* out, float* lse, void* workspace,
                          size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream);
+
+/*
+ * pa_varlen_fwd_noalloc -- pa_varlen_fwd for callers that cannot allocate
+ * device memory, so cannot provide a workspace: for example a serving engine
+ * whose allocator reserved all device memory for its page pool at start-up,
+ * code running while a stream is captured in a mode that forbids cudaMalloc,
+ * or a latency-critical path where cudaMalloc's implicit device
+ * synchronisation is not acceptable. The web pages have no counterpart to
+ * this entry point; it only changes where the scratch lives.
+ *
+ * Arguments, layouts and results are those of pa_varlen_fwd without
+ * workspace / workspace_bytes. The scratch is a fixed, library-owned
+ * PA_NOALLOC_SCRATCH_BYTES (32 MiB) device buffer: every GPU that loads
+ * libpa.so holds it until the process exits. A problem whose
+ * pa_varlen_fwd_workspace_size exceeds it is rejected with
+ * PA_ERR_NOALLOC_LIMIT before anything is launched. The function never calls
+ * cudaMalloc, cudaFree or any allocating routine.
+ *  - The first call on a device looks up that buffer's device address (with
+ *    the device current) and caches it; make that first call before any
+ *    stream capture on the device.
+ *  - Every call uses the same buffer, which keeps the previous call's
+ *    contents; the kernels rewrite everything they read before reading it, so
+ *    nothing needs clearing. Calls that overlap on the GPU (two streams, or
+ *    two host threads without ordering) race on the buffer: serialise them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+pa_status pa_varlen_fwd_noalloc(const void* q, int64_t q_token_stride, const void* key_cache,
+                                const void* value_cache, int64_t cache_block_stride,
+                                const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                                const int32_t* block_table, int bt_stride, int num_seqs,
+                                int total_q, int max_seqlen_q, int max_seqlen_k, int num_heads,
+                                int num_kv_heads, int head_size, int block_size, int num_blocks,
+                                float softmax_scale, int causal, void* out, float* lse, int dtype,
+                                int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -22,6 +22,8 @@ PA_ERR_BLOCK_SIZE = 2
 PA_ERR_UNSUPPORTED = 3
 PA_ERR_WORKSPACE = 4
 PA_ERR_CUDA = 5
+PA_ERR_NOALLOC_LIMIT = 6
+NOALLOC_SCRATCH_BYTES = 32 << 20
 PA_DEV_BAD_PAGE = 1
 PA_DEV_BAD_SLOT = 2
 PA_DEV_BAD_SEQLEN = 4
@@ -38,6 +40,7 @@ EXPORTS = (
     "pa_merge_attn_states",
     "pa_cascade_fwd_workspace_size",
     "pa_cascade_fwd",
+    "pa_varlen_fwd_noalloc",
 )
 
 _lib = None
@@ -56,6 +59,9 @@ _SIGS = {
                        _vp], _i32),
     "pa_merge_attn_states": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "pa_cascade_fwd_workspace_size": ([_i32] * 9, _sz),
+    "pa_varlen_fwd_noalloc": ([_vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                               _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _i32, _vp,
+                               _vp], _i32),
     "pa_cascade_fwd": ([_vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                         _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _i32, _vp,
                         _vp], _i32),
@@ -193,6 +199,30 @@ def varlen_fwd(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, 
         int(bool(causal)), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
         _ptr(dev_status), _stream(q.device))
     _check(code, "pa_varlen_fwd")
+    return out, lse
+
+
+def varlen_fwd_noalloc(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
+                       max_seqlen_q, max_seqlen_k, softmax_scale, causal, out=None, lse=None,
+                       return_lse=True, dev_status=None):
+    """varlen_fwd without a workspace: the library's fixed 32 MiB scratch is
+    used instead (for callers that cannot allocate device memory). Calls that
+    overlap on the GPU race on that buffer. Returns (out, lse or None)."""
+    lib = load_library()
+    _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table)
+    T, H, D = q.shape
+    nb, bs, hk, _ = key_cache.shape
+    S = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    code = lib.pa_varlen_fwd_noalloc(
+        _ptr(q), _row_stride(q), _ptr(key_cache), _ptr(value_cache), _cache_stride(key_cache),
+        _ptr(cu_seqlens_q), _ptr(seqused_k), _ptr(block_table), block_table.stride(0), S, T,
+        int(max_seqlen_q), int(max_seqlen_k), H, hk, D, bs, nb, float(softmax_scale),
+        int(bool(causal)), _ptr(out), _ptr(lse), PA_BF16, _ptr(dev_status), _stream(q.device))
+    _check(code, "pa_varlen_fwd_noalloc")
     return out, lse
 
 

@@ -323,6 +323,9 @@ const char* pa_status_string(pa_status s) {
     case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: head size, dtype or GQA ratio not supported";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA launch or query failed";
+    case PA_ERR_NOALLOC_LIMIT:
+      return "PA_ERR_NOALLOC_LIMIT: the problem needs more scratch than the fixed no-allocation "
+             "buffer (PA_NOALLOC_SCRATCH_BYTES) holds; use pa_varlen_fwd with a workspace";
     default: return "PA_ERR_UNKNOWN";
   }
 }
