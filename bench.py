@@ -328,10 +328,13 @@ def bench_ours(args, rank, world, local):
             pa.varlen_fwd(*args_, w.causal, out=b.out, lse=b.lse, workspace=ws,
                           dev_status=status)
 
-    def step(b, dd=None, ev_a=None, ev_b=None):
+    def scatter(b, dd=None):
         dd = dd or b.d
         pa.reshape_and_cache(dd["k_new"], dd["v_new"], kc0, vc0, dd["slot_mapping"],
                              dev_status=status)
+
+    def step(b, dd=None, ev_a=None, ev_b=None):
+        scatter(b, dd)
         if ev_a is not None:
             ev_a.record(stream)
         attention(b, dd)
@@ -341,6 +344,35 @@ def bench_ours(args, rank, world, local):
     for _ in range(max(3, args.warmup)):
         step(main)
     torch.cuda.synchronize()
+
+    graphs = None
+    if not args.no_graph:
+        # Every C-ABI call is asynchronous, allocation-free and sync-free, so a
+        # step is recorded once as two CUDA graphs (scatter; plan + attention)
+        # and replayed, as a serving engine replays its decode step.
+        g_sc, g_at = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_sc):
+            scatter(main)
+        with torch.cuda.graph(g_at):
+            attention(main)
+        torch.cuda.synchronize()
+        graphs = (g_sc, g_at)
+
+        def step(b, dd=None, ev_a=None, ev_b=None):  # noqa: F811
+            if dd is not None:
+                for k, v in dd.items():
+                    b.d[k].copy_(v, non_blocking=True)
+            g_sc.replay()
+            if ev_a is not None:
+                ev_a.record(stream)
+            g_at.replay()
+            if ev_b is not None:
+                ev_b.record(stream)
+
+        for _ in range(3):
+            step(main)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream(dev)
 
     # ---- device-resident timing -------------------------------------------
     # The K/V pages read per step exceed the 129 MB L2 for the decode and
@@ -390,7 +422,10 @@ def bench_ours(args, rank, world, local):
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(args.steps):
-        dd = {k: v.to(dev, non_blocking=True) for k, v in main.host.items()}
+        if graphs is None:
+            dd = {k: v.to(dev, non_blocking=True) for k, v in main.host.items()}
+        else:
+            dd = main.host   # copied into the graph's input buffers inside step()
         step(main, dd)
         main.out_h.copy_(main.out, non_blocking=True)
         main.lse_h.copy_(main.lse, non_blocking=True)
@@ -471,8 +506,16 @@ def bench_ours(args, rank, world, local):
             r["frac_hbm"] = r["gbs"] / peaks["hbm_gbs"]
             r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
         line["sub_launches"] = sub
-    line["gpu_launches"] = (3 if not cascade else 4) * args.steps + \
-        (args.steps if flush is not None else 0) * 0
+    # Our kernels per step: scatter, planner, then per attention pass the
+    # split-KV kernel and/or the prefill kernel (the host launches a kernel
+    # only when some segment can need it).
+    G = H // wl.num_kv_heads
+    if cascade:
+        per_step = 2 + (1 if T * G > 64 else 1) + 1 + (1 if wl.max_seqlen_q * G > 64 else 0)
+    else:
+        per_step = 3 + (1 if wl.max_seqlen_q * G > 64 else 0)
+    line["gpu_launches"] = per_step * args.steps
+    line["graph"] = graphs is not None
     line["clocks"] = clocks
     if not args.no_cpu_baseline:
         b, f, sec, desc = run_oracle_sample(wl, max_seconds=args.cpu_seconds)
@@ -491,6 +534,8 @@ def main():
     ap.add_argument("--workload", default="decode_llama8b", choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the C-ABI calls directly instead of replaying CUDA graphs")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":

@@ -417,10 +417,18 @@ template <int D>
 static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const AttnArgs& a, int items_bound, cudaStream_t st) {
   using C = SplitCfg<D>;
-  // Per-device attribute; cheap, so it is set on every launch.
-  cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  // The shared-memory opt-in is a per-device function attribute: set it on
+  // the first launch on each device (before any stream capture), not again.
+  static bool configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
+    e = cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
+  }
   dim3 grid(items_bound, a.H_kv);
   attn_split_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmK, tmV, a);
   return cudaGetLastError();

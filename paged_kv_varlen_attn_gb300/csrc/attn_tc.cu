@@ -5,27 +5,34 @@
 // 64 packed query rows (prefill, chunked prefill with prior context, the
 // cascade prefix pass of §6.3).
 //
-// One CTA per work item: 128 packed query rows (128/G tokens x the G query
-// heads of one KV head, so each K/V byte loaded serves G heads) against a key
-// range, in 128-key tiles. Warp roles:
-//   warp 0  TMA producer: the Q tile once, then K and V page boxes (128-byte
-//           swizzle) into a 2-stage ring (full/empty mbarriers), block-table
-//           entries prefetched a group of boxes ahead by the whole warp;
-//   warp 1  MMA issuer (one lane): S = Q K^T into TMEM (double-buffered,
-//           128 fp32 columns each), then O += P V into TMEM (D columns), with
-//           tcgen05.commit arriving on the barriers that free each resource;
-//   warps 2-5  softmax: thread r owns row r (TMEM lane r). It reads its S row
-//           from TMEM, masks (bottom-right causal, key range), keeps a running
-//           max, writes P = exp2(S - m) as bf16 into a swizzled shared-memory
-//           tile that is the A operand of the P V MMA, and at the end reads O
-//           from TMEM, divides by the row sum and writes the output and LSE.
-// The O rescale is lazy: the reference max only moves when a row's max grows
+// One CTA per work item: 256 packed query rows -- two 128-row Q tiles A and
+// B, each 128/G tokens x the G query heads of one KV head -- against a key
+// range, in 64-key tiles. Every K/V byte brought into shared memory serves
+// 256 rows (both Q tiles, all G heads). Warp roles:
+//   warp 0     TMA producer: both Q tiles once, then K and V page boxes
+//              (128-byte swizzle) into a 4-stage ring (full/empty mbarriers),
+//              block-table entries prefetched a group of boxes ahead;
+//   warp 1     MMA issuer (one lane): for each key tile, S_A = Q_A K^T and
+//              S_B = Q_B K^T into TMEM (each double-buffered, 64 fp32
+//              columns), then O_A += P_A V and O_B += P_B V of the previous
+//              tile (O in TMEM, D columns each); tcgen05.commit arrives on the
+//              barriers that free each buffer;
+//   warps 2-5  softmax of tile A, warps 6-9 softmax of tile B: thread r owns
+//              row r of its tile (TMEM lane r). It reads its S row from TMEM,
+//              masks (bottom-right causal, key range), keeps a running max,
+//              writes P = exp2(S - m) as bf16 into a swizzled shared-memory
+//              tile (the A operand of the P V MMA) and finally reads O from
+//              TMEM, divides by the row sum and writes the output and LSE.
+// While one warpgroup computes its softmax the tensor core runs the other
+// tile's MMAs, so the two tiles keep the tensor pipe fed.
+// The O rescale is lazy: a row's reference max only moves when its max grows
 // by more than 2^8, so most tiles need no TMEM round trip for O (exact, since
 // O and the row sum always share the same reference).
 // Causal tile skipping: the key range of an item is clamped to the last key
 // its last row may see, so tiles above the diagonal are never loaded.
 // Every mbarrier wait is bounded; on a timeout the CTA records
-// PA_DEV_TIMEOUT, drains its MMAs and copies, frees TMEM and returns.
+// PA_DEV_TIMEOUT and the call's abort word, drains its MMAs and copies, frees
+// TMEM and returns.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,35 +43,37 @@ namespace pa {
 
 template <int D>
 struct TcCfg {
-  static constexpr int BM = kRowsTc;   // 128 query rows
-  static constexpr int BN = 128;       // keys per tile
+  static constexpr int BM = 128;         // rows per Q tile (TMEM lanes)
+  static constexpr int TILES = 2;        // Q tiles per CTA
+  static constexpr int BN = 64;          // keys per K/V tile
   static constexpr int HALVES = D / 64;
   static constexpr int Q_HALF = BM * 128;
-  static constexpr int Q_BYTES = HALVES * Q_HALF;
+  static constexpr int Q_TILE = HALVES * Q_HALF;
   static constexpr int KV_HALF = BN * 128;
   static constexpr int KV_TILE = HALVES * KV_HALF;
   static constexpr int STAGE = 2 * KV_TILE;
-  static constexpr int STAGES = D == 128 ? 2 : 4;
-  static constexpr int P_HALF = BM * 128;   // 64 keys x 128 rows
-  static constexpr int P_BYTES = 2 * P_HALF;
+  static constexpr int STAGES = 4;
+  static constexpr int P_TILE = BM * 128;   // 64 keys x 128 rows, bf16
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = Q_BYTES;
+  static constexpr int OFF_KV = TILES * Q_TILE;
   static constexpr int OFF_P = OFF_KV + STAGES * STAGE;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_P + TILES * P_TILE;
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 320;
   static constexpr int TMEM_COLS = 512;
+  // TMEM columns: S of tile X, buffer b at X*128 + b*64; O of tile X at 256 + X*D.
   static constexpr int O_COL = 256;
   static constexpr float RESCALE_LOG2 = 8.0f;
 };
+static_assert(kRowsTc == 256, "a prefill work item is two 128-row Q tiles");
 
 struct TcBars {
   uint64_t q_full;
   uint64_t kv_full[4];
   uint64_t kv_empty[4];
-  uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full[2];
+  uint64_t s_full[2][2];   // [tile][buffer]
+  uint64_t s_free[2][2];
+  uint64_t p_full[2];      // [tile]
   uint64_t p_free[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -73,6 +82,187 @@ struct TcBars {
   volatile int issued;
   volatile int consumed;
 };
+
+template <int D>
+__device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars, uint8_t* smem,
+                                                uint32_t tmem, int X, int q_start, int q_len,
+                                                int kv_len, int kb, int ke, int ntiles, int row0,
+                                                int R, int hk, int nsplit, int slot_base, int rt,
+                                                int j) {
+  using C = TcCfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;              // row within tile X (TMEM lane)
+  const int rl = X * C::BM + r;                   // row within the work item
+  const uint32_t tm_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const uint32_t s_col = X * 128, o_col = C::O_COL + X * D;
+  const int G = a.G;
+  const bool rvalid = rl < R;
+  const int pr = row0 + (rvalid ? rl : 0);
+  const int ti = pr / G;
+  const int tok = q_start + ti;
+  const int head = hk * G + (pr - ti * G);
+  // Last key this row may see (bottom-right causal), or the last key.
+  const int lim = !rvalid ? -1 : (a.causal ? kv_len - q_len + ti : kv_len - 1);
+  const float sl2 = a.scale_log2;
+  const int tid = threadIdx.x - 64 - X * 128;      // 0..127 within the warpgroup
+  uint8_t* prow = smem + C::OFF_P + X * C::P_TILE + r * 128;
+  float m_use = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int b = t & 1;
+    if (!mbar_wait(&bars->s_full[X][b], (t >> 1) & 1)) { ok = false; break; }
+    tc_fence_after();
+    float x[C::BN];
+    {
+      uint32_t v[C::BN / 32][32];
+#pragma unroll
+      for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(tm_row + s_col + b * 64 + c * 32, v[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < C::BN / 32; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
+    }
+    tc_fence_before();
+    mbar_arrive(&bars->s_free[X][b]);
+    const int key0 = kb + t * C::BN;
+    const int vis_end = min(ke, lim + 1);   // keys [key0, vis_end) are visible
+    if (key0 + C::BN > vis_end) {
+#pragma unroll
+      for (int e = 0; e < C::BN; ++e) x[e] = (key0 + e < vis_end) ? x[e] : -INFINITY;
+    }
+    // Row max of the raw scores (the scale is positive): eight independent
+    // chains, then into the log2 domain.
+    float mx8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx8[e] = x[e];
+#pragma unroll
+    for (int e = 8; e < C::BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
+    const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+    float m_new = m_use;
+    bool need = false;
+    if (tmax > m_use) {
+      if (m_use == -INFINITY) m_new = tmax;                 // O holds only zeros so far
+      else if (tmax - m_use > C::RESCALE_LOG2) { need = true; m_new = tmax; }
+    }
+    // The previous tile's P V product must be done before this tile's P
+    // overwrites the P buffer, and before O is rescaled.
+    if (t > 0 && !mbar_wait(&bars->p_free[X], (t - 1) & 1)) { ok = false; break; }
+    if (__any_sync(0xffffffffu, need)) {
+      tc_fence_after();
+      const float alpha = need ? fast_exp2(m_use - m_new) : 1.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tm_row + o_col + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+        tmem_st32(tm_row + o_col + c * 32, v);
+      }
+      tmem_wait_st();
+      l *= alpha;
+    }
+    m_use = m_new;
+    const float mu = m_use == -INFINITY ? 0.f : m_use;
+    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < C::BN / 8; ++c) {
+      float p[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        p[e] = fast_exp2(fmaf(x[c * 8 + e], sl2, -mu));   // masked scores are -inf -> 0
+        ls[e] += p[e];
+      }
+      const uint4 v = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
+                                 pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
+      *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = v;
+    }
+    l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+    // V rows past the sequence end hold arbitrary bytes: zero them so the
+    // P V product (P = 0 there) cannot pick up NaN. Tile A's warps do it
+    // before tile A's P is published; the MMA thread issues tile B's product
+    // after observing that, so it sees the zeros too.
+    if (X == 0 && key0 + C::BN > kv_len) {
+      const int first = max(0, kv_len - key0);
+      uint8_t* vt = smem + C::OFF_KV + (t % C::STAGES) * C::STAGE + C::KV_TILE;
+      const int n16 = (C::BN - first) * C::HALVES * 8;
+      for (int idx = tid; idx < n16; idx += 128) {
+        const int rr = first + idx / (C::HALVES * 8);
+        const int rem = idx % (C::HALVES * 8);
+        *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::KV_HALF + rr * 128 + (rem & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    mbar_arrive(&bars->p_full[X]);
+  }
+  if (!ok) {
+    abort_call(a);
+    bars->abort = 1;
+  }
+  // ---------------------------------------------------------- epilogue
+  ok = __all_sync(0xffffffffu, ok);   // TMEM loads below are warp-collective
+  if (ok && ntiles > 0) {
+    if (!mbar_wait(&bars->p_free[X], (ntiles - 1) & 1)) {
+      abort_call(a);
+      bars->abort = 1;
+      ok = false;
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+  }
+  const bool any = ok && l > 0.f;
+  const float inv_l = any ? 1.f / l : 0.f;
+  float lse_nat = any ? (m_use + fast_log2(l)) * kLn2 : -INFINITY;
+  const int64_t obase = (static_cast<int64_t>(tok) * a.H + head) * D;
+  const int slot = slot_base + rt * nsplit + j;
+  const int64_t srow = slot_row(a, slot, hk, rl);
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[32];
+    if (ntiles > 0 && ok) {
+      tmem_ld32(tm_row + o_col + c * 32, v);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = 0u;
+    }
+    if (!rvalid) continue;
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+      float o4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o4[e] = __uint_as_float(v[q4 * 4 + e]) * inv_l;
+      const int col = c * 32 + q4 * 4;
+      if (nsplit > 1) {
+        __stcg(reinterpret_cast<float4*>(a.part_o + srow * D + col),
+               make_float4(o4[0], o4[1], o4[2], o4[3]));
+      } else {
+        float lse_tmp = lse_nat;
+        if (a.merge_o) merge_prefix(a, obase + col, head, tok, lse_tmp, o4, 4);
+        store4(a, obase + col, o4);
+      }
+    }
+  }
+  if (rvalid) {
+    if (nsplit > 1) {
+      __stcg(a.part_lse + srow, lse_nat);
+    } else if (a.lse) {
+      if (a.merge_o) {
+        const float la = a.merge_lse[static_cast<int64_t>(head) * a.lse_stride + tok];
+        const float m = fmaxf(la, lse_nat);
+        lse_nat = m == -INFINITY ? -INFINITY
+                                 : m + fast_log2(fast_exp2((la - m) * kLog2e) +
+                                                 fast_exp2((lse_nat - m) * kLog2e)) * kLn2;
+      }
+      a.lse[static_cast<int64_t>(head) * a.lse_stride + tok] = lse_nat;
+    }
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
@@ -93,8 +283,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const int q_start = sg.x, q_len = sg.y, kv_len = sg.z;
   const int nsplit = sp.x, slot_base = sp.y, chunk = sp.z;
   const int G = a.G;
-  const int row0 = rt * C::BM;
-  const int R = min(C::BM, q_len * G - row0);
+  const int row0 = rt * kRowsTc;
+  const int R = min(kRowsTc, q_len * G - row0);
+  const bool two = R > C::BM;   // tile B has rows
   const int kb = j * chunk;
   int ke = min(kv_len, kb + chunk);
   if (a.causal) ke = min(ke, kv_len - q_len + (row0 + R - 1) / G + 1);
@@ -107,11 +298,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], 128);
-      mbar_init(&bars->p_full[b], 128);
-      mbar_init(&bars->p_free[b], 1);
+    for (int x = 0; x < 2; ++x) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bars->s_full[x][b], 1);
+        mbar_init(&bars->s_free[x][b], 128);
+      }
+      mbar_init(&bars->p_full[x], 128);
+      mbar_init(&bars->p_free[x], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -128,9 +321,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-  const uint32_t sKV = smem_u32(smem + C::OFF_KV);
-  const uint32_t sP = smem_u32(smem + C::OFF_P);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -140,10 +330,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         const int token0 = q_start + row0 / G;
-        mbar_arrive_expect_tx(&bars->q_full, C::Q_BYTES);
-        for (int h = 0; h < C::HALVES; ++h)
-          tma_load_3d(smem + C::OFF_Q + h * C::Q_HALF, &tmQ, &bars->q_full, h * 64, hk * G,
-                      token0);
+        mbar_arrive_expect_tx(&bars->q_full, (two ? 2 : 1) * C::Q_TILE);
+        for (int x = 0; x < (two ? 2 : 1); ++x)
+          for (int h = 0; h < C::HALVES; ++h)
+            tma_load_3d(smem + C::OFF_Q + x * C::Q_TILE + h * C::Q_HALF, &tmQ, &bars->q_full,
+                        h * 64, hk * G, token0 + x * (C::BM / G));
       }
       const int32_t* bt_row =
           a.bt + static_cast<int64_t>(seg) * a.bt_row_stride + a.bt_col_offset;
@@ -156,41 +347,52 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = mma_idesc_bf16(C::BM, C::BN, false);
       constexpr uint32_t idesc_o = mma_idesc_bf16(C::BM, D, true);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+      const uint32_t sKV = smem_u32(smem + C::OFF_KV);
+      const uint32_t sP = smem_u32(smem + C::OFF_P);
+      const int nx = two ? 2 : 1;
       bool ok = mbar_wait(&bars->q_full, 0);
-      int t = 0;
-      for (; ok && t <= ntiles; ++t) {
+      for (int t = 0; ok && t <= ntiles; ++t) {
         if (bars->abort) { ok = false; break; }
         if (t < ntiles) {
           const int s = t % C::STAGES, b = t & 1;
           ok = mbar_wait(&bars->kv_full[s], (t / C::STAGES) & 1);
-          if (ok && t >= 2) ok = mbar_wait(&bars->s_free[b], ((t >> 1) - 1) & 1);
           if (!ok) break;
           bars->consumed = t + 1;
-          tc_fence_after();
           const uint32_t kbase = sKV + s * C::STAGE;
+          for (int x = 0; x < nx; ++x) {
+            if (t >= 2 && !(ok = mbar_wait(&bars->s_free[x][b], ((t >> 1) - 1) & 1))) break;
+            tc_fence_after();
+            const uint32_t qbase = sQ + x * C::Q_TILE;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(sQ + (kk >> 2) * C::Q_HALF + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * C::KV_HALF + (kk & 3) * 32, 16, 1024);
-            tc_mma(tmem + b * 128, ad, bd, idesc_s, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t ad =
+                  smem_desc_sw128(qbase + (kk >> 2) * C::Q_HALF + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd =
+                  smem_desc_sw128(kbase + (kk >> 2) * C::KV_HALF + (kk & 3) * 32, 16, 1024);
+              tc_mma(tmem + x * 128 + b * 64, ad, bd, idesc_s, kk > 0);
+            }
+            tc_commit(&bars->s_full[x][b]);
           }
-          tc_commit(&bars->s_full[b]);
+          if (!ok) break;
         }
         if (t >= 1) {
-          const int u = t - 1, bu = u & 1, su = u % C::STAGES;
-          ok = mbar_wait(&bars->p_full[bu], (u >> 1) & 1);
-          if (!ok) break;
-          tc_fence_after();
+          const int u = t - 1, su = u % C::STAGES;
           const uint32_t vbase = sKV + su * C::STAGE + C::KV_TILE;
-          const uint32_t pbase = sP + bu * C::P_BYTES;
+          for (int x = 0; x < nx; ++x) {
+            if (!(ok = mbar_wait(&bars->p_full[x], u & 1))) break;
+            tc_fence_after();
+            const uint32_t pbase = sP + x * C::P_TILE;
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(pbase + (kk >> 2) * C::P_HALF + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(vbase + kk * 16 * 128, C::KV_HALF, 1024);
-            tc_mma(tmem + C::O_COL, ad, bd, idesc_o, (u > 0 || kk > 0) ? 1 : 0);
+            for (int kk = 0; kk < C::BN / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(vbase + kk * 16 * 128, C::KV_HALF, 1024);
+              tc_mma(tmem + C::O_COL + x * D, ad, bd, idesc_o, (u > 0 || kk > 0) ? 1 : 0);
+            }
+            tc_commit(&bars->p_free[x]);
           }
+          if (!ok) break;
           tc_commit(&bars->kv_empty[su]);
-          tc_commit(&bars->p_free[bu]);
         }
       }
       if (!ok) {
@@ -203,191 +405,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const uint32_t tm_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const bool rvalid = r < R;
-    const int pr = row0 + (rvalid ? r : 0);
-    const int ti = pr / G;
-    const int tok = q_start + ti;
-    const int head = hk * G + (pr - ti * G);
-    // Last key this row may see (bottom-right causal), or the last key.
-    const int lim = !rvalid ? -1 : (a.causal ? kv_len - q_len + ti : kv_len - 1);
-    const float sl2 = a.scale_log2;
-    float m_use = -INFINITY, l = 0.f;
-    const int tid = threadIdx.x - 64;   // 0..127
-    bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      const int b = t & 1;
-      if (!mbar_wait(&bars->s_full[b], (t >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      // Raw scores of this row: four TMEM loads in flight, one wait.
-      float x[C::BN];
-      {
-        uint32_t v[C::BN / 32][32];
-#pragma unroll
-        for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(tm_row + b * 128 + c * 32, v[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < C::BN / 32; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->s_free[b]);
-      const int key0 = kb + t * C::BN;
-      const int vis_end = min(ke, lim + 1);   // keys [key0, vis_end) are visible
-      if (key0 + C::BN > vis_end) {
-#pragma unroll
-        for (int e = 0; e < C::BN; ++e) x[e] = (key0 + e < vis_end) ? x[e] : -INFINITY;
-      }
-      // Row max of the raw scores (the scale is positive) as a tree of eight
-      // independent chains, then into the log2 domain.
-      float mx8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = x[e];
-#pragma unroll
-      for (int e = 8; e < C::BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
-      const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
-      // Lazy rescale of the reference max.
-      float m_new = m_use;
-      bool need = false;
-      if (tmax > m_use) {
-        if (m_use == -INFINITY) m_new = tmax;                 // O holds only zeros so far
-        else if (tmax - m_use > C::RESCALE_LOG2) { need = true; m_new = tmax; }
-      }
-      if (__any_sync(0xffffffffu, need)) {
-        // O must hold P(t-1) V(t-1) before it is rescaled. p_free[(t-1) & 1]
-        // completes when that MMA does (one barrier per parity, so a wait
-        // can never alias a phase two steps away).
-        if (t > 0 && !mbar_wait(&bars->p_free[(t - 1) & 1], ((t - 1) >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float alpha = need ? fast_exp2(m_use - m_new) : 1.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tm_row + C::O_COL + c * 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st32(tm_row + C::O_COL + c * 32, v);
-        }
-        tmem_wait_st();
-        l *= alpha;
-      }
-      m_use = m_new;
-      const float mu = m_use == -INFINITY ? 0.f : m_use;
-      // P = exp2(x - mu) as bf16 into the swizzled P tile (row r).
-      if (t >= 2 && !mbar_wait(&bars->p_free[b], ((t >> 1) - 1) & 1)) { ok = false; break; }
-      uint8_t* prow = smem + C::OFF_P + b * C::P_BYTES + r * 128;
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < C::BN / 8; ++c) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = fast_exp2(fmaf(x[c * 8 + e], sl2, -mu));   // masked scores are -inf -> 0
-          ls[e] += p[e];
-        }
-        uint4 v = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
-                             pack_bf16(p[6], p[7]));
-        const int half = c >> 3, cc = c & 7;
-        *reinterpret_cast<uint4*>(prow + half * C::P_HALF + ((cc ^ (r & 7)) << 4)) = v;
-      }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // V rows past the sequence end hold arbitrary bytes: zero them so the
-      // P V product (P = 0 there) cannot pick up NaN.
-      if (key0 + C::BN > kv_len) {
-        const int first = max(0, kv_len - key0);
-        uint8_t* vt = smem + C::OFF_KV + (t % C::STAGES) * C::STAGE + C::KV_TILE;
-        const int n16 = (C::BN - first) * C::HALVES * 8;
-        for (int idx = tid; idx < n16; idx += 128) {
-          const int rr = first + idx / (C::HALVES * 8);
-          const int rem = idx % (C::HALVES * 8);
-          *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::KV_HALF + rr * 128 + (rem & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[b]);
-    }
-    if (!ok) {
-      abort_call(a);
-      bars->abort = 1;
-    }
-    // ---------------------------------------------------------- epilogue
-    ok = __all_sync(0xffffffffu, ok);   // TMEM loads below are warp-collective
-    if (ok && ntiles > 0) {
-      if (!mbar_wait(&bars->p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
-        abort_call(a);
-        bars->abort = 1;
-        ok = false;
-      }
-      tc_fence_after();
-    }
-    const bool any = ok && l > 0.f;
-    const float inv_l = any ? 1.f / l : 0.f;
-    float lse_nat = any ? (m_use + fast_log2(l)) * kLn2 : -INFINITY;
-    const int H = a.H;
-    const int64_t obase = (static_cast<int64_t>(tok) * H + head) * D;
-    const int slot = slot_base + rt * nsplit + j;
-    const int64_t srow = slot_row(a, slot, hk, r);
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t v[32];
-      if (ntiles > 0 && ok) {
-        tmem_ld32(tm_row + C::O_COL + c * 32, v);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = 0u;
-      }
-      if (!rvalid) continue;
-#pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
-        float o4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o4[e] = __uint_as_float(v[q4 * 4 + e]) * inv_l;
-        const int col = c * 32 + q4 * 4;
-        if (nsplit > 1) {
-          __stcg(reinterpret_cast<float4*>(a.part_o + srow * D + col),
-                 make_float4(o4[0], o4[1], o4[2], o4[3]));
-        } else {
-          float lse_tmp = lse_nat;
-          if (a.merge_o) merge_prefix(a, obase + col, head, tok, lse_tmp, o4, 4);
-          store4(a, obase + col, o4);
-        }
-      }
-    }
-    if (rvalid) {
-      if (nsplit > 1) {
-        __stcg(a.part_lse + srow, lse_nat);
-      } else if (a.lse) {
-        if (a.merge_o) {
-          const float la = a.merge_lse[static_cast<int64_t>(head) * a.lse_stride + tok];
-          const float m = fmaxf(la, lse_nat);
-          lse_nat = m == -INFINITY ? -INFINITY
-                                   : m + fast_log2(fast_exp2((la - m) * kLog2e) +
-                                                   fast_exp2((lse_nat - m) * kLog2e)) * kLn2;
-        }
-        a.lse[static_cast<int64_t>(head) * a.lse_stride + tok] = lse_nat;
-      }
-    }
+    const int X = (warp - 2) >> 2;   // warps 2-5: tile A, 6-9: tile B
+    if (X == 0 || two)
+      tc_softmax_tile<D>(a, bars, smem, tmem, X, q_start, q_len, kv_len, kb, ke, ntiles, row0,
+                         R, hk, nsplit, slot_base, rt, j);
     if (nsplit > 1) {
+      // Both warpgroups (256 threads) take part, active tile or not.
       __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       const int grp = slot_base + rt * nsplit;
       int* counter = a.counters + static_cast<int64_t>(grp) * a.H_kv + hk;
+      const int tid = threadIdx.x - 64;
       if (tid == 0) bars->last = (atomicAdd(counter, 1) == nsplit - 1) ? 1 : 0;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       if (bars->last) {
         __threadfence();
-        combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, tid, 128);
+        combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, tid, 256);
         if (tid == 0) *counter = 0;
       }
     }
@@ -414,9 +447,18 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const CUtensorMap& tmQ, const AttnArgs& a, int items_bound,
                                cudaStream_t st) {
   using C = TcCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  // The shared-memory opt-in is a per-device function attribute: set it on
+  // the first launch on each device (before any stream capture), not again.
+  static bool configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
+    e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
+  }
   dim3 grid(items_bound, a.H_kv);
   attn_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmK, tmV, tmQ, a);
   return cudaGetLastError();

@@ -59,12 +59,14 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
   L.items_bound[1] = tc ? L.target[1] + d.num_segs + cdiv(rows, kRowsTc) + 1 : 0;
   L.slots_bound[0] = sp ? 2 * L.target[0] + 2 : 0;
   L.slots_bound[1] = tc ? 2 * L.target[1] + 2 : 0;
-  // A split-kernel item holds at most min(64, q_len * G) rows; prefill items
-  // hold one 128-row tile.
+  // A work item holds at most min(rows per item of its kernel, q_len * G) rows.
   const long long rows_bound = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
-  L.slot_rows[0] = static_cast<int>(rows_bound < kRowsSplit ? (rows_bound > 0 ? rows_bound : 1)
-                                                            : kRowsSplit);
-  L.slot_rows[1] = kRowsTc;
+  auto clamp_rows = [&](int item_rows) {
+    return static_cast<int>(rows_bound < item_rows ? (rows_bound > 0 ? rows_bound : 1)
+                                                   : item_rows);
+  };
+  L.slot_rows[0] = clamp_rows(kRowsSplit);
+  L.slot_rows[1] = clamp_rows(kRowsTc);
   size_t off = align_up(base);
   L.header = off;                 off = align_up(off + 64 * sizeof(int));
   L.seg = off;                    off = align_up(off + static_cast<size_t>(d.num_segs) * 16);
@@ -265,7 +267,7 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
 }
 
 // Q viewed as (dim, head, token), boxes of 64 dims x G heads x 128/G tokens:
-// exactly the 128 packed rows of one prefill work item, 128-byte swizzled.
+// exactly the 128 packed rows of one prefill Q tile, 128-byte swizzled.
 bool encode_q_map(CUtensorMap* map, const void* q, int D, int H, int total_q, int64_t q_stride,
                   int G) {
   auto fn = encode_fn();
@@ -273,7 +275,7 @@ bool encode_q_map(CUtensorMap* map, const void* q, int D, int H, int total_q, in
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(total_q > 0 ? total_q : 1)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(q_stride) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kRowsTc / G)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kTcTileRows / G)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

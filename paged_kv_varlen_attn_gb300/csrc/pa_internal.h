@@ -15,9 +15,11 @@ namespace pa {
 // one (query token, query head) pair of a KV-head group: packed row r of a
 // segment is token r / G, head-in-group r % G (GQA heads share the K/V tile).
 constexpr int kRowsSplit = 64;     // split-KV kernel (decode and short queries)
-constexpr int kRowsTc = 128;       // tcgen05 prefill kernel (one MMA M tile)
+constexpr int kRowsTc = 256;       // tcgen05 prefill kernel: two 128-row Q tiles
+constexpr int kTcTileRows = 128;   // rows of one Q tile (the MMA M dimension)
 constexpr int kKeyTile = 64;       // keys per pipeline stage / split granularity
 constexpr int kMinChunk = 256;     // smallest KV split (keys)
+constexpr int kMaxDevices = 64;    // per-device host caches
 
 // Work planned for one pass (one attention launch pair) lives in the
 // workspace. Device-side layout, all offsets 256-byte aligned.
