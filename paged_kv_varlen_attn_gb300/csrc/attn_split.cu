@@ -363,9 +363,12 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   sh.empty = sh.full + C::STAGES;
   sh.flags = reinterpret_cast<volatile int*>(sh.empty + C::STAGES);
 
-  if (static_cast<int>(blockIdx.x) >= a.header[0] || call_aborted(a)) return;
-  const int hk = blockIdx.y;
-  const int4 it = a.items[blockIdx.x];
+  // One block per (work item, KV head), KV head fastest: blocks are
+  // dispatched in index order and the planner sorted the items longest first.
+  const int item = static_cast<int>(blockIdx.x) / a.H_kv;
+  const int hk = static_cast<int>(blockIdx.x) - item * a.H_kv;
+  if (item >= a.header[0] || call_aborted(a)) return;
+  const int4 it = a.items[item];
   const int seg = it.x, rt = it.y, j = it.z;
   const int4 sg = a.seg[seg];
   const int4 sp = a.segsplit[seg];
@@ -429,7 +432,7 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
   }
-  dim3 grid(items_bound, a.H_kv);
+  const dim3 grid(static_cast<unsigned>(items_bound) * static_cast<unsigned>(a.H_kv));
   attn_split_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmK, tmV, a);
   return cudaGetLastError();
 }

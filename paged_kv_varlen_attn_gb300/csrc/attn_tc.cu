@@ -274,9 +274,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                                              ~static_cast<uintptr_t>(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(smem + C::OFF_BAR);
 
-  if (static_cast<int>(blockIdx.x) >= a.header[1] || call_aborted(a)) return;
-  const int hk = blockIdx.y;
-  const int4 it = a.items[blockIdx.x];
+  // One block per (work item, KV head), KV head fastest: blocks are
+  // dispatched in index order and the planner sorted the items longest first.
+  const int item = static_cast<int>(blockIdx.x) / a.H_kv;
+  const int hk = static_cast<int>(blockIdx.x) - item * a.H_kv;
+  if (item >= a.header[1] || call_aborted(a)) return;
+  const int4 it = a.items[item];
   const int seg = it.x, rt = it.y, j = it.z;
   const int4 sg = a.seg[seg];
   const int4 sp = a.segsplit[seg];
@@ -459,7 +462,7 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
   }
-  dim3 grid(items_bound, a.H_kv);
+  const dim3 grid(static_cast<unsigned>(items_bound) * static_cast<unsigned>(a.H_kv));
   attn_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmK, tmV, tmQ, a);
   return cudaGetLastError();
 }

@@ -23,7 +23,6 @@
 
 namespace pa {
 
-constexpr int kPlanThreads = 1024;
 
 // Block-wide exclusive scan of four counters; returns the block totals.
 __device__ __forceinline__ int4 block_scan4(int4 v, int4& excl, int* sh /* [4 * 32] */) {
@@ -61,10 +60,30 @@ __device__ __forceinline__ int4 block_scan4(int4 v, int4& excl, int* sh /* [4 * 
   return tot;
 }
 
+constexpr int kPlanThreads = 1024;
+constexpr int kSizeBuckets = 1024;
+
+// Size bucket of work item (segment s, row tile rt, split j): the number of
+// 64-key tiles the attention kernel will process for it (capped).
+__device__ __forceinline__ int item_bucket(int s, int rt, int j, int4 g, int chunk, int G,
+                                           int causal) {
+  const int cls = g.w, q_len = g.y, kv = g.z;
+  const int R = cls ? kRowsTc : kRowsSplit;
+  const int rows = q_len * G;
+  const int last_row = min(rows, (rt + 1) * R) - 1;
+  const int kb = j * chunk;
+  int ke = min(kv, kb + chunk);
+  if (causal) ke = min(ke, kv - q_len + last_row / G + 1);
+  const int tiles = ke > kb ? (ke - kb + kKeyTile - 1) / kKeyTile : 0;
+  return min(tiles, kSizeBuckets - 1);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanPasses pp) {
   const PlanArgs& P = pp.p[blockIdx.x];
   __shared__ int sh[128];
   __shared__ unsigned long long shW[2];
+  __shared__ int hist[2][kSizeBuckets];   // items per (class, size in key tiles)
+  __shared__ int cursor[2][kSizeBuckets];
   uint8_t* ws = P.ws;
   int* header = reinterpret_cast<int*>(ws + P.L.header);
   int4* seg = reinterpret_cast<int4*>(ws + P.L.seg);
@@ -77,6 +96,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   const int G = P.G;
 
   if (threadIdx.x < 2) shW[threadIdx.x] = 0ull;
+  for (int i = threadIdx.x; i < 2 * kSizeBuckets; i += blockDim.x) {
+    (&hist[0][0])[i] = 0;
+    (&cursor[0][0])[i] = 0;
+  }
   __syncthreads();
 
   // Pass 1: segment geometry, validation, class, and total work per class.
@@ -174,16 +197,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       const int item_base = cls ? carry.y + ex.y : carry.x + ex.x;
       const int slot_base = cls ? carry.w + ex.w : carry.z + ex.z;
       segsplit[s] = make_int4(nsplit, slot_base, chunk, item_base);
-      int4* items = cls ? items1 : items0;
-      const int bound = cls ? P.items_bound1 : P.items_bound0;
-      // Row tiles in reverse order: under the causal mask later tiles see more
-      // keys, so the longest items are dispatched first.
-      for (int rt = 0; rt < nrt; ++rt) {
-        for (int j = 0; j < nsplit; ++j) {
-          const int idx = item_base + (nrt - 1 - rt) * nsplit + j;
-          if (idx < bound) items[idx] = make_int4(s, rt, j, 0);
-        }
-      }
+      for (int rt = 0; rt < nrt; ++rt)
+        for (int j = 0; j < nsplit; ++j)
+          atomicAdd(&hist[cls][item_bucket(s, rt, j, seg[s], chunk, G, P.causal)], 1);
       if (nsplit > 1) {
         int* counters = cls ? counters1 : counters0;
         const int sbound = cls ? P.slots_bound1 : P.slots_bound0;
@@ -198,6 +214,35 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     carry.y += tot.y;
     carry.z += tot.z;
     carry.w += tot.w;
+  }
+  // Longest items first: offsets of the size buckets in descending order
+  // (one block scan over the buckets), then every item is placed in its
+  // bucket. The hardware dispatches blocks in order, so the last wave holds
+  // the shortest items. The order inside a bucket does not affect results.
+  __syncthreads();
+  {
+    static_assert(kSizeBuckets == kPlanThreads, "one bucket per planner thread");
+    const int b = kSizeBuckets - 1 - static_cast<int>(threadIdx.x);
+    int4 ex;
+    block_scan4(make_int4(hist[0][b], hist[1][b], 0, 0), ex, sh);
+    cursor[0][b] = ex.x;
+    cursor[1][b] = ex.y;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
+    const int4 g = seg[s];
+    const int4 ss = segsplit[s];
+    const int cls = g.w;
+    const int R = cls ? kRowsTc : kRowsSplit;
+    const int nrt = (g.y * G + R - 1) / R;
+    int4* items = cls ? items1 : items0;
+    const int bound = cls ? P.items_bound1 : P.items_bound0;
+    for (int rt = 0; rt < nrt; ++rt) {
+      for (int j = 0; j < ss.x; ++j) {
+        const int idx = atomicAdd(&cursor[cls][item_bucket(s, rt, j, g, ss.z, G, P.causal)], 1);
+        if (idx < bound) items[idx] = make_int4(s, rt, j, 0);
+      }
+    }
   }
   if (threadIdx.x == 0) {
     int n0 = carry.x, n1 = carry.y;
