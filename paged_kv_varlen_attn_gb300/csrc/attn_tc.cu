@@ -7,25 +7,33 @@
 //
 // One CTA per work item: 256 packed query rows -- two 128-row Q tiles A and
 // B, each 128/G tokens x the G query heads of one KV head -- against a key
-// range, in 64-key tiles. Every K/V byte brought into shared memory serves
-// 256 rows (both Q tiles, all G heads). Warp roles:
+// range, in 128-key tiles. Every K/V byte brought into shared memory serves
+// 256 rows (both Q tiles, all G heads). Three warpgroups:
+//   control (warps 0-3; 0 and 1 work, 2 and 3 idle), registers cut to 56;
+//   softmax A (warps 4-7) and softmax B (warps 8-11), registers raised to 224.
+// Warp roles:
 //   warp 0     TMA producer: both Q tiles once, then K and V page boxes
-//              (128-byte swizzle) into a 4-stage ring (full/empty mbarriers),
+//              (128-byte swizzle) into a ring of stages (full/empty mbarriers),
 //              block-table entries prefetched a group of boxes ahead;
-//   warp 1     MMA issuer (one lane): for each key tile, S_A = Q_A K^T and
-//              S_B = Q_B K^T into TMEM (each double-buffered, 64 fp32
-//              columns), then O_A += P_A V and O_B += P_B V of the previous
-//              tile (O in TMEM, D columns each); tcgen05.commit arrives on the
-//              barriers that free each buffer;
-//   warps 2-5  softmax of tile A, warps 6-9 softmax of tile B: thread r owns
-//              row r of its tile (TMEM lane r). It reads its S row from TMEM,
-//              masks (bottom-right causal, key range), keeps a running max,
-//              writes P = exp2(S - m) as bf16 into a swizzled shared-memory
-//              tile (the A operand of the P V MMA) and finally reads O from
-//              TMEM, divides by the row sum and writes the output and LSE.
-// While one warpgroup computes its softmax the tensor core runs the other
-// tile's MMAs, so the two tiles keep the tensor pipe fed.
-// The O rescale is lazy: a row's reference max only moves when its max grows
+//   warp 1     MMA issuer (one lane): for each key tile, S_X = Q_X K^T into
+//              TMEM (128 fp32 columns per Q tile X), then O_X += P_X V with P_X
+//              read straight from TMEM (the A operand of the MMA) and V from
+//              shared memory; tcgen05.commit arrives on the barriers that free
+//              each buffer;
+//   warps 4-7  softmax of tile A, warps 8-11 softmax of tile B: thread r owns
+//              row r of its tile (TMEM lane r). It reads its 128 scores from
+//              TMEM with one wait, masks (bottom-right causal, key range), keeps
+//              a running max,
+//              writes P = exp2(S - m) as bf16 pairs back into the first 64
+//              columns of its S region, and finally reads O from TMEM, divides
+//              by the row sum and writes the output and LSE.
+// Keeping P in TMEM leaves shared memory to the TMA ring and the Q/K/V
+// operands: per 128-key tile the tensor core reads Q and K (S) and V (P V)
+// from shared memory and nothing else. While one warpgroup computes its
+// softmax the tensor core runs the other tile's MMAs.
+// S_X of the next tile overwrites P_X, so it is issued only after P_X V has
+// completed (its tcgen05.commit barrier); that also means O_X is final for the
+// softmax's lazy rescale: a row's reference max only moves when its max grows
 // by more than 2^8, so most tiles need no TMEM round trip for O (exact, since
 // O and the row sum always share the same reference).
 // Causal tile skipping: the key range of an item is clamped to the last key
@@ -45,23 +53,22 @@ template <int D>
 struct TcCfg {
   static constexpr int BM = 128;         // rows per Q tile (TMEM lanes)
   static constexpr int TILES = 2;        // Q tiles per CTA
-  static constexpr int BN = 64;          // keys per K/V tile
+  static constexpr int BN = 128;         // keys per K/V tile
   static constexpr int HALVES = D / 64;
   static constexpr int Q_HALF = BM * 128;
   static constexpr int Q_TILE = HALVES * Q_HALF;
   static constexpr int KV_HALF = BN * 128;
   static constexpr int KV_TILE = HALVES * KV_HALF;
   static constexpr int STAGE = 2 * KV_TILE;
-  static constexpr int STAGES = 4;
-  static constexpr int P_TILE = BM * 128;   // 64 keys x 128 rows, bf16
+  static constexpr int STAGES = D == 128 ? 2 : 4;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = TILES * Q_TILE;
-  static constexpr int OFF_P = OFF_KV + STAGES * STAGE;
-  static constexpr int OFF_BAR = OFF_P + TILES * P_TILE;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * STAGE;
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;   // 3 warpgroups: control, softmax A, softmax B
   static constexpr int TMEM_COLS = 512;
-  // TMEM columns: S of tile X, buffer b at X*128 + b*64; O of tile X at 256 + X*D.
+  // TMEM columns: S of tile X at X*128 (P of tile X as bf16 pairs in its
+  // first 64 columns); O of tile X at 256 + X*D.
   static constexpr int O_COL = 256;
   static constexpr float RESCALE_LOG2 = 8.0f;
 };
@@ -71,10 +78,9 @@ struct TcBars {
   uint64_t q_full;
   uint64_t kv_full[4];
   uint64_t kv_empty[4];
-  uint64_t s_full[2][2];   // [tile][buffer]
-  uint64_t s_free[2][2];
-  uint64_t p_full[2];      // [tile]
-  uint64_t p_free[2];
+  uint64_t s_full[2];      // [tile]: S = Q K^T of the current key tile is in TMEM
+  uint64_t p_full[2];      // [tile]: P of the current key tile is in TMEM
+  uint64_t pv_done[2];     // [tile]: O += P V of the current key tile completed
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort;
@@ -95,7 +101,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   const int r = quarter * 32 + lane;              // row within tile X (TMEM lane)
   const int rl = X * C::BM + r;                   // row within the work item
   const uint32_t tm_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-  const uint32_t s_col = X * 128, o_col = C::O_COL + X * D;
+  const uint32_t s_col = X * 128, o_col = C::O_COL + X * D;   // S / P and O columns
   const int G = a.G;
   const bool rvalid = rl < R;
   const int pr = row0 + (rvalid ? rl : 0);
@@ -105,40 +111,31 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   // Last key this row may see (bottom-right causal), or the last key.
   const int lim = !rvalid ? -1 : (a.causal ? kv_len - q_len + ti : kv_len - 1);
   const float sl2 = a.scale_log2;
-  const int tid = threadIdx.x - 64 - X * 128;      // 0..127 within the warpgroup
-  uint8_t* prow = smem + C::OFF_P + X * C::P_TILE + r * 128;
+  const int tid = threadIdx.x - 128 - X * 128;     // 0..127 within the warpgroup
   float m_use = -INFINITY, l = 0.f;
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
-    const int b = t & 1;
-    if (!mbar_wait(&bars->s_full[X][b], (t >> 1) & 1)) { ok = false; break; }
+    if (!mbar_wait(&bars->s_full[X], t & 1)) { ok = false; break; }
     tc_fence_after();
-    float x[C::BN];
-    {
-      uint32_t v[C::BN / 32][32];
-#pragma unroll
-      for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(tm_row + s_col + b * 64 + c * 32, v[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < C::BN / 32; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
-    }
-    tc_fence_before();
-    mbar_arrive(&bars->s_free[X][b]);
     const int key0 = kb + t * C::BN;
     const int vis_end = min(ke, lim + 1);   // keys [key0, vis_end) are visible
-    if (key0 + C::BN > vis_end) {
+    const bool edge = key0 + C::BN > vis_end;
+    uint32_t xs_u[C::BN];
 #pragma unroll
-      for (int e = 0; e < C::BN; ++e) x[e] = (key0 + e < vis_end) ? x[e] : -INFINITY;
+    for (int c = 0; c < C::BN / 32; ++c)
+      tmem_ld32(tm_row + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&xs_u[c * 32]));
+    tmem_wait_ld();
+    float* xs = reinterpret_cast<float*>(xs_u);
+    if (edge) {
+#pragma unroll
+      for (int e = 0; e < C::BN; ++e)
+        if (key0 + e >= vis_end) xs[e] = -INFINITY;
     }
-    // Row max of the raw scores (the scale is positive): eight independent
-    // chains, then into the log2 domain.
     float mx8[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) mx8[e] = x[e];
+    for (int e = 0; e < 8; ++e) mx8[e] = xs[e];
 #pragma unroll
-    for (int e = 8; e < C::BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
+    for (int e = 8; e < C::BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], xs[e]);
     const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
     float m_new = m_use;
@@ -147,11 +144,9 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
       if (m_use == -INFINITY) m_new = tmax;                 // O holds only zeros so far
       else if (tmax - m_use > C::RESCALE_LOG2) { need = true; m_new = tmax; }
     }
-    // The previous tile's P V product must be done before this tile's P
-    // overwrites the P buffer, and before O is rescaled.
-    if (t > 0 && !mbar_wait(&bars->p_free[X], (t - 1) & 1)) { ok = false; break; }
+    // O_X is final here: this tile's S was issued after the previous P V
+    // completed, and its commit covers that product.
     if (__any_sync(0xffffffffu, need)) {
-      tc_fence_after();
       const float alpha = need ? fast_exp2(m_use - m_new) : 1.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -162,25 +157,31 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
         tmem_st32(tm_row + o_col + c * 32, v);
       }
-      tmem_wait_st();
       l *= alpha;
     }
     m_use = m_new;
     const float mu = m_use == -INFINITY ? 0.f : m_use;
+    // Pass 2: P = exp2(S * scale * log2(e) - m) as bf16 pairs into the first
+    // 64 columns of this tile's S region (key k -> column k / 2). Chunk c
+    // reads S columns [32c, 32c+32) and writes P columns [16c, 16c+16), which
+    // only the already-read chunks occupy.
     float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < C::BN / 8; ++c) {
-      float p[8];
+    for (int c = 0; c < C::BN / 32; ++c) {
+      uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        p[e] = fast_exp2(fmaf(x[c * 8 + e], sl2, -mu));   // masked scores are -inf -> 0
-        ls[e] += p[e];
+      for (int e = 0; e < 32; e += 2) {
+        const float x0 = xs[c * 32 + e], x1 = xs[c * 32 + e + 1];
+        const float p0 = fast_exp2(fmaf(x0, sl2, -mu));
+        const float p1 = fast_exp2(fmaf(x1, sl2, -mu));
+        ls[e & 7] += p0;
+        ls[(e + 1) & 7] += p1;
+        pk[e >> 1] = pack_bf16(p0, p1);
       }
-      const uint4 v = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
-                                 pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
-      *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = v;
+      tmem_st16(tm_row + s_col + c * 16, pk);
     }
     l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+    tmem_wait_st();
     // V rows past the sequence end hold arbitrary bytes: zero them so the
     // P V product (P = 0 there) cannot pick up NaN. Tile A's warps do it
     // before tile A's P is published; the MMA thread issues tile B's product
@@ -195,8 +196,8 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
         *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::KV_HALF + rr * 128 + (rem & 7) * 16) =
             make_uint4(0, 0, 0, 0);
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     mbar_arrive(&bars->p_full[X]);
   }
@@ -207,7 +208,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   // ---------------------------------------------------------- epilogue
   ok = __all_sync(0xffffffffu, ok);   // TMEM loads below are warp-collective
   if (ok && ntiles > 0) {
-    if (!mbar_wait(&bars->p_free[X], (ntiles - 1) & 1)) {
+    if (!mbar_wait(&bars->pv_done[X], (ntiles - 1) & 1)) {
       abort_call(a);
       bars->abort = 1;
       ok = false;
@@ -274,12 +275,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                                              ~static_cast<uintptr_t>(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(smem + C::OFF_BAR);
 
-  // One block per (work item, KV head), KV head fastest: blocks are
-  // dispatched in index order and the planner sorted the items longest first.
-  const int item = static_cast<int>(blockIdx.x) / a.H_kv;
-  const int hk = static_cast<int>(blockIdx.x) - item * a.H_kv;
-  if (item >= a.header[1] || call_aborted(a)) return;
-  const int4 it = a.items[item];
+  if (static_cast<int>(blockIdx.x) >= a.header[1] || call_aborted(a)) return;
+  const int hk = blockIdx.y;
+  const int4 it = a.items[blockIdx.x];
   const int seg = it.x, rt = it.y, j = it.z;
   const int4 sg = a.seg[seg];
   const int4 sp = a.segsplit[seg];
@@ -302,12 +300,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       mbar_init(&bars->kv_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&bars->s_full[x][b], 1);
-        mbar_init(&bars->s_free[x][b], 128);
-      }
+      mbar_init(&bars->s_full[x], 1);
       mbar_init(&bars->p_full[x], 128);
-      mbar_init(&bars->p_free[x], 1);
+      mbar_init(&bars->pv_done[x], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -324,7 +319,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // Register split: the block is launched with 384 x 168 registers. The
+  // control warpgroup (producer, MMA issuer, two idle warps) drops to 56 and
+  // the two softmax warpgroups rise to 224: 128*56 + 256*224 = 384*168.
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (ntiles > 0) {
@@ -352,51 +352,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       constexpr uint32_t idesc_o = mma_idesc_bf16(C::BM, D, true);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sKV = smem_u32(smem + C::OFF_KV);
-      const uint32_t sP = smem_u32(smem + C::OFF_P);
       const int nx = two ? 2 : 1;
       bool ok = mbar_wait(&bars->q_full, 0);
-      for (int t = 0; ok && t <= ntiles; ++t) {
+      for (int t = 0; ok && t < ntiles; ++t) {
         if (bars->abort) { ok = false; break; }
-        if (t < ntiles) {
-          const int s = t % C::STAGES, b = t & 1;
-          ok = mbar_wait(&bars->kv_full[s], (t / C::STAGES) & 1);
-          if (!ok) break;
-          bars->consumed = t + 1;
-          const uint32_t kbase = sKV + s * C::STAGE;
-          for (int x = 0; x < nx; ++x) {
-            if (t >= 2 && !(ok = mbar_wait(&bars->s_free[x][b], ((t >> 1) - 1) & 1))) break;
-            tc_fence_after();
-            const uint32_t qbase = sQ + x * C::Q_TILE;
+        const int s = t % C::STAGES;
+        if (!(ok = mbar_wait(&bars->kv_full[s], (t / C::STAGES) & 1))) break;
+        bars->consumed = t + 1;
+        const uint32_t kbase = sKV + s * C::STAGE;
+        const uint32_t vbase = kbase + C::KV_TILE;
+        // S_X = Q_X K^T, once P_X of the previous tile has been consumed.
+        for (int x = 0; x < nx; ++x) {
+          if (t > 0 && !(ok = mbar_wait(&bars->pv_done[x], (t - 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t qbase = sQ + x * C::Q_TILE;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t ad =
-                  smem_desc_sw128(qbase + (kk >> 2) * C::Q_HALF + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd =
-                  smem_desc_sw128(kbase + (kk >> 2) * C::KV_HALF + (kk & 3) * 32, 16, 1024);
-              tc_mma(tmem + x * 128 + b * 64, ad, bd, idesc_s, kk > 0);
-            }
-            tc_commit(&bars->s_full[x][b]);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad =
+                smem_desc_sw128(qbase + (kk >> 2) * C::Q_HALF + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd =
+                smem_desc_sw128(kbase + (kk >> 2) * C::KV_HALF + (kk & 3) * 32, 16, 1024);
+            tc_mma(tmem + x * 128, ad, bd, idesc_s, kk > 0);
           }
-          if (!ok) break;
+          tc_commit(&bars->s_full[x]);
         }
-        if (t >= 1) {
-          const int u = t - 1, su = u % C::STAGES;
-          const uint32_t vbase = sKV + su * C::STAGE + C::KV_TILE;
-          for (int x = 0; x < nx; ++x) {
-            if (!(ok = mbar_wait(&bars->p_full[x], u & 1))) break;
-            tc_fence_after();
-            const uint32_t pbase = sP + x * C::P_TILE;
+        if (!ok) break;
+        // O_X += P_X V, P_X from TMEM.
+        for (int x = 0; x < nx; ++x) {
+          if (!(ok = mbar_wait(&bars->p_full[x], t & 1))) break;
+          tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < C::BN / 16; ++kk) {
-              const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(vbase + kk * 16 * 128, C::KV_HALF, 1024);
-              tc_mma(tmem + C::O_COL + x * D, ad, bd, idesc_o, (u > 0 || kk > 0) ? 1 : 0);
-            }
-            tc_commit(&bars->p_free[x]);
+          for (int kk = 0; kk < C::BN / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(vbase + kk * 16 * 128, C::KV_HALF, 1024);
+            tc_mma_ts(tmem + C::O_COL + x * D, tmem + x * 128 + kk * 8, bd, idesc_o,
+                      (t > 0 || kk > 0) ? 1 : 0);
           }
-          if (!ok) break;
-          tc_commit(&bars->kv_empty[su]);
+          tc_commit(&bars->pv_done[x]);
         }
+        if (!ok) break;
+        tc_commit(&bars->kv_empty[s]);
       }
       if (!ok) {
         abort_call(a);
@@ -406,9 +400,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       tc_commit(&bars->drain);
       mbar_wait(&bars->drain, 0);
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
     // ------------------------------------------------------------ softmax
-    const int X = (warp - 2) >> 2;   // warps 2-5: tile A, 6-9: tile B
+    const int X = (warp - 4) >> 2;   // warps 4-7: tile A, 8-11: tile B
     if (X == 0 || two)
       tc_softmax_tile<D>(a, bars, smem, tmem, X, q_start, q_len, kv_len, kb, ke, ntiles, row0,
                          R, hk, nsplit, slot_base, rt, j);
@@ -418,7 +414,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       asm volatile("bar.sync 1, 256;" ::: "memory");
       const int grp = slot_base + rt * nsplit;
       int* counter = a.counters + static_cast<int64_t>(grp) * a.H_kv + hk;
-      const int tid = threadIdx.x - 64;
+      const int tid = threadIdx.x - 128;
       if (tid == 0) bars->last = (atomicAdd(counter, 1) == nsplit - 1) ? 1 : 0;
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (bars->last) {
@@ -462,7 +458,7 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
   }
-  const dim3 grid(static_cast<unsigned>(items_bound) * static_cast<unsigned>(a.H_kv));
+  dim3 grid(items_bound, a.H_kv);
   attn_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmK, tmV, tmQ, a);
   return cudaGetLastError();
 }
