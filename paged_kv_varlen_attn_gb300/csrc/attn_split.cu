@@ -40,7 +40,7 @@ struct SplitCfg {
   static constexpr int HALF_BYTES = BN * 128;          // [64 rows x 128 B]
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K and V
-  static constexpr int STAGES = D == 128 ? 3 : 6;
+  static constexpr int STAGES = D == 128 ? 2 : 6;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
   static constexpr int SMEM_BYTES = RING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int THREADS = 160;
@@ -265,7 +265,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ks > 0) return;
+    if (ks == 0) {
 #pragma unroll
     for (int k2 = 1; k2 < KS; ++k2) {
       const float* w = scratch + (rg + k2 * RGN) * PER_WARP;
@@ -287,9 +287,11 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
         for (int e = 0; e < 4; ++e)
           o[n][e] = o[n][e] * alpha_a[e >> 1] + w[(n * 4 + e) * 32 + lane] * alpha_b[e >> 1];
     }
+    }
   }
 
-  // Epilogue (warps 0 .. RGN-1 hold the merged rows of their group).
+  // Epilogue. Warps 0 .. RGN-1 hold the merged rows of their group; all four
+  // consumer warps take part in a combine.
   float inv_l[2], lse_nat[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -298,60 +300,56 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
     lse_nat[r] = any ? (m[r] + fast_log2(l[r])) * kLn2 : -INFINITY;
   }
   const int H = a.H;
-  if (nsplit == 1) {
+  if (nsplit == 1 && !a.partials_only && !a.merge_parts) {
+    if (ks > 0) return;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       if (!rvalid[r]) continue;
       const int64_t obase = (static_cast<int64_t>(tok[r]) * H + head[r]) * D;
-      float lse_r = lse_nat[r];
 #pragma unroll
       for (int n = 0; n < DN; ++n) {
-        float v[2] = {o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]};
         const int col = n * 8 + 2 * cq;
-        if (a.merge_o) {
-          float lse_tmp = lse_nat[r];
-          merge_prefix(a, obase + col, head[r], tok[r], lse_tmp, v, 2);
-          lse_r = lse_tmp;
-        }
-        if (a.out_f32) {
-          *reinterpret_cast<float2*>(a.out_f32 + obase + col) = make_float2(v[0], v[1]);
-        } else {
-          *reinterpret_cast<uint32_t*>(a.out + obase + col) = pack_bf16(v[0], v[1]);
-        }
+        *reinterpret_cast<uint32_t*>(a.out + obase + col) =
+            pack_bf16(o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]);
       }
-      if (a.lse && cq == 0) a.lse[static_cast<int64_t>(head[r]) * a.lse_stride + tok[r]] = lse_r;
+      if (a.lse && cq == 0) a.lse[static_cast<int64_t>(head[r]) * a.lse_stride + tok[r]] = lse_nat[r];
     }
     return;
   }
 
-  // Split item: publish the normalised partial, then the last CTA merges.
+  // Publish the normalised partial state; then the last CTA of the group
+  // merges every split (and, in a cascade suffix pass, the prefix partials)
+  // with coalesced loads by all 128 consumer threads.
   const int slot = slot_base + rt * nsplit + j;
   const int64_t slot_row0 = slot_row(a, slot, hk, 0);
+  if (ks == 0) {
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int rl = rg * 16 + gq + 8 * r;
-    if (!rvalid[r]) continue;
-    float* po = a.part_o + (slot_row0 + rl) * D;
+    for (int r = 0; r < 2; ++r) {
+      const int rl = rg * 16 + gq + 8 * r;
+      if (!rvalid[r]) continue;
+      float* po = a.part_o + (slot_row0 + rl) * D;
 #pragma unroll
-    for (int n = 0; n < DN; ++n)
-      __stcg(reinterpret_cast<float2*>(po + n * 8 + 2 * cq),
-             make_float2(o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]));
-    if (cq == 0) __stcg(a.part_lse + slot_row0 + rl, lse_nat[r]);
+      for (int n = 0; n < DN; ++n)
+        __stcg(reinterpret_cast<float2*>(po + n * 8 + 2 * cq),
+               make_float2(o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]));
+      if (cq == 0) __stcg(a.part_lse + slot_row0 + rl, lse_nat[r]);
+    }
   }
+  if (a.partials_only) return;   // cascade prefix pass: the suffix pass merges
   __threadfence();
-  asm volatile("bar.sync 2, %0;" ::"r"(32 * RGN) : "memory");
+  asm volatile("bar.sync 2, 128;" ::: "memory");
   const int grp = slot_base + rt * nsplit;
   int* counter = a.counters + static_cast<int64_t>(grp) * a.H_kv + hk;
   if (threadIdx.x == 0) sh.flags[1] = (atomicAdd(counter, 1) == nsplit - 1) ? 1 : 0;
-  asm volatile("bar.sync 2, %0;" ::"r"(32 * RGN) : "memory");
+  asm volatile("bar.sync 2, 128;" ::: "memory");
   if (!sh.flags[1]) return;
   __threadfence();
-  combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, threadIdx.x, 32 * RGN);
+  combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, threadIdx.x, 128);
   if (threadIdx.x == 0) *counter = 0;   // ready for the next call
 }
 
 template <int D>
-__global__ void __launch_bounds__(SplitCfg<D>::THREADS, 2)
+__global__ void __launch_bounds__(SplitCfg<D>::THREADS, 3)
 attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ AttnArgs a) {
   using C = SplitCfg<D>;

@@ -239,27 +239,18 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
 #pragma unroll
       for (int e = 0; e < 4; ++e) o4[e] = __uint_as_float(v[q4 * 4 + e]) * inv_l;
       const int col = c * 32 + q4 * 4;
-      if (nsplit > 1) {
+      if (nsplit > 1 || a.partials_only || a.merge_parts) {
         __stcg(reinterpret_cast<float4*>(a.part_o + srow * D + col),
                make_float4(o4[0], o4[1], o4[2], o4[3]));
       } else {
-        float lse_tmp = lse_nat;
-        if (a.merge_o) merge_prefix(a, obase + col, head, tok, lse_tmp, o4, 4);
         store4(a, obase + col, o4);
       }
     }
   }
   if (rvalid) {
-    if (nsplit > 1) {
+    if (nsplit > 1 || a.partials_only || a.merge_parts) {
       __stcg(a.part_lse + srow, lse_nat);
     } else if (a.lse) {
-      if (a.merge_o) {
-        const float la = a.merge_lse[static_cast<int64_t>(head) * a.lse_stride + tok];
-        const float m = fmaxf(la, lse_nat);
-        lse_nat = m == -INFINITY ? -INFINITY
-                                 : m + fast_log2(fast_exp2((la - m) * kLog2e) +
-                                                 fast_exp2((lse_nat - m) * kLog2e)) * kLn2;
-      }
       a.lse[static_cast<int64_t>(head) * a.lse_stride + tok] = lse_nat;
     }
   }
@@ -408,7 +399,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (X == 0 || two)
       tc_softmax_tile<D>(a, bars, smem, tmem, X, q_start, q_len, kv_len, kb, ke, ntiles, row0,
                          R, hk, nsplit, slot_base, rt, j);
-    if (nsplit > 1) {
+    if ((nsplit > 1 || a.merge_parts) && !a.partials_only) {
       // Both warpgroups (256 threads) take part, active tile or not.
       __threadfence();
       asm volatile("bar.sync 1, 256;" ::: "memory");

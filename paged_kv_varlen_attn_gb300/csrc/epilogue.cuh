@@ -7,31 +7,49 @@
 
 namespace pa {
 
-// out <- merge((prefix_o, prefix_lse), (o, lse_nat)) for n consecutive columns
-// starting at element obase of a [T, H, D] row; updates lse_nat.
-__device__ __forceinline__ void merge_prefix(const AttnArgs& a, int64_t obase, int h, int tok,
-                                             float& lse_nat, float* o, int n) {
-  const float la = a.merge_lse[static_cast<int64_t>(h) * a.lse_stride + tok];
-  const float lb = lse_nat;
-  const float m = fmaxf(la, lb);
-  if (m == -INFINITY) {
+// Cascade: merge the state (o[0..n) at columns col.., lse) of row (token tok,
+// head h) with the prefix pass's partial states of the same row -- one per
+// split of the shared prefix -- weighted by their LSEs. lse becomes the merged
+// LSE. The prefix pass planned one segment holding every query token, so the
+// row's packed index there is tok * G + (h % G).
+__device__ __forceinline__ void merge_prefix(const AttnArgs& a, int h, int tok, int col,
+                                             float& lse, float* o, int n) {
+  const int4 g0 = a.mp_seg[0];
+  const int4 s0 = a.mp_segsplit[0];
+  const int cls = g0.w;
+  const int rows_per_item = cls ? kRowsTc : kRowsSplit;
+  const int G = a.G;
+  const int hk = h / G;
+  const int pr = tok * G + (h - hk * G);
+  const int rt = pr / rows_per_item, rl = pr - rt * rows_per_item;
+  const int nsp = s0.x, base = s0.y + rt * nsp;
+  const float* plse = a.mp_part_lse[cls];
+  const float* po = a.mp_part_o[cls];
+  const int64_t srows = a.mp_slot_rows[cls];
+  float mx = lse;
+  for (int j = 0; j < nsp; ++j)
+    mx = fmaxf(mx, __ldcg(plse + (static_cast<int64_t>(base + j) * a.H_kv + hk) * srows + rl));
+  if (mx == -INFINITY) {
     for (int i = 0; i < n; ++i) o[i] = 0.f;
     return;
   }
-  const float wa = fast_exp2((la - m) * kLog2e), wb = fast_exp2((lb - m) * kLog2e);
-  const float inv = 1.f / (wa + wb);
-  for (int i = 0; i < n; ++i) o[i] = (wa * __ldcg(a.merge_o + obase + i) + wb * o[i]) * inv;
-  lse_nat = m + fast_log2(wa + wb) * kLn2;
+  float tot = fast_exp2((lse - mx) * kLog2e);
+  for (int i = 0; i < n; ++i) o[i] *= tot;
+  for (int j = 0; j < nsp; ++j) {
+    const int64_t row = (static_cast<int64_t>(base + j) * a.H_kv + hk) * srows + rl;
+    const float w = fast_exp2((__ldcg(plse + row) - mx) * kLog2e);
+    tot += w;
+    const float* pj = po + row * a.D + col;
+    for (int i = 0; i < n; ++i) o[i] += w * __ldcg(pj + i);
+  }
+  const float inv = 1.f / tot;
+  for (int i = 0; i < n; ++i) o[i] *= inv;
+  lse = mx + fast_log2(tot) * kLn2;
 }
 
-// Write 4 final values of a row (bf16 or fp32 destination).
+// Write 4 final values of a row as bf16.
 __device__ __forceinline__ void store4(const AttnArgs& a, int64_t obase, const float (&v)[4]) {
-  if (a.out_f32) {
-    *reinterpret_cast<float4*>(a.out_f32 + obase) = make_float4(v[0], v[1], v[2], v[3]);
-  } else {
-    *reinterpret_cast<uint2*>(a.out + obase) =
-        make_uint2(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]));
-  }
+  *reinterpret_cast<uint2*>(a.out + obase) = make_uint2(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]));
 }
 
 // Partial-state slot of (group slot `slot`, KV head hk, row rl).
@@ -74,7 +92,7 @@ __device__ void combine_splits(const AttnArgs& a, int grp, int nsplit, int hk, i
       lse_r = mx + fast_log2(sw) * kLn2;
     }
     const int64_t obase = (static_cast<int64_t>(tk) * a.H + hh) * D + c4 * 4;
-    if (a.merge_o) merge_prefix(a, obase, hh, tk, lse_r, acc, 4);
+    if (a.merge_parts) merge_prefix(a, hh, tk, c4 * 4, lse_r, acc, 4);
     store4(a, obase, acc);
     if (a.lse && c4 == 0) a.lse[static_cast<int64_t>(hh) * a.lse_stride + tk] = lse_r;
   }

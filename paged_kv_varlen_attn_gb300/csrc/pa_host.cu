@@ -39,6 +39,7 @@ struct PassDims {
   bool single;    // one segment of total_q queries (cascade prefix pass)
   int G, H, H_kv, D;
   int sms;
+  bool all_partial = false;   // every item keeps a partial-state slot (cascade prefix pass)
 };
 
 // Which kernels a pass can need, from host-known bounds only.
@@ -59,6 +60,10 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
   L.items_bound[1] = tc ? L.target[1] + d.num_segs + cdiv(rows, kRowsTc) + 1 : 0;
   L.slots_bound[0] = sp ? 2 * L.target[0] + 2 : 0;
   L.slots_bound[1] = tc ? 2 * L.target[1] + 2 : 0;
+  if (d.all_partial) {
+    L.slots_bound[0] = L.items_bound[0];
+    L.slots_bound[1] = L.items_bound[1];
+  }
   // A work item holds at most min(rows per item of its kernel, q_len * G) rows.
   const long long rows_bound = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
   auto clamp_rows = [&](int item_rows) {
@@ -85,20 +90,17 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
 
 struct CascadeLayout {
   PassLayout prefix, suffix;
-  size_t prefix_o, prefix_lse, end;
+  size_t end;
 };
 
 CascadeLayout layout_cascade(int num_seqs, int total_q, int max_q, int G, int H, int H_kv, int D,
                              int sms) {
   CascadeLayout C{};
-  PassDims pd{1, total_q, total_q, true, G, H, H_kv, D, sms};
+  PassDims pd{1, total_q, total_q, true, G, H, H_kv, D, sms, true};
   C.prefix = layout_pass(pd, 0);
-  PassDims sd{num_seqs, total_q, max_q, false, G, H, H_kv, D, sms};
+  PassDims sd{num_seqs, total_q, max_q, false, G, H, H_kv, D, sms, true};
   C.suffix = layout_pass(sd, C.prefix.end);
-  size_t off = C.suffix.end;
-  C.prefix_o = off;   off = align_up(off + static_cast<size_t>(total_q) * H * D * 4);
-  C.prefix_lse = off; off = align_up(off + static_cast<size_t>(total_q) * H * 4);
-  C.end = off;
+  C.end = C.suffix.end;
   return C;
 }
 
@@ -204,7 +206,7 @@ struct CommonAttn {
 };
 
 PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int single, int single_kv,
-                   int kv_off, int kv_cap, int causal, int check_cascade) {
+                   int kv_off, int kv_cap, int causal, int check_cascade, int partials_only = 0) {
   PlanArgs p{};
   p.cu_seqlens_q = c.cu;
   p.seqused_k = c.lens;
@@ -230,12 +232,12 @@ PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int si
   p.L = L;
   p.status = c.status;
   p.check_cascade = check_cascade;
+  p.partials_only = partials_only;
   return p;
 }
 
 AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt_row_stride,
-                   int bt_col_offset, int causal, void* out, float* out_f32, float* lse,
-                   const float* merge_o, const float* merge_lse) {
+                   int bt_col_offset, int causal, void* out, float* lse) {
   AttnArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(c.q);
   a.q_stride = c.q_stride;
@@ -251,11 +253,8 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
   a.scale_log2 = c.scale * 1.4426950408889634f;
   a.causal = causal;
   a.out = static_cast<__nv_bfloat16*>(out);
-  a.out_f32 = out_f32;
   a.lse = lse;
   a.lse_stride = c.total_q;
-  a.merge_o = merge_o;
-  a.merge_lse = merge_lse;
   a.header = reinterpret_cast<const int*>(ws + L.header);
   a.abort_all = reinterpret_cast<int*>(ws + L.header) + 2;
   a.seg = reinterpret_cast<const int4*>(ws + L.seg);
@@ -434,7 +433,7 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
   pp.p[0] = make_plan(c, ws, L, 0, 0, 0, cap > 0x7fffffff ? 0x7fffffff : static_cast<int>(cap),
                       causal, 0);
   if (launch_plan(pp, 1, c.st) != cudaSuccess) return PA_ERR_CUDA;
-  AttnArgs a = make_attn(c, ws, L, bt_stride, 0, causal, out, nullptr, lse, nullptr, nullptr);
+  AttnArgs a = make_attn(c, ws, L, bt_stride, 0, causal, out, lse);
   return launch_pass(c, tmK, tmV, tmQ, a, ws, L);
 }
 
@@ -502,24 +501,31 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
   if (!encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride, G))
     return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* prefix_o = reinterpret_cast<float*>(ws + CL.prefix_o);
-  float* prefix_lse = reinterpret_cast<float*>(ws + CL.prefix_lse);
   const int P = common_prefix_len;
   const int pages = P / block_size;
   const long long cap = (static_cast<long long>(bt_stride) - pages) * block_size;
   PlanPasses pp{};
-  // Pass A: all queries, one non-causal segment, row 0's first P keys.
-  pp.p[0] = make_plan(c, ws, CL.prefix, 1, P, 0, P, 0, 0);
-  // Pass B: each sequence, causal, its own keys from position P on.
+  // Pass A: all queries, one non-causal segment, row 0's first P keys; every
+  // work item leaves its partial state in its slot.
+  pp.p[0] = make_plan(c, ws, CL.prefix, 1, P, 0, P, 0, 0, 1);
+  // Pass B: each sequence, causal, its own keys from position P on; each final
+  // row is merged with pass A's partial states of the same row.
   pp.p[1] = make_plan(c, ws, CL.suffix, 0, 0, P,
-                      cap > 0x7fffffff ? 0x7fffffff : static_cast<int>(cap), 1, 1);
+                      cap > 0x7fffffff ? 0x7fffffff : static_cast<int>(cap), 1, 1, 1);
   if (launch_plan(pp, 2, c.st) != cudaSuccess) return PA_ERR_CUDA;
-  AttnArgs pa_ = make_attn(c, ws, CL.prefix, 0, 0, 0, nullptr, prefix_o, prefix_lse, nullptr,
-                           nullptr);
+  AttnArgs pa_ = make_attn(c, ws, CL.prefix, 0, 0, 0, nullptr, nullptr);
+  pa_.partials_only = 1;
   st = launch_pass(c, tmK, tmV, tmQ, pa_, ws, CL.prefix);
   if (st != PA_OK) return st;
-  AttnArgs pb = make_attn(c, ws, CL.suffix, bt_stride, pages, 1, out, nullptr, lse, prefix_o,
-                          prefix_lse);
+  AttnArgs pb = make_attn(c, ws, CL.suffix, bt_stride, pages, 1, out, lse);
+  pb.merge_parts = 1;
+  pb.mp_seg = reinterpret_cast<const int4*>(ws + CL.prefix.seg);
+  pb.mp_segsplit = reinterpret_cast<const int4*>(ws + CL.prefix.segsplit);
+  for (int k = 0; k < 2; ++k) {
+    pb.mp_part_lse[k] = reinterpret_cast<const float*>(ws + CL.prefix.part_lse[k]);
+    pb.mp_part_o[k] = reinterpret_cast<const float*>(ws + CL.prefix.part_o[k]);
+    pb.mp_slot_rows[k] = CL.prefix.slot_rows[k];
+  }
   return launch_pass(c, tmK, tmV, tmQ, pb, ws, CL.suffix);
 }
 

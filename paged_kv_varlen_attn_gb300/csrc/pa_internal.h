@@ -58,6 +58,7 @@ struct PlanArgs {
   PassLayout L;
   int32_t* status;
   int check_cascade;     // flag q_len > kv_len (suffix pass of cascade)
+  int partials_only;     // every item gets a partial-state slot and a zeroed counter (cascade)
 };
 
 struct PlanPasses {
@@ -75,11 +76,19 @@ struct AttnArgs {
   float scale_log2;          // softmax_scale * log2(e)
   int causal;
   __nv_bfloat16* out;        // [T, H, D] bf16 (final) or NULL
-  float* out_f32;            // [T, H, D] fp32 (final, cascade prefix) or NULL
   float* lse;                // [H, lse_stride] natural log or NULL
   int lse_stride;            // = total_q
-  const float* merge_o;      // cascade: prefix state to merge with ([T,H,D] fp32)
-  const float* merge_lse;    // [H, lse_stride]
+  // Cascade. Prefix pass: partials_only = 1, every work item writes its
+  // partial state to its slot and nothing is combined. Suffix pass:
+  // merge_parts = 1, each final row is merged with the prefix pass's partial
+  // states of the same row (prefix segment 0's split info and slot pools).
+  int partials_only;
+  int merge_parts;
+  const int4* mp_seg;
+  const int4* mp_segsplit;
+  const float* mp_part_lse[2];
+  const float* mp_part_o[2];
+  int mp_slot_rows[2];
   // plan of this pass
   const int* header;         // [0], [1]: item counts of the two kernels
   int* abort_all;            // header[2]: set by any CTA whose wait timed out

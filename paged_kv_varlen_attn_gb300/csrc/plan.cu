@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         chunk = kKeyTile;
       }
       const int n_items = nrt * nsplit;
-      const int n_slots = nsplit > 1 ? n_items : 0;
+      const int n_slots = (nsplit > 1 || P.partials_only) ? n_items : 0;
       v = cls ? make_int4(0, n_items, 0, n_slots) : make_int4(n_items, 0, n_slots, 0);
     }
     int4 ex;
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       for (int rt = 0; rt < nrt; ++rt)
         for (int j = 0; j < nsplit; ++j)
           atomicAdd(&hist[cls][item_bucket(s, rt, j, seg[s], chunk, G, P.causal)], 1);
-      if (nsplit > 1) {
+      if (nsplit > 1 || P.partials_only) {
         int* counters = cls ? counters1 : counters0;
         const int sbound = cls ? P.slots_bound1 : P.slots_bound0;
         for (int rt = 0; rt < nrt; ++rt) {

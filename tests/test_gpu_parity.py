@@ -295,6 +295,24 @@ def test_cascade_small_matches_flat():
     assert int(status.item()) == 0
 
 
+@pytest.mark.parametrize("seed,S,H,Hk,D,P,qmax,smax", [
+    (72, 4, 8, 2, 128, 64, 1, 40),       # prefix pass rows 4*4 = 16: split-KV kernel
+    (73, 40, 32, 4, 128, 512, 2, 200),   # prefix rows up to 80*8 = 640: several 256-row tiles
+    (74, 12, 16, 16, 64, 256, 3, 90),    # GQA 1, head 64
+])
+def test_cascade_prefix_row_tiles(seed, S, H, Hk, D, P, qmax, smax):
+    g = torch.Generator().manual_seed(seed)
+    suffix = [int(x) for x in torch.randint(qmax + 1, smax, (S,), generator=g)]
+    q_lens = [int(x) for x in torch.randint(1, qmax + 1, (S,), generator=g)]
+    wl = W._build(f"cascade_{seed}", seed, H, Hk, D, 16, q_lens, [P + s for s in suffix], g,
+                  shared_prefix_pages=P // 16)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse, _ = run_gpu(wl, cascade=True, status=status)
+    ref_o, ref_l = oracle_full(wl, cascade=True)
+    assert_close(out, lse, ref_o, ref_l)
+    assert int(status.item()) == 0
+
+
 def test_cascade_shared_prefix_config():
     wl = W.cascade_shared_prefix()
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
