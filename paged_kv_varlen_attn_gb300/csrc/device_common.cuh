@@ -268,16 +268,19 @@ __device__ __forceinline__ void abort_call(const AttnArgs& a) {
 // STAGES stages, each [K tile | V tile], each tile HALVES x [BN rows x 128 B]
 // (128-byte swizzle). A tile is BN / box_rows TMA boxes per half; every box
 // lies inside one page. The warp loads the page ids of the next 32 boxes
-// (one per lane, coalesced) while lane 0 issues the current ones, so the
-// block-table reads stay off the issue path. A page id outside the pool, or
+// (one per lane, coalesced) while the current ones are issued, so the
+// block-table reads stay off the issue path; the boxes of a tile are issued
+// by parallel lanes. A page id outside the pool, or
 // a box past the sequence end, becomes the out-of-range coordinate
-// num_blocks, which TMA fills with zeros. Returns false on timeout/abort.
+// num_blocks, which TMA fills with zeros. The unit's first tile is tile t0 of
+// the ring's running sequence (stages and phases continue across units).
+// Returns false on timeout/abort.
 template <int BN, int HALVES, int STAGES>
 __device__ bool produce_kv(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnArgs& a,
                            uint8_t* ring, uint64_t* full, uint64_t* empty,
                            volatile int* cta_abort, volatile int* issued,
                            const int32_t* bt_row, int hk, int kb, int kv_len, int ntiles,
-                           int lane) {
+                           int lane, int t0 = 0) {
   constexpr int HALF = BN * 128;
   constexpr int TILE = HALVES * HALF;
   constexpr int STAGE = 2 * TILE;
@@ -285,27 +288,38 @@ __device__ bool produce_kv(const CUtensorMap* tmK, const CUtensorMap* tmV, const
   const int bpt = BN / box_rows;         // boxes per tile
   const int tpg = 32 / bpt;              // tiles per group of 32 boxes
   const int ngroups = (ntiles + tpg - 1) / tpg;
-  auto load_page = [&](int g) -> int {
+  // Lane i holds the page id and page row of box i of a group.
+  auto load_page = [&](int g, int& prow) -> int {
     const int k = kb + g * tpg * BN + lane * box_rows;
     int page = a.num_blocks;
+    prow = 0;
     if (k < kv_len) {
-      const int pg = __ldg(bt_row + k / a.bs);
+      const int lp = k / a.bs;
+      prow = k - lp * a.bs;
+      const int pg = __ldg(bt_row + lp);
       if (pg >= 0 && pg < a.num_blocks) page = pg;
       else flag_status(a.status, PA_DEV_BAD_PAGE);
     }
     return page;
   };
-  int next = ngroups > 0 ? load_page(0) : 0;
+  // The boxes of one tile are issued by parallel lanes: lane L takes box
+  // L / (2*HALVES), half (L/2) % HALVES, K for even L and V for odd L.
+  const int nbox = bpt * HALVES * 2;   // <= 32: box_rows >= 16, BN <= 128
+  const int my_b = lane / (2 * HALVES), my_h = (lane >> 1) % HALVES, my_v = lane & 1;
+  int next_row = 0, cur_row = 0;
+  int next = ngroups > 0 ? load_page(0, next_row) : 0;
   for (int g = 0; g < ngroups; ++g) {
     const int cur = next;
-    if (g + 1 < ngroups) next = load_page(g + 1);
+    cur_row = next_row;
+    if (g + 1 < ngroups) next = load_page(g + 1, next_row);
     for (int tt = 0; tt < tpg; ++tt) {
       const int t = g * tpg + tt;
       if (t >= ntiles) break;
-      const int s = t % STAGES;
+      const int tr = t0 + t;   // position in the ring's sequence of tiles
+      const int s = tr % STAGES;
       int ok = 1;
       if (lane == 0) {
-        if (t >= STAGES && !mbar_wait(&empty[s], ((t / STAGES) - 1) & 1)) {
+        if (tr >= STAGES && !mbar_wait(&empty[s], ((tr / STAGES) - 1) & 1)) {
           abort_call(a);
           *cta_abort = 1;
         }
@@ -315,21 +329,13 @@ __device__ bool produce_kv(const CUtensorMap* tmK, const CUtensorMap* tmV, const
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) return false;
       uint8_t* kdst = ring + s * STAGE;
-      for (int b = 0; b < bpt; ++b) {
-        const int page = __shfl_sync(0xffffffffu, cur, tt * bpt + b);
-        if (lane == 0) {
-          const int k = kb + t * BN + b * box_rows;
-          const int prow = k % a.bs;
-#pragma unroll
-          for (int h = 0; h < HALVES; ++h) {
-            tma_load_4d(kdst + h * HALF + b * box_rows * 128, tmK, &full[s], h * 64, hk, prow,
-                        page);
-            tma_load_4d(kdst + TILE + h * HALF + b * box_rows * 128, tmV, &full[s], h * 64, hk,
-                        prow, page);
-          }
-        }
-      }
-      if (lane == 0) *issued = t + 1;
+      const int src = (tt * bpt + my_b) & 31;
+      const int page = __shfl_sync(0xffffffffu, cur, src);
+      const int prow = __shfl_sync(0xffffffffu, cur_row, src);
+      if (lane < nbox)
+        tma_load_4d(kdst + my_v * TILE + my_h * HALF + my_b * box_rows * 128, my_v ? tmV : tmK,
+                    &full[s], my_h * 64, hk, prow, page);
+      if (lane == 0) *issued = tr + 1;
     }
   }
   return true;
