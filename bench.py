@@ -41,7 +41,11 @@ METRIC = "paged-attn decode HBM GB/s + prefill TFLOPS on 1 GB300, % of roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
-SPLIT_KERNEL_SRC = os.path.join(ROOT, "paged_kv_varlen_attn_gb300", "csrc", "attn_split.cu")
+_CSRC = os.path.join(ROOT, "paged_kv_varlen_attn_gb300", "csrc")
+# Sources the split kernel's code comes from; the recorded DRAM traffic is
+# valid only while all of them are unchanged.
+SPLIT_KERNEL_SRCS = [os.path.join(_CSRC, f) for f in
+                     ("attn_split.cu", "device_common.cuh", "epilogue.cuh", "pa_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -102,9 +106,12 @@ def load_peaks():
             "source": "fallback"}
 
 
-def file_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def sources_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_traffic(kernel, workload):
@@ -115,7 +122,7 @@ def load_traffic(kernel, workload):
     with open(TRAFFIC_FILE) as f:
         t = json.load(f)
     e = t.get(kernel, {}).get(workload)
-    if not e or e.get("source_sha") != file_sha(SPLIT_KERNEL_SRC):
+    if not e or e.get("source_sha") != sources_sha(SPLIT_KERNEL_SRCS):
         return None
     return e.get("dram_bytes_per_launch")
 
