@@ -344,6 +344,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
   asm volatile("bar.sync 2, 128;" ::: "memory");
   if (!sh.flags[1]) return;
   __threadfence();
+  if (a.merge_parts) pdl_wait();   // the prefix pass's partials are complete
   combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, threadIdx.x, 128);
   if (threadIdx.x == 0) *counter = 0;   // ready for the next call
 }
@@ -365,6 +366,7 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   // dispatched in index order and the planner sorted the items longest first.
   const int item = static_cast<int>(blockIdx.x) / a.H_kv;
   const int hk = static_cast<int>(blockIdx.x) - item * a.H_kv;
+  pdl_enter(a.pdl_first);
   if (item >= a.header[0] || call_aborted(a)) return;
   const int4 it = a.items[item];
   const int seg = it.x, rt = it.y, j = it.z;
@@ -430,8 +432,18 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
   }
-  const dim3 grid(static_cast<unsigned>(items_bound) * static_cast<unsigned>(a.H_kv));
-  attn_split_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmK, tmV, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(items_bound) * static_cast<unsigned>(a.H_kv));
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_split_kernel<D>, tmK, tmV, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

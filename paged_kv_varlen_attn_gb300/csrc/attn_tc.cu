@@ -266,6 +266,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                                              ~static_cast<uintptr_t>(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(smem + C::OFF_BAR);
 
+  pdl_enter(a.pdl_first);
   if (static_cast<int>(blockIdx.x) >= a.header[1] || call_aborted(a)) return;
   const int hk = blockIdx.y;
   const int4 it = a.items[blockIdx.x];
@@ -410,6 +411,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (bars->last) {
         __threadfence();
+        if (a.merge_parts) pdl_wait();   // the prefix pass's partials are complete
         combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, tid, 256);
         if (tid == 0) *counter = 0;
       }
@@ -449,8 +451,18 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
   }
-  dim3 grid(items_bound, a.H_kv);
-  attn_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tmK, tmV, tmQ, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(items_bound, a.H_kv);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, tmK, tmV, tmQ, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -253,6 +253,25 @@ __host__ __device__ constexpr uint32_t mma_idesc_bf16(int M, int N, bool b_mn_ma
 
 namespace pa {
 
+// Programmatic dependent launch (griddepcontrol, sm_90 and later).
+// pdl_wait: block until the grids this one depends on have completed and
+// their writes are visible (a no-op for a grid launched without the
+// attribute). pdl_trigger: allow the dependent grid to be scheduled once every
+// block of this grid has executed it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Entry of an attention kernel: the first kernel after the planner waits in
+// every block (it reads the plan next); a later kernel waits only in its last
+// block, so that it cannot complete before its predecessor. Then the next
+// kernel of the call may be scheduled.
+__device__ __forceinline__ void pdl_enter(int pdl_first) {
+  const bool last = blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1;
+  if (pdl_first || last) pdl_wait();
+  pdl_trigger();
+}
+
 // A timeout anywhere in a launch sets the call's abort word; CTAs that start
 // later see it and return at once, so a failing launch ends quickly.
 __device__ __forceinline__ bool call_aborted(const AttnArgs& a) {

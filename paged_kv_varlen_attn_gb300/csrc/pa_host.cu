@@ -291,18 +291,25 @@ void set_class(AttnArgs& a, uint8_t* ws, const PassLayout& L, int c) {
   a.slot_rows = L.slot_rows[c];
 }
 
+// Launch the kernels of one pass. *first is set while no attention kernel of
+// the call has been launched since the planner; that kernel waits for the
+// plan in every block (see AttnArgs::pdl_first).
 pa_status launch_pass(const CommonAttn& c, const CUtensorMap& tmK, const CUtensorMap& tmV,
                       const CUtensorMap& tmQ, const AttnArgs& a, uint8_t* ws,
-                      const PassLayout& L) {
+                      const PassLayout& L, bool* first) {
   if (L.items_bound[1] > 0) {
     AttnArgs a1 = a;
     set_class(a1, ws, L, 1);
+    a1.pdl_first = *first ? 1 : 0;
+    *first = false;
     if (launch_attn_tc(tmK, tmV, tmQ, a1, L.items_bound[1], c.st) != cudaSuccess)
       return PA_ERR_CUDA;
   }
   if (L.items_bound[0] > 0) {
     AttnArgs a0 = a;
     set_class(a0, ws, L, 0);
+    a0.pdl_first = *first ? 1 : 0;
+    *first = false;
     if (launch_attn_split(tmK, tmV, a0, L.items_bound[0], c.st) != cudaSuccess)
       return PA_ERR_CUDA;
   }
@@ -434,7 +441,8 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
                       causal, 0);
   if (launch_plan(pp, 1, c.st) != cudaSuccess) return PA_ERR_CUDA;
   AttnArgs a = make_attn(c, ws, L, bt_stride, 0, causal, out, lse);
-  return launch_pass(c, tmK, tmV, tmQ, a, ws, L);
+  bool first = true;
+  return launch_pass(c, tmK, tmV, tmQ, a, ws, L, &first);
 }
 
 pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
@@ -515,7 +523,8 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
   if (launch_plan(pp, 2, c.st) != cudaSuccess) return PA_ERR_CUDA;
   AttnArgs pa_ = make_attn(c, ws, CL.prefix, 0, 0, 0, nullptr, nullptr);
   pa_.partials_only = 1;
-  st = launch_pass(c, tmK, tmV, tmQ, pa_, ws, CL.prefix);
+  bool first = true;
+  st = launch_pass(c, tmK, tmV, tmQ, pa_, ws, CL.prefix, &first);
   if (st != PA_OK) return st;
   AttnArgs pb = make_attn(c, ws, CL.suffix, bt_stride, pages, 1, out, lse);
   pb.merge_parts = 1;
@@ -526,7 +535,7 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
     pb.mp_part_o[k] = reinterpret_cast<const float*>(ws + CL.prefix.part_o[k]);
     pb.mp_slot_rows[k] = CL.prefix.slot_rows[k];
   }
-  return launch_pass(c, tmK, tmV, tmQ, pb, ws, CL.suffix);
+  return launch_pass(c, tmK, tmV, tmQ, pb, ws, CL.suffix, &first);
 }
 
 }  // extern "C"

@@ -101,6 +101,14 @@ struct AttnArgs {
   int slot_rows;
   int32_t* status;
   int box_rows;              // rows per TMA box (divides block_size and 64)
+  // Launch order inside one call. The kernels after the planner are launched
+  // as programmatic dependents of the kernel before them, so a grid can start
+  // while its predecessor drains. pdl_first = 1 for the first kernel after the
+  // planner: each block waits for the planner before reading the plan. For
+  // the later kernels the plan is already complete when they start (the first
+  // kernel signals its dependents only after its own wait), so only the
+  // grid's last block waits, which keeps the grids finishing in launch order.
+  int pdl_first;
 };
 
 // Host launchers (defined in the kernel translation units).

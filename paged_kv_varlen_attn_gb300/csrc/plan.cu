@@ -80,6 +80,9 @@ __device__ __forceinline__ int item_bucket(int s, int rt, int j, int4 g, int chu
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanPasses pp) {
   const PlanArgs& P = pp.p[blockIdx.x];
+  // The first attention kernel may be scheduled now; its blocks wait for
+  // this grid to complete before they read the plan.
+  pdl_trigger();
   __shared__ int sh[128];
   __shared__ unsigned long long shW[2];
   __shared__ int hist[2][kSizeBuckets];   // items per (class, size in key tiles)
