@@ -278,6 +278,49 @@ def bench_reference(args, rank, world):
     print(json.dumps(line))
 
 
+def timed_flushed(fn, n, flush, stream):
+    """Mean device time (ms) of fn over n launches, L2 flushed before each."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for i in range(n):
+        flush.fill_(i & 0xff)
+        evs[i][0].record(stream)
+        fn()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / n
+
+
+def row_figures(pa, wl, counts, dev, stream, scatter_fn, steps):
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    n = max(5, min(50, steps))
+    T, H, D = wl.q.shape
+    Tn = wl.k_new.shape[0]
+    out = {}
+    for _ in range(3):
+        scatter_fn()
+    ms = timed_flushed(scatter_fn, n, flush, stream)
+    b = counts["scatter_bytes"] + Tn * 8
+    out["reshape_and_cache"] = {"tokens": Tn, "bytes": b, "ms": ms, "gbs": b / (ms * 1e-3) / 1e9}
+    g = torch.Generator(device="cpu").manual_seed(7)
+    for name, tm in (("merge_attn_states", T), ("merge_attn_states_16k_tokens", 16384)):
+        oa = torch.randn((tm, H, D), generator=g).to(torch.bfloat16).to(dev)
+        ob = torch.randn((tm, H, D), generator=g).to(torch.bfloat16).to(dev)
+        la = (torch.randn((H, tm), generator=g) * 3).to(dev)
+        lb = (torch.randn((H, tm), generator=g) * 3).to(dev)
+        o = torch.empty_like(oa)
+        lo = torch.empty_like(la)
+
+        def merge():
+            pa.merge_attn_states(oa, la, ob, lb, out=o, out_lse=lo)
+        for _ in range(3):
+            merge()
+        ms = timed_flushed(merge, n, flush, stream)
+        b = 3 * tm * H * D * 2 + 3 * H * tm * 4
+        out[name] = {"tokens": tm, "bytes": b, "ms": ms, "gbs": b / (ms * 1e-3) / 1e9}
+    return out
+
+
 class DeviceBatch:
     """Device copies of one batch's per-step inputs, plus its outputs."""
 
@@ -463,6 +506,12 @@ def bench_ours(args, rank, world, local):
             ms = x0.elapsed_time(x1) / n
             sub[kind] = {"ms": ms, "gbs": c["attn_bytes"] / (ms * 1e-3) / 1e9,
                          "tflops": c["flops"] / (ms * 1e-3) / 1e12, "seqs": len(seqs)}
+    # ---- per-step figures of the standalone steps --------------------------
+    # The scatter of this step's new tokens (the first graph of a step) and
+    # pa_merge_attn_states on partial states of this batch's shape and of a
+    # 16,384-token batch, each launch timed alone after an L2 flush.
+    rows_fig = row_figures(pa, wl, counts, dev, stream, lambda: graphs[0].replay()
+                           if graphs is not None else scatter(main), args.steps)
     assert int(status.item()) == 0, f"device status bits {int(status.item())}"
 
     if rank != 0:
@@ -522,6 +571,9 @@ def bench_ours(args, rank, world, local):
     else:
         per_step = 3 + (1 if wl.max_seqlen_q * G > 64 else 0)
     line["gpu_launches"] = per_step * args.steps
+    for r in rows_fig.values():
+        r["frac_hbm"] = r["gbs"] / peaks["hbm_gbs"]
+    line["steps_standalone"] = rows_fig
     line["graph"] = graphs is not None
     line["clocks"] = clocks
     if not args.no_cpu_baseline:

@@ -43,6 +43,10 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
       const int rem = static_cast<int>(idx - t * 2 * vpt);
       const int which = rem >= vpt;            // 0: key, 1: value
       const int vi = rem - which * vpt;
+      // The source vector does not depend on the slot: both loads are in
+      // flight together.
+      const uint4* src = which ? value + t * vstride_v : key + t * kstride_v;
+      v[u] = __ldcs(src + vi);
       const int64_t slot = __ldg(slots + t);
       if (slot < 0) continue;                  // padding token
       if (slot >= num_slots) {
@@ -51,8 +55,6 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
       }
       const int64_t page = slot / bs;
       const int64_t row = slot - page * bs;
-      const uint4* src = which ? value + t * vstride_v : key + t * kstride_v;
-      v[u] = __ldcs(src + vi);
       uint4* pool = which ? vc : kc;
       dst[u] = pool + page * block_stride_v + row * vpt + vi;
     }

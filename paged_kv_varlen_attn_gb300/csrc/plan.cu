@@ -62,6 +62,7 @@ __device__ __forceinline__ int4 block_scan4(int4 v, int4& excl, int* sh /* [4 * 
 
 constexpr int kPlanThreads = 1024;
 constexpr int kSizeBuckets = 1024;
+constexpr int kPlanSmemSegs = 1024;   // segment tables kept in shared memory up to this many
 
 // Size bucket of work item (segment s, row tile rt, split j): the number of
 // 64-key tiles the attention kernel will process for it (capped).
@@ -78,15 +79,30 @@ __device__ __forceinline__ int item_bucket(int s, int rt, int j, int4 g, int chu
   return min(tiles, kSizeBuckets - 1);
 }
 
+// Segment owning combined item index idx: the last segment whose first item
+// (segsplit.w, items of both classes numbered in segment order) is <= idx.
+__device__ __forceinline__ int find_segment(const int4* spl, int nseg, int idx) {
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (spl[mid].w <= idx) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanPasses pp) {
-  const PlanArgs& P = pp.p[blockIdx.x];
   // The first attention kernel may be scheduled now; its blocks wait for
   // this grid to complete before they read the plan.
   pdl_trigger();
+  const PlanArgs& P = pp.p[blockIdx.x];
   __shared__ int sh[128];
   __shared__ unsigned long long shW[2];
-  __shared__ int hist[2][kSizeBuckets];   // items per (class, size in key tiles)
-  __shared__ int cursor[2][kSizeBuckets];
+  // Items per (class, size in key tiles); turned in place into the placement
+  // cursors of the size buckets.
+  __shared__ int hist[2][kSizeBuckets];
+  // Segment tables of this pass when they fit (else the global copies).
+  __shared__ int4 tab_geo[kPlanSmemSegs];
+  __shared__ int4 tab_spl[kPlanSmemSegs];
   uint8_t* ws = P.ws;
   int* header = reinterpret_cast<int*>(ws + P.L.header);
   int4* seg = reinterpret_cast<int4*>(ws + P.L.seg);
@@ -96,18 +112,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   int* counters0 = reinterpret_cast<int*>(ws + P.L.counters[0]);
   int* counters1 = reinterpret_cast<int*>(ws + P.L.counters[1]);
   const int nseg = P.single_segment ? 1 : P.num_segs;
+  const bool in_smem = nseg <= kPlanSmemSegs;
+  int4* geo_tab = in_smem ? tab_geo : seg;
+  int4* spl_tab = in_smem ? tab_spl : segsplit;
   const int G = P.G;
+  const int tid = threadIdx.x;
 
-  if (threadIdx.x < 2) shW[threadIdx.x] = 0ull;
-  for (int i = threadIdx.x; i < 2 * kSizeBuckets; i += blockDim.x) {
-    (&hist[0][0])[i] = 0;
-    (&cursor[0][0])[i] = 0;
+  // Inputs of this thread's first segment are fetched before the first
+  // barrier, so their latency overlaps the clearing of the histograms.
+  int q0 = 0, q1 = 0, used = 0;
+  if (!P.single_segment && tid < nseg) {
+    q0 = P.cu_seqlens_q[tid];
+    q1 = P.cu_seqlens_q[tid + 1];
+    used = P.seqused_k[tid];
   }
+  if (tid < 2) shW[tid] = 0ull;
+  for (int i = tid; i < 2 * kSizeBuckets; i += blockDim.x) (&hist[0][0])[i] = 0;
   __syncthreads();
 
   // Pass 1: segment geometry, validation, class, and total work per class.
   unsigned long long w0 = 0, w1 = 0;
-  for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
+  for (int s = tid; s < nseg; s += blockDim.x) {
     int q_start, q_len, kv;
     int bad = 0;
     if (P.single_segment) {
@@ -115,7 +140,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       q_len = P.total_q;
       kv = P.single_kv_len;
     } else {
-      const int q0 = P.cu_seqlens_q[s], q1 = P.cu_seqlens_q[s + 1];
+      if (s != tid) {
+        q0 = P.cu_seqlens_q[s];
+        q1 = P.cu_seqlens_q[s + 1];
+        used = P.seqused_k[s];
+      }
       q_start = q0;
       q_len = q1 - q0;
       if (q0 < 0 || q1 > P.total_q || q_len < 0 || q_len > P.max_q) {
@@ -123,7 +152,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         q_len = 0;
         q_start = 0;
       }
-      const int used = P.seqused_k[s];
       if (used < 0 || used > P.max_k) bad |= PA_DEV_BAD_SEQLEN;
       kv = used - P.kv_len_offset;
     }
@@ -142,14 +170,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const int nrt = (rows + (cls ? kRowsTc : kRowsSplit) - 1) / (cls ? kRowsTc : kRowsSplit);
     const unsigned long long w = static_cast<unsigned long long>(nrt) * static_cast<unsigned>(kv);
     if (cls) w1 += w; else w0 += w;
-    seg[s] = make_int4(q_start, q_len, kv, cls);
+    const int4 g = make_int4(q_start, q_len, kv, cls);
+    seg[s] = g;
+    if (in_smem) tab_geo[s] = g;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     w0 += __shfl_xor_sync(0xffffffffu, w0, o);
     w1 += __shfl_xor_sync(0xffffffffu, w1, o);
   }
-  if ((threadIdx.x & 31) == 0) {
+  if ((tid & 31) == 0 && (w0 | w1)) {
     atomicAdd(&shW[0], w0);
     atomicAdd(&shW[1], w1);
   }
@@ -166,21 +196,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     chunk_max[c] = static_cast<int>(L);
   }
 
-  // Pass 2: splits, item and slot offsets (block scans in chunks of the
-  // block size, carried across chunks), then the item lists.
+  // Pass 2: splits, then item and slot offsets by block scans (in chunks of
+  // the block size, carried across chunks). segsplit = (nsplit, first slot,
+  // chunk, first item in the numbering of both classes in segment order).
   int4 carry = make_int4(0, 0, 0, 0);
   for (int base = 0; base < nseg; base += blockDim.x) {
-    const int s = base + threadIdx.x;
-    int nsplit = 1, chunk = 0, nrt = 0, cls = 0;
+    const int s = base + tid;
+    int nsplit = 1, chunk = 0, cls = 0;
     int4 v = make_int4(0, 0, 0, 0);
     if (s < nseg) {
-      const int4 g = seg[s];
+      const int4 g = geo_tab[s];
       cls = g.w;
-      const int rows = g.y * G;
       const int R = cls ? kRowsTc : kRowsSplit;
-      nrt = (rows + R - 1) / R;
+      const int nrt = (g.y * G + R - 1) / R;
       const int kv = g.z;
-      const int L = chunk_max[cls];
+      const int L = cls ? chunk_max[1] : chunk_max[0];
       if (kv > 0) {
         nsplit = (kv + L - 1) / L;
         chunk = (kv + nsplit - 1) / nsplit;
@@ -197,57 +227,63 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     int4 ex;
     const int4 tot = block_scan4(v, ex, sh);
     if (s < nseg) {
-      const int item_base = cls ? carry.y + ex.y : carry.x + ex.x;
       const int slot_base = cls ? carry.w + ex.w : carry.z + ex.z;
-      segsplit[s] = make_int4(nsplit, slot_base, chunk, item_base);
-      for (int rt = 0; rt < nrt; ++rt)
-        for (int j = 0; j < nsplit; ++j)
-          atomicAdd(&hist[cls][item_bucket(s, rt, j, seg[s], chunk, G, P.causal)], 1);
-      if (nsplit > 1 || P.partials_only) {
-        int* counters = cls ? counters1 : counters0;
-        const int sbound = cls ? P.slots_bound1 : P.slots_bound0;
-        for (int rt = 0; rt < nrt; ++rt) {
-          const int grp = slot_base + rt * nsplit;
-          if (grp + nsplit <= sbound)
-            for (int hk = 0; hk < P.H_kv; ++hk) counters[grp * P.H_kv + hk] = 0;
-        }
-      }
+      const int first = carry.x + carry.y + ex.x + ex.y;
+      const int4 sp = make_int4(nsplit, slot_base, chunk, first);
+      segsplit[s] = sp;
+      if (in_smem) tab_spl[s] = sp;
     }
     carry.x += tot.x;
     carry.y += tot.y;
     carry.z += tot.z;
     carry.w += tot.w;
   }
-  // Longest items first: offsets of the size buckets in descending order
-  // (one block scan over the buckets), then every item is placed in its
-  // bucket. The hardware dispatches blocks in order, so the last wave holds
-  // the shortest items. The order inside a bucket does not affect results.
   __syncthreads();
-  {
-    static_assert(kSizeBuckets == kPlanThreads, "one bucket per planner thread");
-    const int b = kSizeBuckets - 1 - static_cast<int>(threadIdx.x);
-    int4 ex;
-    block_scan4(make_int4(hist[0][b], hist[1][b], 0, 0), ex, sh);
-    cursor[0][b] = ex.x;
-    cursor[1][b] = ex.y;
-  }
-  __syncthreads();
-  for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
-    const int4 g = seg[s];
-    const int4 ss = segsplit[s];
-    const int cls = g.w;
-    const int R = cls ? kRowsTc : kRowsSplit;
-    const int nrt = (g.y * G + R - 1) / R;
-    int4* items = cls ? items1 : items0;
-    const int bound = cls ? P.items_bound1 : P.items_bound0;
-    for (int rt = 0; rt < nrt; ++rt) {
-      for (int j = 0; j < ss.x; ++j) {
-        const int idx = atomicAdd(&cursor[cls][item_bucket(s, rt, j, g, ss.z, G, P.causal)], 1);
-        if (idx < bound) items[idx] = make_int4(s, rt, j, 0);
-      }
+  const int n_all = carry.x + carry.y;
+
+  // Pass 3, one thread per work item: size histogram (for the longest-first
+  // order) and the cleared combine counter of each split group.
+  for (int idx = tid; idx < n_all; idx += blockDim.x) {
+    const int s = find_segment(spl_tab, nseg, idx);
+    const int4 sp = spl_tab[s];
+    const int4 g = geo_tab[s];
+    const int local = idx - sp.w;
+    const int rt = local / sp.x, j = local - rt * sp.x;
+    atomicAdd(&hist[g.w][item_bucket(s, rt, j, g, sp.z, G, P.causal)], 1);
+    if (j == 0 && (sp.x > 1 || P.partials_only)) {
+      const int grp = sp.y + rt * sp.x;
+      const int sbound = g.w ? P.slots_bound1 : P.slots_bound0;
+      if (grp + sp.x <= sbound)
+        for (int hk = 0; hk < P.H_kv; ++hk) (g.w ? counters1 : counters0)[grp * P.H_kv + hk] = 0;
     }
   }
-  if (threadIdx.x == 0) {
+  __syncthreads();
+  // Longest items first: offsets of the size buckets in descending order
+  // (one block scan over the buckets). The hardware dispatches blocks in
+  // order, so the last wave holds the shortest items. The order inside a
+  // bucket does not affect results.
+  {
+    static_assert(kSizeBuckets == kPlanThreads, "one bucket per planner thread");
+    const int b = kSizeBuckets - 1 - tid;
+    int4 ex;
+    block_scan4(make_int4(hist[0][b], hist[1][b], 0, 0), ex, sh);
+    hist[0][b] = ex.x;
+    hist[1][b] = ex.y;
+  }
+  __syncthreads();
+  // Pass 4, one thread per work item: place it at its bucket's cursor.
+  for (int idx = tid; idx < n_all; idx += blockDim.x) {
+    const int s = find_segment(spl_tab, nseg, idx);
+    const int4 sp = spl_tab[s];
+    const int4 g = geo_tab[s];
+    const int local = idx - sp.w;
+    const int rt = local / sp.x, j = local - rt * sp.x;
+    const int cls = g.w;
+    const int pos = atomicAdd(&hist[cls][item_bucket(s, rt, j, g, sp.z, G, P.causal)], 1);
+    if (pos < (cls ? P.items_bound1 : P.items_bound0))
+      (cls ? items1 : items0)[pos] = make_int4(s, rt, j, 0);
+  }
+  if (tid == 0) {
     int n0 = carry.x, n1 = carry.y;
     // Cannot happen for inputs within the stated bounds; refuse the work
     // rather than run past the reserved workspace.
