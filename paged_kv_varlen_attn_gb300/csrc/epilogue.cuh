@@ -7,44 +7,61 @@
 
 namespace pa {
 
-// Cascade: merge the state (o[0..n) at columns col.., lse) of row (token tok,
-// head h) with the prefix pass's partial states of the same row -- one per
-// split of the shared prefix -- weighted by their LSEs. lse becomes the merged
-// LSE. The prefix pass planned one segment holding every query token, so the
-// row's packed index there is tok * G + (h % G).
-__device__ __forceinline__ void merge_prefix(const AttnArgs& a, int h, int tok, int col,
-                                             float& lse, float* o, int n) {
-  const int4 g0 = a.mp_seg[0];
-  const int4 s0 = a.mp_segsplit[0];
-  const int cls = g0.w;
-  const int rows_per_item = cls ? kRowsTc : kRowsSplit;
-  const int G = a.G;
-  const int hk = h / G;
-  const int pr = tok * G + (h - hk * G);
-  const int rt = pr / rows_per_item, rl = pr - rt * rows_per_item;
-  const int nsp = s0.x, base = s0.y + rt * nsp;
-  const float* plse = a.mp_part_lse[cls];
-  const float* po = a.mp_part_o[cls];
-  const int64_t srows = a.mp_slot_rows[cls];
-  float mx = lse;
-  for (int j = 0; j < nsp; ++j)
-    mx = fmaxf(mx, __ldcg(plse + (static_cast<int64_t>(base + j) * a.H_kv + hk) * srows + rl));
-  if (mx == -INFINITY) {
-    for (int i = 0; i < n; ++i) o[i] = 0.f;
-    return;
+// Partial states are merged in batches of kBatch whose loads are all issued
+// before any is used, so a merge costs a few memory latencies rather than one
+// per state.
+constexpr int kBatch = 4;
+
+// Running LSE-weighted merge of (o[0..4), lse) with one batch of partial
+// states given by their LSEs l[] and values v[] (n <= kBatch valid):
+// the maximum moves to the batch's, both sides are rescaled, and sw sums the
+// weights. o stays unnormalised until the end.
+__device__ __forceinline__ void merge_batch(float& mx, float& sw, float (&o)[4],
+                                            const float (&l)[kBatch], const float4 (&v)[kBatch],
+                                            int n) {
+  float bm = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u)
+    if (u < n) bm = fmaxf(bm, l[u]);
+  if (bm == -INFINITY) return;
+  const float nm = fmaxf(mx, bm);
+  const float r = mx == -INFINITY ? 0.f : fast_exp2((mx - nm) * kLog2e);
+  sw *= r;
+#pragma unroll
+  for (int x = 0; x < 4; ++x) o[x] *= r;
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    if (u >= n) continue;
+    const float w = fast_exp2((l[u] - nm) * kLog2e);
+    sw += w;
+    o[0] += w * v[u].x;
+    o[1] += w * v[u].y;
+    o[2] += w * v[u].z;
+    o[3] += w * v[u].w;
   }
-  float tot = fast_exp2((lse - mx) * kLog2e);
-  for (int i = 0; i < n; ++i) o[i] *= tot;
-  for (int j = 0; j < nsp; ++j) {
-    const int64_t row = (static_cast<int64_t>(base + j) * a.H_kv + hk) * srows + rl;
-    const float w = fast_exp2((__ldcg(plse + row) - mx) * kLog2e);
-    tot += w;
-    const float* pj = po + row * a.D + col;
-    for (int i = 0; i < n; ++i) o[i] += w * __ldcg(pj + i);
+  mx = nm;
+}
+
+// Merge the n partial states of one row held at rows row(j) = first + j*step
+// of (lse_base, o_base + col) into the running (mx, sw, o).
+__device__ __forceinline__ void merge_states(float& mx, float& sw, float (&o)[4],
+                                             const float* lse_base, const float* o_base,
+                                             int64_t first, int64_t step, int n, int D,
+                                             int col) {
+  for (int j0 = 0; j0 < n; j0 += kBatch) {
+    float l[kBatch];
+    float4 v[kBatch];
+    const int m = min(kBatch, n - j0);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (u < m) {
+        const int64_t row = first + static_cast<int64_t>(j0 + u) * step;
+        l[u] = __ldcg(lse_base + row);
+        v[u] = __ldcg(reinterpret_cast<const float4*>(o_base + row * D + col));
+      }
+    }
+    merge_batch(mx, sw, o, l, v, m);
   }
-  const float inv = 1.f / tot;
-  for (int i = 0; i < n; ++i) o[i] *= inv;
-  lse = mx + fast_log2(tot) * kLn2;
 }
 
 // Write 4 final values of a row as bf16.
@@ -57,42 +74,56 @@ __device__ __forceinline__ int64_t slot_row(const AttnArgs& a, int slot, int hk,
   return (static_cast<int64_t>(slot) * a.H_kv + hk) * a.slot_rows + rl;
 }
 
-// The last CTA of a split group merges the nsplit partial states of its R
-// rows in split order (deterministic) and writes the final output. Threads
-// tid in [0, nthreads) share the work, 4 columns each.
+// The last CTA of a split group (or the cascade combine kernel) merges the
+// nsplit partial states of its R rows -- and, in a cascade, the prefix pass's
+// states of the same rows -- and writes the final output. Threads tid in
+// [0, nthreads) share the work, 4 columns each. The merge is associative and
+// its order is fixed, so results are deterministic.
 template <int D>
 __device__ void combine_splits(const AttnArgs& a, int grp, int nsplit, int hk, int R, int row0,
                                int q_start, int tid, int nthreads) {
   constexpr int C4 = D / 4;
   const int G = a.G;
+  // Prefix pass geometry (cascade): one segment holding every query token.
+  int p_nsp = 0, p_base = 0, p_rows = 1, p_cls = 0;
+  if (a.merge_parts) {
+    const int4 g0 = a.mp_seg[0];
+    const int4 s0 = a.mp_segsplit[0];
+    p_cls = g0.w;
+    p_rows = p_cls ? kRowsTc : kRowsSplit;
+    p_nsp = s0.x;
+    p_base = s0.y;
+  }
+  const int64_t own_step = static_cast<int64_t>(a.H_kv) * a.slot_rows;
   for (int idx = tid; idx < R * C4; idx += nthreads) {
     const int rl = idx / C4, c4 = idx - rl * C4;
     const int pr = row0 + rl;
     const int i = pr / G;
     const int tk = q_start + i, hh = hk * G + (pr - i * G);
-    float mx = -INFINITY;
-    for (int jj = 0; jj < nsplit; ++jj) mx = fmaxf(mx, __ldcg(a.part_lse + slot_row(a, grp + jj, hk, rl)));
+    float mx = -INFINITY, sw = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    merge_states(mx, sw, acc, a.part_lse, a.part_o, slot_row(a, grp, hk, rl), own_step, nsplit,
+                 D, c4 * 4);
+    if (a.merge_parts) {
+      // The row's packed index in the prefix pass is tk * G + (hh % G).
+      const int ppr = tk * G + (hh - hk * G);
+      const int prt = ppr / p_rows, prl = ppr - prt * p_rows;
+      const int64_t srows = a.mp_slot_rows[p_cls];
+      const int64_t first = (static_cast<int64_t>(p_base + prt * p_nsp) * a.H_kv + hk) * srows + prl;
+      merge_states(mx, sw, acc, a.mp_part_lse[p_cls], a.mp_part_o[p_cls], first,
+                   static_cast<int64_t>(a.H_kv) * srows, p_nsp, D, c4 * 4);
+    }
     float lse_r = -INFINITY;
-    if (mx != -INFINITY) {
-      float sw = 0.f;
-      for (int jj = 0; jj < nsplit; ++jj) {
-        const int64_t sr = slot_row(a, grp + jj, hk, rl);
-        const float w = fast_exp2((__ldcg(a.part_lse + sr) - mx) * kLog2e);
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + sr * D) + c4);
-        sw += w;
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2] += w * v.z;
-        acc[3] += w * v.w;
-      }
+    if (sw > 0.f) {
       const float inv = 1.f / sw;
 #pragma unroll
       for (int x = 0; x < 4; ++x) acc[x] *= inv;
       lse_r = mx + fast_log2(sw) * kLn2;
+    } else {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) acc[x] = 0.f;
     }
     const int64_t obase = (static_cast<int64_t>(tk) * a.H + hh) * D + c4 * 4;
-    if (a.merge_parts) merge_prefix(a, hh, tk, c4 * 4, lse_r, acc, 4);
     store4(a, obase, acc);
     if (a.lse && c4 == 0) a.lse[static_cast<int64_t>(hh) * a.lse_stride + tk] = lse_r;
   }

@@ -78,6 +78,8 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
   L.segsplit = off;               off = align_up(off + static_cast<size_t>(d.num_segs) * 16);
   L.items[0] = off;               off = align_up(off + static_cast<size_t>(L.items_bound[0]) * 16);
   L.items[1] = off;               off = align_up(off + static_cast<size_t>(L.items_bound[1]) * 16);
+  L.groups[0] = off;              off = align_up(off + static_cast<size_t>(d.all_partial ? L.items_bound[0] : 0) * 16);
+  L.groups[1] = off;              off = align_up(off + static_cast<size_t>(d.all_partial ? L.items_bound[1] : 0) * 16);
   for (int c = 0; c < 2; ++c) {
     const size_t slot_rows = static_cast<size_t>(L.slots_bound[c]) * d.H_kv * L.slot_rows[c];
     L.counters[c] = off;          off = align_up(off + static_cast<size_t>(L.slots_bound[c]) * d.H_kv * 4);
@@ -285,6 +287,7 @@ bool encode_q_map(CUtensorMap* map, const void* q, int D, int H, int total_q, in
 // Point a kernel's arguments at its class's work list and partial-slot pool.
 void set_class(AttnArgs& a, uint8_t* ws, const PassLayout& L, int c) {
   a.items = reinterpret_cast<const int4*>(ws + L.items[c]);
+  a.groups = reinterpret_cast<const int4*>(ws + L.groups[c]);
   a.counters = reinterpret_cast<int*>(ws + L.counters[c]);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse[c]);
   a.part_o = reinterpret_cast<float*>(ws + L.part_o[c]);
@@ -520,22 +523,38 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
   // row is merged with pass A's partial states of the same row.
   pp.p[1] = make_plan(c, ws, CL.suffix, 0, 0, P,
                       cap > 0x7fffffff ? 0x7fffffff : static_cast<int>(cap), 1, 1, 1);
+  pp.p[1].make_groups = 1;
   if (launch_plan(pp, 2, c.st) != cudaSuccess) return PA_ERR_CUDA;
   AttnArgs pa_ = make_attn(c, ws, CL.prefix, 0, 0, 0, nullptr, nullptr);
   pa_.partials_only = 1;
   bool first = true;
   st = launch_pass(c, tmK, tmV, tmQ, pa_, ws, CL.prefix, &first);
   if (st != PA_OK) return st;
+  // Pass B: each sequence, causal, its own keys from position P on; every
+  // work item leaves its partial state too, so no block of either pass waits
+  // for the other.
   AttnArgs pb = make_attn(c, ws, CL.suffix, bt_stride, pages, 1, out, lse);
-  pb.merge_parts = 1;
-  pb.mp_seg = reinterpret_cast<const int4*>(ws + CL.prefix.seg);
-  pb.mp_segsplit = reinterpret_cast<const int4*>(ws + CL.prefix.segsplit);
+  pb.partials_only = 1;
+  st = launch_pass(c, tmK, tmV, tmQ, pb, ws, CL.suffix, &first);
+  if (st != PA_OK) return st;
+  // Combine: each row of pass B merges its own partial states with pass A's.
+  AttnArgs cb = pb;
+  cb.partials_only = 0;
+  cb.merge_parts = 1;
+  cb.mp_seg = reinterpret_cast<const int4*>(ws + CL.prefix.seg);
+  cb.mp_segsplit = reinterpret_cast<const int4*>(ws + CL.prefix.segsplit);
   for (int k = 0; k < 2; ++k) {
-    pb.mp_part_lse[k] = reinterpret_cast<const float*>(ws + CL.prefix.part_lse[k]);
-    pb.mp_part_o[k] = reinterpret_cast<const float*>(ws + CL.prefix.part_o[k]);
-    pb.mp_slot_rows[k] = CL.prefix.slot_rows[k];
+    cb.mp_part_lse[k] = reinterpret_cast<const float*>(ws + CL.prefix.part_lse[k]);
+    cb.mp_part_o[k] = reinterpret_cast<const float*>(ws + CL.prefix.part_o[k]);
+    cb.mp_slot_rows[k] = CL.prefix.slot_rows[k];
   }
-  return launch_pass(c, tmK, tmV, tmQ, pb, ws, CL.suffix, &first);
+  AttnArgs c0 = cb, c1 = cb;
+  set_class(c0, ws, CL.suffix, 0);
+  set_class(c1, ws, CL.suffix, 1);
+  if (launch_cascade_combine(c0, c1, CL.suffix.items_bound[0], CL.suffix.items_bound[1], c.st) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
 }
 
 }  // extern "C"

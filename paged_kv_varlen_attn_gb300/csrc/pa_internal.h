@@ -18,16 +18,24 @@ constexpr int kRowsSplit = 64;     // split-KV kernel (decode and short queries)
 constexpr int kRowsTc = 256;       // tcgen05 prefill kernel: two 128-row Q tiles
 constexpr int kTcTileRows = 128;   // rows of one Q tile (the MMA M dimension)
 constexpr int kKeyTile = 64;       // keys per pipeline stage / split granularity
-constexpr int kMinChunk = 256;     // smallest KV split (keys)
+// Smallest KV split (keys) per class. A split-KV block spends a few
+// microseconds before its first tile arrives, about the time it takes to
+// stream 8 key tiles, so splits shorter than 512 keys cost more than they
+// gain; prefill tiles are compute-bound and split down to 256 keys.
+constexpr int kMinChunkSplit = 512;   // split-KV kernel
+constexpr int kMinChunkTc = 256;      // prefill kernel
 constexpr int kMaxDevices = 64;    // per-device host caches
 
 // Work planned for one pass (one attention launch pair) lives in the
 // workspace. Device-side layout, all offsets 256-byte aligned.
 struct PassLayout {
-  size_t header;       // int[64]: [0] items class 0, [1] items class 1, [2] abort word
+  size_t header;       // int[64]: [0] items class 0, [1] items class 1, [2] abort word,
+                       // [4], [5]: row groups of class 0 / 1 (when the pass lists them)
   size_t seg;          // int4[num_segs]: q_start, q_len, kv_len, class
-  size_t segsplit;     // int4[num_segs]: nsplit, slot_base (in its class pool), chunk, item_base
+  size_t segsplit;     // int4[num_segs]: nsplit, slot_base (in its class pool), chunk,
+                       // first item in the numbering of both classes in segment order
   size_t items[2];     // int4[items_bound[c]]: seg, row tile, split index, 0
+  size_t groups[2];    // int4[items_bound[c]]: seg, row tile, 0, 0 -- one per row tile
   size_t counters[2];  // int[slots_bound[c] * H_kv]
   size_t part_lse[2];  // float[slots_bound[c] * H_kv * slot_rows[c]]
   size_t part_o[2];    // float[slots_bound[c] * H_kv * slot_rows[c] * D]
@@ -59,6 +67,7 @@ struct PlanArgs {
   int32_t* status;
   int check_cascade;     // flag q_len > kv_len (suffix pass of cascade)
   int partials_only;     // every item gets a partial-state slot and a zeroed counter (cascade)
+  int make_groups;       // list the (segment, row tile) groups of each class (cascade suffix)
 };
 
 struct PlanPasses {
@@ -95,6 +104,7 @@ struct AttnArgs {
   const int4* seg;
   const int4* segsplit;
   const int4* items;
+  const int4* groups;        // this class's row groups (combine kernel)
   int* counters;             // this kernel's class pool
   float* part_lse;
   float* part_o;
@@ -122,6 +132,12 @@ cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* 
 cudaError_t launch_plan(const PlanPasses& passes, int npasses, cudaStream_t st);
 cudaError_t launch_attn_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
                               int items_bound, cudaStream_t st);
+// Final combine of a cascade: for every row group of the suffix pass (both
+// classes), merge its split partial states with the prefix pass's partial
+// states and write out / lse. a0, a1: the suffix pass's arguments pointed at
+// class 0 / 1 (merge_parts set); gb0, gb1: group bounds per class.
+cudaError_t launch_cascade_combine(const AttnArgs& a0, const AttnArgs& a1, int gb0, int gb1,
+                                   cudaStream_t st);
 cudaError_t launch_attn_tc(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
                            const AttnArgs& a, int items_bound, cudaStream_t st);
 

@@ -11,7 +11,7 @@
 // i.e. decode and short queries), 1: the tensor-core prefill kernel -- cuts the
 // packed rows into row tiles, and splits the keys into equal chunks so that
 // each class has about `target` work items per KV head. Chunk length
-//   L = max(kMinChunk, ceil(W / target)) rounded up to kKeyTile,
+//   L = max(min chunk of the class, ceil(W / target)) rounded up to kKeyTile,
 // where W = sum over segments of (row tiles x keys). Then
 //   sum of items <= target + sum of row tiles, and
 //   slots (items of segments split more than once) <= 2 * target,
@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   // Segment tables of this pass when they fit (else the global copies).
   __shared__ int4 tab_geo[kPlanSmemSegs];
   __shared__ int4 tab_spl[kPlanSmemSegs];
+  __shared__ int ngroups[2];
   uint8_t* ws = P.ws;
   int* header = reinterpret_cast<int*>(ws + P.L.header);
   int4* seg = reinterpret_cast<int4*>(ws + P.L.seg);
@@ -111,6 +112,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   int4* items1 = reinterpret_cast<int4*>(ws + P.L.items[1]);
   int* counters0 = reinterpret_cast<int*>(ws + P.L.counters[0]);
   int* counters1 = reinterpret_cast<int*>(ws + P.L.counters[1]);
+  int4* groups0 = reinterpret_cast<int4*>(ws + P.L.groups[0]);
+  int4* groups1 = reinterpret_cast<int4*>(ws + P.L.groups[1]);
   const int nseg = P.single_segment ? 1 : P.num_segs;
   const bool in_smem = nseg <= kPlanSmemSegs;
   int4* geo_tab = in_smem ? tab_geo : seg;
@@ -126,7 +129,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     q1 = P.cu_seqlens_q[tid + 1];
     used = P.seqused_k[tid];
   }
-  if (tid < 2) shW[tid] = 0ull;
+  if (tid < 2) {
+    shW[tid] = 0ull;
+    ngroups[tid] = 0;
+  }
   for (int i = tid; i < 2 * kSizeBuckets; i += blockDim.x) (&hist[0][0])[i] = 0;
   __syncthreads();
 
@@ -190,7 +196,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   for (int c = 0; c < 2; ++c) {
     const unsigned long long W = shW[c];
     unsigned long long L = (W + target[c] - 1) / (target[c] > 0 ? target[c] : 1);
-    if (L < static_cast<unsigned long long>(kMinChunk)) L = kMinChunk;
+    const int min_chunk = c ? kMinChunkTc : kMinChunkSplit;
+    if (L < static_cast<unsigned long long>(min_chunk)) L = min_chunk;
     L = (L + kKeyTile - 1) / kKeyTile * kKeyTile;
     if (L > 0x40000000ull) L = 0x40000000ull;
     chunk_max[c] = static_cast<int>(L);
@@ -242,7 +249,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   const int n_all = carry.x + carry.y;
 
   // Pass 3, one thread per work item: size histogram (for the longest-first
-  // order) and the cleared combine counter of each split group.
+  // order), the cleared combine counter of each split group, and (cascade
+  // suffix) the list of row groups, one per (segment, row tile).
   for (int idx = tid; idx < n_all; idx += blockDim.x) {
     const int s = find_segment(spl_tab, nseg, idx);
     const int4 sp = spl_tab[s];
@@ -255,6 +263,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       const int sbound = g.w ? P.slots_bound1 : P.slots_bound0;
       if (grp + sp.x <= sbound)
         for (int hk = 0; hk < P.H_kv; ++hk) (g.w ? counters1 : counters0)[grp * P.H_kv + hk] = 0;
+    }
+    if (j == 0 && P.make_groups) {
+      const int gpos = atomicAdd(&ngroups[g.w], 1);
+      if (gpos < (g.w ? P.items_bound1 : P.items_bound0))
+        (g.w ? groups1 : groups0)[gpos] = make_int4(s, rt, 0, 0);
     }
   }
   __syncthreads();
@@ -298,6 +311,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     header[0] = n0;
     header[1] = n1;
     header[2] = 0;   // abort word of this call
+    header[4] = n0 ? ngroups[0] : 0;
+    header[5] = n1 ? ngroups[1] : 0;
   }
 }
 

@@ -141,6 +141,8 @@ CASES = [
     (109, 2, 8, 2, 128, 16, 300, 1100, True, 0.0),    # multi-tile causal prefill, prior context
     (110, 2, 16, 2, 64, 32, 260, 700, False, 0.0),    # multi-tile non-causal, D = 64
     (111, 3, 32, 8, 128, 128, 200, 900, True, 0.0),   # GQA 4, block 128
+    (112, 4, 8, 2, 128, 16, 1, 6000, True, 1.0),      # decode, long keys: many KV splits
+    (113, 3, 16, 2, 64, 32, 8, 4000, True, 0.0),      # up to 64 packed rows, split KV
 ]
 
 
