@@ -219,10 +219,20 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   const bool any = ok && l > 0.f;
   const float inv_l = any ? 1.f / l : 0.f;
   float lse_nat = any ? (m_use + fast_log2(l)) * kLn2 : -INFINITY;
-  const int64_t obase = (static_cast<int64_t>(tok) * a.H + head) * D;
   const int slot = slot_base + rt * nsplit + j;
   const int64_t srow = slot_row(a, slot, hk, rl);
-#pragma unroll
+  const bool partial = nsplit > 1 || a.partials_only || a.merge_parts;
+  // The output leaves through shared memory: each warp stages 32 rows x 32
+  // columns in its quarter of Q tile X (free once the last S_X product has
+  // completed, which the pv_done wait above implies) and stores them so that
+  // every instruction writes whole row segments (fp32 partial rows of 128 B,
+  // bf16 output rows of 64 B) instead of one 8- or 16-byte piece per row.
+  // 16-byte granules are XOR-swizzled by row to keep the shared-memory
+  // accesses free of bank conflicts.
+  uint8_t* stage = smem + C::OFF_Q + X * C::Q_TILE + quarter * (C::Q_TILE / 4);
+  const int rl0 = X * C::BM + quarter * 32;          // first row of this warp in the item
+  const int64_t srow0 = slot_row(a, slot, hk, rl0);  // rows of a slot are consecutive
+#pragma unroll 1
   for (int c = 0; c < D / 32; ++c) {
     uint32_t v[32];
     if (ntiles > 0 && ok) {
@@ -232,20 +242,44 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] = 0u;
     }
-    if (!rvalid) continue;
+    if (partial) {
 #pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-      float o4[4];
+      for (int g = 0; g < 8; ++g)
+        *reinterpret_cast<float4*>(stage + lane * 128 + ((g ^ (lane & 7)) << 4)) =
+            make_float4(__uint_as_float(v[4 * g]) * inv_l, __uint_as_float(v[4 * g + 1]) * inv_l,
+                        __uint_as_float(v[4 * g + 2]) * inv_l, __uint_as_float(v[4 * g + 3]) * inv_l);
+      __syncwarp();
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o4[e] = __uint_as_float(v[q4 * 4 + e]) * inv_l;
-      const int col = c * 32 + q4 * 4;
-      if (nsplit > 1 || a.partials_only || a.merge_parts) {
-        __stcg(reinterpret_cast<float4*>(a.part_o + srow * D + col),
-               make_float4(o4[0], o4[1], o4[2], o4[3]));
-      } else {
-        store4(a, obase + col, o4);
+      for (int i = 0; i < 8; ++i) {
+        const int r = i * 4 + (lane >> 3), g = lane & 7;
+        if (rl0 + r < R)
+          __stcg(reinterpret_cast<float4*>(a.part_o + (srow0 + r) * D + c * 32 + g * 4),
+                 *reinterpret_cast<const float4*>(stage + r * 128 + ((g ^ (r & 7)) << 4)));
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint4 pk;
+        pk.x = pack_bf16(__uint_as_float(v[8 * g]) * inv_l, __uint_as_float(v[8 * g + 1]) * inv_l);
+        pk.y = pack_bf16(__uint_as_float(v[8 * g + 2]) * inv_l, __uint_as_float(v[8 * g + 3]) * inv_l);
+        pk.z = pack_bf16(__uint_as_float(v[8 * g + 4]) * inv_l, __uint_as_float(v[8 * g + 5]) * inv_l);
+        pk.w = pack_bf16(__uint_as_float(v[8 * g + 6]) * inv_l, __uint_as_float(v[8 * g + 7]) * inv_l);
+        *reinterpret_cast<uint4*>(stage + lane * 64 + ((g ^ ((lane >> 1) & 3)) << 4)) = pk;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = i * 8 + (lane >> 2), g = lane & 3;
+        if (rl0 + r < R) {
+          const int prr = row0 + rl0 + r;
+          const int tr = prr / G;
+          const int64_t ob = (static_cast<int64_t>(q_start + tr) * a.H + hk * G + (prr - tr * G)) * D;
+          *reinterpret_cast<uint4*>(a.out + ob + c * 32 + g * 8) =
+              *reinterpret_cast<const uint4*>(stage + r * 64 + ((g ^ ((r >> 1) & 3)) << 4));
+        }
       }
     }
+    __syncwarp();
   }
   if (rvalid) {
     if (nsplit > 1 || a.partials_only || a.merge_parts) {
