@@ -195,7 +195,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const unsigned long long W = shW[c];
-    unsigned long long L = (W + target[c] - 1) / (target[c] > 0 ? target[c] : 1);
+    const unsigned tg = target[c] > 0 ? static_cast<unsigned>(target[c]) : 1u;
+    // ceil(W / target): a 32-bit division unless W needs more bits (a 64-bit
+    // division is a long software sequence).
+    unsigned long long L;
+    if (W == 0) L = 0;
+    else if (W < 0xffffffffull - tg) L = (static_cast<unsigned>(W) + tg - 1) / tg;
+    else L = (W + tg - 1) / tg;
     const int min_chunk = c ? kMinChunkTc : kMinChunkSplit;
     if (L < static_cast<unsigned long long>(min_chunk)) L = min_chunk;
     L = (L + kKeyTile - 1) / kKeyTile * kKeyTile;
