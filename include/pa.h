@@ -199,7 +199,6 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
  * pa_varlen_fwd_noalloc -- pa_varlen_fwd for callers that cannot allocate
  * device memory, so cannot provide a workspace: for example a serving engine
  * whose allocator reserved all device memory for its page pool at start-up,
- * code running while a stream is captured in a mode that forbids cudaMalloc,
  * or a latency-critical path where cudaMalloc's implicit device
  * synchronisation is not acceptable. The web pages have no counterpart to
  * this entry point; it only changes where the scratch lives.
