@@ -31,11 +31,15 @@
 // operands: per 128-key tile the tensor core reads Q and K (S) and V (P V)
 // from shared memory and nothing else. While one warpgroup computes its
 // softmax the tensor core runs the other tile's MMAs.
-// S_X of the next tile overwrites P_X, so it is issued only after P_X V has
-// completed (its tcgen05.commit barrier); that also means O_X is final for the
-// softmax's lazy rescale: a row's reference max only moves when its max grows
-// by more than 2^8, so most tiles need no TMEM round trip for O (exact, since
-// O and the row sum always share the same reference).
+// The MMA issuer orders each tile as P_A V, S_A(next), P_B V, S_B(next): S_X
+// of the next tile overwrites P_X, and the tensor core executes one thread's
+// MMAs in issue order, so it runs after P_X V has read P_X; tile A's softmax
+// thus starts its next tile without waiting for tile B's. The commit after
+// S_X(next) covers P_X V, so O_X is final for the softmax's lazy rescale: a
+// row's reference max only moves when its max grows by more than 2^8, so
+// most tiles need no TMEM round trip for O (exact, since O and the row sum
+// always share the same reference). K and V of a ring stage have separate
+// barriers, so K(t) is refilled as soon as both S(t) are done.
 // Causal tile skipping: the key range of an item is clamped to the last key
 // its last row may see, so tiles above the diagonal are never loaded.
 // Every mbarrier wait is bounded; on a timeout the CTA records
@@ -76,8 +80,8 @@ static_assert(kRowsTc == 256, "a prefill work item is two 128-row Q tiles");
 
 struct TcBars {
   uint64_t q_full;
-  uint64_t kv_full[4];
-  uint64_t kv_empty[4];
+  uint64_t kv_full[8];     // [s]: K of stage s, [STAGES + s]: V of stage s
+  uint64_t kv_empty[8];
   uint64_t s_full[2];      // [tile]: S = Q K^T of the current key tile is in TMEM
   uint64_t p_full[2];      // [tile]: P of the current key tile is in TMEM
   uint64_t pv_done[2];     // [tile]: O += P V of the current key tile completed
@@ -85,8 +89,8 @@ struct TcBars {
   uint32_t tmem_base;
   volatile int abort;
   volatile int last;
-  volatile int issued;
-  volatile int consumed;
+  volatile int issued[2];    // K / V tiles issued by the producer
+  volatile int consumed[2];  // K / V tiles whose arrival the MMA issuer observed
 };
 
 template <int D>
@@ -187,6 +191,12 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
     // before tile A's P is published; the MMA thread issues tile B's product
     // after observing that, so it sees the zeros too.
     if (X == 0 && key0 + C::BN > kv_len) {
+      // V(t) has its own barrier and may land after S(t): wait for it first
+      // so the copy cannot overwrite the zeros.
+      if (!mbar_wait(&bars->kv_full[C::STAGES + t % C::STAGES], (t / C::STAGES) & 1)) {
+        ok = false;
+        break;
+      }
       const int first = max(0, kv_len - key0);
       uint8_t* vt = smem + C::OFF_KV + (t % C::STAGES) * C::STAGE + C::KV_TILE;
       const int n16 = (C::BN - first) * C::HALVES * 8;
@@ -321,7 +331,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < 2 * C::STAGES; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
@@ -333,8 +343,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     bars->last = 0;
-    bars->issued = 0;
-    bars->consumed = 0;
+    bars->issued[0] = bars->issued[1] = 0;
+    bars->consumed[0] = bars->consumed[1] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -367,8 +377,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       }
       const int32_t* bt_row =
           a.bt + static_cast<int64_t>(seg) * a.bt_row_stride + a.bt_col_offset;
-      produce_kv<C::BN, C::HALVES, C::STAGES>(&tmK, &tmV, a, smem + C::OFF_KV, bars->kv_full,
-                                              bars->kv_empty, &bars->abort, &bars->issued,
+      produce_kv<C::BN, C::HALVES, C::STAGES, true>(&tmK, &tmV, a, smem + C::OFF_KV, bars->kv_full,
+                                              bars->kv_empty, &bars->abort, bars->issued,
                                               bt_row, hk, kb, kv_len, ntiles, lane);
     }
   } else if (warp == 1) {
@@ -378,45 +388,70 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       constexpr uint32_t idesc_o = mma_idesc_bf16(C::BM, D, true);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sKV = smem_u32(smem + C::OFF_KV);
-      const int nx = two ? 2 : 1;
-      bool ok = mbar_wait(&bars->q_full, 0);
+      // S_X(t) = Q_X K(t)^T into TMEM columns [128 X, 128 X + 128).
+      auto issue_s = [&](int x, int t) {
+        tc_fence_after();
+        const uint32_t kbase = sKV + (t % C::STAGES) * C::STAGE;
+        const uint32_t qbase = sQ + x * C::Q_TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad =
+              smem_desc_sw128(qbase + (kk >> 2) * C::Q_HALF + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd =
+              smem_desc_sw128(kbase + (kk >> 2) * C::KV_HALF + (kk & 3) * 32, 16, 1024);
+          tc_mma(tmem + x * 128, ad, bd, idesc_s, kk > 0);
+        }
+        tc_commit(&bars->s_full[x]);
+      };
+      // O_X += P_X(t) V(t), P_X read from TMEM (the first 64 columns of S_X).
+      auto issue_pv = [&](int x, int t) {
+        tc_fence_after();
+        const uint32_t vbase = sKV + (t % C::STAGES) * C::STAGE + C::KV_TILE;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          const uint64_t bd = smem_desc_sw128(vbase + kk * 16 * 128, C::KV_HALF, 1024);
+          tc_mma_ts(tmem + C::O_COL + x * D, tmem + x * 128 + kk * 8, bd, idesc_o,
+                    (t > 0 || kk > 0) ? 1 : 0);
+        }
+        tc_commit(&bars->pv_done[x]);
+      };
+      // Issue order per tile t: P_A V, S_A(t+1), P_B V, S_B(t+1). The
+      // tensor core executes one thread's MMAs in issue order, so S_X(t+1)
+      // overwrites P_X(t) only after P_X(t) V has read it, and the softmax
+      // of tile A moves on as soon as its own product is done instead of
+      // waiting for tile B's softmax. The commit after S_X(t+1) also covers
+      // P_X(t) V, so O_X is final when the softmax sees S_X(t+1). K and V
+      // have their own ring barriers: K(t) is released once both S(t) are
+      // done, so its stage refills while V(t) is still in use.
+      constexpr int S_ = C::STAGES;
+      bool ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->kv_full[0], 0);
+      if (ok) {
+        bars->consumed[0] = 1;
+        issue_s(0, 0);
+        if (two) issue_s(1, 0);
+        tc_commit(&bars->kv_empty[0]);
+      }
       for (int t = 0; ok && t < ntiles; ++t) {
         if (bars->abort) { ok = false; break; }
-        const int s = t % C::STAGES;
-        if (!(ok = mbar_wait(&bars->kv_full[s], (t / C::STAGES) & 1))) break;
-        bars->consumed = t + 1;
-        const uint32_t kbase = sKV + s * C::STAGE;
-        const uint32_t vbase = kbase + C::KV_TILE;
-        // S_X = Q_X K^T, once P_X of the previous tile has been consumed.
-        for (int x = 0; x < nx; ++x) {
-          if (t > 0 && !(ok = mbar_wait(&bars->pv_done[x], (t - 1) & 1))) break;
-          tc_fence_after();
-          const uint32_t qbase = sQ + x * C::Q_TILE;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad =
-                smem_desc_sw128(qbase + (kk >> 2) * C::Q_HALF + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                smem_desc_sw128(kbase + (kk >> 2) * C::KV_HALF + (kk & 3) * 32, 16, 1024);
-            tc_mma(tmem + x * 128, ad, bd, idesc_s, kk > 0);
-          }
-          tc_commit(&bars->s_full[x]);
+        const bool more = t + 1 < ntiles;
+        if (!(ok = mbar_wait(&bars->p_full[0], t & 1))) break;
+        if (!(ok = mbar_wait(&bars->kv_full[S_ + t % S_], (t / S_) & 1))) break;
+        bars->consumed[1] = t + 1;
+        issue_pv(0, t);
+        if (more) {
+          if (!(ok = mbar_wait(&bars->kv_full[(t + 1) % S_], ((t + 1) / S_) & 1))) break;
+          bars->consumed[0] = t + 2;
+          issue_s(0, t + 1);
         }
-        if (!ok) break;
-        // O_X += P_X V, P_X from TMEM.
-        for (int x = 0; x < nx; ++x) {
-          if (!(ok = mbar_wait(&bars->p_full[x], t & 1))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk) {
-            const uint64_t bd = smem_desc_sw128(vbase + kk * 16 * 128, C::KV_HALF, 1024);
-            tc_mma_ts(tmem + C::O_COL + x * D, tmem + x * 128 + kk * 8, bd, idesc_o,
-                      (t > 0 || kk > 0) ? 1 : 0);
-          }
-          tc_commit(&bars->pv_done[x]);
+        if (two) {
+          if (!(ok = mbar_wait(&bars->p_full[1], t & 1))) break;
+          issue_pv(1, t);
         }
-        if (!ok) break;
-        tc_commit(&bars->kv_empty[s]);
+        tc_commit(&bars->kv_empty[S_ + t % S_]);
+        if (more) {
+          if (two) issue_s(1, t + 1);
+          tc_commit(&bars->kv_empty[(t + 1) % S_]);
+        }
       }
       if (!ok) {
         abort_call(a);
@@ -458,8 +493,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   if (threadIdx.x == 0 && bars->abort) {
     // After an abort, wait (bounded) for the copies still in flight.
     if (ntiles > 0) mbar_wait(&bars->q_full, 0);
-    for (int t = bars->consumed; t < bars->issued; ++t)
-      if (!mbar_wait(&bars->kv_full[t % C::STAGES], (t / C::STAGES) & 1)) break;
+    for (int p = 0; p < 2; ++p)
+      for (int t = bars->consumed[p]; t < bars->issued[p]; ++t)
+        if (!mbar_wait(&bars->kv_full[p * C::STAGES + t % C::STAGES], (t / C::STAGES) & 1)) break;
   }
   __syncthreads();
   if (warp == 1) {

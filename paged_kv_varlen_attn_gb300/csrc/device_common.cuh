@@ -293,8 +293,13 @@ __device__ __forceinline__ void abort_call(const AttnArgs& a) {
 // a box past the sequence end, becomes the out-of-range coordinate
 // num_blocks, which TMA fills with zeros. The unit's first tile is tile t0 of
 // the ring's running sequence (stages and phases continue across units).
+// SEP = false: one full/empty barrier pair per stage covers K and V, and
+// issued[0] counts issued tiles. SEP = true: K and V of a stage have their own
+// barriers -- full/empty[s] for K, full/empty[STAGES + s] for V -- so a
+// consumer that is done with K(t) before V(t) can release it early, and
+// issued[0] / issued[1] count the issued K / V tiles.
 // Returns false on timeout/abort.
-template <int BN, int HALVES, int STAGES>
+template <int BN, int HALVES, int STAGES, bool SEP = false>
 __device__ bool produce_kv(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnArgs& a,
                            uint8_t* ring, uint64_t* full, uint64_t* empty,
                            volatile int* cta_abort, volatile int* issued,
@@ -336,25 +341,30 @@ __device__ bool produce_kv(const CUtensorMap* tmK, const CUtensorMap* tmV, const
       if (t >= ntiles) break;
       const int tr = t0 + t;   // position in the ring's sequence of tiles
       const int s = tr % STAGES;
-      int ok = 1;
-      if (lane == 0) {
-        if (tr >= STAGES && !mbar_wait(&empty[s], ((tr / STAGES) - 1) & 1)) {
-          abort_call(a);
-          *cta_abort = 1;
-        }
-        if (*cta_abort) ok = 0;
-        if (ok) mbar_arrive_expect_tx(&full[s], STAGE);
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) return false;
       uint8_t* kdst = ring + s * STAGE;
       const int src = (tt * bpt + my_b) & 31;
       const int page = __shfl_sync(0xffffffffu, cur, src);
       const int prow = __shfl_sync(0xffffffffu, cur_row, src);
-      if (lane < nbox)
-        tma_load_4d(kdst + my_v * TILE + my_h * HALF + my_b * box_rows * 128, my_v ? tmV : tmK,
-                    &full[s], my_h * 64, hk, prow, page);
-      if (lane == 0) *issued = tr + 1;
+      // One pass per barrier pair: K and V together, or K then V.
+#pragma unroll
+      for (int part = 0; part < (SEP ? 2 : 1); ++part) {
+        const int bi = SEP ? part * STAGES + s : s;
+        int ok = 1;
+        if (lane == 0) {
+          if (tr >= STAGES && !mbar_wait(&empty[bi], ((tr / STAGES) - 1) & 1)) {
+            abort_call(a);
+            *cta_abort = 1;
+          }
+          if (*cta_abort) ok = 0;
+          if (ok) mbar_arrive_expect_tx(&full[bi], SEP ? TILE : STAGE);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return false;
+        if (lane < nbox && (!SEP || my_v == part))
+          tma_load_4d(kdst + my_v * TILE + my_h * HALF + my_b * box_rows * 128, my_v ? tmV : tmK,
+                      &full[bi], my_h * 64, hk, prow, page);
+        if (lane == 0) issued[SEP ? part : 0] = tr + 1;
+      }
     }
   }
   return true;
