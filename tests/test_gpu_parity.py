@@ -299,8 +299,9 @@ def test_cascade_small_matches_flat():
 
 @pytest.mark.parametrize("seed,S,H,Hk,D,P,qmax,smax", [
     (72, 4, 8, 2, 128, 64, 1, 40),       # prefix pass rows 4*4 = 16: split-KV kernel
-    (73, 40, 32, 4, 128, 512, 2, 200),   # prefix rows up to 80*8 = 640: several 256-row tiles
+    (73, 40, 32, 4, 128, 512, 2, 200),   # prefix rows 61*8 = 488: two 256-row tiles
     (74, 12, 16, 16, 64, 256, 3, 90),    # GQA 1, head 64
+    (75, 40, 32, 4, 128, 256, 4, 100),   # prefix rows 99*8 = 792: four row tiles, last partial
 ])
 def test_cascade_prefix_row_tiles(seed, S, H, Hk, D, P, qmax, smax):
     g = torch.Generator().manual_seed(seed)
