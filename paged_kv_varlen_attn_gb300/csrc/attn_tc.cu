@@ -9,8 +9,8 @@
 // B, each 128/G tokens x the G query heads of one KV head -- against a key
 // range, in 128-key tiles. Every K/V byte brought into shared memory serves
 // 256 rows (both Q tiles, all G heads). Three warpgroups:
-//   control (warps 0-3; 0 and 1 work, 2 and 3 idle), registers cut to 56;
-//   softmax A (warps 4-7) and softmax B (warps 8-11), registers raised to 224.
+//   control (warps 0-3; 0 and 1 work, 2 and 3 idle), registers cut to 120;
+//   softmax A (warps 4-7) and softmax B (warps 8-11), registers raised to 192.
 // Warp roles:
 //   warp 0     TMA producer: both Q tiles once, then K and V page boxes
 //              (128-byte swizzle) into a ring of stages (full/empty mbarriers),
@@ -356,11 +356,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   // Register split: the block is launched with 384 x 168 registers. The
-  // control warpgroup (producer, MMA issuer, two idle warps) drops to 56 and
-  // the two softmax warpgroups rise to 224: 128*56 + 256*224 = 384*168.
+  // control warpgroup (producer, MMA issuer, two idle warps) drops to 120 and
+  // the two softmax warpgroups rise to 192: 128*120 + 256*192 = 384*168. The
+  // MMA issuer's loop must not spill (a spilled descriptor puts local-memory
+  // latency between consecutive MMAs); a few softmax spills cost less
+  // (measured: 56/224 ran 11% slower than 120/192, 152/176 8% slower).
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (ntiles > 0) {
@@ -463,7 +466,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int X = (warp - 4) >> 2;   // warps 4-7: tile A, 8-11: tile B
     if (X == 0 || two)
