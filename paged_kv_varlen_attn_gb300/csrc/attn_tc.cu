@@ -135,13 +135,18 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
       for (int e = 0; e < C::BN; ++e)
         if (key0 + e >= vis_end) xs[e] = -INFINITY;
     }
+    // Row max: eight independent chains of three-input maxima over the
+    // values j, j+8, j+16, ... of the tile.
+    static_assert(C::BN % 16 == 0, "max chains take two values per step");
     float mx8[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) mx8[e] = xs[e];
+    for (int j = 0; j < 8; ++j) mx8[j] = fmaxf(xs[j], xs[8 + j]);
 #pragma unroll
-    for (int e = 8; e < C::BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], xs[e]);
-    const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+    for (int e = 16; e < C::BN; e += 16)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx8[j] = fmax3(mx8[j], xs[e + j], xs[e + 8 + j]);
+    const float tmax = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                             fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7])) * sl2;
     float m_new = m_use;
     bool need = false;
     if (tmax > m_use) {
