@@ -12,12 +12,16 @@
 namespace pa {
 
 // ---------------------------------------------------------------------------
-// Scatter. Every thread moves 16-byte vectors; consecutive threads move
-// consecutive vectors of one token's [H_kv, D] row, so both the read of the
-// new token and the write into its page row are fully coalesced. The grid is
-// a multiple of the SM count and strides over all vectors.
+// Scatter. One warp per token at a time (warps stride over the tokens): the
+// lanes move the token's K row and V row ([H_kv, D], vpt 16-byte vectors
+// each) with consecutive lanes on consecutive vectors, so the read of the new
+// token and the write into its page row are fully coalesced, and each lane
+// keeps up to 2 * kScatterUnroll loads in flight. The source loads do not
+// depend on the slot, so they are issued together with the slot load, and
+// no per-vector index division is needed.
 // ---------------------------------------------------------------------------
 constexpr int kScatterThreads = 256;
+constexpr int kScatterWarps = kScatterThreads / 32;
 constexpr int kScatterUnroll = 4;
 
 __global__ void __launch_bounds__(kScatterThreads)
@@ -26,41 +30,41 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
                          uint4* __restrict__ vc, int64_t block_stride_v,
                          const int64_t* __restrict__ slots, int num_tokens, int vpt, int bs,
                          int64_t num_slots, int32_t* status) {
-  // vpt = 16-byte vectors per token row (H_kv * D / 8); each token has a K and
-  // a V row, so the flat index space is num_tokens * 2 * vpt.
-  const int64_t total = static_cast<int64_t>(num_tokens) * 2 * vpt;
-  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
-       base += step * kScatterUnroll) {
-    uint4 v[kScatterUnroll];
-    uint4* dst[kScatterUnroll];
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kScatterWarps;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kScatterWarps + (threadIdx.x >> 5);
+       t < num_tokens; t += nwarps) {
+    const uint4* ksrc = key + t * kstride_v;
+    const uint4* vsrc = value + t * vstride_v;
+    const int64_t slot = __ldg(slots + t);
+    for (int v0 = lane; v0 < vpt; v0 += 32 * kScatterUnroll) {
+      uint4 kv[kScatterUnroll], vv[kScatterUnroll];
 #pragma unroll
-    for (int u = 0; u < kScatterUnroll; ++u) {
-      dst[u] = nullptr;
-      const int64_t idx = base + u * step;
-      if (idx >= total) continue;
-      const int64_t t = idx / (2 * vpt);
-      const int rem = static_cast<int>(idx - t * 2 * vpt);
-      const int which = rem >= vpt;            // 0: key, 1: value
-      const int vi = rem - which * vpt;
-      // The source vector does not depend on the slot: both loads are in
-      // flight together.
-      const uint4* src = which ? value + t * vstride_v : key + t * kstride_v;
-      v[u] = __ldcs(src + vi);
-      const int64_t slot = __ldg(slots + t);
+      for (int u = 0; u < kScatterUnroll; ++u) {
+        const int i = v0 + u * 32;
+        if (i < vpt) {
+          kv[u] = __ldcs(ksrc + i);
+          vv[u] = __ldcs(vsrc + i);
+        }
+      }
       if (slot < 0) continue;                  // padding token
       if (slot >= num_slots) {
-        flag_status(status, PA_DEV_BAD_SLOT);
+        if (lane == 0 && v0 == lane) flag_status(status, PA_DEV_BAD_SLOT);
         continue;
       }
       const int64_t page = slot / bs;
       const int64_t row = slot - page * bs;
-      uint4* pool = which ? vc : kc;
-      dst[u] = pool + page * block_stride_v + row * vpt + vi;
-    }
+      uint4* kdst = kc + page * block_stride_v + row * vpt;
+      uint4* vdst = vc + page * block_stride_v + row * vpt;
 #pragma unroll
-    for (int u = 0; u < kScatterUnroll; ++u)
-      if (dst[u]) *dst[u] = v[u];
+      for (int u = 0; u < kScatterUnroll; ++u) {
+        const int i = v0 + u * 32;
+        if (i < vpt) {
+          kdst[i] = kv[u];
+          vdst[i] = vv[u];
+        }
+      }
+    }
   }
 }
 
@@ -70,9 +74,7 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
                                      int num_blocks, int32_t* status, cudaStream_t st, int sms) {
   if (num_tokens == 0) return cudaSuccess;
   const int vpt = H_kv * D / 8;
-  const int64_t total = static_cast<int64_t>(num_tokens) * 2 * vpt;
-  const int64_t want = (total + kScatterThreads * kScatterUnroll - 1) /
-                       (kScatterThreads * kScatterUnroll);
+  const int64_t want = (static_cast<int64_t>(num_tokens) + kScatterWarps - 1) / kScatterWarps;
   const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 CTAs of 256 threads per SM
   const int grid = static_cast<int>(want < cap ? want : cap);
   reshape_and_cache_kernel<<<grid, kScatterThreads, 0, st>>>(
