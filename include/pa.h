@@ -196,6 +196,57 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
                          size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream);
 
 /*
+ * New tokens' K/V for the update-and-attend entry points below: the
+ * arguments of pa_reshape_and_cache that are not already arguments of the
+ * attention call. key / value: [num_tokens, num_kv_heads, head_size] bf16,
+ * token t at key + t*key_token_stride; slot_mapping: int64 [num_tokens]
+ * (slot < 0 skips the token). All device pointers, owned by the caller.
+ */
+typedef struct pa_kv_update {
+  const void* key;
+  const void* value;
+  int64_t key_token_stride;
+  int64_t value_token_stride;
+  const int64_t* slot_mapping;
+  int num_tokens;
+} pa_kv_update;
+
+/*
+ * pa_varlen_fwd_with_update / pa_cascade_fwd_with_update -- one serving step
+ * ([FA-vLLM] §4.2: the forward pass first writes the step's new K/V into the
+ * paged cache by slot_mapping, then attends): the same result as
+ * pa_reshape_and_cache(update, key_cache, value_cache, ...) followed by
+ * pa_varlen_fwd / pa_cascade_fwd with the remaining arguments, on the same
+ * stream. In one call the planner and the scatter run concurrently (the
+ * planner reads only the sequence metadata), and the attention kernels start
+ * once both have finished. update may be NULL or have num_tokens = 0 (then
+ * these equal pa_varlen_fwd / pa_cascade_fwd). The cache arguments
+ * (cache_block_stride, num_kv_heads, head_size, block_size, num_blocks) and
+ * dev_status serve both parts; the update's arguments are checked like
+ * pa_reshape_and_cache's before anything is launched.
+ */
+pa_status pa_varlen_fwd_with_update(const pa_kv_update* update, const void* q,
+                                    int64_t q_token_stride, void* key_cache, void* value_cache,
+                                    int64_t cache_block_stride, const int32_t* cu_seqlens_q,
+                                    const int32_t* seqused_k, const int32_t* block_table,
+                                    int bt_stride, int num_seqs, int total_q, int max_seqlen_q,
+                                    int max_seqlen_k, int num_heads, int num_kv_heads,
+                                    int head_size, int block_size, int num_blocks,
+                                    float softmax_scale, int causal, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes, int dtype,
+                                    int32_t* dev_status, void* stream);
+pa_status pa_cascade_fwd_with_update(const pa_kv_update* update, const void* q,
+                                     int64_t q_token_stride, void* key_cache, void* value_cache,
+                                     int64_t cache_block_stride, const int32_t* cu_seqlens_q,
+                                     const int32_t* seqused_k, const int32_t* block_table,
+                                     int bt_stride, int num_seqs, int total_q, int max_seqlen_q,
+                                     int max_seqlen_k, int num_heads, int num_kv_heads,
+                                     int head_size, int block_size, int num_blocks,
+                                     float softmax_scale, int common_prefix_len, void* out,
+                                     float* lse, void* workspace, size_t workspace_bytes,
+                                     int dtype, int32_t* dev_status, void* stream);
+
+/*
  * pa_varlen_fwd_noalloc -- pa_varlen_fwd for callers that cannot allocate
  * device memory, so cannot provide a workspace: for example a serving engine
  * whose allocator reserved all device memory for its page pool at start-up,

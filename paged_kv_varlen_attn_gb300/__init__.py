@@ -41,12 +41,24 @@ EXPORTS = (
     "pa_cascade_fwd_workspace_size",
     "pa_cascade_fwd",
     "pa_varlen_fwd_noalloc",
+    "pa_varlen_fwd_with_update",
+    "pa_cascade_fwd_with_update",
 )
 
 _lib = None
 
 _c = ctypes
 _vp, _i64, _i32, _f32, _sz = _c.c_void_p, _c.c_int64, _c.c_int, _c.c_float, _c.c_size_t
+
+
+class KvUpdate(ctypes.Structure):
+    """struct pa_kv_update of include/pa.h."""
+    _fields_ = [("key", _vp), ("value", _vp), ("key_token_stride", _i64),
+                ("value_token_stride", _i64), ("slot_mapping", _vp), ("num_tokens", _i32)]
+
+
+_ATTN_ARGS = [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+              _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _i32, _vp, _vp]
 
 _SIGS = {
     "pa_status_string": ([_i32], _c.c_char_p),
@@ -65,6 +77,8 @@ _SIGS = {
     "pa_cascade_fwd": ([_vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                         _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _i32, _vp,
                         _vp], _i32),
+    "pa_varlen_fwd_with_update": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS, _i32),
+    "pa_cascade_fwd_with_update": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS, _i32),
 }
 
 
@@ -176,10 +190,17 @@ def _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table
         raise ValueError("block_table must be [num_seqs, max_blocks] with unit column stride")
 
 
-def varlen_fwd(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
-               max_seqlen_k, softmax_scale, causal, out=None, lse=None, return_lse=True,
-               workspace=None, dev_status=None):
-    """Varlen attention over a paged KV cache. Returns (out, lse or None)."""
+def _kv_update(key, value, slot_mapping):
+    if key is None:
+        return None
+    _need_cuda(key, value, slot_mapping)
+    return KvUpdate(key.data_ptr(), value.data_ptr(), _row_stride(key), _row_stride(value),
+                    slot_mapping.data_ptr(), key.shape[0])
+
+
+def _attend(entry, update, q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
+            max_seqlen_q, max_seqlen_k, softmax_scale, mode_arg, out, lse, return_lse,
+            workspace, dev_status, size_fn):
     lib = load_library()
     _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table)
     T, H, D = q.shape
@@ -190,16 +211,40 @@ def varlen_fwd(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, 
     if lse is None and return_lse:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     if workspace is None:
-        workspace = alloc_workspace(varlen_fwd_workspace_size(
-            S, T, max_seqlen_q, max_seqlen_k, H, hk, D, bs, _sm_count(q.device)), q.device)
-    code = lib.pa_varlen_fwd(
-        _ptr(q), _row_stride(q), _ptr(key_cache), _ptr(value_cache), _cache_stride(key_cache),
-        _ptr(cu_seqlens_q), _ptr(seqused_k), _ptr(block_table), block_table.stride(0), S, T,
-        int(max_seqlen_q), int(max_seqlen_k), H, hk, D, bs, nb, float(softmax_scale),
-        int(bool(causal)), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
-        _ptr(dev_status), _stream(q.device))
-    _check(code, "pa_varlen_fwd")
+        workspace = alloc_workspace(size_fn(S, T, max_seqlen_q, max_seqlen_k, H, hk, D, bs,
+                                            _sm_count(q.device)), q.device)
+    args = (_ptr(q), _row_stride(q), _ptr(key_cache), _ptr(value_cache), _cache_stride(key_cache),
+            _ptr(cu_seqlens_q), _ptr(seqused_k), _ptr(block_table), block_table.stride(0), S, T,
+            int(max_seqlen_q), int(max_seqlen_k), H, hk, D, bs, nb, float(softmax_scale),
+            int(mode_arg), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
+            _ptr(dev_status), _stream(q.device))
+    fn = getattr(lib, entry)
+    code = fn(ctypes.byref(update) if update is not None else None, *args) \
+        if entry.endswith("_with_update") else fn(*args)
+    _check(code, entry)
     return out, lse
+
+
+def varlen_fwd(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
+               max_seqlen_k, softmax_scale, causal, out=None, lse=None, return_lse=True,
+               workspace=None, dev_status=None):
+    """Varlen attention over a paged KV cache. Returns (out, lse or None)."""
+    return _attend("pa_varlen_fwd", None, q, key_cache, value_cache, cu_seqlens_q, seqused_k,
+                   block_table, max_seqlen_q, max_seqlen_k, softmax_scale, bool(causal), out,
+                   lse, return_lse, workspace, dev_status, varlen_fwd_workspace_size)
+
+
+def varlen_fwd_with_update(key, value, slot_mapping, q, key_cache, value_cache, cu_seqlens_q,
+                           seqused_k, block_table, max_seqlen_q, max_seqlen_k, softmax_scale,
+                           causal, out=None, lse=None, return_lse=True, workspace=None,
+                           dev_status=None):
+    """One step: scatter the new tokens' K/V (key, value by slot_mapping) into
+    the caches, then varlen attention; the planner overlaps the scatter.
+    Returns (out, lse or None)."""
+    return _attend("pa_varlen_fwd_with_update", _kv_update(key, value, slot_mapping), q,
+                   key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
+                   max_seqlen_k, softmax_scale, bool(causal), out, lse, return_lse, workspace,
+                   dev_status, varlen_fwd_workspace_size)
 
 
 def varlen_fwd_noalloc(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
@@ -250,23 +295,18 @@ def cascade_fwd(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
                 max_seqlen_k, softmax_scale, common_prefix_len, out=None, lse=None,
                 return_lse=True, workspace=None, dev_status=None):
     """Shared-prefix (cascade) attention. Returns (out, lse or None)."""
-    lib = load_library()
-    _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table)
-    T, H, D = q.shape
-    nb, bs, hk, _ = key_cache.shape
-    S = cu_seqlens_q.numel() - 1
-    if out is None:
-        out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
-    if lse is None and return_lse:
-        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
-    if workspace is None:
-        workspace = alloc_workspace(cascade_fwd_workspace_size(
-            S, T, max_seqlen_q, max_seqlen_k, H, hk, D, bs, _sm_count(q.device)), q.device)
-    code = lib.pa_cascade_fwd(
-        _ptr(q), _row_stride(q), _ptr(key_cache), _ptr(value_cache), _cache_stride(key_cache),
-        _ptr(cu_seqlens_q), _ptr(seqused_k), _ptr(block_table), block_table.stride(0), S, T,
-        int(max_seqlen_q), int(max_seqlen_k), H, hk, D, bs, nb, float(softmax_scale),
-        int(common_prefix_len), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
-        _ptr(dev_status), _stream(q.device))
-    _check(code, "pa_cascade_fwd")
-    return out, lse
+    return _attend("pa_cascade_fwd", None, q, key_cache, value_cache, cu_seqlens_q, seqused_k,
+                   block_table, max_seqlen_q, max_seqlen_k, softmax_scale, common_prefix_len,
+                   out, lse, return_lse, workspace, dev_status, cascade_fwd_workspace_size)
+
+
+def cascade_fwd_with_update(key, value, slot_mapping, q, key_cache, value_cache, cu_seqlens_q,
+                            seqused_k, block_table, max_seqlen_q, max_seqlen_k, softmax_scale,
+                            common_prefix_len, out=None, lse=None, return_lse=True,
+                            workspace=None, dev_status=None):
+    """One step: scatter the new tokens' K/V into the caches, then cascade
+    attention. Returns (out, lse or None)."""
+    return _attend("pa_cascade_fwd_with_update", _kv_update(key, value, slot_mapping), q,
+                   key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
+                   max_seqlen_k, softmax_scale, common_prefix_len, out, lse, return_lse,
+                   workspace, dev_status, cascade_fwd_workspace_size)

@@ -30,6 +30,10 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
                          uint4* __restrict__ vc, int64_t block_stride_v,
                          const int64_t* __restrict__ slots, int num_tokens, int vpt, int bs,
                          int64_t num_slots, int32_t* status) {
+  // Launched after the planner inside an update-and-attend call (a no-op
+  // otherwise): its inputs predate the planner, so only the last block waits
+  // for it, which keeps the grids completing in launch order.
+  pdl_enter(0);
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kScatterWarps;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kScatterWarps + (threadIdx.x >> 5);
@@ -71,16 +75,28 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t kstride,
                                      int64_t vstride, void* kc, void* vc, int64_t block_stride,
                                      const int64_t* slots, int num_tokens, int H_kv, int D, int bs,
-                                     int num_blocks, int32_t* status, cudaStream_t st, int sms) {
+                                     int num_blocks, int32_t* status, cudaStream_t st, int sms,
+                                     bool pdl) {
   if (num_tokens == 0) return cudaSuccess;
   const int vpt = H_kv * D / 8;
   const int64_t want = (static_cast<int64_t>(num_tokens) + kScatterWarps - 1) / kScatterWarps;
   const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 CTAs of 256 threads per SM
-  const int grid = static_cast<int>(want < cap ? want : cap);
-  reshape_and_cache_kernel<<<grid, kScatterThreads, 0, st>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value), kstride / 8, vstride / 8,
-      static_cast<uint4*>(kc), static_cast<uint4*>(vc), block_stride / 8, slots, num_tokens, vpt,
-      bs, static_cast<int64_t>(num_blocks) * bs, status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
+  cfg.blockDim = dim3(kScatterThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(
+      &cfg, reshape_and_cache_kernel, static_cast<const uint4*>(key),
+      static_cast<const uint4*>(value), kstride / 8, vstride / 8, static_cast<uint4*>(kc),
+      static_cast<uint4*>(vc), block_stride / 8, slots, num_tokens, vpt, bs,
+      static_cast<int64_t>(num_blocks) * bs, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -319,6 +319,52 @@ pa_status launch_pass(const CommonAttn& c, const CUtensorMap& tmK, const CUtenso
   return PA_OK;
 }
 
+// Checks of pa_reshape_and_cache's arguments (nothing launched).
+pa_status check_update(const void* key, const void* value, int64_t key_token_stride,
+                       int64_t value_token_stride, const void* key_cache, const void* value_cache,
+                       int64_t cache_block_stride, const int64_t* slot_mapping, int num_tokens,
+                       int num_kv_heads, int head_size, int block_size, int num_blocks,
+                       int dtype) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (head_size != 64 && head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size <= 0 || block_size % 16 != 0 || block_size > 1024) return PA_ERR_BLOCK_SIZE;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+    return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0) return PA_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_size;
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 ||
+      value_token_stride % 8)
+    return PA_ERR_INVALID_ARG;
+  if (cache_block_stride < row * block_size || cache_block_stride % 8) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+// Validate an optional K/V update of an update-and-attend call.
+pa_status check_kv_update(const pa_kv_update* u, const CommonAttn& c, void* key_cache,
+                          void* value_cache, int dtype) {
+  if (!u || u->num_tokens == 0) return u && u->num_tokens < 0 ? PA_ERR_INVALID_ARG : PA_OK;
+  return check_update(u->key, u->value, u->key_token_stride, u->value_token_stride, key_cache,
+                      value_cache, c.block_stride, u->slot_mapping, u->num_tokens, c.H_kv, c.D,
+                      c.bs, c.num_blocks, dtype);
+}
+
+// Launch the update's scatter right after the planner, as a programmatic
+// dependent: it overlaps the planner (its inputs predate the call), and the
+// first attention kernel waits for it before reading the cache.
+pa_status launch_kv_update(const pa_kv_update* u, const CommonAttn& c, void* key_cache,
+                           void* value_cache, int sms) {
+  if (!u || u->num_tokens == 0) return PA_OK;
+  return launch_reshape_and_cache(u->key, u->value, u->key_token_stride, u->value_token_stride,
+                                  key_cache, value_cache, c.block_stride, u->slot_mapping,
+                                  u->num_tokens, c.H_kv, c.D, c.bs, c.num_blocks, c.status, c.st,
+                                  sms, true) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace pa
 
@@ -348,27 +394,17 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, int64_t key_t
                                int64_t cache_block_stride, const int64_t* slot_mapping,
                                int num_tokens, int num_kv_heads, int head_size, int block_size,
                                int num_blocks, int dtype, int32_t* dev_status, void* stream) {
-  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
-  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  if (head_size != 64 && head_size != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size <= 0 || block_size % 16 != 0 || block_size > 1024) return PA_ERR_BLOCK_SIZE;
-  if (num_tokens == 0) return PA_OK;
-  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
-  if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
-    return PA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0) return PA_ERR_INVALID_ARG;
-  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_size;
-  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 ||
-      value_token_stride % 8)
-    return PA_ERR_INVALID_ARG;
-  if (cache_block_stride < row * block_size || cache_block_stride % 8) return PA_ERR_INVALID_ARG;
+  const pa_status st = check_update(key, value, key_token_stride, value_token_stride, key_cache,
+                                    value_cache, cache_block_stride, slot_mapping, num_tokens,
+                                    num_kv_heads, head_size, block_size, num_blocks, dtype);
+  if (st != PA_OK || num_tokens == 0) return st;
   const int sms = query_sms(0);
   if (sms <= 0) return PA_ERR_CUDA;
   cudaError_t e = launch_reshape_and_cache(key, value, key_token_stride, value_token_stride,
                                            key_cache, value_cache, cache_block_stride,
                                            slot_mapping, num_tokens, num_kv_heads, head_size,
                                            block_size, num_blocks, dev_status,
-                                           static_cast<cudaStream_t>(stream), sms);
+                                           static_cast<cudaStream_t>(stream), sms, false);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -398,14 +434,16 @@ size_t pa_cascade_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q
       .end;
 }
 
-pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_cache,
-                        const void* value_cache, int64_t cache_block_stride,
-                        const int32_t* cu_seqlens_q, const int32_t* seqused_k,
-                        const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
-                        int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
-                        int head_size, int block_size, int num_blocks, float softmax_scale,
-                        int causal, void* out, float* lse, void* workspace,
-                        size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream) {
+// pa_varlen_fwd, optionally preceded by a K/V update of the same cache.
+static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_token_stride,
+                             void* key_cache, void* value_cache, int64_t cache_block_stride,
+                             const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                             const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
+                             int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                             int head_size, int block_size, int num_blocks, float softmax_scale,
+                             int causal, void* out, float* lse, void* workspace,
+                             size_t workspace_bytes, int dtype, int32_t* dev_status,
+                             void* stream) {
   pa_status st = check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
                              num_kv_heads, head_size, block_size, dtype);
   if (st != PA_OK) return st;
@@ -413,7 +451,24 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
                        seqused_k, block_table, bt_stride, num_seqs, total_q, num_blocks, num_heads,
                        num_kv_heads, head_size, block_size, softmax_scale, causal, out, lse);
   if (st != PA_OK) return st;
-  if (num_seqs == 0 || total_q == 0) return PA_OK;
+  CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
+               seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+               num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
+               dev_status, static_cast<cudaStream_t>(stream)};
+  st = check_kv_update(upd, c, key_cache, value_cache, dtype);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0 || total_q == 0) {   // nothing to attend: the update alone
+    if (!upd || upd->num_tokens == 0) return PA_OK;
+    const int sms = query_sms(0);
+    if (sms <= 0) return PA_ERR_CUDA;
+    return launch_reshape_and_cache(upd->key, upd->value, upd->key_token_stride,
+                                    upd->value_token_stride, key_cache, value_cache,
+                                    cache_block_stride, upd->slot_mapping, upd->num_tokens,
+                                    num_kv_heads, head_size, block_size, num_blocks, dev_status,
+                                    c.st, sms, false) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+  }
   const int sms = query_sms(0);
   if (sms <= 0) return PA_ERR_CUDA;
   PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
@@ -422,10 +477,6 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < L.end)
     return PA_ERR_WORKSPACE;
-  CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
-               seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
-               num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
-               dev_status, static_cast<cudaStream_t>(stream)};
   const int box_rows = gcd_int(block_size, kKeyTile);
   CUtensorMap tmK, tmV;
   if (!encode_pool_map(&tmK, key_cache, head_size, num_kv_heads, block_size, num_blocks,
@@ -443,9 +494,43 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
   pp.p[0] = make_plan(c, ws, L, 0, 0, 0, cap > 0x7fffffff ? 0x7fffffff : static_cast<int>(cap),
                       causal, 0);
   if (launch_plan(pp, 1, c.st) != cudaSuccess) return PA_ERR_CUDA;
+  st = launch_kv_update(upd, c, key_cache, value_cache, sms);
+  if (st != PA_OK) return st;
   AttnArgs a = make_attn(c, ws, L, bt_stride, 0, causal, out, lse);
   bool first = true;
   return launch_pass(c, tmK, tmV, tmQ, a, ws, L, &first);
+}
+
+pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_cache,
+                        const void* value_cache, int64_t cache_block_stride,
+                        const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                        const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
+                        int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                        int head_size, int block_size, int num_blocks, float softmax_scale,
+                        int causal, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream) {
+  return varlen_impl(nullptr, q, q_token_stride, const_cast<void*>(key_cache),
+                     const_cast<void*>(value_cache), cache_block_stride, cu_seqlens_q, seqused_k,
+                     block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+                     num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
+                     causal, out, lse, workspace, workspace_bytes, dtype, dev_status, stream);
+}
+
+pa_status pa_varlen_fwd_with_update(const pa_kv_update* update, const void* q,
+                                    int64_t q_token_stride, void* key_cache, void* value_cache,
+                                    int64_t cache_block_stride, const int32_t* cu_seqlens_q,
+                                    const int32_t* seqused_k, const int32_t* block_table,
+                                    int bt_stride, int num_seqs, int total_q, int max_seqlen_q,
+                                    int max_seqlen_k, int num_heads, int num_kv_heads,
+                                    int head_size, int block_size, int num_blocks,
+                                    float softmax_scale, int causal, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes, int dtype,
+                                    int32_t* dev_status, void* stream) {
+  return varlen_impl(update, q, q_token_stride, key_cache, value_cache, cache_block_stride,
+                     cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
+                     max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size, block_size,
+                     num_blocks, softmax_scale, causal, out, lse, workspace, workspace_bytes,
+                     dtype, dev_status, stream);
 }
 
 pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
@@ -470,14 +555,16 @@ pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_cache,
-                         const void* value_cache, int64_t cache_block_stride,
-                         const int32_t* cu_seqlens_q, const int32_t* seqused_k,
-                         const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
-                         int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
-                         int head_size, int block_size, int num_blocks, float softmax_scale,
-                         int common_prefix_len, void* out, float* lse, void* workspace,
-                         size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream) {
+// pa_cascade_fwd, optionally preceded by a K/V update of the same cache.
+static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_token_stride,
+                              void* key_cache, void* value_cache, int64_t cache_block_stride,
+                              const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                              const int32_t* block_table, int bt_stride, int num_seqs,
+                              int total_q, int max_seqlen_q, int max_seqlen_k, int num_heads,
+                              int num_kv_heads, int head_size, int block_size, int num_blocks,
+                              float softmax_scale, int common_prefix_len, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, int dtype,
+                              int32_t* dev_status, void* stream) {
   pa_status st = check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
                              num_kv_heads, head_size, block_size, dtype);
   if (st != PA_OK) return st;
@@ -488,7 +575,27 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
   if (common_prefix_len < 0 || common_prefix_len % block_size != 0) return PA_ERR_INVALID_ARG;
   if (static_cast<long long>(common_prefix_len) > static_cast<long long>(bt_stride) * block_size)
     return PA_ERR_INVALID_ARG;
-  if (num_seqs == 0 || total_q == 0) return PA_OK;
+  {
+    const CommonAttn cu{q, q_token_stride, key_cache, value_cache, cache_block_stride,
+                        cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
+                        max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size,
+                        block_size, num_blocks, softmax_scale, dev_status,
+                        static_cast<cudaStream_t>(stream)};
+    st = check_kv_update(upd, cu, key_cache, value_cache, dtype);
+    if (st != PA_OK) return st;
+  }
+  if (num_seqs == 0 || total_q == 0) {   // nothing to attend: the update alone
+    if (!upd || upd->num_tokens == 0) return PA_OK;
+    const int sms = query_sms(0);
+    if (sms <= 0) return PA_ERR_CUDA;
+    return launch_reshape_and_cache(upd->key, upd->value, upd->key_token_stride,
+                                    upd->value_token_stride, key_cache, value_cache,
+                                    cache_block_stride, upd->slot_mapping, upd->num_tokens,
+                                    num_kv_heads, head_size, block_size, num_blocks, dev_status,
+                                    static_cast<cudaStream_t>(stream), sms, false) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+  }
   const int sms = query_sms(0);
   if (sms <= 0) return PA_ERR_CUDA;
   const int G = num_heads / num_kv_heads;
@@ -525,6 +632,8 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
                       cap > 0x7fffffff ? 0x7fffffff : static_cast<int>(cap), 1, 1, 1);
   pp.p[1].make_groups = 1;
   if (launch_plan(pp, 2, c.st) != cudaSuccess) return PA_ERR_CUDA;
+  st = launch_kv_update(upd, c, key_cache, value_cache, sms);
+  if (st != PA_OK) return st;
   AttnArgs pa_ = make_attn(c, ws, CL.prefix, 0, 0, 0, nullptr, nullptr);
   pa_.partials_only = 1;
   bool first = true;
@@ -555,6 +664,39 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
       cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
+}
+
+pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_cache,
+                         const void* value_cache, int64_t cache_block_stride,
+                         const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                         const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
+                         int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                         int head_size, int block_size, int num_blocks, float softmax_scale,
+                         int common_prefix_len, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream) {
+  return cascade_impl(nullptr, q, q_token_stride, const_cast<void*>(key_cache),
+                      const_cast<void*>(value_cache), cache_block_stride, cu_seqlens_q, seqused_k,
+                      block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+                      num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
+                      common_prefix_len, out, lse, workspace, workspace_bytes, dtype, dev_status,
+                      stream);
+}
+
+pa_status pa_cascade_fwd_with_update(const pa_kv_update* update, const void* q,
+                                     int64_t q_token_stride, void* key_cache, void* value_cache,
+                                     int64_t cache_block_stride, const int32_t* cu_seqlens_q,
+                                     const int32_t* seqused_k, const int32_t* block_table,
+                                     int bt_stride, int num_seqs, int total_q, int max_seqlen_q,
+                                     int max_seqlen_k, int num_heads, int num_kv_heads,
+                                     int head_size, int block_size, int num_blocks,
+                                     float softmax_scale, int common_prefix_len, void* out,
+                                     float* lse, void* workspace, size_t workspace_bytes,
+                                     int dtype, int32_t* dev_status, void* stream) {
+  return cascade_impl(update, q, q_token_stride, key_cache, value_cache, cache_block_stride,
+                      cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
+                      max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size, block_size,
+                      num_blocks, softmax_scale, common_prefix_len, out, lse, workspace,
+                      workspace_bytes, dtype, dev_status, stream);
 }
 
 }  // extern "C"

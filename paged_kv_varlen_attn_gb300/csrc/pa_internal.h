@@ -125,7 +125,8 @@ struct AttnArgs {
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t kstride,
                                      int64_t vstride, void* kc, void* vc, int64_t block_stride,
                                      const int64_t* slots, int num_tokens, int H_kv, int D, int bs,
-                                     int num_blocks, int32_t* status, cudaStream_t st, int sms);
+                                     int num_blocks, int32_t* status, cudaStream_t st, int sms,
+                                     bool pdl);
 cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* alse,
                          const void* b, const float* blse, int T, int H, int D, cudaStream_t st,
                          int sms);

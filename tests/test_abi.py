@@ -148,3 +148,41 @@ def test_binding_refuses_cpu_tensors():
     c = torch.zeros(4, 16, 8, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         pa.reshape_and_cache(x, x, c, c, torch.zeros(2, dtype=torch.int64))
+
+
+def _upd(**kw):
+    a = dict(key=FAKE, value=FAKE, ks=1024, vs=1024, slots=FAKE, n=4)
+    a.update(kw)
+    return pa.KvUpdate(a["key"], a["value"], a["ks"], a["vs"], a["slots"], a["n"])
+
+
+def _varlen_upd(lib, upd, **kw):
+    a = dict(q=FAKE, qs=32 * 128, kc=FAKE, vc=FAKE, cbs=16 * 8 * 128, cu=FAKE, lens=FAKE,
+             bt=FAKE, bts=4, S=2, T=2, mq=1, mk=64, H=32, Hk=8, D=128, bs=16, nb=10,
+             scale=0.088, causal=1, out=FAKE, lse=None, ws=FAKE, wsb=1 << 20, dtype=0)
+    a.update(kw)
+    return lib.pa_varlen_fwd_with_update(
+        ctypes.byref(upd) if upd is not None else None, a["q"], a["qs"], a["kc"], a["vc"],
+        a["cbs"], a["cu"], a["lens"], a["bt"], a["bts"], a["S"], a["T"], a["mq"], a["mk"], a["H"],
+        a["Hk"], a["D"], a["bs"], a["nb"], a["scale"], a["causal"], a["out"], a["lse"], a["ws"],
+        a["wsb"], a["dtype"], None, None)
+
+
+def test_update_entry_validation(lib):
+    """The K/V update of an update-and-attend call is checked like
+    pa_reshape_and_cache's arguments before anything is launched."""
+    assert _varlen_upd(lib, _upd(n=-1)) == pa.PA_ERR_INVALID_ARG
+    assert _varlen_upd(lib, _upd(key=None)) == pa.PA_ERR_INVALID_ARG
+    assert _varlen_upd(lib, _upd(key=FAKE + 2)) == pa.PA_ERR_INVALID_ARG   # misaligned
+    assert _varlen_upd(lib, _upd(slots=FAKE + 4)) == pa.PA_ERR_INVALID_ARG
+    assert _varlen_upd(lib, _upd(ks=512)) == pa.PA_ERR_INVALID_ARG        # shorter than a row
+    assert _varlen_upd(lib, _upd(), bs=24) == pa.PA_ERR_BLOCK_SIZE
+    # attention arguments are still checked
+    assert _varlen_upd(lib, _upd(), scale=0.0) == pa.PA_ERR_INVALID_ARG
+    # nothing to do: no update and an empty batch, or an update of zero tokens
+    assert _varlen_upd(lib, None, S=0, T=0) == pa.PA_OK
+    assert _varlen_upd(lib, _upd(n=0), S=0, T=0) == pa.PA_OK
+    args = [ctypes.byref(_upd(n=-1)), FAKE, 32 * 128, FAKE, FAKE, 16 * 8 * 128, FAKE, FAKE, FAKE,
+            200, 2, 2, 1, 64, 32, 8, 128, 16, 10, 0.088, 16, FAKE, None, FAKE, 1 << 20, 0, None,
+            None]
+    assert lib.pa_cascade_fwd_with_update(*args) == pa.PA_ERR_INVALID_ARG
