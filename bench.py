@@ -51,8 +51,8 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 # ---------------------------------------------------------------------------
 def is_prefill(wl, s):
-    """Segments with more than 64 packed query rows run on the tensor-core kernel."""
-    return wl.q_lens[s] * (wl.num_heads // wl.num_kv_heads) > 64
+    """Segments with more than 32 packed query rows run on the tensor-core kernel."""
+    return wl.q_lens[s] * (wl.num_heads // wl.num_kv_heads) > 32
 
 
 def algorithmic_counts(wl: W.Workload, seqs=None, cascade=False):

@@ -64,7 +64,12 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
   using C = SplitCfg<D>;
   constexpr int KS = 4 / RGN;       // warps per row group
   constexpr int KW = C::BN / KS;    // keys per warp per tile
-  constexpr int NT = KW / 8;        // 8-key n-tiles per warp per tile
+  // A warp's keys of a tile are processed in chunks of at most 32 (one online
+  // softmax step each), so the score fragments of a 64-key slice (RGN = 4)
+  // do not push the consumer past its register budget.
+  constexpr int KWC = KW < 32 ? KW : 32;   // keys per chunk
+  constexpr int NCH = KW / KWC;            // chunks per tile
+  constexpr int NT = KWC / 8;              // 8-key n-tiles per chunk
   constexpr int DK = D / 16;        // 16-dim k-steps
   constexpr int DN = D / 8;         // 8-dim n-tiles of O
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -146,6 +151,11 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
       }
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+      const int cs = slice0 + ch * KWC;        // first key of the chunk in the tile
+      const int ckey = tile_key0 + cs;
+      if (ckey >= ke || ckey > lim_max) break;  // later chunks are past the range too
       float sacc[NT][4];
 #pragma unroll
       for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
@@ -156,7 +166,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
         const int half = kk >> 2, col = (kk & 3) * 16;
 #pragma unroll
         for (int np = 0; np < NT / 2; ++np) {
-          const int key = slice0 + np * 16 + rr + ((mat >> 1) << 3);
+          const int key = cs + np * 16 + rr + ((mat >> 1) << 3);
           const int c = col + ((mat & 1) << 3);
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kbase + half * C::HALF_BYTES + sw128(key, c), b0, b1, b2, b3);
@@ -170,7 +180,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
       for (int n = 0; n < NT; ++n) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int key = key_base + n * 8 + 2 * cq + (e & 1);
+          const int key = ckey + n * 8 + 2 * cq + (e & 1);
           const int r = e >> 1;
           const bool ok = key < ke && key <= lim[r];
           const float v = ok ? sacc[n][e] * sl2 : -INFINITY;
@@ -216,7 +226,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
 #pragma unroll
         for (int dp = 0; dp < D / 16; ++dp) {
           const int half = dp >> 2, col = (dp & 3) * 16;
-          const int key = slice0 + kk * 16 + rr + ((mat & 1) << 3);
+          const int key = cs + kk * 16 + rr + ((mat & 1) << 3);
           const int c = col + ((mat >> 1) << 3);
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(vbase + half * C::HALF_BYTES + sw128(key, c), b0, b1, b2, b3);
@@ -224,6 +234,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
           mma_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
         }
       }
+      }   // chunk
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);

@@ -45,7 +45,7 @@ struct PassDims {
 // Which kernels a pass can need, from host-known bounds only.
 bool pass_has_tc(const PassDims& d) {
   const long long rows = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
-  return kTcAvailable && rows > kRowsSplit;
+  return kTcAvailable && rows > kTcMinRows;
 }
 bool pass_has_split(const PassDims& d) { return !d.single || !pass_has_tc(d); }
 

@@ -15,6 +15,11 @@ namespace pa {
 // one (query token, query head) pair of a KV-head group: packed row r of a
 // segment is token r / G, head-in-group r % G (GQA heads share the K/V tile).
 constexpr int kRowsSplit = 64;     // split-KV kernel (decode and short queries)
+// Segments with more packed query rows than this run on the prefill kernel
+// (measured on 64-row segments: 3.8 TB/s there against 3.3 TB/s through the
+// split kernel's four 16-row groups; 32-row segments stay on the split kernel
+// at 5.2 TB/s).
+constexpr int kTcMinRows = 32;
 constexpr int kRowsTc = 256;       // tcgen05 prefill kernel: two 128-row Q tiles
 constexpr int kTcTileRows = 128;   // rows of one Q tile (the MMA M dimension)
 constexpr int kKeyTile = 64;       // keys per pipeline stage / split granularity

@@ -7,8 +7,9 @@
 // reads a device value and the call needs no synchronisation.
 //
 // For each segment (a sequence, or the whole batch in the cascade prefix pass)
-// the planner picks a class -- 0: the split-KV kernel (<= 64 packed query rows,
-// i.e. decode and short queries), 1: the tensor-core prefill kernel -- cuts the
+// the planner picks a class -- 0: the split-KV kernel (at most kTcMinRows = 32
+// packed query rows, i.e. decode and short queries; items of up to 64 rows when
+// the prefill kernel is not used), 1: the tensor-core prefill kernel -- cuts the
 // packed rows into row tiles, and splits the keys into equal chunks so that
 // each class has about `target` work items per KV head. Chunk length
 //   L = max(min chunk of the class, ceil(W / target)) rounded up to kKeyTile,
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (P.check_cascade && q_len > kv) bad |= PA_DEV_CASCADE;
     if (bad) flag_status(P.status, bad);
     const int rows = q_len * G;
-    const int cls = (P.tc_enabled && rows > kRowsSplit) ? 1 : 0;
+    const int cls = (P.tc_enabled && rows > kTcMinRows) ? 1 : 0;
     const int nrt = (rows + (cls ? kRowsTc : kRowsSplit) - 1) / (cls ? kRowsTc : kRowsSplit);
     const unsigned long long w = static_cast<unsigned long long>(nrt) * static_cast<unsigned>(kv);
     if (cls) w1 += w; else w0 += w;
