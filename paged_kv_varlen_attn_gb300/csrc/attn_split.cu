@@ -311,7 +311,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
     lse_nat[r] = any ? (m[r] + fast_log2(l[r])) * kLn2 : -INFINITY;
   }
   const int H = a.H;
-  if (nsplit == 1 && !a.partials_only && !a.merge_parts) {
+  if (nsplit == 1 && !a.partials_only) {
     if (ks > 0) return;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -355,7 +355,6 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
   asm volatile("bar.sync 2, 128;" ::: "memory");
   if (!sh.flags[1]) return;
   __threadfence();
-  if (a.merge_parts) pdl_wait();   // the prefix pass's partials are complete
   combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, threadIdx.x, 128);
   if (threadIdx.x == 0) *counter = 0;   // ready for the next call
 }

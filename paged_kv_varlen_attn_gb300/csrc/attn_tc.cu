@@ -236,7 +236,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   float lse_nat = any ? (m_use + fast_log2(l)) * kLn2 : -INFINITY;
   const int slot = slot_base + rt * nsplit + j;
   const int64_t srow = slot_row(a, slot, hk, rl);
-  const bool partial = nsplit > 1 || a.partials_only || a.merge_parts;
+  const bool partial = nsplit > 1 || a.partials_only;
   // The output leaves through shared memory: each warp stages 32 rows x 32
   // columns in its quarter of Q tile X (free once the last S_X product has
   // completed, which the pv_done wait above implies) and stores them so that
@@ -297,7 +297,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
     __syncwarp();
   }
   if (rvalid) {
-    if (nsplit > 1 || a.partials_only || a.merge_parts) {
+    if (nsplit > 1 || a.partials_only) {
       __stcg(a.part_lse + srow, lse_nat);
     } else if (a.lse) {
       a.lse[static_cast<int64_t>(head) * a.lse_stride + tok] = lse_nat;
@@ -477,7 +477,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (X == 0 || two)
       tc_softmax_tile<D>(a, bars, smem, tmem, X, q_start, q_len, kv_len, kb, ke, ntiles, row0,
                          R, hk, nsplit, slot_base, rt, j);
-    if ((nsplit > 1 || a.merge_parts) && !a.partials_only) {
+    if (nsplit > 1 && !a.partials_only) {
       // Both warpgroups (256 threads) take part, active tile or not.
       __threadfence();
       asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -488,7 +488,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (bars->last) {
         __threadfence();
-        if (a.merge_parts) pdl_wait();   // the prefix pass's partials are complete
         combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, tid, 256);
         if (tid == 0) *counter = 0;
       }

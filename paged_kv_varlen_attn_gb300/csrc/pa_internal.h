@@ -92,10 +92,11 @@ struct AttnArgs {
   __nv_bfloat16* out;        // [T, H, D] bf16 (final) or NULL
   float* lse;                // [H, lse_stride] natural log or NULL
   int lse_stride;            // = total_q
-  // Cascade. Prefix pass: partials_only = 1, every work item writes its
-  // partial state to its slot and nothing is combined. Suffix pass:
-  // merge_parts = 1, each final row is merged with the prefix pass's partial
-  // states of the same row (prefix segment 0's split info and slot pools).
+  // Cascade. Both passes run with partials_only = 1: every work item writes
+  // its partial state to its slot and nothing is combined. The combine
+  // kernel then runs with merge_parts = 1: each suffix row's states are
+  // merged with the prefix pass's states of the same row (prefix segment 0's
+  // split info and slot pools, mp_*).
   int partials_only;
   int merge_parts;
   const int4* mp_seg;
