@@ -354,3 +354,34 @@ def test_full_size_config_sampled(name, seqs):
     for s, (tok, ro, rl) in ref.items():
         assert_close(out, lse, ro, rl, tokens=tok)
     assert int(status.item()) == 0
+
+
+# ---------------------------------------------------------------- size edges
+def test_many_sequences_planner_global_tables():
+    """More sequences than the planner keeps in shared memory (1,024): its
+    segment tables live in the workspace instead; mixed decode and short
+    prefill rows, ragged lengths."""
+    g = torch.Generator().manual_seed(91)
+    S = 1100
+    kv = [int(x) for x in torch.randint(1, 160, (S,), generator=g)]
+    ql = [1 if float(torch.rand((1,), generator=g)) < 0.8 else min(k, int(torch.randint(2, 24, (1,), generator=g)))
+          for k in kv]
+    wl = W._build("many_seqs", 91, 8, 2, 64, 16, ql, kv, g)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse, _ = run_gpu(wl, status=status)
+    ref_o, ref_l = oracle_full(wl)
+    assert_close(out, lse, ref_o, ref_l)
+    assert int(status.item()) == 0
+
+
+def test_long_context_decode_many_splits():
+    """Two decode sequences of 131,072 and 65,535 keys: one row tile split
+    into many KV chunks whose partial states the last CTA merges."""
+    g = torch.Generator().manual_seed(92)
+    wl = W._build("long_decode", 92, 32, 8, 128, 16, [1, 1], [131072, 65535], g)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse, _ = run_gpu(wl, status=status)
+    ref = oracle_sampled(wl, {0: [0], 1: [0]})
+    for s, (tokens, ro, rl) in ref.items():
+        assert_close(out, lse, ro, rl, tokens=tokens)
+    assert int(status.item()) == 0
