@@ -196,6 +196,28 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
                          size_t workspace_bytes, int dtype, int32_t* dev_status, void* stream);
 
 /*
+ * pa_use_cascade_attention -- should a batch run as cascade attention?
+ * ([FA-vLLM] §6.2, use_cascade_attention: a shared prefix of at least 256
+ * tokens, at least 8 requests, no ALiBi / sliding window / local attention
+ * and no DCP -- none of which this library has -- then cascade outright if
+ * split-KV decoding is off, else whichever of the two is estimated faster.)
+ * The pages leave the estimate open; this one compares bytes: flat attention
+ * reads the shared prefix once per sequence, cascade reads it once and pays
+ * a fixed cost for its extra pass and merge, so cascade is chosen when
+ *   (num_seqs - 1) * common_prefix_len * num_kv_heads * head_size * 4 bytes
+ *     > PA_CASCADE_FIXED_US * 1e-6 * PA_CASCADE_HBM_GBS * 1e9,
+ * i.e. when re-reading the prefix would cost more than the extra pass.
+ *   split_kv : 1 if the flat path may split keys over CTAs (pa_varlen_fwd
+ *              does), 0 if not.
+ * Writes 1 (cascade) or 0 (flat) to *use_cascade. Host only, no CUDA call.
+ * PA_ERR_INVALID_ARG for negative sizes or a NULL use_cascade.
+ */
+#define PA_CASCADE_FIXED_US 20.0
+#define PA_CASCADE_HBM_GBS 6500.0
+pa_status pa_use_cascade_attention(int common_prefix_len, int num_seqs, int num_kv_heads,
+                                   int head_size, int split_kv, int* use_cascade);
+
+/*
  * New tokens' K/V for the update-and-attend entry points below: the
  * arguments of pa_reshape_and_cache that are not already arguments of the
  * attention call. key / value: [num_tokens, num_kv_heads, head_size] bf16,

@@ -43,6 +43,7 @@ EXPORTS = (
     "pa_varlen_fwd_noalloc",
     "pa_varlen_fwd_with_update",
     "pa_cascade_fwd_with_update",
+    "pa_use_cascade_attention",
 )
 
 _lib = None
@@ -79,6 +80,7 @@ _SIGS = {
                         _vp], _i32),
     "pa_varlen_fwd_with_update": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS, _i32),
     "pa_cascade_fwd_with_update": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS, _i32),
+    "pa_use_cascade_attention": ([_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)], _i32),
 }
 
 
@@ -171,6 +173,17 @@ def cascade_fwd_workspace_size(num_seqs, total_q, max_seqlen_q, max_seqlen_k, nu
     return load_library().pa_cascade_fwd_workspace_size(
         num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size,
         block_size, sm_count)
+
+
+def use_cascade_attention(common_prefix_len, num_seqs, num_kv_heads, head_size, split_kv=True):
+    """Whether a batch whose sequences share common_prefix_len tokens should
+    run as cascade attention (host-side policy, no GPU needed)."""
+    out = _i32(0)
+    _check(load_library().pa_use_cascade_attention(int(common_prefix_len), int(num_seqs),
+                                                   int(num_kv_heads), int(head_size),
+                                                   int(bool(split_kv)), ctypes.byref(out)),
+           "pa_use_cascade_attention")
+    return bool(out.value)
 
 
 def alloc_workspace(nbytes, device):

@@ -501,6 +501,26 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
   return launch_pass(c, tmK, tmV, tmQ, a, ws, L, &first);
 }
 
+pa_status pa_use_cascade_attention(int common_prefix_len, int num_seqs, int num_kv_heads,
+                                   int head_size, int split_kv, int* use_cascade) {
+  if (!use_cascade || common_prefix_len < 0 || num_seqs < 0 || num_kv_heads <= 0 ||
+      head_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  *use_cascade = 0;
+  if (common_prefix_len < 256 || num_seqs < 8) return PA_OK;   // the pages' two thresholds
+  if (!split_kv) {
+    *use_cascade = 1;
+    return PA_OK;
+  }
+  // Bytes of the shared prefix that flat attention re-reads (K and V, bf16)
+  // against the bytes the cascade's fixed cost could have moved.
+  const double reread = static_cast<double>(num_seqs - 1) * common_prefix_len * num_kv_heads *
+                        head_size * 4.0;
+  const double fixed = PA_CASCADE_FIXED_US * 1e-6 * PA_CASCADE_HBM_GBS * 1e9;
+  *use_cascade = reread > fixed ? 1 : 0;
+  return PA_OK;
+}
+
 pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_cache,
                         const void* value_cache, int64_t cache_block_stride,
                         const int32_t* cu_seqlens_q, const int32_t* seqused_k,

@@ -186,3 +186,29 @@ def test_update_entry_validation(lib):
             200, 2, 2, 1, 64, 32, 8, 128, 16, 10, 0.088, 16, FAKE, None, FAKE, 1 << 20, 0, None,
             None]
     assert lib.pa_cascade_fwd_with_update(*args) == pa.PA_ERR_INVALID_ARG
+
+
+def test_use_cascade_attention_policy(lib):
+    """The pages' use_cascade_attention rules (a shared prefix of >= 256
+    tokens, >= 8 requests; cascade outright without split-KV), then this
+    library's byte estimate: cascade iff re-reading the prefix per sequence
+    costs more than the cascade's fixed 20 us at 6.5 TB/s."""
+    def use(P, S, Hk=8, D=128, split=1):
+        out = ctypes.c_int(-1)
+        assert lib.pa_use_cascade_attention(P, S, Hk, D, split, ctypes.byref(out)) == pa.PA_OK
+        return out.value
+    assert use(255, 64, split=0) == 0          # prefix too short
+    assert use(256, 7, split=0) == 0           # too few requests
+    assert use(256, 8, split=0) == 1           # no split-KV: cascade outright
+    assert use(2048, 64) == 1                  # the shared-prompt workload
+    assert use(256, 8) == 0                    # small prefix, few requests: flat
+    # boundary of the estimate: (S-1)*P*Hk*D*4 > 20e-6 * 6.5e12 = 1.3e8 bytes
+    assert use(4534, 8) == 0                   # 7*4534*4096 = 129,998,848 bytes: just below
+    bound = 20e-6 * 6500.0 * 1e9
+    for P in (4530, 4531, 4532, 4533, 4534, 4535, 4536):
+        assert use(P, 8) == int(7 * P * 8 * 128 * 4 > bound)
+    out = ctypes.c_int(0)
+    assert lib.pa_use_cascade_attention(-1, 8, 8, 128, 1, ctypes.byref(out)) == \
+        pa.PA_ERR_INVALID_ARG
+    assert lib.pa_use_cascade_attention(256, 8, 8, 128, 1, None) == pa.PA_ERR_INVALID_ARG
+    assert pa.use_cascade_attention(2048, 64, 8, 128) is True
