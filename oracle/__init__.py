@@ -11,4 +11,11 @@ from .paged_attention import (  # noqa: F401
     merge_attn_states,
     cascade_attention,
     cascade_attention_steps,
+    e4m3_decode,
+    e4m3_encode,
+    e4m3_round,
+    quantize_e4m3,
+    dequantize_e4m3,
+    reshape_and_cache_e4m3,
+    varlen_attention_e4m3,
 )

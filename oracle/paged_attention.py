@@ -249,3 +249,130 @@ def cascade_attention_steps(q, key_cache, value_cache, cu_seqlens_q, seqused_k, 
         suf_out[q0:q1] = o
         suf_lse[:, q0:q1] = l
     return merge_attn_states(pfx_out, pfx_lse, suf_out, suf_lse)
+
+
+# --------------------------------------------------------------------------
+# FP8 (e4m3) KV cache ([FA/FI] 役割 and 境界と失敗: FlashInfer and FA3 accept an
+# fp8 / fp8_e4m3 KV cache with per-head quant scales; [FA-vLLM] §10 lists an FP8
+# KV cache among the backends' features). The pools hold e4m3 bytes; a byte c
+# of KV head h means e4m3(c) * scale[h], and a new row is written as
+# e4m3(x / scale[h]). The pages do not define the format, so it is the OCP
+# 8-bit floating point "E4M3" one: 1 sign, 4 exponent bits (bias 7), 3
+# mantissa bits; normal values 2^(e-7) * (1 + m/8) for e = 1..15, except the
+# all-ones pattern S.1111.111, which is NaN; subnormals 2^-6 * m/8; largest
+# finite 448; no infinities. Readings where the pages are silent: rounding is
+# to nearest with ties to even, values beyond 448 saturate to +-448, and the
+# division x / scale is IEEE float32 (the precision that decides the code
+# is the kernel's).
+# --------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one e4m3 byte (NaN for S.1111.111)."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def e4m3_round(y: float) -> float:
+    """Nearest e4m3 value to y (ties to even), saturating at +-448.
+
+    Within [2^E, 2^(E+1)) (E >= -6; E = -6 also covers the subnormals
+    [0, 2^-6)) the e4m3 values are the multiples of q = 2^(E-3), so y rounds
+    to the nearest multiple of q; on a tie the even multiple wins, which is
+    the value whose last mantissa bit is 0.
+    """
+    if y != y:
+        return y
+    a = abs(y)
+    if a >= E4M3_MAX:
+        return math.copysign(E4M3_MAX, y)
+    if a == 0.0:
+        return math.copysign(0.0, y)
+    E = -6
+    while E < 8 and 2.0 ** (E + 1) <= a:
+        E += 1
+    q = 2.0 ** (E - 3)
+    n = a / q                  # exact: q is a power of two
+    r = math.floor(n)
+    frac = n - r
+    if frac > 0.5 or (frac == 0.5 and r % 2 == 1):
+        r += 1
+    return math.copysign(min(r * q, E4M3_MAX), y)
+
+
+def e4m3_encode(y: float) -> int:
+    """The e4m3 byte of e4m3_round(y); NaN encodes as 0x7F."""
+    v = e4m3_round(y)
+    if v != v:
+        return 0x7F
+    sign = 0x80 if math.copysign(1.0, v) < 0 else 0
+    a = abs(v)
+    if a == 0.0:
+        return sign
+    if a < 2.0 ** -6:                      # subnormal: a = (m/8) * 2^-6
+        return sign | int(a / 2.0 ** -9)
+    e = 0
+    while 2.0 ** (e + 1) <= a:
+        e += 1
+    while 2.0 ** e > a:
+        e -= 1
+    m = int((a / 2.0 ** e - 1.0) * 8.0)    # exact: a has at most 4 significant bits
+    return sign | ((e + 7) << 3) | m
+
+
+def e4m3_table():
+    """float64 [256]: the value of every e4m3 byte."""
+    return torch.tensor([e4m3_decode(c) for c in range(256)], dtype=F64)
+
+
+def quantize_e4m3(x, scale):
+    """e4m3 bytes (uint8, same shape) of x / scale[h] for x [..., H_kv, D].
+
+    x / scale is IEEE float32 division; the quotient then rounds to the
+    nearest e4m3 value as in e4m3_round, found here by searching the sorted
+    finite non-negative values (codes 0x00 .. 0x7E, increasing with the code):
+    the closer neighbour wins, a tie goes to the even code, |y| >= 448 gives
+    0x7E, and the sign bit is copied.
+    """
+    s = torch.as_tensor(scale, dtype=torch.float32).reshape(-1)
+    y = (x.to(torch.float32) / s[:, None]).to(F64)          # float32 quotient, exact in f64
+    vals = e4m3_table()[:0x7F]                              # 0, 2^-9, ..., 448
+    a = y.abs()
+    hi = torch.searchsorted(vals, a.contiguous()).clamp(max=0x7E)
+    lo = (hi - 1).clamp(min=0)
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = torch.where(pick_hi, hi, lo)
+    code = torch.where(a >= E4M3_MAX, torch.full_like(code, 0x7E), code)
+    code = torch.where(torch.signbit(y), code | 0x80, code)
+    code = torch.where(torch.isnan(y), torch.full_like(code, 0x7F), code)
+    return code.to(torch.uint8)
+
+
+def dequantize_e4m3(codes, scale):
+    """float64 e4m3(codes) * scale[h] for codes [..., H_kv, D]."""
+    s = torch.as_tensor(scale, dtype=torch.float32).to(F64).reshape(-1)
+    return e4m3_table()[codes.long()] * s[:, None]
+
+
+def reshape_and_cache_e4m3(key, value, slot_mapping, key_cache, value_cache, k_scale, v_scale):
+    """The FP8 cache write: reshape_and_cache of the e4m3 bytes of
+    key / k_scale[h] and value / v_scale[h] into uint8 pools."""
+    reshape_and_cache(quantize_e4m3(key, k_scale), quantize_e4m3(value, v_scale), slot_mapping,
+                      key_cache, value_cache)
+
+
+def varlen_attention_e4m3(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
+                          softmax_scale, causal, k_scale, v_scale, rows=None):
+    """Varlen attention over e4m3 pools: the plain definition applied to the
+    dequantized keys and values e4m3(c) * scale[h]."""
+    return varlen_attention(q, dequantize_e4m3(key_cache, k_scale),
+                            dequantize_e4m3(value_cache, v_scale), cu_seqlens_q, seqused_k,
+                            block_table, softmax_scale, causal, rows=rows)

@@ -478,3 +478,175 @@ def test_planted_dropped_scale_is_caught(monkeypatch):
         return real(q, k, v, 1.0, *a, **kw)
     monkeypatch.setattr(oracle, "attend_dense", no_scale)
     assert _fails(check_golden_two_key)
+
+
+# ----------------------------------------------------------------------------
+# FP8 (e4m3) KV cache ("FlashAttention と FlashInfer" 役割 / 境界と失敗: fp8_e4m3
+# KV cache with per-head quant scales). The format is the OCP 8-bit floating
+# point E4M3 one (bias 7, 3 mantissa bits, max 448, S.1111.111 = NaN).
+# ----------------------------------------------------------------------------
+E4M3_POINTS = {
+    0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9,   # subnormals m/8 * 2^-6
+    0x08: 2.0 ** -6,                                   # smallest normal
+    0x38: 1.0, 0x39: 1.125, 0x3F: 1.875,               # e = 7: 1 + m/8
+    0x77: 240.0, 0x7E: 448.0,                          # e = 14, e = 15 (m <= 6)
+    0xB8: -1.0, 0xFE: -448.0,
+}
+
+
+def check_e4m3_points():
+    for code, v in E4M3_POINTS.items():
+        assert P.e4m3_decode(code) == v, hex(code)
+        assert P.e4m3_encode(v) == code, hex(code)
+    assert math.isnan(P.e4m3_decode(0x7F)) and math.isnan(P.e4m3_decode(0xFF))
+    assert P.e4m3_encode(-0.0) == 0x80
+
+
+def check_e4m3_round_vs_torch():
+    """Every value near a rounding boundary: all e4m3 values, the midpoints
+    between neighbours, and one float32 step either side of each, plus a random
+    spread; torch's float8_e4m3fn conversion rounds to nearest even (and agrees
+    with saturation for |x| < 464)."""
+    vals = P.e4m3_table()[:0x7F]
+    pts = set(vals.tolist())
+    for a, b in zip(vals[:-1].tolist(), vals[1:].tolist()):
+        mid = torch.tensor((a + b) / 2, dtype=torch.float32)
+        pts.update([float(mid), float(torch.nextafter(mid, torch.tensor(0.0))),
+                    float(torch.nextafter(mid, torch.tensor(1e9)))])
+    pts.update([452.0, 455.99, 460.0, 463.9])
+    g = torch.Generator().manual_seed(7)
+    pts.update((torch.randn(2000, generator=g) * 30).tolist())
+    pts.update((torch.rand(2000, generator=g) * 2.0 ** -5).tolist())
+    x = torch.tensor(sorted(pts), dtype=torch.float32)
+    x = torch.cat([x, -x])
+    x = x[x.abs() < 464]
+    ref = x.to(torch.float8_e4m3fn)
+    got_codes = P.quantize_e4m3(x.view(-1, 1, 1), [1.0]).view(-1)
+    assert torch.equal(got_codes, ref.view(torch.uint8)), "vector quantizer"
+    for xi, ri in zip(x.tolist()[::7], ref.float().tolist()[::7]):
+        assert P.e4m3_round(xi) == ri, xi
+
+
+def test_e4m3_format_points():
+    check_e4m3_points()
+
+
+def test_e4m3_decode_matches_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(F64)
+    got = P.e4m3_table()
+    nan = torch.isnan(ref)
+    assert torch.equal(nan, torch.isnan(got)) and nan.sum() == 2
+    assert torch.equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_round_matches_torch():
+    check_e4m3_round_vs_torch()
+
+
+def test_e4m3_code_roundtrip_and_saturation():
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        assert P.e4m3_encode(P.e4m3_decode(c)) == c
+    # Beyond the largest finite value the write saturates (torch does not).
+    for v, code in ((464.0, 0x7E), (1e6, 0x7E), (math.inf, 0x7E), (-500.0, 0xFE),
+                    (-math.inf, 0xFE)):
+        assert P.e4m3_encode(v) == code
+        assert int(P.quantize_e4m3(torch.tensor([[[v]]]), [1.0])) == code
+    assert int(P.quantize_e4m3(torch.tensor([[[math.nan]]]), [1.0])) == 0x7F
+
+
+def test_e4m3_quotient_is_float32():
+    # 5.28125 / 0x1.018618p+0 is 5.25000012 in float64 -- above the midpoint
+    # of 5.0 and 5.5 -- but exactly 5.25 in float32, a tie that goes to the
+    # even neighbour 5.0 (code 0x4A). The code is decided by the float32
+    # quotient, as the kernel computes it.
+    s = float.fromhex("0x1.018618p+0")
+    x = torch.tensor([[[5.28125]]], dtype=torch.bfloat16)
+    assert int(P.quantize_e4m3(x, [s])) == 0x4A
+    assert P.e4m3_encode(5.28125 / s) == 0x4B
+
+
+def test_e4m3_per_head_scale_and_error_bound():
+    g = torch.Generator().manual_seed(3)
+    x = (torch.randn(6, 4, 16, generator=g) * 3).to(torch.bfloat16)
+    sc = [0.5, 1.0, 0.0625, 3.0]
+    codes = P.quantize_e4m3(x, sc)
+    for h in range(4):
+        brute = [P.e4m3_encode(float(torch.tensor(float(v), dtype=torch.float32) /
+                                     torch.tensor(sc[h], dtype=torch.float32)))
+                 for v in x[:, h].reshape(-1).tolist()]
+        assert codes[:, h].reshape(-1).tolist() == brute
+    dq = P.dequantize_e4m3(codes, sc)
+    xs = x.to(F64)
+    s = torch.tensor(sc, dtype=F64)[:, None]
+    # Half a unit in the last place: 2^-4 relative in the normal range, and
+    # 2^-10 * scale absolute among the subnormals.
+    bound = torch.maximum(xs.abs() * 2.0 ** -4, 2.0 ** -10 * s.expand_as(xs))
+    assert ((dq - xs).abs() <= bound + 1e-12).all()
+
+
+def test_e4m3_scatter_brute_force():
+    g = torch.Generator().manual_seed(5)
+    key = torch.randn(5, 2, 128, generator=g).to(torch.bfloat16)
+    value = torch.randn(5, 2, 128, generator=g).to(torch.bfloat16)
+    kc = torch.full((3, 16, 2, 128), 0x55, dtype=torch.uint8)
+    vc = kc.clone()
+    slots = torch.tensor([17, -1, 0, 47, 5], dtype=torch.int64)
+    P.reshape_and_cache_e4m3(key, value, slots, kc, vc, [0.25, 2.0], [1.0, 0.5])
+    for t, slot in enumerate(slots.tolist()):
+        if slot < 0:
+            continue
+        b, r = divmod(slot, 16)
+        for h, (ks, vs) in enumerate(((0.25, 1.0), (2.0, 0.5))):
+            assert kc[b, r, h].tolist() == [P.e4m3_encode(float(torch.tensor(float(v)) / ks))
+                                            for v in key[t, h].tolist()]
+            assert vc[b, r, h].tolist() == [P.e4m3_encode(float(torch.tensor(float(v)) / vs))
+                                            for v in value[t, h].tolist()]
+    untouched = torch.ones(3 * 16, dtype=torch.bool)
+    untouched[[17, 0, 47, 5]] = False
+    assert (kc.view(48, -1)[untouched] == 0x55).all()
+
+
+def test_e4m3_attention_is_attention_of_dequantized_pool():
+    # Codes 0x38 (1.0) and 0xB8 (-1.0) with scale 0.5 are keys of +-0.5: two
+    # keys whose scores differ by q.(k0 - k1); closed form of a 2-key softmax.
+    D = 128
+    kc = torch.zeros(1, 16, 1, D, dtype=torch.uint8)
+    vc = torch.zeros(1, 16, 1, D, dtype=torch.uint8)
+    kc[0, 0, 0, 0] = 0x38
+    kc[0, 1, 0, 0] = 0xB8
+    vc[0, 0, 0, :] = 0x40          # 2.0
+    vc[0, 1, 0, :] = 0x00          # 0.0
+    q = torch.zeros(1, 1, D, dtype=torch.bfloat16)
+    q[0, 0, 0] = 2.0
+    out, lse = P.varlen_attention_e4m3(q, kc, vc, torch.tensor([0, 1]), torch.tensor([2]),
+                                       torch.tensor([[0]], dtype=torch.int32), 1.0, False,
+                                       [0.5], [3.0])
+    s0, s1 = 2.0 * 0.5, 2.0 * -0.5
+    w0 = math.exp(s0) / (math.exp(s0) + math.exp(s1))
+    assert abs(float(out[0, 0, 5]) - w0 * 6.0) < 1e-12
+    assert abs(float(lse[0, 0]) - math.log(math.exp(s0) + math.exp(s1))) < 1e-12
+
+
+def test_planted_ties_away_is_caught(monkeypatch):
+    def away(y):
+        a = abs(y)
+        if a >= P.E4M3_MAX:
+            return math.copysign(P.E4M3_MAX, y)
+        E = -6
+        while E < 8 and 2.0 ** (E + 1) <= a:
+            E += 1
+        q = 2.0 ** (E - 3)
+        return math.copysign(min(math.floor(a / q + 0.5) * q, P.E4M3_MAX), y)
+    monkeypatch.setattr(P, "e4m3_round", away)
+    with pytest.raises(AssertionError):
+        check_e4m3_round_vs_torch()
+
+
+def test_planted_exponent_bias_is_caught(monkeypatch):
+    orig = P.e4m3_decode
+    monkeypatch.setattr(P, "e4m3_decode", lambda c: orig(c) * 2.0 if c & 0x78 else orig(c))
+    with pytest.raises(AssertionError):
+        check_e4m3_points()
