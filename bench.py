@@ -12,8 +12,12 @@ pages randomly permuted). Metric: algorithmic HBM bytes per step / step time
 LSE, the block-table rows read and the scatter's read+write of the new tokens;
 workspace (split partial) traffic is not counted.
 
+With --kv-cache fp8 the page pools hold e4m3 bytes with per-KV-head scales
+(the FP8 KV cache of the FlashAttention/FlashInfer backend page): each K/V
+byte of the pool counts once, the scatter reads bf16 rows and writes bytes.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload NAME]
+                       [--workload NAME] [--kv-cache bf16|fp8]
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling, no collective on the data path); rank 0 prints one JSON line.
 """
@@ -50,12 +54,14 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 # ---------------------------------------------------------------------------
-def is_prefill(wl, s):
-    """Segments with more than 32 packed query rows run on the tensor-core kernel."""
+def is_prefill(wl, s, fp8=False):
+    """Segments with more than 32 packed query rows run on the tensor-core
+    kernel (bf16 pools; FP8 pools run every segment on the split-KV kernel,
+    but such segments are still counted as the compute-heavy prefill side)."""
     return wl.q_lens[s] * (wl.num_heads // wl.num_kv_heads) > 32
 
 
-def algorithmic_counts(wl: W.Workload, seqs=None, cascade=False):
+def algorithmic_counts(wl: W.Workload, seqs=None, cascade=False, fp8=False):
     """Bytes and FLOPs of one step by the counting rule in the module docstring.
 
     Each visible K/V byte counts once per step (for cascade, the shared prefix
@@ -68,7 +74,8 @@ def algorithmic_counts(wl: W.Workload, seqs=None, cascade=False):
     flops = {"decode": 0, "prefill": 0}
     T = 0
     bt = 0
-    per_key = Hk * D * 2 * 2
+    kv_elem = 1 if fp8 else 2
+    per_key = Hk * D * 2 * kv_elem
     for s in seqs:
         ql, kl = wl.q_lens[s], wl.kv_lens[s]
         kind = "prefill" if is_prefill(wl, s) else "decode"
@@ -85,7 +92,7 @@ def algorithmic_counts(wl: W.Workload, seqs=None, cascade=False):
         kv_bytes["decode"] += wl.common_prefix_len * per_key
     qo = 2 * T * H * D * 2
     lse = H * T * 4
-    scatter = 2 * 2 * T * Hk * D * 2
+    scatter = 2 * T * Hk * D * (2 + kv_elem)   # read bf16 K and V rows, write the pool's
     attn_bytes = kv_bytes["decode"] + kv_bytes["prefill"] + qo + lse + bt
     return {"attn_bytes": attn_bytes, "scatter_bytes": scatter,
             "step_bytes": attn_bytes + scatter, "flops": flops["decode"] + flops["prefill"],
@@ -211,7 +218,7 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
-def run_oracle_sample(wl, max_seconds=12.0, max_seqs=None):
+def run_oracle_sample(wl, max_seconds=12.0, max_seqs=None, fp8=False):
     """Returns (algorithmic bytes covered, flops covered, seconds, description)."""
     import oracle
     torch.set_num_threads(os.cpu_count() or 1)
@@ -224,7 +231,10 @@ def run_oracle_sample(wl, max_seconds=12.0, max_seqs=None):
             break
         sub = wl.sub_batch([s])
         pages = sub.pages_of(0)
-        kp, vp = sub.pool_pages(0, pages), sub.pool_pages(1, pages)
+        if fp8:
+            kp, vp = sub.fp8_pool_pages(0, pages), sub.fp8_pool_pages(1, pages)
+        else:
+            kp, vp = sub.pool_pages(0, pages), sub.pool_pages(1, pages)
         kc = torch.stack([kp[p] for p in pages])
         vc = torch.stack([vp[p] for p in pages])
         bt = torch.arange(len(pages), dtype=torch.int32)[None]
@@ -238,16 +248,24 @@ def run_oracle_sample(wl, max_seconds=12.0, max_seqs=None):
             g = torch.Generator().manual_seed(s)
             rows = {0: sorted(set(int(x) for x in torch.randint(0, ql, (64,), generator=g)))}
         t0 = time.perf_counter()
-        oracle.reshape_and_cache(sub.k_new, sub.v_new, slots, kc, vc)
-        oracle.varlen_attention(sub.q, kc, vc, sub.cu_seqlens_q, sub.seqused_k, bt,
-                                wl.softmax_scale, wl.causal, rows=rows)
+        if fp8:
+            ks, vs = wl.kv_scales(0), wl.kv_scales(1)
+            oracle.reshape_and_cache_e4m3(sub.k_new, sub.v_new, slots, kc, vc, ks, vs)
+            oracle.varlen_attention_e4m3(sub.q, kc, vc, sub.cu_seqlens_q, sub.seqused_k, bt,
+                                         wl.softmax_scale, wl.causal, ks, vs, rows=rows)
+        else:
+            oracle.reshape_and_cache(sub.k_new, sub.v_new, slots, kc, vc)
+            oracle.varlen_attention(sub.q, kc, vc, sub.cu_seqlens_q, sub.seqused_k, bt,
+                                    wl.softmax_scale, wl.causal, rows=rows)
         secs += time.perf_counter() - t0
         nrows = ql if rows is None else len(rows[0])
-        covered_bytes += kl * Hk * D * 2 * 2 + 2 * ql * H * D * 2 + H * ql * 4 + 2 * 2 * ql * Hk * D * 2
+        e = 1 if fp8 else 2
+        covered_bytes += kl * Hk * D * 2 * e + 2 * ql * H * D * 2 + H * ql * 4 + 2 * ql * Hk * D * (2 + e)
         covered_flops += 4 * D * H * nrows * kl
         n += 1
-    desc = f"{n} of {wl.num_seqs} sequences of {wl.name} (all query rows of decode sequences, " \
-           f"64 seeded rows of longer ones), scatter + attention, fp64 torch CPU"
+    desc = f"{n} of {wl.num_seqs} sequences of {wl.name}{' (e4m3 KV)' if fp8 else ''} " \
+           f"(all query rows of decode sequences, 64 seeded rows of longer ones), " \
+           f"scatter + attention, fp64 torch CPU"
     return covered_bytes, covered_flops, secs, desc
 
 
@@ -260,7 +278,8 @@ def bench_reference(args, rank, world):
     total_bytes = 0
     desc = ""
     for i in range(args.warmup + args.steps):
-        b, f, s, desc = run_oracle_sample(wl, max_seconds=3.0, max_seqs=4)
+        b, f, s, desc = run_oracle_sample(wl, max_seconds=3.0, max_seqs=4,
+                                          fp8=args.kv_cache == "fp8")
         if i >= args.warmup:
             times.append(s)
             total_bytes += b
@@ -270,7 +289,8 @@ def bench_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "sample": desc},
+            "config": {"workload": wl.name + ("+fp8_kv" if args.kv_cache == "fp8" else ""),
+                       "sample": desc},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": torch.get_num_threads(),
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -363,14 +383,24 @@ def bench_ours(args, rank, world, local):
 
     wl = W.CONFIGS[args.workload]()
     cascade = wl.common_prefix_len > 0
-    counts = algorithmic_counts(wl, cascade=cascade)
-    kc0 = wl.pool(0, device=dev)
-    vc0 = wl.pool(1, device=dev)
+    fp8 = args.kv_cache == "fp8"
+    counts = algorithmic_counts(wl, cascade=cascade, fp8=fp8)
+    if fp8:
+        kc0, vc0 = wl.fp8_pool(0, device=dev), wl.fp8_pool(1, device=dev)
+        ksc = torch.tensor(wl.kv_scales(0), dtype=torch.float32, device=dev)
+        vsc = torch.tensor(wl.kv_scales(1), dtype=torch.float32, device=dev)
+    else:
+        kc0 = wl.pool(0, device=dev)
+        vc0 = wl.pool(1, device=dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     T, H, D = wl.q.shape
-    size_fn = pa.cascade_fwd_workspace_size if cascade else pa.varlen_fwd_workspace_size
+    if fp8:
+        size_fn = pa.cascade_fwd_fp8kv_workspace_size if cascade else \
+            pa.varlen_fwd_fp8kv_workspace_size
+    else:
+        size_fn = pa.cascade_fwd_workspace_size if cascade else pa.varlen_fwd_workspace_size
     ws = pa.alloc_workspace(size_fn(wl.num_seqs, T, wl.max_seqlen_q, wl.max_seqlen_k, H,
                                     wl.num_kv_heads, D, wl.block_size, sms), dev)
     main = DeviceBatch(wl, dev)
@@ -380,7 +410,13 @@ def bench_ours(args, rank, world, local):
         w = b.wl
         args_ = (dd["q"], kc0, vc0, dd["cu_seqlens_q"], dd["seqused_k"], dd["block_table"],
                  w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale)
-        if cascade:
+        if fp8 and cascade:
+            pa.cascade_fwd_fp8kv(*args_, w.common_prefix_len, ksc, vsc, out=b.out, lse=b.lse,
+                                 workspace=ws, dev_status=status)
+        elif fp8:
+            pa.varlen_fwd_fp8kv(*args_, w.causal, ksc, vsc, out=b.out, lse=b.lse, workspace=ws,
+                                dev_status=status)
+        elif cascade:
             pa.cascade_fwd(*args_, w.common_prefix_len, out=b.out, lse=b.lse, workspace=ws,
                            dev_status=status)
         else:
@@ -389,8 +425,12 @@ def bench_ours(args, rank, world, local):
 
     def scatter(b, dd=None):
         dd = dd or b.d
-        pa.reshape_and_cache(dd["k_new"], dd["v_new"], kc0, vc0, dd["slot_mapping"],
-                             dev_status=status)
+        if fp8:
+            pa.reshape_and_cache_fp8(dd["k_new"], dd["v_new"], kc0, vc0, dd["slot_mapping"], ksc,
+                                     vsc, dev_status=status)
+        else:
+            pa.reshape_and_cache(dd["k_new"], dd["v_new"], kc0, vc0, dd["slot_mapping"],
+                                 dev_status=status)
 
     def fused(b, dd=None):
         # One serving step through the public API: the step's new K/V are
@@ -398,6 +438,16 @@ def bench_ours(args, rank, world, local):
         # overlaps the scatter).
         dd = dd or b.d
         w = b.wl
+        if fp8:
+            args_ = (dd["q"], kc0, vc0, dd["cu_seqlens_q"], dd["seqused_k"], dd["block_table"],
+                     w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale)
+            upd = dict(key=dd["k_new"], value=dd["v_new"], slot_mapping=dd["slot_mapping"],
+                       out=b.out, lse=b.lse, workspace=ws, dev_status=status)
+            if cascade:
+                pa.cascade_fwd_fp8kv(*args_, w.common_prefix_len, ksc, vsc, **upd)
+            else:
+                pa.varlen_fwd_fp8kv(*args_, w.causal, ksc, vsc, **upd)
+            return
         args_ = (dd["k_new"], dd["v_new"], dd["slot_mapping"], dd["q"], kc0, vc0,
                  dd["cu_seqlens_q"], dd["seqused_k"], dd["block_table"], w.max_seqlen_q,
                  w.max_seqlen_k, w.softmax_scale)
@@ -531,7 +581,7 @@ def bench_ours(args, rank, world, local):
     if not cascade and kinds["prefill"] and kinds["decode"]:
         for kind, seqs in kinds.items():
             b = DeviceBatch(wl.sub_batch(seqs), dev)
-            c = algorithmic_counts(wl, seqs)
+            c = algorithmic_counts(wl, seqs, fp8=fp8)
             for _ in range(3):
                 attention(b)
             torch.cuda.synchronize()
@@ -557,7 +607,8 @@ def bench_ours(args, rank, world, local):
         return
     peaks = load_peaks()
     attn_ms_avg = attn_ms / args.steps
-    config = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": H,
+    config = {"workload": wl.name + ("+fp8_kv" if fp8 else ""), "num_seqs": wl.num_seqs,
+              "num_heads": H,
               "num_kv_heads": wl.num_kv_heads, "head_size": D, "block_size": wl.block_size,
               "kv_tokens": int(sum(wl.kv_lens)), "query_tokens": T,
               "step_bytes": counts["step_bytes"], "step_flops": counts["flops"],
@@ -570,8 +621,12 @@ def bench_ours(args, rank, world, local):
         config["common_prefix_len"] = wl.common_prefix_len
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": config}
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 kv (f16 mma)" if fp8 else "bf16", "data": "synthetic",
+            "config": config}
+    if fp8:
+        config["kv_cache"] = ("e4m3 bytes, per-KV-head scales k %s v %s"
+                              % (wl.kv_scales(0), wl.kv_scales(1)))
     prefill_heavy = counts["flops_by_kind"]["prefill"] > 0
     if prefill_heavy:
         # Mixed batch: one figure of merit = t_ideal / t_measured, where
@@ -591,17 +646,21 @@ def bench_ours(args, rank, world, local):
         achieved = counts["attn_bytes"] / (attn_ms_avg * 1e-3) / 1e9
         line["e2e"] = {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        kname = "attn_split_kernel<128, fp8>" if fp8 else "attn_split_kernel<128>"
         line["roofline"] = {"bound": "hbm",
                             "kernel": ("plan + attn_tc_kernel<128> (prefix) + attn_split_kernel<128> "
-                                       "(suffix) + cascade_combine_kernel<128>" if cascade else
-                                       "plan + attn_split_kernel<128> (+ split combine)"),
+                                       "(suffix) + cascade_combine_kernel<128>" if cascade and not fp8
+                                       else "plan + %s (both passes) + cascade_combine_kernel<128>"
+                                       % kname if cascade else
+                                       "plan + %s (+ split combine)" % kname),
                             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": achieved / peaks["hbm_gbs"],
-                            "traffic": load_traffic("attn_split_kernel<128>", wl.name),
+                            "traffic": load_traffic(kname, config["workload"]),
                             "peak_source": peaks["source"], "attn_ms_per_launch": attn_ms_avg}
     line["roofline"]["timing"] = ("the attention call alone (same inputs), replayed once per "
                                   "timed step right after the timed steps, CUDA events per launch")
-    line["config"]["step"] = ("cascade_fwd_with_update" if cascade else "varlen_fwd_with_update") + \
+    line["config"]["step"] = (("cascade_fwd_fp8kv" if cascade else "varlen_fwd_fp8kv") if fp8 else
+                              ("cascade_fwd_with_update" if cascade else "varlen_fwd_with_update")) + \
         " (scatter of the new K/V + attention in one call)"
     if sub:
         for kind, r in sub.items():
@@ -612,11 +671,14 @@ def bench_ours(args, rank, world, local):
     # split-KV kernel and/or the prefill kernel (the host launches a kernel
     # only when some segment can need it).
     G = H // wl.num_kv_heads
+    tc_rows = (lambda rows: False) if fp8 else (lambda rows: rows > 32)
     if cascade:
-        # scatter, planner, prefix pass, suffix pass (one or two kernels), combine
-        per_step = 2 + 1 + 1 + (1 if wl.max_seqlen_q * G > 64 else 0) + 1
+        # scatter, planner, prefix pass (prefill kernel for more than 32
+        # packed rows, else split-KV), suffix pass (split-KV and/or prefill
+        # kernel), combine
+        per_step = 2 + 1 + 1 + (1 if tc_rows(wl.max_seqlen_q * G) else 0) + 1
     else:
-        per_step = 3 + (1 if wl.max_seqlen_q * G > 64 else 0)
+        per_step = 3 + (1 if tc_rows(wl.max_seqlen_q * G) else 0)
     line["gpu_launches"] = per_step * args.steps
     for r in rows_fig.values():
         r["frac_hbm"] = r["gbs"] / peaks["hbm_gbs"]
@@ -624,7 +686,7 @@ def bench_ours(args, rank, world, local):
     line["graph"] = graphs is not None
     line["clocks"] = clocks
     if not args.no_cpu_baseline:
-        b, f, sec, desc = run_oracle_sample(wl, max_seconds=args.cpu_seconds)
+        b, f, sec, desc = run_oracle_sample(wl, max_seconds=args.cpu_seconds, fp8=fp8)
         line["cpu_baseline"] = {"value": b / sec / 1e9, "unit": "GB/s",
                                 "cores": torch.get_num_threads(), "kind": "oracle",
                                 "sample": desc}
@@ -639,6 +701,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_llama8b", choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--kv-cache", default="bf16", choices=["bf16", "fp8"],
+                    help="page pool element type: bf16, or e4m3 bytes with per-KV-head scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the C-ABI calls directly instead of replaying CUDA graphs")

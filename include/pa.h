@@ -7,10 +7,10 @@
  *             vllm-analysis/07): §1.1 tiled online softmax, §4 forward() and the
  *             flash_attn_varlen_func call, §4.2 KV-cache update, §5 PagedAttention
  *             integration (block_table addressing), §6.3 cascade execution,
- *             §8.2 reshape_and_cache_flash / merge_attn_states.
+ *             §8.2 reshape_and_cache_flash / merge_attn_states, §10 feature table.
  *   [FA/FI]   "FlashAttention と FlashInfer:2 大 GPU アテンションバックエンド":
  *             データフロー (KV cache shape, block size multiple of 16),
- *             境界と失敗 (head-size and dtype limits).
+ *             境界と失敗 (head-size and dtype limits, FP8 KV cache).
  *   [Backend] "AttentionBackend:アテンションバックエンド抽象レイヤー": 境界と失敗
  *             (head size, block size ValueError, natural-log LSE).
  *
@@ -301,6 +301,79 @@ pa_status pa_varlen_fwd_noalloc(const void* q, int64_t q_token_stride, const voi
                                 int num_kv_heads, int head_size, int block_size, int num_blocks,
                                 float softmax_scale, int causal, void* out, float* lse, int dtype,
                                 int32_t* dev_status, void* stream);
+
+/*
+ * FP8 (e4m3) KV cache ([FA/FI] 役割 and 境界と失敗: FlashInfer and FA3 accept
+ * an fp8 / fp8_e4m3 KV cache with per-head quant scales; [FA-vLLM] §10 lists an
+ * FP8 KV cache among the backends' features).
+ *
+ * The pools hold one byte per element: the OCP 8-bit floating point "E4M3"
+ * format (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest
+ * finite value 448, no infinities, S.1111.111 is NaN). A stored byte c of KV
+ * head h means the value e4m3(c) * scale[h]. Writes store
+ * e4m3(x / scale[h]): x is the bf16 input widened to float32, the division
+ * is IEEE float32 (correctly rounded), the result is rounded to the nearest
+ * e4m3 value (ties to even) and saturates at +-448 (a NaN stays NaN).
+ * Attention computes exactly the bf16 path's definition on the dequantized
+ * keys and values e4m3(c) * scale[h]; q.k is formed in f16 x e4m3 products
+ * with float32 accumulation, so q must lie within the f16 range (|q| < 65504).
+ * Layout: the NHD pools of pa_reshape_and_cache with 1-byte elements;
+ * cache_block_stride is in elements (= bytes) and a multiple of 16.
+ * head_size must be 128 (PA_ERR_UNSUPPORTED otherwise). Every FP8 segment
+ * runs on the split-KV kernel (warp-level MMA), including long prefills.
+ */
+typedef struct pa_kv_fp8 {
+  const float* k_scale; /* device float32 [num_kv_heads], finite and > 0 (not checked) */
+  const float* v_scale; /* device float32 [num_kv_heads], finite and > 0 (not checked) */
+} pa_kv_fp8;
+
+/*
+ * pa_reshape_and_cache_fp8 -- pa_reshape_and_cache into e4m3 pools: key /
+ * value are bf16 rows as there (dtype = PA_BF16); each element is quantized
+ * with its KV head's scale as described above. scales must be non-NULL with
+ * both pointers 4-byte aligned (PA_ERR_INVALID_ARG).
+ */
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, int64_t key_token_stride,
+                                   int64_t value_token_stride, void* key_cache, void* value_cache,
+                                   int64_t cache_block_stride, const int64_t* slot_mapping,
+                                   int num_tokens, int num_kv_heads, int head_size,
+                                   int block_size, int num_blocks, const pa_kv_fp8* scales,
+                                   int dtype, int32_t* dev_status, void* stream);
+
+/* Workspace bytes of pa_varlen_fwd_fp8kv / pa_cascade_fwd_fp8kv (0 if invalid). */
+size_t pa_varlen_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
+                                          int max_seqlen_k, int num_heads, int num_kv_heads,
+                                          int head_size, int block_size, int sm_count);
+size_t pa_cascade_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
+                                           int max_seqlen_k, int num_heads, int num_kv_heads,
+                                           int head_size, int block_size, int sm_count);
+
+/*
+ * pa_varlen_fwd_fp8kv / pa_cascade_fwd_fp8kv -- pa_varlen_fwd_with_update /
+ * pa_cascade_fwd_with_update over e4m3 pools: the optional update (NULL or
+ * num_tokens = 0 for none) is quantized into the pools as by
+ * pa_reshape_and_cache_fp8, then the attention reads the dequantized cache.
+ * q, out and lse are as in the bf16 entry points (dtype = PA_BF16).
+ */
+pa_status pa_varlen_fwd_fp8kv(const pa_kv_update* update, const void* q, int64_t q_token_stride,
+                              void* key_cache, void* value_cache, int64_t cache_block_stride,
+                              const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                              const int32_t* block_table, int bt_stride, int num_seqs,
+                              int total_q, int max_seqlen_q, int max_seqlen_k, int num_heads,
+                              int num_kv_heads, int head_size, int block_size, int num_blocks,
+                              float softmax_scale, int causal, const pa_kv_fp8* scales, void* out,
+                              float* lse, void* workspace, size_t workspace_bytes, int dtype,
+                              int32_t* dev_status, void* stream);
+pa_status pa_cascade_fwd_fp8kv(const pa_kv_update* update, const void* q,
+                               int64_t q_token_stride, void* key_cache, void* value_cache,
+                               int64_t cache_block_stride, const int32_t* cu_seqlens_q,
+                               const int32_t* seqused_k, const int32_t* block_table,
+                               int bt_stride, int num_seqs, int total_q, int max_seqlen_q,
+                               int max_seqlen_k, int num_heads, int num_kv_heads, int head_size,
+                               int block_size, int num_blocks, float softmax_scale,
+                               int common_prefix_len, const pa_kv_fp8* scales, void* out,
+                               float* lse, void* workspace, size_t workspace_bytes, int dtype,
+                               int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

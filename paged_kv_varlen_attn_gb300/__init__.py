@@ -44,6 +44,11 @@ EXPORTS = (
     "pa_varlen_fwd_with_update",
     "pa_cascade_fwd_with_update",
     "pa_use_cascade_attention",
+    "pa_reshape_and_cache_fp8",
+    "pa_varlen_fwd_fp8kv_workspace_size",
+    "pa_cascade_fwd_fp8kv_workspace_size",
+    "pa_varlen_fwd_fp8kv",
+    "pa_cascade_fwd_fp8kv",
 )
 
 _lib = None
@@ -56,6 +61,11 @@ class KvUpdate(ctypes.Structure):
     """struct pa_kv_update of include/pa.h."""
     _fields_ = [("key", _vp), ("value", _vp), ("key_token_stride", _i64),
                 ("value_token_stride", _i64), ("slot_mapping", _vp), ("num_tokens", _i32)]
+
+
+class KvFp8(ctypes.Structure):
+    """struct pa_kv_fp8 of include/pa.h (device float32 [num_kv_heads] scales)."""
+    _fields_ = [("k_scale", _vp), ("v_scale", _vp)]
 
 
 _ATTN_ARGS = [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
@@ -81,6 +91,14 @@ _SIGS = {
     "pa_varlen_fwd_with_update": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS, _i32),
     "pa_cascade_fwd_with_update": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS, _i32),
     "pa_use_cascade_attention": ([_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)], _i32),
+    "pa_reshape_and_cache_fp8": ([_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _i32, _i32, _i32,
+                                  _i32, _i32, ctypes.POINTER(KvFp8), _i32, _vp, _vp], _i32),
+    "pa_varlen_fwd_fp8kv_workspace_size": ([_i32] * 9, _sz),
+    "pa_cascade_fwd_fp8kv_workspace_size": ([_i32] * 9, _sz),
+    "pa_varlen_fwd_fp8kv": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS[:20] +
+                            [ctypes.POINTER(KvFp8)] + _ATTN_ARGS[20:], _i32),
+    "pa_cascade_fwd_fp8kv": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS[:20] +
+                             [ctypes.POINTER(KvFp8)] + _ATTN_ARGS[20:], _i32),
 }
 
 
@@ -213,7 +231,7 @@ def _kv_update(key, value, slot_mapping):
 
 def _attend(entry, update, q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
             max_seqlen_q, max_seqlen_k, softmax_scale, mode_arg, out, lse, return_lse,
-            workspace, dev_status, size_fn):
+            workspace, dev_status, size_fn, fp8=None):
     lib = load_library()
     _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table)
     T, H, D = q.shape
@@ -229,11 +247,12 @@ def _attend(entry, update, q, key_cache, value_cache, cu_seqlens_q, seqused_k, b
     args = (_ptr(q), _row_stride(q), _ptr(key_cache), _ptr(value_cache), _cache_stride(key_cache),
             _ptr(cu_seqlens_q), _ptr(seqused_k), _ptr(block_table), block_table.stride(0), S, T,
             int(max_seqlen_q), int(max_seqlen_k), H, hk, D, bs, nb, float(softmax_scale),
-            int(mode_arg), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
+            int(mode_arg)) + ((ctypes.byref(fp8),) if fp8 is not None else ()) + (
+            _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
             _ptr(dev_status), _stream(q.device))
     fn = getattr(lib, entry)
-    code = fn(ctypes.byref(update) if update is not None else None, *args) \
-        if entry.endswith("_with_update") else fn(*args)
+    upd = ctypes.byref(update) if update is not None else None
+    code = fn(upd, *args) if entry.endswith(("_with_update", "_fp8kv")) else fn(*args)
     _check(code, entry)
     return out, lse
 
@@ -323,3 +342,96 @@ def cascade_fwd_with_update(key, value, slot_mapping, q, key_cache, value_cache,
                    key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
                    max_seqlen_k, softmax_scale, common_prefix_len, out, lse, return_lse,
                    workspace, dev_status, cascade_fwd_workspace_size)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) KV cache: uint8 (or float8_e4m3fn) pools of e4m3 codes with one
+# scale per KV head; a stored code c means e4m3(c) * scale.
+def _fp8_pool(c):
+    if c.element_size() != 1:
+        raise ValueError("FP8 caches hold one byte per element (uint8 or float8_e4m3fn)")
+    return c
+
+
+def _scales(s, hk, device):
+    """Per-KV-head float32 scales on the device: a number, or a tensor of 1 or
+    num_kv_heads values."""
+    if not torch.is_tensor(s):
+        return torch.full((hk,), float(s), dtype=torch.float32, device=device)
+    s = s.to(device=device, dtype=torch.float32).reshape(-1)
+    if s.numel() == 1:
+        s = s.expand(hk)
+    if s.numel() != hk:
+        raise ValueError(f"expected 1 or {hk} scales, got {s.numel()}")
+    return s.contiguous()
+
+
+def _fp8_desc(k_scale, v_scale, hk, device):
+    ks, vs = _scales(k_scale, hk, device), _scales(v_scale, hk, device)
+    return KvFp8(ks.data_ptr(), vs.data_ptr()), (ks, vs)
+
+
+def varlen_fwd_fp8kv_workspace_size(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                                    num_kv_heads, head_size, block_size, sm_count):
+    return load_library().pa_varlen_fwd_fp8kv_workspace_size(
+        num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size,
+        block_size, sm_count)
+
+
+def cascade_fwd_fp8kv_workspace_size(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                                     num_kv_heads, head_size, block_size, sm_count):
+    return load_library().pa_cascade_fwd_fp8kv_workspace_size(
+        num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size,
+        block_size, sm_count)
+
+
+def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale,
+                          dev_status=None):
+    """Quantize new bf16 K/V rows to e4m3 (x / scale of their KV head) and
+    scatter them into the FP8 pools (in place)."""
+    lib = load_library()
+    _need_cuda(key, value, key_cache, value_cache, slot_mapping, dev_status)
+    _fp8_pool(key_cache), _fp8_pool(value_cache)
+    if key_cache.stride(0) != value_cache.stride(0):
+        raise ValueError("key and value caches must share the page stride")
+    nb, bs, hk, d = key_cache.shape
+    desc, keep = _fp8_desc(k_scale, v_scale, hk, key.device)
+    code = lib.pa_reshape_and_cache_fp8(
+        _ptr(key), _ptr(value), _row_stride(key), _row_stride(value), _ptr(key_cache),
+        _ptr(value_cache), _cache_stride(key_cache), _ptr(slot_mapping), key.shape[0], hk, d, bs,
+        nb, ctypes.byref(desc), PA_BF16, _ptr(dev_status), _stream(key.device))
+    _check(code, "pa_reshape_and_cache_fp8")
+    del keep
+
+
+def varlen_fwd_fp8kv(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
+                     max_seqlen_q, max_seqlen_k, softmax_scale, causal, k_scale, v_scale,
+                     key=None, value=None, slot_mapping=None, out=None, lse=None,
+                     return_lse=True, workspace=None, dev_status=None):
+    """Varlen attention over FP8 pools, optionally first quantizing and
+    scattering the new tokens' K/V (key, value, slot_mapping). Returns
+    (out, lse or None)."""
+    _fp8_pool(key_cache), _fp8_pool(value_cache)
+    desc, keep = _fp8_desc(k_scale, v_scale, key_cache.shape[2], q.device)
+    res = _attend("pa_varlen_fwd_fp8kv", _kv_update(key, value, slot_mapping), q, key_cache,
+                  value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q, max_seqlen_k,
+                  softmax_scale, bool(causal), out, lse, return_lse, workspace, dev_status,
+                  varlen_fwd_fp8kv_workspace_size, fp8=desc)
+    del keep
+    return res
+
+
+def cascade_fwd_fp8kv(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
+                      max_seqlen_q, max_seqlen_k, softmax_scale, common_prefix_len, k_scale,
+                      v_scale, key=None, value=None, slot_mapping=None, out=None, lse=None,
+                      return_lse=True, workspace=None, dev_status=None):
+    """Cascade attention over FP8 pools (optional update as in
+    varlen_fwd_fp8kv). Returns (out, lse or None)."""
+    _fp8_pool(key_cache), _fp8_pool(value_cache)
+    desc, keep = _fp8_desc(k_scale, v_scale, key_cache.shape[2], q.device)
+    res = _attend("pa_cascade_fwd_fp8kv", _kv_update(key, value, slot_mapping), q, key_cache,
+                  value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q, max_seqlen_k,
+                  softmax_scale, common_prefix_len, out, lse, return_lse, workspace, dev_status,
+                  cascade_fwd_fp8kv_workspace_size, fp8=desc)
+    del keep
+    return res

@@ -25,6 +25,18 @@
 //    workspace; the last CTA of a (row tile, KV head) group -- found with one
 //    atomic counter, no spinning -- merges all splits in a fixed order, so the
 //    result is deterministic.
+//  * FP8 (e4m3) pools ("FlashAttention と FlashInfer" 役割 / 境界と失敗: FP8
+//    KV cache with per-head quant scales), head size 128: a key row is one
+//    128-byte swizzled line, so a stage holds twice the keys' worth of bytes
+//    per barrier round trip. Each warp widens its own slice straight from the
+//    staged bytes into f16 MMA fragments (e4m3 -> f16 is exact), with Q in
+//    f16. For Q.K^T the head dimension is permuted -- MMA k-index
+//    16*kk + {2c, 2c+1, 2c+8, 2c+9} of lane quad c is dim 32*c + 4*kk + {0..3}
+//    in both Q and K -- so a lane's K bytes of a key are 32 contiguous bytes.
+//    For P.V the output dimension is permuted -- MMA column g of n-tile n is
+//    dim 16*g + n -- so a lane reads 16 contiguous bytes of each of its four
+//    keys and pairs them with byte permutes. k_scale folds into the softmax
+//    scale and v_scale into the final normalisation.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -33,14 +45,17 @@
 
 namespace pa {
 
-template <int D>
+template <int D, bool FP8 = false>
 struct SplitCfg {
   static constexpr int BN = kKeyTile;                  // keys per stage
-  static constexpr int HALVES = D / 64;                // 64-dim swizzled halves
+  static constexpr int HALVES = FP8 ? 1 : D / 64;      // 128-byte swizzled row segments
   static constexpr int HALF_BYTES = BN * 128;          // [64 rows x 128 B]
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K and V
-  static constexpr int STAGES = D == 128 ? 2 : 6;
+  // FP8 runs 2 CTAs per SM (its consumer needs more than 128 registers)
+  // with 6 stages, the same bytes in flight per SM as bf16's 3 x 2 stages.
+  static constexpr int STAGES = FP8 ? 6 : (D == 128 ? 2 : 6);
+  static constexpr int CTAS_PER_SM = FP8 ? 2 : 3;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
   static constexpr int SMEM_BYTES = RING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int THREADS = 160;
@@ -56,12 +71,13 @@ struct SplitShared {
 // Consumers. RGN = number of 16-row groups (1, 2 or 4); 4 / RGN warps share
 // each group and split every key tile between them.
 // ---------------------------------------------------------------------------
-template <int D, int RGN>
+template <int D, int RGN, bool FP8>
 __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring, SplitShared sh,
                                                int hk, int seg, int rt, int j, int q_start,
                                                int q_len, int kv_len, int kb, int ke, int ntiles,
                                                int nsplit, int slot_base) {
-  using C = SplitCfg<D>;
+  using C = SplitCfg<D, FP8>;
+  static_assert(!FP8 || D == 128, "FP8 pools: head size 128");
   constexpr int KS = 4 / RGN;       // warps per row group
   constexpr int KW = C::BN / KS;    // keys per warp per tile
   // A warp's keys of a tile are processed in chunks of at most 32 (one online
@@ -96,20 +112,29 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
   int lim_max = max(lim[0], lim[1]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) lim_max = max(lim_max, __shfl_xor_sync(0xffffffffu, lim_max, o));
+  // Smallest limit over the warp's valid rows (rows past R are never written).
+  int lim_min = min(rvalid[0] ? lim[0] : 0x7fffffff, rvalid[1] ? lim[1] : 0x7fffffff);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lim_min = min(lim_min, __shfl_xor_sync(0xffffffffu, lim_min, o));
 
-  // Q fragments (A operand, 16 x D), loaded once from global memory.
+  // Q fragments (A operand, 16 x D), loaded once from global memory: bf16,
+  // or for FP8 pools f16 in the permuted dim order of the K fragments.
   uint32_t qf[DK][4];
 #pragma unroll
   for (int kk = 0; kk < DK; ++kk) {
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       const int r = x & 1;                    // a0,a2: row gq; a1,a3: row gq+8
-      const int col = kk * 16 + 2 * cq + (x >> 1) * 8;
+      const int col = FP8 ? cq * 32 + kk * 4 + (x >> 1) * 2 : kk * 16 + 2 * cq + (x >> 1) * 8;
       uint32_t v = 0;
       if (rvalid[r]) {
         const __nv_bfloat16* p = a.q + static_cast<int64_t>(tok[r]) * a.q_stride +
                                  static_cast<int64_t>(head[r]) * D + col;
         v = __ldg(reinterpret_cast<const uint32_t*>(p));
+        if constexpr (FP8) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+          v = pack_f16(f.x, f.y);
+        }
       }
       qf[kk][x] = v;
     }
@@ -119,7 +144,10 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
 #pragma unroll
   for (int n = 0; n < DN; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  const float sl2 = a.scale_log2;
+  // FP8: scores use the stored codes, so k_scale joins the softmax scale;
+  // v_scale multiplies the normalised output.
+  const float sl2 = FP8 ? a.scale_log2 * __ldg(a.k_scale + hk) : a.scale_log2;
+  const float vsc = FP8 ? __ldg(a.v_scale + hk) : 1.f;
   const int slice0 = ks * KW;
   int consumed = 0;
 
@@ -161,6 +189,23 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
       for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
       const uint32_t kbase = smem_u32(ktile);
       const int mat = lane >> 3, rr = lane & 7;
+      if constexpr (FP8) {
+        // Lane (gq, cq) holds key cs + 8n + gq, bytes 32*cq .. +31 (16-byte
+        // granules 2cq, 2cq+1 of the swizzled row); word kk gives b0 (low
+        // half) and b1 (high half) of k-step kk.
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const int key = cs + n * 8 + gq;
+          const uint8_t* row = ktile + key * 128;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(row + (((2 * cq) ^ (key & 7)) << 4));
+          const uint4 w1 = *reinterpret_cast<const uint4*>(row + (((2 * cq + 1) ^ (key & 7)) << 4));
+          const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int kk = 0; kk < DK; ++kk)
+            mma_16816_f16(sacc[n], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
+                          e4m3x2_to_f16x2(w[kk]), e4m3x2_to_f16x2(w[kk] >> 16));
+        }
+      } else {
 #pragma unroll
       for (int kk = 0; kk < DK; ++kk) {
         const int half = kk >> 2, col = (kk & 3) * 16;
@@ -174,8 +219,21 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
           mma_16816(sacc[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
         }
       }
-      // Mask, scale into the log2 domain, running max.
+      }
+      // Mask, scale into the log2 domain, running max. A chunk inside every
+      // valid row's visible range needs no mask.
       float mx[2] = {-INFINITY, -INFINITY};
+      if (ckey + KWC <= ke && ckey + KWC - 1 <= lim_min) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v = sacc[n][e] * sl2;
+            sacc[n][e] = v;
+            mx[e >> 1] = fmaxf(mx[e >> 1], v);
+          }
+        }
+      } else {
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
 #pragma unroll
@@ -188,23 +246,30 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
           mx[r] = fmaxf(mx[r], v);
         }
       }
+      }
       float alpha[2], muse[2];
+      bool grew = false;
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
         const float mn = fmaxf(m[r], mx[r]);
+        grew |= mn != m[r];
         muse[r] = mn == -INFINITY ? 0.f : mn;
         alpha[r] = fast_exp2(m[r] - muse[r]);
         m[r] = mn;
         l[r] *= alpha[r];
       }
+      // alpha is exactly 1 for a row whose maximum did not move; skip the
+      // rescale unless some row's did.
+      if (__any_sync(0xffffffffu, grew)) {
 #pragma unroll
       for (int n = 0; n < DN; ++n) {
         o[n][0] *= alpha[0];
         o[n][1] *= alpha[0];
         o[n][2] *= alpha[1];
         o[n][3] *= alpha[1];
+      }
       }
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
@@ -217,6 +282,40 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
       }
       // O += P V.
       const uint32_t vbase = smem_u32(vtile);
+      if constexpr (FP8) {
+        // Lane (gq, cq) needs, for the keys of MMA k-index 2cq, 2cq+1, 2cq+8,
+        // 2cq+9 of each 16-key step, the dims 16*gq + n of n-tile n: granule
+        // gq of those four rows. prmt pairs byte n of two rows into the
+        // (low, high) e4m3 pair of one B register.
+#pragma unroll
+        for (int kk = 0; kk < NT / 2; ++kk) {
+          const uint32_t pa0 = pack_f16(sacc[2 * kk][0], sacc[2 * kk][1]);
+          const uint32_t pa1 = pack_f16(sacc[2 * kk][2], sacc[2 * kk][3]);
+          const uint32_t pa2 = pack_f16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+          const uint32_t pa3 = pack_f16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+          uint4 vr[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int key = cs + kk * 16 + 2 * cq + (x & 1) + (x >> 1) * 8;
+            vr[x] = *reinterpret_cast<const uint4*>(vtile + key * 128 + ((gq ^ (key & 7)) << 4));
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t x0 = (&vr[0].x)[j], x1 = (&vr[1].x)[j];
+            const uint32_t x2 = (&vr[2].x)[j], x3 = (&vr[3].x)[j];
+            const uint32_t lo01 = prmt(x0, x1, 0x5140), hi01 = prmt(x0, x1, 0x7362);
+            const uint32_t lo23 = prmt(x2, x3, 0x5140), hi23 = prmt(x2, x3, 0x7362);
+            mma_16816_f16(o[4 * j], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(lo01),
+                          e4m3x2_to_f16x2(lo23));
+            mma_16816_f16(o[4 * j + 1], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(lo01 >> 16),
+                          e4m3x2_to_f16x2(lo23 >> 16));
+            mma_16816_f16(o[4 * j + 2], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(hi01),
+                          e4m3x2_to_f16x2(hi23));
+            mma_16816_f16(o[4 * j + 3], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(hi01 >> 16),
+                          e4m3x2_to_f16x2(hi23 >> 16));
+          }
+        }
+      } else {
 #pragma unroll
       for (int kk = 0; kk < NT / 2; ++kk) {
         const uint32_t pa0 = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
@@ -233,6 +332,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
           mma_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
           mma_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
         }
+      }
       }
       }   // chunk
     }
@@ -307,7 +407,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const bool any = l[r] > 0.f;
-    inv_l[r] = any ? 1.f / l[r] : 0.f;
+    inv_l[r] = any ? vsc / l[r] : 0.f;
     lse_nat[r] = any ? (m[r] + fast_log2(l[r])) * kLn2 : -INFINITY;
   }
   const int H = a.H;
@@ -317,11 +417,25 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
     for (int r = 0; r < 2; ++r) {
       if (!rvalid[r]) continue;
       const int64_t obase = (static_cast<int64_t>(tok[r]) * H + head[r]) * D;
+      if constexpr (FP8) {
+        // Column e of the lane's pair holds dims 16 * (2cq + e) + n, n = 0..15.
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int n = 0; n < DN; n += 2)
+            pk[n / 2] = pack_bf16(o[n][2 * r + e] * inv_l[r], o[n + 1][2 * r + e] * inv_l[r]);
+          uint4* dst = reinterpret_cast<uint4*>(a.out + obase + 16 * (2 * cq + e));
+          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      } else {
 #pragma unroll
       for (int n = 0; n < DN; ++n) {
         const int col = n * 8 + 2 * cq;
         *reinterpret_cast<uint32_t*>(a.out + obase + col) =
             pack_bf16(o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]);
+      }
       }
       if (a.lse && cq == 0) a.lse[static_cast<int64_t>(head[r]) * a.lse_stride + tok[r]] = lse_nat[r];
     }
@@ -339,10 +453,20 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
       const int rl = rg * 16 + gq + 8 * r;
       if (!rvalid[r]) continue;
       float* po = a.part_o + (slot_row0 + rl) * D;
+      if constexpr (FP8) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int n = 0; n < DN; n += 4)
+            __stcg(reinterpret_cast<float4*>(po + 16 * (2 * cq + e) + n),
+                   make_float4(o[n][2 * r + e] * inv_l[r], o[n + 1][2 * r + e] * inv_l[r],
+                               o[n + 2][2 * r + e] * inv_l[r], o[n + 3][2 * r + e] * inv_l[r]));
+      } else {
 #pragma unroll
       for (int n = 0; n < DN; ++n)
         __stcg(reinterpret_cast<float2*>(po + n * 8 + 2 * cq),
                make_float2(o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]));
+      }
       if (cq == 0) __stcg(a.part_lse + slot_row0 + rl, lse_nat[r]);
     }
   }
@@ -359,11 +483,11 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
   if (threadIdx.x == 0) *counter = 0;   // ready for the next call
 }
 
-template <int D>
-__global__ void __launch_bounds__(SplitCfg<D>::THREADS, 3)
+template <int D, bool FP8>
+__global__ void __launch_bounds__(SplitCfg<D, FP8>::THREADS, SplitCfg<D, FP8>::CTAS_PER_SM)
 attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ AttnArgs a) {
-  using C = SplitCfg<D>;
+  using C = SplitCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -416,20 +540,20 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     return;
   }
   if (R <= 16)
-    split_consumer<D, 1>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke, ntiles,
-                         nsplit, slot_base);
+    split_consumer<D, 1, FP8>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke,
+                              ntiles, nsplit, slot_base);
   else if (R <= 32)
-    split_consumer<D, 2>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke, ntiles,
-                         nsplit, slot_base);
+    split_consumer<D, 2, FP8>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke,
+                              ntiles, nsplit, slot_base);
   else
-    split_consumer<D, 4>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke, ntiles,
-                         nsplit, slot_base);
+    split_consumer<D, 4, FP8>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke,
+                              ntiles, nsplit, slot_base);
 }
 
-template <int D>
+template <int D, bool FP8>
 static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const AttnArgs& a, int items_bound, cudaStream_t st) {
-  using C = SplitCfg<D>;
+  using C = SplitCfg<D, FP8>;
   // The shared-memory opt-in is a per-device function attribute: set it on
   // the first launch on each device (before any stream capture), not again.
   static bool configured[kMaxDevices] = {};
@@ -437,7 +561,7 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
-    e = cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_split_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
@@ -452,7 +576,7 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_split_kernel<D>, tmK, tmV, a);
+  e = cudaLaunchKernelEx(&cfg, attn_split_kernel<D, FP8>, tmK, tmV, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -460,8 +584,9 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
 cudaError_t launch_attn_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
                               int items_bound, cudaStream_t st) {
   if (items_bound <= 0) return cudaSuccess;
-  if (a.D == 128) return launch_split_d<128>(tmK, tmV, a, items_bound, st);
-  return launch_split_d<64>(tmK, tmV, a, items_bound, st);
+  if (a.kv_fp8) return launch_split_d<128, true>(tmK, tmV, a, items_bound, st);
+  if (a.D == 128) return launch_split_d<128, false>(tmK, tmV, a, items_bound, st);
+  return launch_split_d<64, false>(tmK, tmV, a, items_bound, st);
 }
 
 }  // namespace pa

@@ -101,6 +101,103 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
 }
 
 // ---------------------------------------------------------------------------
+// Scatter into an FP8 (e4m3) cache ("FlashAttention と FlashInfer" 役割 and
+// 境界と失敗: FP8 KV cache with per-head quant scales). Same warp-per-token
+// walk as above; a lane reads 8 bf16 values (16 bytes) of one head, divides
+// them by that KV head's scale (IEEE float division, correctly rounded) and
+// writes the 8 e4m3 bytes (round to nearest even, saturating at +-448).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint2 quantize8(uint4 x, float s) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+  uint32_t w[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float2 a = __bfloat1622float2(h[2 * k]);
+    const float2 b = __bfloat1622float2(h[2 * k + 1]);
+    w[k] = f32x2_to_e4m3x2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)) |
+           (f32x2_to_e4m3x2(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)) << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+__global__ void __launch_bounds__(kScatterThreads)
+reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                             int64_t kstride_v, int64_t vstride_v, uint2* __restrict__ kc,
+                             uint2* __restrict__ vc, int64_t block_stride_v,
+                             const int64_t* __restrict__ slots, int num_tokens, int vpt,
+                             int vph, int bs, int64_t num_slots,
+                             const float* __restrict__ k_scale,
+                             const float* __restrict__ v_scale, int32_t* status) {
+  pdl_enter(0);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kScatterWarps;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kScatterWarps + (threadIdx.x >> 5);
+       t < num_tokens; t += nwarps) {
+    const uint4* ksrc = key + t * kstride_v;
+    const uint4* vsrc = value + t * vstride_v;
+    const int64_t slot = __ldg(slots + t);
+    for (int v0 = lane; v0 < vpt; v0 += 32 * kScatterUnroll) {
+      uint4 kv[kScatterUnroll], vv[kScatterUnroll];
+#pragma unroll
+      for (int u = 0; u < kScatterUnroll; ++u) {
+        const int i = v0 + u * 32;
+        if (i < vpt) {
+          kv[u] = __ldcs(ksrc + i);
+          vv[u] = __ldcs(vsrc + i);
+        }
+      }
+      if (slot < 0) continue;                  // padding token
+      if (slot >= num_slots) {
+        if (lane == 0 && v0 == lane) flag_status(status, PA_DEV_BAD_SLOT);
+        continue;
+      }
+      const int64_t page = slot / bs;
+      const int64_t row = slot - page * bs;
+      uint2* kdst = kc + page * block_stride_v + row * vpt;
+      uint2* vdst = vc + page * block_stride_v + row * vpt;
+#pragma unroll
+      for (int u = 0; u < kScatterUnroll; ++u) {
+        const int i = v0 + u * 32;
+        if (i < vpt) {
+          const int h = i / vph;
+          kdst[i] = quantize8(kv[u], __ldg(k_scale + h));
+          vdst[i] = quantize8(vv[u], __ldg(v_scale + h));
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int64_t kstride,
+                                         int64_t vstride, void* kc, void* vc,
+                                         int64_t block_stride, const int64_t* slots,
+                                         int num_tokens, int H_kv, int D, int bs, int num_blocks,
+                                         const float* k_scale, const float* v_scale,
+                                         int32_t* status, cudaStream_t st, int sms, bool pdl) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int vpt = H_kv * D / 8;
+  const int64_t want = (static_cast<int64_t>(num_tokens) + kScatterWarps - 1) / kScatterWarps;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
+  cfg.blockDim = dim3(kScatterThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(
+      &cfg, reshape_and_cache_fp8_kernel, static_cast<const uint4*>(key),
+      static_cast<const uint4*>(value), kstride / 8, vstride / 8, static_cast<uint2*>(kc),
+      static_cast<uint2*>(vc), block_stride / 8, slots, num_tokens, vpt, D / 8, bs,
+      static_cast<int64_t>(num_blocks) * bs, k_scale, v_scale, status);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // merge_attn_states. One thread per 8 output elements (one 16-byte vector) of
 // a (token, head) row; the two LSEs of the row are read per thread (they hit
 // L1). With m = max(a, b): out = (e^(a-m) oa + e^(b-m) ob) / (e^(a-m) + e^(b-m)),

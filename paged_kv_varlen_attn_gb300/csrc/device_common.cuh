@@ -1,9 +1,12 @@
-// Device helpers: inline PTX for mbarriers, TMA tile loads, ldmatrix and the
-// warp-level bf16 MMA, plus bounded waits. Included by the kernel files only.
+// Device helpers: inline PTX for mbarriers, TMA tile loads, ldmatrix, the
+// warp-level bf16 / f16 MMA and the e4m3 conversions, plus bounded waits.
+// Included by the kernel files only.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "pa_internal.h"
@@ -114,6 +117,41 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------- FP8 (e4m3)
+// D += A(16x16, row) * B(16x8, col), f16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// f16x2 of two floats, lo in the low half (round to nearest even).
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// Two e4m3 bytes (low byte = element 0) to f16x2 (element 0 in the low
+// half). Every e4m3 value is exact in f16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  const __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+// e4m3 bytes of two floats, lo in the low byte: round to nearest even,
+// saturating to +-448 (NaN stays NaN).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  return __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+// Byte permute: bytes of {a, b} (a = bytes 0-3, b = 4-7) selected by sel.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
 }
 
 // Hardware base-2 exponential / logarithm (MUFU). ex2.approx of -inf is +0.

@@ -40,12 +40,13 @@ struct PassDims {
   int G, H, H_kv, D;
   int sms;
   bool all_partial = false;   // every item keeps a partial-state slot (cascade prefix pass)
+  bool kv_fp8 = false;        // FP8 pools: every segment runs on the split-KV kernel
 };
 
 // Which kernels a pass can need, from host-known bounds only.
 bool pass_has_tc(const PassDims& d) {
   const long long rows = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
-  return kTcAvailable && rows > kTcMinRows;
+  return kTcAvailable && !d.kv_fp8 && rows > kTcMinRows;
 }
 bool pass_has_split(const PassDims& d) { return !d.single || !pass_has_tc(d); }
 
@@ -96,11 +97,11 @@ struct CascadeLayout {
 };
 
 CascadeLayout layout_cascade(int num_seqs, int total_q, int max_q, int G, int H, int H_kv, int D,
-                             int sms) {
+                             int sms, bool kv_fp8) {
   CascadeLayout C{};
-  PassDims pd{1, total_q, total_q, true, G, H, H_kv, D, sms, true};
+  PassDims pd{1, total_q, total_q, true, G, H, H_kv, D, sms, true, kv_fp8};
   C.prefix = layout_pass(pd, 0);
-  PassDims sd{num_seqs, total_q, max_q, false, G, H, H_kv, D, sms, true};
+  PassDims sd{num_seqs, total_q, max_q, false, G, H, H_kv, D, sms, true, kv_fp8};
   C.suffix = layout_pass(sd, C.prefix.end);
   C.end = C.suffix.end;
   return C;
@@ -128,19 +129,34 @@ pa_status check_shape(int num_seqs, int total_q, int max_seqlen_q, int max_seqle
   return PA_OK;
 }
 
+// Element type of the K/V pools: bf16, or e4m3 codes with per-KV-head scales.
+struct KvFormat {
+  bool fp8;
+  const float* k_scale;
+  const float* v_scale;
+};
+constexpr KvFormat kKvBf16{false, nullptr, nullptr};
+
 pa_status check_attn_ptrs(const void* q, int64_t q_stride, const void* kc, const void* vc,
                           int64_t block_stride, const int32_t* cu, const int32_t* lens,
                           const int32_t* bt, int bt_stride, int num_seqs, int total_q,
                           int num_blocks, int H, int H_kv, int D, int bs, float scale, int causal,
-                          const void* out, const float* lse) {
+                          const void* out, const float* lse, const KvFormat& kv) {
   if (num_seqs > 0 && (!cu || !lens || !bt)) return PA_ERR_INVALID_ARG;
   if (total_q > 0 && (!q || !out)) return PA_ERR_INVALID_ARG;
   if (!kc || !vc) return PA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(out)) return PA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return PA_ERR_INVALID_ARG;
   if (q_stride < static_cast<int64_t>(H) * D || q_stride % 8 != 0) return PA_ERR_INVALID_ARG;
-  if (block_stride < static_cast<int64_t>(bs) * H_kv * D || block_stride % 8 != 0)
+  // Page strides are whole 16-byte units (a TMA rule): 8 bf16 or 16 e4m3 elements.
+  if (block_stride < static_cast<int64_t>(bs) * H_kv * D || block_stride % (kv.fp8 ? 16 : 8) != 0)
     return PA_ERR_INVALID_ARG;
+  if (kv.fp8) {
+    if (D != 128) return PA_ERR_UNSUPPORTED;
+    if (!kv.k_scale || !kv.v_scale) return PA_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(kv.k_scale) | reinterpret_cast<uintptr_t>(kv.v_scale)) & 3u) != 0)
+      return PA_ERR_INVALID_ARG;
+  }
   if (bt_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return PA_ERR_INVALID_ARG;
@@ -164,20 +180,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 4-D view of a page pool: (dim, kv head, row in page, page), 128-byte
-// swizzled boxes of 64 dims x 1 head x box_rows rows x 1 page. Coordinates
-// past the pool (a page id == num_blocks) read as zeros.
+// swizzled boxes of 128 bytes of dims (64 bf16 or 128 e4m3) x 1 head x
+// box_rows rows x 1 page. Coordinates past the pool (a page id == num_blocks)
+// read as zeros.
 bool encode_pool_map(CUtensorMap* map, const void* base, int D, int H_kv, int bs, int num_blocks,
-                     int64_t block_stride, int box_rows) {
+                     int64_t block_stride, int box_rows, bool fp8 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const cuuint64_t esz = fp8 ? 1 : 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_kv),
                         static_cast<cuuint64_t>(bs),
                         static_cast<cuuint64_t>(num_blocks > 0 ? num_blocks : 1)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H_kv) * D * 2,
-                           static_cast<cuuint64_t>(block_stride) * 2};
-  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * esz,
+                           static_cast<cuuint64_t>(H_kv) * D * esz,
+                           static_cast<cuuint64_t>(block_stride) * esz};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), 1, static_cast<cuuint32_t>(box_rows),
+                       1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -205,6 +226,7 @@ struct CommonAttn {
   float scale;
   int32_t* status;
   cudaStream_t st;
+  KvFormat kv;
 };
 
 PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int single, int single_kv,
@@ -264,6 +286,9 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
   a.items = reinterpret_cast<const int4*>(ws + L.items[0]);
   a.status = c.status;
   a.box_rows = gcd_int(c.bs, kKeyTile);
+  a.kv_fp8 = c.kv.fp8 ? 1 : 0;
+  a.k_scale = c.kv.k_scale;
+  a.v_scale = c.kv.v_scale;
   return a;
 }
 
@@ -324,12 +349,17 @@ pa_status check_update(const void* key, const void* value, int64_t key_token_str
                        int64_t value_token_stride, const void* key_cache, const void* value_cache,
                        int64_t cache_block_stride, const int64_t* slot_mapping, int num_tokens,
                        int num_kv_heads, int head_size, int block_size, int num_blocks,
-                       int dtype) {
+                       int dtype, const KvFormat& kv = kKvBf16) {
   if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
   if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (head_size != 64 && head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (kv.fp8 && head_size != 128) return PA_ERR_UNSUPPORTED;
   if (block_size <= 0 || block_size % 16 != 0 || block_size > 1024) return PA_ERR_BLOCK_SIZE;
   if (num_tokens == 0) return PA_OK;
+  if (kv.fp8 && (!kv.k_scale || !kv.v_scale ||
+                 ((reinterpret_cast<uintptr_t>(kv.k_scale) |
+                   reinterpret_cast<uintptr_t>(kv.v_scale)) & 3u) != 0))
+    return PA_ERR_INVALID_ARG;
   if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
   if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
     return PA_ERR_INVALID_ARG;
@@ -338,8 +368,23 @@ pa_status check_update(const void* key, const void* value, int64_t key_token_str
   if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 ||
       value_token_stride % 8)
     return PA_ERR_INVALID_ARG;
-  if (cache_block_stride < row * block_size || cache_block_stride % 8) return PA_ERR_INVALID_ARG;
+  if (cache_block_stride < row * block_size || cache_block_stride % (kv.fp8 ? 16 : 8))
+    return PA_ERR_INVALID_ARG;
   return PA_OK;
+}
+
+// The scatter of pa_reshape_and_cache(_fp8) for the cache format kv.
+cudaError_t launch_scatter(const void* key, const void* value, int64_t kstride, int64_t vstride,
+                           void* kc, void* vc, int64_t block_stride, const int64_t* slots,
+                           int num_tokens, int H_kv, int D, int bs, int num_blocks,
+                           const KvFormat& kv, int32_t* status, cudaStream_t st, int sms,
+                           bool pdl) {
+  if (kv.fp8)
+    return launch_reshape_and_cache_fp8(key, value, kstride, vstride, kc, vc, block_stride, slots,
+                                        num_tokens, H_kv, D, bs, num_blocks, kv.k_scale,
+                                        kv.v_scale, status, st, sms, pdl);
+  return launch_reshape_and_cache(key, value, kstride, vstride, kc, vc, block_stride, slots,
+                                  num_tokens, H_kv, D, bs, num_blocks, status, st, sms, pdl);
 }
 
 // Validate an optional K/V update of an update-and-attend call.
@@ -348,7 +393,7 @@ pa_status check_kv_update(const pa_kv_update* u, const CommonAttn& c, void* key_
   if (!u || u->num_tokens == 0) return u && u->num_tokens < 0 ? PA_ERR_INVALID_ARG : PA_OK;
   return check_update(u->key, u->value, u->key_token_stride, u->value_token_stride, key_cache,
                       value_cache, c.block_stride, u->slot_mapping, u->num_tokens, c.H_kv, c.D,
-                      c.bs, c.num_blocks, dtype);
+                      c.bs, c.num_blocks, dtype, c.kv);
 }
 
 // Launch the update's scatter right after the planner, as a programmatic
@@ -357,10 +402,9 @@ pa_status check_kv_update(const pa_kv_update* u, const CommonAttn& c, void* key_
 pa_status launch_kv_update(const pa_kv_update* u, const CommonAttn& c, void* key_cache,
                            void* value_cache, int sms) {
   if (!u || u->num_tokens == 0) return PA_OK;
-  return launch_reshape_and_cache(u->key, u->value, u->key_token_stride, u->value_token_stride,
-                                  key_cache, value_cache, c.block_stride, u->slot_mapping,
-                                  u->num_tokens, c.H_kv, c.D, c.bs, c.num_blocks, c.status, c.st,
-                                  sms, true) == cudaSuccess
+  return launch_scatter(u->key, u->value, u->key_token_stride, u->value_token_stride, key_cache,
+                        value_cache, c.block_stride, u->slot_mapping, u->num_tokens, c.H_kv, c.D,
+                        c.bs, c.num_blocks, c.kv, c.status, c.st, sms, true) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }
@@ -430,7 +474,7 @@ size_t pa_cascade_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q
   const int sms = query_sms(sm_count);
   if (sms <= 0) return 0;
   return layout_cascade(num_seqs, total_q, max_seqlen_q, num_heads / num_kv_heads, num_heads,
-                        num_kv_heads, head_size, sms)
+                        num_kv_heads, head_size, sms, false)
       .end;
 }
 
@@ -443,29 +487,28 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
                              int head_size, int block_size, int num_blocks, float softmax_scale,
                              int causal, void* out, float* lse, void* workspace,
                              size_t workspace_bytes, int dtype, int32_t* dev_status,
-                             void* stream) {
+                             void* stream, const KvFormat& kv) {
   pa_status st = check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
                              num_kv_heads, head_size, block_size, dtype);
   if (st != PA_OK) return st;
   st = check_attn_ptrs(q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
                        seqused_k, block_table, bt_stride, num_seqs, total_q, num_blocks, num_heads,
-                       num_kv_heads, head_size, block_size, softmax_scale, causal, out, lse);
+                       num_kv_heads, head_size, block_size, softmax_scale, causal, out, lse, kv);
   if (st != PA_OK) return st;
   CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
                seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
                num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
-               dev_status, static_cast<cudaStream_t>(stream)};
+               dev_status, static_cast<cudaStream_t>(stream), kv};
   st = check_kv_update(upd, c, key_cache, value_cache, dtype);
   if (st != PA_OK) return st;
   if (num_seqs == 0 || total_q == 0) {   // nothing to attend: the update alone
     if (!upd || upd->num_tokens == 0) return PA_OK;
     const int sms = query_sms(0);
     if (sms <= 0) return PA_ERR_CUDA;
-    return launch_reshape_and_cache(upd->key, upd->value, upd->key_token_stride,
-                                    upd->value_token_stride, key_cache, value_cache,
-                                    cache_block_stride, upd->slot_mapping, upd->num_tokens,
-                                    num_kv_heads, head_size, block_size, num_blocks, dev_status,
-                                    c.st, sms, false) == cudaSuccess
+    return launch_scatter(upd->key, upd->value, upd->key_token_stride, upd->value_token_stride,
+                          key_cache, value_cache, cache_block_stride, upd->slot_mapping,
+                          upd->num_tokens, num_kv_heads, head_size, block_size, num_blocks, kv,
+                          dev_status, c.st, sms, false) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
   }
@@ -473,6 +516,7 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
   if (sms <= 0) return PA_ERR_CUDA;
   PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
              num_kv_heads, head_size, sms};
+  d.kv_fp8 = kv.fp8;
   const PassLayout L = layout_pass(d, 0);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < L.end)
@@ -480,9 +524,9 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
   const int box_rows = gcd_int(block_size, kKeyTile);
   CUtensorMap tmK, tmV;
   if (!encode_pool_map(&tmK, key_cache, head_size, num_kv_heads, block_size, num_blocks,
-                       cache_block_stride, box_rows) ||
+                       cache_block_stride, box_rows, kv.fp8) ||
       !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
-                       cache_block_stride, box_rows))
+                       cache_block_stride, box_rows, kv.fp8))
     return PA_ERR_CUDA;
   CUtensorMap tmQ;
   if (!encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride,
@@ -533,7 +577,8 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
                      const_cast<void*>(value_cache), cache_block_stride, cu_seqlens_q, seqused_k,
                      block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
                      num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
-                     causal, out, lse, workspace, workspace_bytes, dtype, dev_status, stream);
+                     causal, out, lse, workspace, workspace_bytes, dtype, dev_status, stream,
+                     kKvBf16);
 }
 
 pa_status pa_varlen_fwd_with_update(const pa_kv_update* update, const void* q,
@@ -550,7 +595,7 @@ pa_status pa_varlen_fwd_with_update(const pa_kv_update* update, const void* q,
                      cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
                      max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size, block_size,
                      num_blocks, softmax_scale, causal, out, lse, workspace, workspace_bytes,
-                     dtype, dev_status, stream);
+                     dtype, dev_status, stream, kKvBf16);
 }
 
 pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
@@ -584,13 +629,13 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
                               int num_kv_heads, int head_size, int block_size, int num_blocks,
                               float softmax_scale, int common_prefix_len, void* out, float* lse,
                               void* workspace, size_t workspace_bytes, int dtype,
-                              int32_t* dev_status, void* stream) {
+                              int32_t* dev_status, void* stream, const KvFormat& kv) {
   pa_status st = check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
                              num_kv_heads, head_size, block_size, dtype);
   if (st != PA_OK) return st;
   st = check_attn_ptrs(q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
                        seqused_k, block_table, bt_stride, num_seqs, total_q, num_blocks, num_heads,
-                       num_kv_heads, head_size, block_size, softmax_scale, 1, out, lse);
+                       num_kv_heads, head_size, block_size, softmax_scale, 1, out, lse, kv);
   if (st != PA_OK) return st;
   if (common_prefix_len < 0 || common_prefix_len % block_size != 0) return PA_ERR_INVALID_ARG;
   if (static_cast<long long>(common_prefix_len) > static_cast<long long>(bt_stride) * block_size)
@@ -600,7 +645,7 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
                         cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
                         max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size,
                         block_size, num_blocks, softmax_scale, dev_status,
-                        static_cast<cudaStream_t>(stream)};
+                        static_cast<cudaStream_t>(stream), kv};
     st = check_kv_update(upd, cu, key_cache, value_cache, dtype);
     if (st != PA_OK) return st;
   }
@@ -608,11 +653,10 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
     if (!upd || upd->num_tokens == 0) return PA_OK;
     const int sms = query_sms(0);
     if (sms <= 0) return PA_ERR_CUDA;
-    return launch_reshape_and_cache(upd->key, upd->value, upd->key_token_stride,
-                                    upd->value_token_stride, key_cache, value_cache,
-                                    cache_block_stride, upd->slot_mapping, upd->num_tokens,
-                                    num_kv_heads, head_size, block_size, num_blocks, dev_status,
-                                    static_cast<cudaStream_t>(stream), sms, false) == cudaSuccess
+    return launch_scatter(upd->key, upd->value, upd->key_token_stride, upd->value_token_stride,
+                          key_cache, value_cache, cache_block_stride, upd->slot_mapping,
+                          upd->num_tokens, num_kv_heads, head_size, block_size, num_blocks, kv,
+                          dev_status, static_cast<cudaStream_t>(stream), sms, false) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
   }
@@ -620,20 +664,20 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
   if (sms <= 0) return PA_ERR_CUDA;
   const int G = num_heads / num_kv_heads;
   const CascadeLayout CL = layout_cascade(num_seqs, total_q, max_seqlen_q, G, num_heads,
-                                          num_kv_heads, head_size, sms);
+                                          num_kv_heads, head_size, sms, kv.fp8);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < CL.end)
     return PA_ERR_WORKSPACE;
   CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
                seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
                num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
-               dev_status, static_cast<cudaStream_t>(stream)};
+               dev_status, static_cast<cudaStream_t>(stream), kv};
   const int box_rows = gcd_int(block_size, kKeyTile);
   CUtensorMap tmK, tmV;
   if (!encode_pool_map(&tmK, key_cache, head_size, num_kv_heads, block_size, num_blocks,
-                       cache_block_stride, box_rows) ||
+                       cache_block_stride, box_rows, kv.fp8) ||
       !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
-                       cache_block_stride, box_rows))
+                       cache_block_stride, box_rows, kv.fp8))
     return PA_ERR_CUDA;
   CUtensorMap tmQ;
   if (!encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride, G))
@@ -699,7 +743,7 @@ pa_status pa_cascade_fwd(const void* q, int64_t q_token_stride, const void* key_
                       block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
                       num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
                       common_prefix_len, out, lse, workspace, workspace_bytes, dtype, dev_status,
-                      stream);
+                      stream, kKvBf16);
 }
 
 pa_status pa_cascade_fwd_with_update(const pa_kv_update* update, const void* q,
@@ -716,7 +760,94 @@ pa_status pa_cascade_fwd_with_update(const pa_kv_update* update, const void* q,
                       cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
                       max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size, block_size,
                       num_blocks, softmax_scale, common_prefix_len, out, lse, workspace,
-                      workspace_bytes, dtype, dev_status, stream);
+                      workspace_bytes, dtype, dev_status, stream, kKvBf16);
+}
+
+// ---------------------------------------------------------------- FP8 cache
+static KvFormat fp8_format(const pa_kv_fp8* f) {
+  return KvFormat{true, f ? f->k_scale : nullptr, f ? f->v_scale : nullptr};
+}
+
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, int64_t key_token_stride,
+                                   int64_t value_token_stride, void* key_cache, void* value_cache,
+                                   int64_t cache_block_stride, const int64_t* slot_mapping,
+                                   int num_tokens, int num_kv_heads, int head_size,
+                                   int block_size, int num_blocks, const pa_kv_fp8* scales,
+                                   int dtype, int32_t* dev_status, void* stream) {
+  const KvFormat kv = fp8_format(scales);
+  const pa_status st =
+      check_update(key, value, key_token_stride, value_token_stride, key_cache, value_cache,
+                   cache_block_stride, slot_mapping, num_tokens, num_kv_heads, head_size,
+                   block_size, num_blocks, dtype, kv);
+  if (st != PA_OK || num_tokens == 0) return st;
+  const int sms = query_sms(0);
+  if (sms <= 0) return PA_ERR_CUDA;
+  return launch_scatter(key, value, key_token_stride, value_token_stride, key_cache, value_cache,
+                        cache_block_stride, slot_mapping, num_tokens, num_kv_heads, head_size,
+                        block_size, num_blocks, kv, dev_status, static_cast<cudaStream_t>(stream),
+                        sms, false) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+size_t pa_varlen_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
+                                          int max_seqlen_k, int num_heads, int num_kv_heads,
+                                          int head_size, int block_size, int sm_count) {
+  if (check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
+                  head_size, block_size, PA_BF16) != PA_OK || head_size != 128)
+    return 0;
+  const int sms = query_sms(sm_count);
+  if (sms <= 0) return 0;
+  PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
+             num_kv_heads, head_size, sms};
+  d.kv_fp8 = true;
+  return layout_pass(d, 0).end;
+}
+
+size_t pa_cascade_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
+                                           int max_seqlen_k, int num_heads, int num_kv_heads,
+                                           int head_size, int block_size, int sm_count) {
+  if (check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
+                  head_size, block_size, PA_BF16) != PA_OK || head_size != 128)
+    return 0;
+  const int sms = query_sms(sm_count);
+  if (sms <= 0) return 0;
+  return layout_cascade(num_seqs, total_q, max_seqlen_q, num_heads / num_kv_heads, num_heads,
+                        num_kv_heads, head_size, sms, true)
+      .end;
+}
+
+pa_status pa_varlen_fwd_fp8kv(const pa_kv_update* update, const void* q, int64_t q_token_stride,
+                              void* key_cache, void* value_cache, int64_t cache_block_stride,
+                              const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                              const int32_t* block_table, int bt_stride, int num_seqs,
+                              int total_q, int max_seqlen_q, int max_seqlen_k, int num_heads,
+                              int num_kv_heads, int head_size, int block_size, int num_blocks,
+                              float softmax_scale, int causal, const pa_kv_fp8* scales, void* out,
+                              float* lse, void* workspace, size_t workspace_bytes, int dtype,
+                              int32_t* dev_status, void* stream) {
+  return varlen_impl(update, q, q_token_stride, key_cache, value_cache, cache_block_stride,
+                     cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
+                     max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size, block_size,
+                     num_blocks, softmax_scale, causal, out, lse, workspace, workspace_bytes,
+                     dtype, dev_status, stream, fp8_format(scales));
+}
+
+pa_status pa_cascade_fwd_fp8kv(const pa_kv_update* update, const void* q,
+                               int64_t q_token_stride, void* key_cache, void* value_cache,
+                               int64_t cache_block_stride, const int32_t* cu_seqlens_q,
+                               const int32_t* seqused_k, const int32_t* block_table,
+                               int bt_stride, int num_seqs, int total_q, int max_seqlen_q,
+                               int max_seqlen_k, int num_heads, int num_kv_heads, int head_size,
+                               int block_size, int num_blocks, float softmax_scale,
+                               int common_prefix_len, const pa_kv_fp8* scales, void* out,
+                               float* lse, void* workspace, size_t workspace_bytes, int dtype,
+                               int32_t* dev_status, void* stream) {
+  return cascade_impl(update, q, q_token_stride, key_cache, value_cache, cache_block_stride,
+                      cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
+                      max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size, block_size,
+                      num_blocks, softmax_scale, common_prefix_len, out, lse, workspace,
+                      workspace_bytes, dtype, dev_status, stream, fp8_format(scales));
 }
 
 }  // extern "C"

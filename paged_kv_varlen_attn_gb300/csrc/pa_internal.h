@@ -117,6 +117,11 @@ struct AttnArgs {
   int slot_rows;
   int32_t* status;
   int box_rows;              // rows per TMA box (divides block_size and 64)
+  // FP8 pools (split-KV kernel only, head size 128): K/V hold e4m3 codes and
+  // a stored value means code * scale[kv head].
+  int kv_fp8;
+  const float* k_scale;      // [H_kv], device
+  const float* v_scale;      // [H_kv], device
   // Launch order inside one call. The kernels after the planner are launched
   // as programmatic dependents of the kernel before them, so a grid can start
   // while its predecessor drains. pdl_first = 1 for the first kernel after the
@@ -133,6 +138,14 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
                                      const int64_t* slots, int num_tokens, int H_kv, int D, int bs,
                                      int num_blocks, int32_t* status, cudaStream_t st, int sms,
                                      bool pdl);
+// The same scatter into e4m3 pools (kc, vc, block_stride in bytes): each
+// value is stored as e4m3(x / scale[kv head]).
+cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int64_t kstride,
+                                         int64_t vstride, void* kc, void* vc,
+                                         int64_t block_stride, const int64_t* slots,
+                                         int num_tokens, int H_kv, int D, int bs, int num_blocks,
+                                         const float* k_scale, const float* v_scale,
+                                         int32_t* status, cudaStream_t st, int sms, bool pdl);
 cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* alse,
                          const void* b, const float* blse, int T, int H, int D, cudaStream_t st,
                          int sms);

@@ -212,3 +212,46 @@ def test_use_cascade_attention_policy(lib):
         pa.PA_ERR_INVALID_ARG
     assert lib.pa_use_cascade_attention(256, 8, 8, 128, 1, None) == pa.PA_ERR_INVALID_ARG
     assert pa.use_cascade_attention(2048, 64, 8, 128) is True
+
+
+def _fp8(ks=FAKE, vs=FAKE):
+    return pa.KvFp8(ks, vs)
+
+
+def _varlen_fp8(lib, upd, fp8, **kw):
+    a = dict(q=FAKE, qs=32 * 128, kc=FAKE, vc=FAKE, cbs=16 * 8 * 128, cu=FAKE, lens=FAKE,
+             bt=FAKE, bts=4, S=2, T=2, mq=1, mk=64, H=32, Hk=8, D=128, bs=16, nb=10,
+             scale=0.088, causal=1, out=FAKE, lse=None, ws=FAKE, wsb=1 << 20, dtype=0)
+    a.update(kw)
+    return lib.pa_varlen_fwd_fp8kv(
+        ctypes.byref(upd) if upd is not None else None, a["q"], a["qs"], a["kc"], a["vc"],
+        a["cbs"], a["cu"], a["lens"], a["bt"], a["bts"], a["S"], a["T"], a["mq"], a["mk"], a["H"],
+        a["Hk"], a["D"], a["bs"], a["nb"], a["scale"], a["causal"],
+        ctypes.byref(fp8) if fp8 is not None else None, a["out"], a["lse"], a["ws"], a["wsb"],
+        a["dtype"], None, None)
+
+
+def test_fp8_entry_validation(lib):
+    """FP8 pools: head size 128 only, scales required (4-byte aligned), page
+    stride a multiple of 16 bytes; checked before anything is launched."""
+    assert _varlen_fp8(lib, None, _fp8(), D=64, qs=32 * 64, cbs=16 * 8 * 64) == \
+        pa.PA_ERR_UNSUPPORTED
+    assert _varlen_fp8(lib, None, None) == pa.PA_ERR_INVALID_ARG
+    assert _varlen_fp8(lib, None, _fp8(ks=None)) == pa.PA_ERR_INVALID_ARG
+    assert _varlen_fp8(lib, None, _fp8(vs=FAKE + 2)) == pa.PA_ERR_INVALID_ARG
+    assert _varlen_fp8(lib, None, _fp8(), cbs=16 * 8 * 128 + 8) == pa.PA_ERR_INVALID_ARG
+    assert _varlen_fp8(lib, _upd(key=FAKE + 2), _fp8()) == pa.PA_ERR_INVALID_ARG
+    assert _varlen_fp8(lib, None, _fp8(), S=0, T=0) == pa.PA_OK
+    args = [FAKE, FAKE, 1024, 1024, FAKE, FAKE, 16 * 8 * 128, FAKE, 4, 8, 128, 16, 10]
+    assert lib.pa_reshape_and_cache_fp8(*args, None, 0, None, None) == pa.PA_ERR_INVALID_ARG
+    bad_d = [FAKE, FAKE, 512, 512, FAKE, FAKE, 16 * 8 * 64, FAKE, 4, 8, 64, 16, 10]
+    assert lib.pa_reshape_and_cache_fp8(*bad_d, ctypes.byref(_fp8()), 0, None, None) == \
+        pa.PA_ERR_UNSUPPORTED
+    bad_stride = args[:6] + [16 * 8 * 128 + 8] + args[7:]
+    assert lib.pa_reshape_and_cache_fp8(*bad_stride, ctypes.byref(_fp8()), 0, None, None) == \
+        pa.PA_ERR_INVALID_ARG
+    zero = args[:8] + [0] + args[9:]
+    assert lib.pa_reshape_and_cache_fp8(*zero, None, 0, None, None) == pa.PA_OK
+    assert lib.pa_varlen_fwd_fp8kv_workspace_size(2, 2, 1, 64, 32, 8, 64, 16, 152) == 0
+    assert lib.pa_varlen_fwd_fp8kv_workspace_size(2, 2, 1, 64, 32, 8, 128, 16, 152) > 0
+    assert lib.pa_cascade_fwd_fp8kv_workspace_size(2, 2, 1, 64, 32, 8, 128, 16, 152) > 0

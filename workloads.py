@@ -20,6 +20,11 @@ Recipe (every workload):
     slot is (physical page) * block_size + (position % block_size);
   * all values are drawn in fp32 and rounded to bf16; both the oracle and the
     GPU path consume the same bf16 values.
+  * FP8 (e4m3) pools: the prior context of KV head h is the same N(0,1) pages
+    divided by the pool's scale for h (kv_scales) and cast by torch to
+    float8_e4m3fn (bytes kept as uint8), after clamping to +-448 -- synthetic
+    bytes that both sides read as they are. New tokens stay bf16; the oracle
+    and the GPU path each quantize them with their own code.
 """
 from __future__ import annotations
 
@@ -138,6 +143,40 @@ class Workload:
         res = {}
         for c, ps in by_chunk.items():
             chunk = self.pool_chunk(which, c)
+            for p in ps:
+                res[p] = chunk[p - c * PAGES_PER_CHUNK].clone()
+        return res
+
+    # ---- FP8 (e4m3) pools ----------------------------------------------------
+    def kv_scales(self, which: int) -> list:
+        """Per-KV-head e4m3 scales of the K (0) or V (1) pool: amax (4 + (h + which) % 4)
+        of an N(0,1) head maps to the largest e4m3 value 448."""
+        return [(4 + (h + which) % 4) / 448.0 for h in range(self.num_kv_heads)]
+
+    def fp8_pool_chunk(self, which: int, chunk: int) -> torch.Tensor:
+        """uint8 e4m3 pages of chunk ``chunk`` (see the module recipe)."""
+        x = self.pool_chunk(which, chunk).to(torch.float32)
+        s = torch.tensor(self.kv_scales(which), dtype=torch.float32)[:, None]
+        return (x / s).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+    def fp8_pool(self, which: int, device="cpu") -> torch.Tensor:
+        """The whole e4m3 K or V pool [num_blocks, block_size, H_kv, D] (uint8)."""
+        out = torch.empty((self.num_blocks,) + self.page_shape, dtype=torch.uint8,
+                          device=device)
+        for c in range(self.num_chunks()):
+            first = c * PAGES_PER_CHUNK
+            chunk = self.fp8_pool_chunk(which, c)
+            out[first:first + chunk.shape[0]].copy_(chunk)
+        return out
+
+    def fp8_pool_pages(self, which: int, pages) -> dict:
+        """{page id: uint8 [bs, H_kv, D]} e4m3 pages (pre-scatter contents)."""
+        by_chunk = {}
+        for p in sorted(set(int(p) for p in pages)):
+            by_chunk.setdefault(p // PAGES_PER_CHUNK, []).append(p)
+        res = {}
+        for c, ps in by_chunk.items():
+            chunk = self.fp8_pool_chunk(which, c)
             for p in ps:
                 res[p] = chunk[p - c * PAGES_PER_CHUNK].clone()
         return res
