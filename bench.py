@@ -638,7 +638,9 @@ def bench_ours(args, rank, world, local):
         line["e2e"] = {"value": 100.0 * t_ideal / (e2e_ms * 1e-3), "unit": "% of roofline",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
         ach = counts["flops"] / (attn_ms_avg * 1e-3) / 1e12
-        line["roofline"] = {"bound": "tensor", "kernel": "plan + attn_tc_kernel<128> + attn_split_kernel<128>",
+        line["roofline"] = {"bound": "tensor",
+                            "kernel": ("plan + attn_split_kernel<128, fp8> (every segment)" if fp8
+                                       else "plan + attn_tc_kernel<128> + attn_split_kernel<128>"),
                             "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                             "frac": ach / peaks["bf16_tflops"], "traffic": None,
                             "peak_source": peaks["source"], "attn_ms_per_launch": attn_ms_avg}

@@ -130,6 +130,17 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// D += A(16x32, row) * B(32x8, col), e4m3 inputs (4 per register, lowest
+// k-index in the lowest byte), fp32 accumulate. Every product is exact.
+__device__ __forceinline__ void mma_16832_e4m3(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 // f16x2 of two floats, lo in the low half (round to nearest even).
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
@@ -146,6 +157,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
 // saturating to +-448 (NaN stays NaN).
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+// Transpose of an 8x8 matrix of 16-bit elements held in the MMA fragment
+// layout (lane i: row i / 4, elements 2 * (i % 4) and +1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
 }
 // Byte permute: bytes of {a, b} (a = bytes 0-3, b = 4-7) selected by sel.
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
