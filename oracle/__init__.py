@@ -9,6 +9,8 @@ from .paged_attention import (  # noqa: F401
     attend_dense,
     varlen_attention,
     merge_attn_states,
+    merge_attn_states_n,
+    dcp_decode_attention,
     cascade_attention,
     cascade_attention_steps,
     e4m3_decode,

@@ -202,6 +202,56 @@ def merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse):
     return out, lse
 
 
+def merge_attn_states_n(parts_out, parts_lse):
+    """Combine n partial attention results over disjoint key sets ([FA-vLLM]
+    §9: DCP merges the ranks' partial results by their LSEs; §6.3 / §8.2 give
+    the two-state merge this generalises).
+
+    parts_out: [n, T, H, D]; parts_lse: [n, H, T] natural log. With
+    m = max_r lse_r and w_r = exp(lse_r - m): out = sum_r w_r out_r / sum_r w_r,
+    lse = m + ln(sum_r w_r). A row whose LSEs are all -inf saw no key: out 0,
+    lse -inf.
+    """
+    po, pl = parts_out.to(F64), parts_lse.to(F64)
+    n, T, H, D = po.shape
+    out = torch.zeros((T, H, D), dtype=F64)
+    lse = torch.full((H, T), NEG_INF, dtype=F64)
+    for h in range(H):
+        for t in range(T):
+            ls = [float(pl[r, h, t]) for r in range(n)]
+            m = max(ls)
+            if m == NEG_INF:
+                continue
+            ws = [math.exp(x - m) for x in ls]
+            acc = torch.zeros(D, dtype=F64)
+            for r in range(n):
+                acc += ws[r] * po[r, t, h]
+            tot = math.fsum(ws)
+            out[t, h] = acc / tot
+            lse[h, t] = m + math.log(tot)
+    return out, lse
+
+
+def dcp_decode_attention(q, key_cache, value_cache, cu_seqlens_q, shard_tables, shard_lens,
+                         softmax_scale):
+    """Decode context parallelism over virtual ranks ([FA-vLLM] §9 and the
+    DCP branch of §4): every rank holds some of each sequence's KV blocks;
+    each computes the attention of all the queries against its own shard,
+    non-causal (the decode query follows every key), and the ranks' partial
+    (out, lse) are merged by their LSEs.
+
+    shard_tables[r]: int32 [S, max_blocks] block table of rank r's shard,
+    shard_lens[r]: int32 [S] its key counts. Returns the merged (out, lse).
+    """
+    outs, lses = [], []
+    for bt, lens in zip(shard_tables, shard_lens):
+        o, l = varlen_attention(q, key_cache, value_cache, cu_seqlens_q, lens, bt,
+                                softmax_scale, causal=False)
+        outs.append(o)
+        lses.append(l)
+    return merge_attn_states_n(torch.stack(outs), torch.stack(lses))
+
+
 # --------------------------------------------------------------------------
 # Cascade (shared-prefix) attention ([FA-vLLM] §6.3).
 # --------------------------------------------------------------------------

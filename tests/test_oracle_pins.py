@@ -650,3 +650,88 @@ def test_planted_exponent_bias_is_caught(monkeypatch):
     monkeypatch.setattr(P, "e4m3_decode", lambda c: orig(c) * 2.0 if c & 0x78 else orig(c))
     with pytest.raises(AssertionError):
         check_e4m3_points()
+
+
+# ----------------------------------------------------------------------------
+# n-state merge and decode context parallelism over virtual ranks
+# ("FlashAttention 在 vLLM 中的实现分析" §9: each rank attends over its KV shard,
+# the partial (out, lse) are merged by LSE).
+# ----------------------------------------------------------------------------
+def check_merge_n_partition():
+    """Attention over a partition of the keys into n interleaved groups,
+    merged, equals attention over all keys (attend_dense is pinned by brute
+    force and torch SDPA)."""
+    g = torch.Generator().manual_seed(12)
+    q = torch.randn(3, 4, 8, generator=g, dtype=F64)
+    k = torch.randn(17, 2, 8, generator=g, dtype=F64)
+    v = torch.randn(17, 2, 8, generator=g, dtype=F64)
+    full_o, full_l = oracle.attend_dense(q, k, v, 0.7, False, 3, 17)
+    for n in (1, 2, 3, 5):
+        outs, lses = [], []
+        for r in range(n):
+            idx = torch.arange(r, 17, n)
+            o, l = oracle.attend_dense(q, k[idx], v[idx], 0.7, False, 3, idx.numel())
+            outs.append(o)
+            lses.append(l)
+        o, l = P.merge_attn_states_n(torch.stack(outs), torch.stack(lses))
+        assert torch.allclose(o, full_o, atol=1e-12, rtol=0), n
+        assert torch.allclose(l, full_l, atol=1e-12, rtol=0), n
+
+
+def test_merge_n_partition_invariance():
+    check_merge_n_partition()
+
+
+def test_merge_n_identity_order_and_empty():
+    g = torch.Generator().manual_seed(13)
+    po = torch.randn(4, 3, 2, 8, generator=g, dtype=F64)
+    pl = torch.randn(4, 2, 3, generator=g, dtype=F64) * 3
+    o1, l1 = P.merge_attn_states_n(po[:1], pl[:1])
+    assert torch.equal(o1, po[0]) and torch.allclose(l1, pl[0], atol=1e-15, rtol=0)
+    perm = torch.tensor([2, 0, 3, 1])
+    oa, la = P.merge_attn_states_n(po, pl)
+    ob, lb = P.merge_attn_states_n(po[perm], pl[perm])
+    assert torch.allclose(oa, ob, atol=1e-13, rtol=0) and torch.allclose(la, lb, atol=1e-13, rtol=0)
+    # two states: the pinned two-state merge
+    o2, l2 = P.merge_attn_states_n(po[:2], pl[:2])
+    r2o, r2l = oracle.merge_attn_states(po[0], pl[0], po[1], pl[1])
+    assert torch.allclose(o2, r2o, atol=1e-13, rtol=0) and torch.allclose(l2, r2l, atol=1e-13, rtol=0)
+    # -inf parts carry no weight; a row with only -inf parts is empty
+    pl2 = pl.clone()
+    pl2[1:] = float("-inf")
+    o3, l3 = P.merge_attn_states_n(po, pl2)
+    assert torch.equal(o3, po[0]) and torch.allclose(l3, pl[0], atol=1e-15, rtol=0)
+    pl2[0] = float("-inf")
+    o4, l4 = P.merge_attn_states_n(po, pl2)
+    assert torch.equal(o4, torch.zeros_like(o4)) and torch.isinf(l4).all()
+
+
+@pytest.mark.parametrize("ranks", [1, 2, 3, 4])
+def test_dcp_virtual_ranks_equal_flat_decode(ranks):
+    """Decode over R virtual ranks (block b on rank b % R, each rank
+    non-causal over its shard, states merged) equals flat causal decode,
+    including sequences with fewer blocks than ranks (empty shards)."""
+    wl = W.random_case(31 + ranks, num_seqs=5, num_heads=4, num_kv_heads=2, head_size=16,
+                       block_size=16, max_q=1, max_kv=90, decode_frac=1.0)
+    assert all(q == 1 for q in wl.q_lens)
+    kc, vc = wl.pool(0), wl.pool(1)
+    oracle.reshape_and_cache(wl.k_new, wl.v_new, wl.slot_mapping, kc, vc)
+    ref_o, ref_l = oracle.varlen_attention(wl.q, kc, vc, wl.cu_seqlens_q, wl.seqused_k,
+                                           wl.block_table, wl.softmax_scale, True)
+    tables, lens = W.dcp_shards(wl, ranks)
+    assert [int(sum(l[s] for l in lens)) for s in range(wl.num_seqs)] == wl.kv_lens
+    o, l = oracle.dcp_decode_attention(wl.q, kc, vc, wl.cu_seqlens_q, tables, lens,
+                                       wl.softmax_scale)
+    assert torch.allclose(o, ref_o, atol=1e-12, rtol=0)
+    assert torch.allclose(l, ref_l, atol=1e-12, rtol=0)
+
+
+def test_planted_max_instead_of_logsumexp_is_caught(monkeypatch):
+    orig = P.merge_attn_states_n
+
+    def bad(po, pl):
+        o, l = orig(po, pl)
+        return o, pl.to(F64).max(dim=0).values
+    monkeypatch.setattr(P, "merge_attn_states_n", bad)
+    with pytest.raises(AssertionError):
+        check_merge_n_partition()

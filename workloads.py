@@ -209,6 +209,30 @@ class Workload:
             common_prefix_len=self.common_prefix_len, meta=dict(self.meta))
 
 
+def dcp_shards(wl: "Workload", ranks: int):
+    """Block tables of ``ranks`` virtual context-parallel ranks: block b of a
+    sequence (its b-th logical page) lives on rank b % ranks. Returns
+    ([int32 [S, max_blocks]] per rank, [int32 [S] key counts] per rank); a
+    rank's row lists its pages in logical order (INT32_MAX after them), so
+    the sequence's partial last page, if it is the rank's, comes last."""
+    S, bs = wl.num_seqs, wl.block_size
+    width = max(1, (wl.block_table.shape[1] + ranks - 1) // ranks)
+    tables, lens = [], []
+    for r in range(ranks):
+        bt = torch.full((S, width), INT32_MAX, dtype=torch.int32)
+        ln = torch.zeros(S, dtype=torch.int32)
+        for s in range(S):
+            pages = wl.pages_of(s)
+            mine = [b for b in range(len(pages)) if b % ranks == r]
+            if mine:
+                bt[s, :len(mine)] = torch.tensor([pages[b] for b in mine], dtype=torch.int32)
+            kv = wl.kv_lens[s]
+            ln[s] = sum(min(bs, kv - b * bs) for b in mine)
+        tables.append(bt)
+        lens.append(ln)
+    return tables, lens
+
+
 def _build(name, seed, H, H_kv, D, bs, q_lens, kv_lens, g, causal=True, scale=None,
            num_blocks=None, shared_prefix_pages=0, pool_slack=1.1, meta=None):
     """Lay out pages, draw Q and new K/V. ``g`` has already drawn the lengths."""
