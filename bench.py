@@ -347,6 +347,22 @@ def row_figures(pa, wl, counts, dev, stream, scatter_fn, steps):
         ms = timed_flushed(merge, n, flush, stream, flush_rd)
         b = 3 * tm * H * D * 2 + 3 * H * tm * 4
         out[name] = {"tokens": tm, "bytes": b, "ms": ms, "gbs": b / (ms * 1e-3) / 1e9}
+    # The n-state merge of decode context parallelism: 4 virtual ranks'
+    # partial states of a 16,384-token batch.
+    nr, tm = 4, 16384
+    po = torch.randn((nr, tm, H, D), generator=g).to(torch.bfloat16).to(dev)
+    pl = (torch.randn((nr, H, tm), generator=g) * 3).to(dev)
+    o = torch.empty((tm, H, D), dtype=torch.bfloat16, device=dev)
+    lo = torch.empty((H, tm), dtype=torch.float32, device=dev)
+
+    def merge_n():
+        pa.merge_attn_states_n(po, pl, out=o, out_lse=lo)
+    for _ in range(3):
+        merge_n()
+    ms = timed_flushed(merge_n, n, flush, stream, flush_rd)
+    b = (nr + 1) * tm * H * D * 2 + (nr + 1) * H * tm * 4
+    out["merge_attn_states_n_4parts_16k_tokens"] = {"tokens": tm, "parts": nr, "bytes": b,
+                                                    "ms": ms, "gbs": b / (ms * 1e-3) / 1e9}
     return out
 
 

@@ -7,7 +7,8 @@
  *             vllm-analysis/07): §1.1 tiled online softmax, §4 forward() and the
  *             flash_attn_varlen_func call, §4.2 KV-cache update, §5 PagedAttention
  *             integration (block_table addressing), §6.3 cascade execution,
- *             §8.2 reshape_and_cache_flash / merge_attn_states, §10 feature table.
+ *             §8.2 reshape_and_cache_flash / merge_attn_states, §9 DCP, §10 feature
+ *             table.
  *   [FA/FI]   "FlashAttention と FlashInfer:2 大 GPU アテンションバックエンド":
  *             データフロー (KV cache shape, block size multiple of 16),
  *             境界と失敗 (head-size and dtype limits, FP8 KV cache).
@@ -163,6 +164,38 @@ pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out
                                const float* prefix_lse, const void* suffix_out,
                                const float* suffix_lse, int num_tokens, int num_heads,
                                int head_size, int dtype, void* stream);
+
+/*
+ * pa_merge_attn_states_n -- LSE-weighted combine of num_parts partial
+ * attention results over disjoint key sets: the merge step of decode context
+ * parallelism ([FA-vLLM] §9 and the DCP branch of §4: every rank attends over
+ * its own KV shard, non-causal for decode, and the ranks' partial (out, lse)
+ * are merged by LSE -- there by all-gather + reduce-scatter across GPUs; here
+ * on one GPU, for ranks that are virtual), and the n-part form of
+ * pa_merge_attn_states.
+ *
+ *   parts_out : bf16; part r is [num_tokens, num_heads, head_size] contiguous
+ *               at parts_out + r * part_stride_out (elements, a multiple of 8,
+ *               >= num_tokens * num_heads * head_size when num_parts > 1).
+ *   parts_lse : float32; part r is [num_heads, num_tokens] at
+ *               parts_lse + r * part_stride_lse (>= num_heads * num_tokens).
+ *   out       : [num_tokens, num_heads, head_size] bf16; may alias a part.
+ *   out_lse   : float32 [num_heads, num_tokens] or NULL; must not overlap the
+ *               parts' LSEs (PA_ERR_INVALID_ARG).
+ * With m = max_r lse_r and w_r = e^(lse_r - m): out = sum_r w_r out_r /
+ * sum_r w_r, out_lse = m + ln sum_r w_r (float32 throughout, out rounded to
+ * bf16 once). A row whose LSEs are all -inf gets out = 0, out_lse = -inf.
+ * 1 <= num_parts <= PA_MERGE_N_MAX.
+ *
+ * A virtual-rank decode over R ranks is R pa_varlen_fwd calls (causal = 0),
+ * one per rank with that rank's block table and key counts, writing into the
+ * parts of one stacked buffer, followed by this merge.
+ */
+#define PA_MERGE_N_MAX 1024
+pa_status pa_merge_attn_states_n(void* out, float* out_lse, const void* parts_out,
+                                 int64_t part_stride_out, const float* parts_lse,
+                                 int64_t part_stride_lse, int num_parts, int num_tokens,
+                                 int num_heads, int head_size, int dtype, void* stream);
 
 /* Workspace bytes pa_cascade_fwd needs (same arguments as the varlen query). */
 size_t pa_cascade_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,

@@ -49,6 +49,7 @@ EXPORTS = (
     "pa_cascade_fwd_fp8kv_workspace_size",
     "pa_varlen_fwd_fp8kv",
     "pa_cascade_fwd_fp8kv",
+    "pa_merge_attn_states_n",
 )
 
 _lib = None
@@ -94,6 +95,8 @@ _SIGS = {
     "pa_reshape_and_cache_fp8": ([_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _i32, _i32, _i32,
                                   _i32, _i32, ctypes.POINTER(KvFp8), _i32, _vp, _vp], _i32),
     "pa_varlen_fwd_fp8kv_workspace_size": ([_i32] * 9, _sz),
+    "pa_merge_attn_states_n": ([_vp, _vp, _vp, _i64, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp],
+                               _i32),
     "pa_cascade_fwd_fp8kv_workspace_size": ([_i32] * 9, _sz),
     "pa_varlen_fwd_fp8kv": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS[:20] +
                             [ctypes.POINTER(KvFp8)] + _ATTN_ARGS[20:], _i32),
@@ -320,6 +323,28 @@ def merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse, out=None, 
         _ptr(out), _ptr(out_lse), _ptr(prefix_out), _ptr(prefix_lse), _ptr(suffix_out),
         _ptr(suffix_lse), T, H, D, PA_BF16, _stream(prefix_out.device))
     _check(code, "pa_merge_attn_states")
+    return out, out_lse
+
+
+def merge_attn_states_n(parts_out, parts_lse, out=None, out_lse=None, return_lse=True):
+    """LSE-weighted combine of n partial states: parts_out [n, T, H, D] bf16
+    (each part contiguous), parts_lse [n, H, T] float32. Returns (out, lse or None)."""
+    lib = load_library()
+    _need_cuda(parts_out, parts_lse)
+    n, T, H, D = parts_out.shape
+    if parts_out[0].numel() and not parts_out[0].is_contiguous():
+        raise ValueError("each part must be a contiguous [tokens, heads, head_size] tensor")
+    if parts_lse.shape != (n, H, T) or (T and parts_lse.stride(2) != 1) or \
+            (T and parts_lse.stride(1) != T):
+        raise ValueError("parts_lse must be [n, heads, tokens] with contiguous parts")
+    if out is None:
+        out = torch.empty((T, H, D), dtype=parts_out.dtype, device=parts_out.device)
+    if out_lse is None and return_lse:
+        out_lse = torch.empty((H, T), dtype=torch.float32, device=parts_out.device)
+    code = lib.pa_merge_attn_states_n(
+        _ptr(out), _ptr(out_lse), _ptr(parts_out), parts_out.stride(0), _ptr(parts_lse),
+        parts_lse.stride(0), n, T, H, D, PA_BF16, _stream(parts_out.device))
+    _check(code, "pa_merge_attn_states_n")
     return out, out_lse
 
 

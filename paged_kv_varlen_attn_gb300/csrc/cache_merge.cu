@@ -269,4 +269,81 @@ cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// n-state merge: the LSE merge of the partial results of n ranks of decode
+// context parallelism ("FlashAttention 在 vLLM 中的实现分析" §9) or of any n
+// disjoint key sets. One thread per 16-byte vector of a (token, head) row:
+// the row's n LSEs (L1 hits after the first thread) give the maximum m, then
+// the n vectors are read in batches of kBatchN loads in flight and summed
+// with weights e^(lse_r - m); out = sum / sum of weights, lse = m + ln(sum
+// of weights), a row whose LSEs are all -inf gets out 0, lse -inf.
+// ---------------------------------------------------------------------------
+constexpr int kBatchN = 4;
+
+__global__ void __launch_bounds__(kMergeThreads)
+merge_attn_states_n_kernel(uint4* out, float* out_lse, const uint4* __restrict__ parts,
+                           int64_t pstride_v, const float* __restrict__ plse, int64_t lstride,
+                           int n, int T, int H, int vpr) {
+  const int64_t total = static_cast<int64_t>(T) * H * vpr;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += step) {
+    const int64_t row = idx / vpr;            // row = t * H + h
+    const int vi = static_cast<int>(idx - row * vpr);
+    const int t = static_cast<int>(row / H);
+    const int h = static_cast<int>(row - static_cast<int64_t>(t) * H);
+    const float* lp = plse + static_cast<int64_t>(h) * T + t;
+    float m = -INFINITY;
+    for (int r = 0; r < n; ++r) m = fmaxf(m, __ldg(lp + r * lstride));
+    uint4 res = make_uint4(0, 0, 0, 0);
+    float lse_out = -INFINITY;
+    if (m != -INFINITY) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float sw = 0.f;
+      for (int r0 = 0; r0 < n; r0 += kBatchN) {
+        uint4 v[kBatchN];
+        float w[kBatchN];
+#pragma unroll
+        for (int u = 0; u < kBatchN; ++u) {
+          if (r0 + u < n) {
+            w[u] = fast_exp2((__ldg(lp + (r0 + u) * lstride) - m) * kLog2e);
+            v[u] = __ldcs(parts + (r0 + u) * pstride_v + idx);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatchN; ++u) {
+          if (r0 + u >= n) continue;
+          float f[8];
+          bf16x8_to_float(v[u], f);
+          sw += w[u];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] += w[u] * f[i];
+        }
+      }
+      const float inv = 1.0f / sw;
+      uint32_t* rr = reinterpret_cast<uint32_t*>(&res);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rr[i] = pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+      lse_out = m + fast_log2(sw) * kLn2;
+    }
+    out[idx] = res;
+    if (out_lse && vi == 0) out_lse[static_cast<int64_t>(h) * T + t] = lse_out;
+  }
+}
+
+cudaError_t launch_merge_n(void* out, float* out_lse, const void* parts, int64_t part_stride,
+                           const float* parts_lse, int64_t lse_stride, int n, int T, int H, int D,
+                           cudaStream_t st, int sms) {
+  if (T == 0) return cudaSuccess;
+  const int vpr = D / 8;
+  const int64_t total = static_cast<int64_t>(T) * H * vpr;
+  const int64_t want = (total + kMergeThreads - 1) / kMergeThreads;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  merge_attn_states_n_kernel<<<grid, kMergeThreads, 0, st>>>(
+      static_cast<uint4*>(out), out_lse, static_cast<const uint4*>(parts), part_stride / 8,
+      parts_lse, lse_stride, n, T, H, vpr);
+  return cudaGetLastError();
+}
+
 }  // namespace pa

@@ -620,6 +620,37 @@ pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_merge_attn_states_n(void* out, float* out_lse, const void* parts_out,
+                                 int64_t part_stride_out, const float* parts_lse,
+                                 int64_t part_stride_lse, int num_parts, int num_tokens,
+                                 int num_heads, int head_size, int dtype, void* stream) {
+  if (num_parts < 1 || num_parts > PA_MERGE_N_MAX || num_tokens < 0 || num_heads <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (head_size <= 0 || head_size % 8 != 0 || head_size > 256) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!out || !parts_out || !parts_lse) return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(parts_out)) return PA_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(parts_lse) | reinterpret_cast<uintptr_t>(out_lse)) & 3u) != 0)
+    return PA_ERR_INVALID_ARG;
+  const int64_t row_elems = static_cast<int64_t>(num_tokens) * num_heads * head_size;
+  const int64_t lse_elems = static_cast<int64_t>(num_heads) * num_tokens;
+  if (num_parts > 1 && (part_stride_out < row_elems || part_stride_out % 8 != 0 ||
+                        part_stride_lse < lse_elems))
+    return PA_ERR_INVALID_ARG;
+  if (out_lse) {   // out_lse must not overlap any part's LSE (other threads still read them)
+    const float* lo = parts_lse;
+    const float* hi = parts_lse + (num_parts - 1) * part_stride_lse + lse_elems;
+    if (out_lse + lse_elems > lo && out_lse < hi) return PA_ERR_INVALID_ARG;
+  }
+  const int sms = query_sms(0);
+  if (sms <= 0) return PA_ERR_CUDA;
+  cudaError_t e = launch_merge_n(out, out_lse, parts_out, part_stride_out, parts_lse,
+                                 part_stride_lse, num_parts, num_tokens, num_heads, head_size,
+                                 static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 // pa_cascade_fwd, optionally preceded by a K/V update of the same cache.
 static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_token_stride,
                               void* key_cache, void* value_cache, int64_t cache_block_stride,

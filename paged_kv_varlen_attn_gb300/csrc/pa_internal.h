@@ -149,6 +149,11 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int
 cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* alse,
                          const void* b, const float* blse, int T, int H, int D, cudaStream_t st,
                          int sms);
+// n-state merge: part r's out at parts + r * part_stride (elements), its
+// LSE at parts_lse + r * lse_stride.
+cudaError_t launch_merge_n(void* out, float* out_lse, const void* parts, int64_t part_stride,
+                           const float* parts_lse, int64_t lse_stride, int n, int T, int H, int D,
+                           cudaStream_t st, int sms);
 cudaError_t launch_plan(const PlanPasses& passes, int npasses, cudaStream_t st);
 cudaError_t launch_attn_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
                               int items_bound, cudaStream_t st);

@@ -255,3 +255,26 @@ def test_fp8_entry_validation(lib):
     assert lib.pa_varlen_fwd_fp8kv_workspace_size(2, 2, 1, 64, 32, 8, 64, 16, 152) == 0
     assert lib.pa_varlen_fwd_fp8kv_workspace_size(2, 2, 1, 64, 32, 8, 128, 16, 152) > 0
     assert lib.pa_cascade_fwd_fp8kv_workspace_size(2, 2, 1, 64, 32, 8, 128, 16, 152) > 0
+
+
+def test_merge_n_validation(lib):
+    """pa_merge_attn_states_n checks its arguments before launching."""
+    T, H, D = 4, 2, 128
+    rowe, lsee = T * H * D, H * T
+    args = dict(out=FAKE, olse=None, po=FAKE, ps=rowe, pl=FAKE, pls=lsee, n=3, T=T, H=H, D=D)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return lib.pa_merge_attn_states_n(a["out"], a["olse"], a["po"], a["ps"], a["pl"], a["pls"],
+                                          a["n"], a["T"], a["H"], a["D"], 0, None)
+    assert call(n=0) == pa.PA_ERR_INVALID_ARG
+    assert call(n=1025) == pa.PA_ERR_INVALID_ARG
+    assert call(D=12) == pa.PA_ERR_UNSUPPORTED
+    assert call(T=0) == pa.PA_OK
+    assert call(ps=rowe - 8) == pa.PA_ERR_INVALID_ARG          # parts overlap
+    assert call(ps=rowe + 4) == pa.PA_ERR_INVALID_ARG          # not a 16-byte multiple
+    assert call(pls=lsee - 1) == pa.PA_ERR_INVALID_ARG
+    assert call(po=FAKE + 8) == pa.PA_ERR_INVALID_ARG          # misaligned
+    assert call(olse=FAKE + 4 * lsee) == pa.PA_ERR_INVALID_ARG  # out_lse inside part 1's LSE
+    assert call(po=None) == pa.PA_ERR_INVALID_ARG

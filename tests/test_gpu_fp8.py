@@ -128,6 +128,7 @@ CASES = [
     (214, 3, 8, 1, 64, 90, 500, False, 0.0),     # non-causal, GQA 8, page 64
     (215, 7, 32, 8, 128, 33, 1500, True, 0.5),   # page 128, ragged
     (216, 5, 16, 16, 48, 20, 200, True, 0.3),    # page 48 (boxes of 16 rows)
+    (219, 4, 32, 2, 16, 1, 700, True, 1.0),      # decode, GQA 16: 16-row items
 ]
 
 
