@@ -100,11 +100,16 @@ def log_sum_exp_from(m, l):
 # --------------------------------------------------------------------------
 # Attention of one sequence ([FA-vLLM] §1.1 target result; §4 varlen call).
 # --------------------------------------------------------------------------
-def attend_dense(q, k, v, softmax_scale, causal, q_len, kv_len, rows=None, row_chunk=512):
+def attend_dense(q, k, v, softmax_scale, causal, q_len, kv_len, rows=None, row_chunk=512,
+                 sinks=None):
     """Exact softmax attention of query rows against dense keys of one sequence.
 
     q: [q_len, H, D], k, v: [kv_len, H_kv, D] (any float type; computed in
     float64). ``rows`` selects which of the q_len rows to compute (default all).
+    ``sinks``: optional per-query-head logits ([FA-vLLM] §1.2 and §1.3: the
+    `s_aux` learnable sink token of FA3/FA4), read as one extra key of logit
+    sinks[h] (in the units of softmax_scale * q.k) and value zero: it joins
+    the softmax denominator and the LSE only.
     Returns out [n_rows, H, D] float64 and lse [H, n_rows] float64.
     """
     H, D = q.shape[1], q.shape[2]
@@ -114,6 +119,9 @@ def attend_dense(q, k, v, softmax_scale, causal, q_len, kv_len, rows=None, row_c
     n = rows.numel()
     out = torch.zeros((n, H, D), dtype=F64)
     lse = torch.full((H, n), NEG_INF, dtype=F64)
+    if sinks is not None:
+        for h in range(H):
+            lse[h, :] = float(sinks[h])      # a row with no visible key sees only the sink
     if n == 0 or kv_len == 0:
         return out, lse
     q64, k64, v64 = q.to(F64), k.to(F64), v.to(F64)
@@ -132,25 +140,29 @@ def attend_dense(q, k, v, softmax_scale, causal, q_len, kv_len, rows=None, row_c
             logits = softmax_scale * (q64[r, h, :] @ k64[:, hk, :].T)
             logits = logits.masked_fill(~visible, NEG_INF)
             m = torch.where(any_visible, logits.max(dim=1).values, torch.zeros_like(any_visible, dtype=F64))
+            if sinks is not None:
+                m = torch.where(any_visible, torch.maximum(m, torch.tensor(float(sinks[h]), dtype=F64)), m)
             p = torch.exp(logits - m[:, None])
             l = p.sum(dim=1)
+            if sinks is not None:
+                l = l + torch.exp(float(sinks[h]) - m)
             safe_l = torch.where(any_visible, l, torch.ones_like(l))
             o = (p @ v64[:, hk, :]) / safe_l[:, None]
             out[c0:c0 + r.numel(), h, :] = torch.where(any_visible[:, None], o, torch.zeros_like(o))
             lse_h = log_sum_exp_from(m, safe_l)
-            lse[h, c0:c0 + r.numel()] = torch.where(any_visible, lse_h,
-                                                    torch.full_like(lse_h, NEG_INF))
+            lse[h, c0:c0 + r.numel()] = torch.where(any_visible, lse_h, lse[h, c0:c0 + r.numel()])
     return out, lse
 
 
 def varlen_attention(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
-                     softmax_scale, causal, rows=None):
+                     softmax_scale, causal, rows=None, sinks=None):
     """Varlen attention over a paged KV cache ([FA-vLLM] §4 and §5).
 
     q: [T, H, D] packed by cu_seqlens_q [S+1]; seqused_k [S]; block_table
     [S, max_blocks] int32; caches [num_blocks, block_size, H_kv, D].
     ``rows``: optional {seq index: list of local query rows} to compute only
-    those rows (others stay out = 0, lse = -inf).
+    those rows (others stay out = 0, lse = -inf). ``sinks``: optional [H]
+    sink logits (see attend_dense).
     Returns out [T, H, D] float64 and lse [H, T] float64.
     """
     T, H, D = q.shape
@@ -167,7 +179,8 @@ def varlen_attention(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_t
         k = gather_kv(key_cache, block_table[s], kv_len)
         v = gather_kv(value_cache, block_table[s], kv_len)
         local = None if rows is None else torch.as_tensor(rows[s], dtype=torch.long)
-        o, l = attend_dense(q[q0:q1], k, v, softmax_scale, causal, q_len, kv_len, rows=local)
+        o, l = attend_dense(q[q0:q1], k, v, softmax_scale, causal, q_len, kv_len, rows=local,
+                            sinks=sinks)
         idx = torch.arange(q0, q1) if local is None else q0 + local
         out[idx] = o
         lse[:, idx] = l
@@ -256,7 +269,7 @@ def dcp_decode_attention(q, key_cache, value_cache, cu_seqlens_q, shard_tables, 
 # Cascade (shared-prefix) attention ([FA-vLLM] §6.3).
 # --------------------------------------------------------------------------
 def cascade_attention(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
-                      softmax_scale, common_prefix_len, rows=None):
+                      softmax_scale, common_prefix_len, rows=None, sinks=None):
     """What cascade attention computes: flat causal attention over prefix || suffix.
 
     With every query in the private suffix (kv_len - q_len >= common_prefix_len),
@@ -264,7 +277,7 @@ def cascade_attention(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_
     so the result is ordinary causal varlen attention over the whole KV.
     """
     return varlen_attention(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
-                            softmax_scale, causal=True, rows=rows)
+                            softmax_scale, causal=True, rows=rows, sinks=sinks)
 
 
 def cascade_attention_steps(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,

@@ -735,3 +735,78 @@ def test_planted_max_instead_of_logsumexp_is_caught(monkeypatch):
     monkeypatch.setattr(P, "merge_attn_states_n", bad)
     with pytest.raises(AssertionError):
         check_merge_n_partition()
+
+
+# ----------------------------------------------------------------------------
+# Attention sinks ("FlashAttention 在 vLLM 中的实现分析" §1.2 / §1.3: the s_aux
+# learnable sink token of FA3/FA4): one extra logit per query head with no
+# value, in the softmax denominator and the LSE.
+# ----------------------------------------------------------------------------
+def check_sinks_merge_identity():
+    """Attention with sinks = the two-state merge (pinned) of attention
+    without them and the state (out 0, lse = sink)."""
+    wl = W.random_case(41, num_seqs=4, num_heads=8, num_kv_heads=2, head_size=16,
+                       block_size=16, max_q=9, max_kv=40, empty_ok=True)
+    kc, vc = wl.pool(0), wl.pool(1)
+    oracle.reshape_and_cache(wl.k_new, wl.v_new, wl.slot_mapping, kc, vc)
+    sinks = torch.linspace(-2.0, 3.0, 8, dtype=F64)
+    args = (wl.q, kc, vc, wl.cu_seqlens_q, wl.seqused_k, wl.block_table, wl.softmax_scale, True)
+    o_s, l_s = oracle.varlen_attention(*args, sinks=sinks)
+    o, l = oracle.varlen_attention(*args)
+    T = wl.q.shape[0]
+    mo, ml = oracle.merge_attn_states(o, l, torch.zeros_like(o), sinks[:, None].expand(8, T))
+    assert torch.allclose(o_s, mo, atol=1e-12, rtol=0)
+    assert torch.allclose(l_s, ml, atol=1e-12, rtol=0)
+
+
+def test_sinks_merge_identity():
+    check_sinks_merge_identity()
+
+
+def test_sinks_minus_inf_is_no_sink():
+    wl = W.random_case(42, num_seqs=3, num_heads=4, num_kv_heads=4, head_size=16, block_size=16)
+    kc, vc = wl.pool(0), wl.pool(1)
+    args = (wl.q, kc, vc, wl.cu_seqlens_q, wl.seqused_k, wl.block_table, wl.softmax_scale, True)
+    o, l = oracle.varlen_attention(*args)
+    o2, l2 = oracle.varlen_attention(*args, sinks=torch.full((4,), float("-inf"), dtype=F64))
+    assert torch.equal(o, o2) and torch.equal(l, l2)
+
+
+def test_sinks_as_an_extra_key():
+    """A sink of logit s behaves as one more key k* with scale * q.k* = s and
+    value 0 (one query row, no GQA, so k* can be built per head)."""
+    g = torch.Generator().manual_seed(43)
+    H, D, n = 3, 8, 7
+    q = torch.randn(1, H, D, generator=g, dtype=F64)
+    k = torch.randn(n, H, D, generator=g, dtype=F64)
+    v = torch.randn(n, H, D, generator=g, dtype=F64)
+    scale = 0.4
+    sinks = torch.tensor([0.5, -1.0, 2.5], dtype=F64)
+    kx = torch.stack([q[0, h] * (sinks[h] / (scale * q[0, h].dot(q[0, h]))) for h in range(H)])
+    k2 = torch.cat([k, kx[None]], dim=0)
+    v2 = torch.cat([v, torch.zeros(1, H, D, dtype=F64)], dim=0)
+    o_ref, l_ref = oracle.attend_dense(q, k2, v2, scale, False, 1, n + 1)
+    o, l = oracle.attend_dense(q, k, v, scale, False, 1, n, sinks=sinks)
+    assert torch.allclose(o, o_ref, atol=1e-12, rtol=0)
+    assert torch.allclose(l, l_ref, atol=1e-12, rtol=0)
+
+
+def test_sinks_keyless_rows():
+    q = torch.randn(2, 2, 8, dtype=F64)
+    k = torch.zeros(0, 2, 8, dtype=F64)
+    o, l = oracle.attend_dense(q, k, k, 0.5, True, 2, 0, sinks=torch.tensor([1.5, -0.5]))
+    assert torch.equal(o, torch.zeros_like(o))
+    assert l[0].tolist() == [1.5, 1.5] and l[1].tolist() == [-0.5, -0.5]
+
+
+def test_planted_sink_in_lse_only_is_caught(monkeypatch):
+    orig = P.attend_dense
+
+    def bad(q, k, v, scale, causal, q_len, kv_len, rows=None, row_chunk=512, sinks=None):
+        o, _ = orig(q, k, v, scale, causal, q_len, kv_len, rows=rows, row_chunk=row_chunk)
+        _, l = orig(q, k, v, scale, causal, q_len, kv_len, rows=rows, row_chunk=row_chunk,
+                    sinks=sinks)
+        return o, l                       # the sink missing from the denominator of out
+    monkeypatch.setattr(P, "attend_dense", bad)
+    with pytest.raises(AssertionError):
+        check_sinks_merge_identity()
