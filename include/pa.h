@@ -408,6 +408,50 @@ pa_status pa_cascade_fwd_fp8kv(const pa_kv_update* update, const void* q,
                                float* lse, void* workspace, size_t workspace_bytes, int dtype,
                                int32_t* dev_status, void* stream);
 
+/*
+ * Options of the pa_*_fwd_ex entry points (NULL, or a NULL field, means the
+ * default).
+ *   sinks : attention sinks ([FA-vLLM] §1.2 and §1.3: the s_aux learnable sink
+ *           token of FA3/FA4) -- device float32 [num_heads], one logit per
+ *           query head in the units of softmax_scale * q.k, 4-byte aligned.
+ *           Each acts as one more key of that logit and value zero: with
+ *           s_j = softmax_scale * q.k_j over the visible keys,
+ *           out = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink)) and
+ *           lse = ln(sum_j e^(s_j) + e^(sink)); a row with no visible key gets
+ *           out = 0 and lse = sink.
+ *   fp8   : NULL for bf16 pools, else the pools hold e4m3 bytes with these
+ *           scales (as in pa_varlen_fwd_fp8kv; workspace then per
+ *           pa_*_fwd_fp8kv_workspace_size).
+ */
+typedef struct pa_attn_opts {
+  const float* sinks;
+  const pa_kv_fp8* fp8;
+} pa_attn_opts;
+
+/*
+ * pa_varlen_fwd_ex / pa_cascade_fwd_ex -- pa_varlen_fwd_with_update /
+ * pa_cascade_fwd_with_update with options (opts may be NULL: then they are
+ * those entry points exactly).
+ */
+pa_status pa_varlen_fwd_ex(const pa_kv_update* update, const void* q, int64_t q_token_stride,
+                           void* key_cache, void* value_cache, int64_t cache_block_stride,
+                           const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                           const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
+                           int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                           int head_size, int block_size, int num_blocks, float softmax_scale,
+                           int causal, const pa_attn_opts* opts, void* out, float* lse,
+                           void* workspace, size_t workspace_bytes, int dtype,
+                           int32_t* dev_status, void* stream);
+pa_status pa_cascade_fwd_ex(const pa_kv_update* update, const void* q, int64_t q_token_stride,
+                            void* key_cache, void* value_cache, int64_t cache_block_stride,
+                            const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                            const int32_t* block_table, int bt_stride, int num_seqs,
+                            int total_q, int max_seqlen_q, int max_seqlen_k, int num_heads,
+                            int num_kv_heads, int head_size, int block_size, int num_blocks,
+                            float softmax_scale, int common_prefix_len, const pa_attn_opts* opts,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            int dtype, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

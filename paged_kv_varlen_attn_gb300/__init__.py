@@ -50,6 +50,8 @@ EXPORTS = (
     "pa_varlen_fwd_fp8kv",
     "pa_cascade_fwd_fp8kv",
     "pa_merge_attn_states_n",
+    "pa_varlen_fwd_ex",
+    "pa_cascade_fwd_ex",
 )
 
 _lib = None
@@ -67,6 +69,11 @@ class KvUpdate(ctypes.Structure):
 class KvFp8(ctypes.Structure):
     """struct pa_kv_fp8 of include/pa.h (device float32 [num_kv_heads] scales)."""
     _fields_ = [("k_scale", _vp), ("v_scale", _vp)]
+
+
+class AttnOpts(ctypes.Structure):
+    """struct pa_attn_opts of include/pa.h."""
+    _fields_ = [("sinks", _vp), ("fp8", ctypes.POINTER(KvFp8))]
 
 
 _ATTN_ARGS = [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
@@ -97,6 +104,10 @@ _SIGS = {
     "pa_varlen_fwd_fp8kv_workspace_size": ([_i32] * 9, _sz),
     "pa_merge_attn_states_n": ([_vp, _vp, _vp, _i64, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp],
                                _i32),
+    "pa_varlen_fwd_ex": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS[:20] +
+                         [ctypes.POINTER(AttnOpts)] + _ATTN_ARGS[20:], _i32),
+    "pa_cascade_fwd_ex": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS[:20] +
+                          [ctypes.POINTER(AttnOpts)] + _ATTN_ARGS[20:], _i32),
     "pa_cascade_fwd_fp8kv_workspace_size": ([_i32] * 9, _sz),
     "pa_varlen_fwd_fp8kv": ([ctypes.POINTER(KvUpdate)] + _ATTN_ARGS[:20] +
                             [ctypes.POINTER(KvFp8)] + _ATTN_ARGS[20:], _i32),
@@ -234,7 +245,7 @@ def _kv_update(key, value, slot_mapping):
 
 def _attend(entry, update, q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
             max_seqlen_q, max_seqlen_k, softmax_scale, mode_arg, out, lse, return_lse,
-            workspace, dev_status, size_fn, fp8=None):
+            workspace, dev_status, size_fn, fp8=None, sinks=None):
     lib = load_library()
     _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table)
     T, H, D = q.shape
@@ -253,8 +264,20 @@ def _attend(entry, update, q, key_cache, value_cache, cu_seqlens_q, seqused_k, b
             int(mode_arg)) + ((ctypes.byref(fp8),) if fp8 is not None else ()) + (
             _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
             _ptr(dev_status), _stream(q.device))
-    fn = getattr(lib, entry)
     upd = ctypes.byref(update) if update is not None else None
+    if sinks is not None:
+        # Options (attention sinks) go through the _ex entry points.
+        _need_cuda(sinks)
+        if sinks.dtype != torch.float32 or sinks.shape != (H,) or not sinks.is_contiguous():
+            raise ValueError("sinks must be a contiguous float32 tensor of num_heads values")
+        opts = AttnOpts(sinks.data_ptr(), ctypes.pointer(fp8) if fp8 is not None else None)
+        entry = "pa_varlen_fwd_ex" if entry.startswith("pa_varlen") else "pa_cascade_fwd_ex"
+        if fp8 is not None:
+            args = args[:20] + args[21:]          # the descriptor travels in opts
+        code = getattr(lib, entry)(upd, *args[:20], ctypes.byref(opts), *args[20:])
+        _check(code, entry)
+        return out, lse
+    fn = getattr(lib, entry)
     code = fn(upd, *args) if entry.endswith(("_with_update", "_fp8kv")) else fn(*args)
     _check(code, entry)
     return out, lse
@@ -262,24 +285,24 @@ def _attend(entry, update, q, key_cache, value_cache, cu_seqlens_q, seqused_k, b
 
 def varlen_fwd(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
                max_seqlen_k, softmax_scale, causal, out=None, lse=None, return_lse=True,
-               workspace=None, dev_status=None):
+               workspace=None, dev_status=None, sinks=None):
     """Varlen attention over a paged KV cache. Returns (out, lse or None)."""
     return _attend("pa_varlen_fwd", None, q, key_cache, value_cache, cu_seqlens_q, seqused_k,
                    block_table, max_seqlen_q, max_seqlen_k, softmax_scale, bool(causal), out,
-                   lse, return_lse, workspace, dev_status, varlen_fwd_workspace_size)
+                   lse, return_lse, workspace, dev_status, varlen_fwd_workspace_size, sinks=sinks)
 
 
 def varlen_fwd_with_update(key, value, slot_mapping, q, key_cache, value_cache, cu_seqlens_q,
                            seqused_k, block_table, max_seqlen_q, max_seqlen_k, softmax_scale,
                            causal, out=None, lse=None, return_lse=True, workspace=None,
-                           dev_status=None):
+                           dev_status=None, sinks=None):
     """One step: scatter the new tokens' K/V (key, value by slot_mapping) into
     the caches, then varlen attention; the planner overlaps the scatter.
     Returns (out, lse or None)."""
     return _attend("pa_varlen_fwd_with_update", _kv_update(key, value, slot_mapping), q,
                    key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
                    max_seqlen_k, softmax_scale, bool(causal), out, lse, return_lse, workspace,
-                   dev_status, varlen_fwd_workspace_size)
+                   dev_status, varlen_fwd_workspace_size, sinks=sinks)
 
 
 def varlen_fwd_noalloc(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
@@ -350,23 +373,23 @@ def merge_attn_states_n(parts_out, parts_lse, out=None, out_lse=None, return_lse
 
 def cascade_fwd(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
                 max_seqlen_k, softmax_scale, common_prefix_len, out=None, lse=None,
-                return_lse=True, workspace=None, dev_status=None):
+                return_lse=True, workspace=None, dev_status=None, sinks=None):
     """Shared-prefix (cascade) attention. Returns (out, lse or None)."""
     return _attend("pa_cascade_fwd", None, q, key_cache, value_cache, cu_seqlens_q, seqused_k,
                    block_table, max_seqlen_q, max_seqlen_k, softmax_scale, common_prefix_len,
-                   out, lse, return_lse, workspace, dev_status, cascade_fwd_workspace_size)
+                   out, lse, return_lse, workspace, dev_status, cascade_fwd_workspace_size, sinks=sinks)
 
 
 def cascade_fwd_with_update(key, value, slot_mapping, q, key_cache, value_cache, cu_seqlens_q,
                             seqused_k, block_table, max_seqlen_q, max_seqlen_k, softmax_scale,
                             common_prefix_len, out=None, lse=None, return_lse=True,
-                            workspace=None, dev_status=None):
+                            workspace=None, dev_status=None, sinks=None):
     """One step: scatter the new tokens' K/V into the caches, then cascade
     attention. Returns (out, lse or None)."""
     return _attend("pa_cascade_fwd_with_update", _kv_update(key, value, slot_mapping), q,
                    key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
                    max_seqlen_k, softmax_scale, common_prefix_len, out, lse, return_lse,
-                   workspace, dev_status, cascade_fwd_workspace_size)
+                   workspace, dev_status, cascade_fwd_workspace_size, sinks=sinks)
 
 
 # ---------------------------------------------------------------------------
@@ -432,7 +455,7 @@ def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_sc
 def varlen_fwd_fp8kv(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
                      max_seqlen_q, max_seqlen_k, softmax_scale, causal, k_scale, v_scale,
                      key=None, value=None, slot_mapping=None, out=None, lse=None,
-                     return_lse=True, workspace=None, dev_status=None):
+                     return_lse=True, workspace=None, dev_status=None, sinks=None):
     """Varlen attention over FP8 pools, optionally first quantizing and
     scattering the new tokens' K/V (key, value, slot_mapping). Returns
     (out, lse or None)."""
@@ -441,7 +464,7 @@ def varlen_fwd_fp8kv(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_t
     res = _attend("pa_varlen_fwd_fp8kv", _kv_update(key, value, slot_mapping), q, key_cache,
                   value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q, max_seqlen_k,
                   softmax_scale, bool(causal), out, lse, return_lse, workspace, dev_status,
-                  varlen_fwd_fp8kv_workspace_size, fp8=desc)
+                  varlen_fwd_fp8kv_workspace_size, fp8=desc, sinks=sinks)
     del keep
     return res
 
@@ -449,7 +472,7 @@ def varlen_fwd_fp8kv(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_t
 def cascade_fwd_fp8kv(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
                       max_seqlen_q, max_seqlen_k, softmax_scale, common_prefix_len, k_scale,
                       v_scale, key=None, value=None, slot_mapping=None, out=None, lse=None,
-                      return_lse=True, workspace=None, dev_status=None):
+                      return_lse=True, workspace=None, dev_status=None, sinks=None):
     """Cascade attention over FP8 pools (optional update as in
     varlen_fwd_fp8kv). Returns (out, lse or None)."""
     _fp8_pool(key_cache), _fp8_pool(value_cache)
@@ -457,6 +480,6 @@ def cascade_fwd_fp8kv(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_
     res = _attend("pa_cascade_fwd_fp8kv", _kv_update(key, value, slot_mapping), q, key_cache,
                   value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q, max_seqlen_k,
                   softmax_scale, common_prefix_len, out, lse, return_lse, workspace, dev_status,
-                  cascade_fwd_fp8kv_workspace_size, fp8=desc)
+                  cascade_fwd_fp8kv_workspace_size, fp8=desc, sinks=sinks)
     del keep
     return res

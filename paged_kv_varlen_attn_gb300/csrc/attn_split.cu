@@ -448,6 +448,16 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
   const int H = a.H;
   if (nsplit == 1 && !a.partials_only) {
     if (ks > 0) return;
+    if (a.sinks) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (!rvalid[r]) continue;
+        float mm = m[r], ll = l[r];
+        const float f = add_sink(mm, ll, __ldg(a.sinks + head[r]) * kLog2e);
+        inv_l[r] = ll > 0.f ? vsc * f / ll : 0.f;
+        lse_nat[r] = ll > 0.f ? (mm + fast_log2(ll)) * kLn2 : -INFINITY;
+      }
+    }
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       if (!rvalid[r]) continue;
@@ -823,6 +833,16 @@ __device__ __forceinline__ void split_consumer_fp8_dec(const AttnArgs& a, uint8_
   // 64 + 8g + mt (o[mt][2 + e]), mt = 0..7.
   if (nsplit == 1 && !a.partials_only) {
     if (warp > 0) return;
+    if (a.sinks) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if (!rvalid[e]) continue;
+        float mm = m[e], ll = l[e];
+        const float f = add_sink(mm, ll, __ldg(a.sinks + head[e]) * kLog2e);
+        inv_l[e] = ll > 0.f ? vsc * f / ll : 0.f;
+        lse_nat[e] = ll > 0.f ? (mm + fast_log2(ll)) * kLn2 : -INFINITY;
+      }
+    }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       if (!rvalid[e]) continue;

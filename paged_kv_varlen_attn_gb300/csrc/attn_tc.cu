@@ -231,12 +231,14 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
   }
-  const bool any = ok && l > 0.f;
-  const float inv_l = any ? 1.f / l : 0.f;
-  float lse_nat = any ? (m_use + fast_log2(l)) * kLn2 : -INFINITY;
+  const bool partial = nsplit > 1 || a.partials_only;
+  float mf = m_use, lf = ok ? l : 0.f, of = 1.f;
+  if (a.sinks && !partial && rvalid) of = add_sink(mf, lf, __ldg(a.sinks + head) * kLog2e);
+  const bool any = ok && lf > 0.f;
+  const float inv_l = any ? of / lf : 0.f;
+  float lse_nat = any ? (mf + fast_log2(lf)) * kLn2 : -INFINITY;
   const int slot = slot_base + rt * nsplit + j;
   const int64_t srow = slot_row(a, slot, hk, rl);
-  const bool partial = nsplit > 1 || a.partials_only;
   // The output leaves through shared memory: each warp stages 32 rows x 32
   // columns in its quarter of Q tile X (free once the last S_X product has
   // completed, which the pv_done wait above implies) and stores them so that

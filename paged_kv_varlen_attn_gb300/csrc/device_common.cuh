@@ -334,6 +334,20 @@ __device__ __forceinline__ void pdl_enter(int pdl_first) {
   pdl_trigger();
 }
 
+// Fold a sink of logit s2 (base-2 units) into a row's final state kept as
+// maximum m (base 2, -inf if no key was seen) and sum l relative to it: the
+// new maximum is max(m, s2), the old sum (and the row's output, by the
+// returned factor) are rescaled to it and 2^(s2 - max) joins the sum.
+// Returns the factor for the unnormalised output; m and l are updated.
+__device__ __forceinline__ float add_sink(float& m, float& l, float s2) {
+  const float nm = fmaxf(m, s2);
+  if (nm == -INFINITY) return 1.f;
+  const float f = m == -INFINITY ? 0.f : fast_exp2(m - nm);
+  l = l * f + fast_exp2(s2 - nm);
+  m = nm;
+  return f;
+}
+
 // A timeout anywhere in a launch sets the call's abort word; CTAs that start
 // later see it and return at once, so a failing launch ends quickly.
 __device__ __forceinline__ bool call_aborted(const AttnArgs& a) {

@@ -113,6 +113,11 @@ __device__ void combine_splits(const AttnArgs& a, int grp, int nsplit, int hk, i
       merge_states(mx, sw, acc, a.mp_part_lse[p_cls], a.mp_part_o[p_cls], first,
                    static_cast<int64_t>(a.H_kv) * srows, p_nsp, D, c4 * 4);
     }
+    if (a.sinks) {   // the sink: one more state, LSE = its logit, value 0
+      const float lsk[kBatch] = {__ldg(a.sinks + hh)};
+      const float4 vz[kBatch] = {make_float4(0.f, 0.f, 0.f, 0.f)};
+      merge_batch(mx, sw, acc, lsk, vz, 1);
+    }
     float lse_r = -INFINITY;
     if (sw > 0.f) {
       const float inv = 1.f / sw;

@@ -227,6 +227,7 @@ struct CommonAttn {
   int32_t* status;
   cudaStream_t st;
   KvFormat kv;
+  const float* sinks;   // [H] or NULL
 };
 
 PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int single, int single_kv,
@@ -286,6 +287,7 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
   a.items = reinterpret_cast<const int4*>(ws + L.items[0]);
   a.status = c.status;
   a.box_rows = gcd_int(c.bs, kKeyTile);
+  a.sinks = c.sinks;
   a.kv_fp8 = c.kv.fp8 ? 1 : 0;
   a.k_scale = c.kv.k_scale;
   a.v_scale = c.kv.v_scale;
@@ -487,7 +489,7 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
                              int head_size, int block_size, int num_blocks, float softmax_scale,
                              int causal, void* out, float* lse, void* workspace,
                              size_t workspace_bytes, int dtype, int32_t* dev_status,
-                             void* stream, const KvFormat& kv) {
+                             void* stream, const KvFormat& kv, const float* sinks = nullptr) {
   pa_status st = check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
                              num_kv_heads, head_size, block_size, dtype);
   if (st != PA_OK) return st;
@@ -495,10 +497,11 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
                        seqused_k, block_table, bt_stride, num_seqs, total_q, num_blocks, num_heads,
                        num_kv_heads, head_size, block_size, softmax_scale, causal, out, lse, kv);
   if (st != PA_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(sinks) & 3u) != 0) return PA_ERR_INVALID_ARG;
   CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
                seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
                num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
-               dev_status, static_cast<cudaStream_t>(stream), kv};
+               dev_status, static_cast<cudaStream_t>(stream), kv, sinks};
   st = check_kv_update(upd, c, key_cache, value_cache, dtype);
   if (st != PA_OK) return st;
   if (num_seqs == 0 || total_q == 0) {   // nothing to attend: the update alone
@@ -660,13 +663,16 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
                               int num_kv_heads, int head_size, int block_size, int num_blocks,
                               float softmax_scale, int common_prefix_len, void* out, float* lse,
                               void* workspace, size_t workspace_bytes, int dtype,
-                              int32_t* dev_status, void* stream, const KvFormat& kv) {
+                              int32_t* dev_status, void* stream, const KvFormat& kv,
+                              const float* sinks = nullptr) {
   pa_status st = check_shape(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads,
                              num_kv_heads, head_size, block_size, dtype);
   if (st != PA_OK) return st;
   st = check_attn_ptrs(q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
                        seqused_k, block_table, bt_stride, num_seqs, total_q, num_blocks, num_heads,
                        num_kv_heads, head_size, block_size, softmax_scale, 1, out, lse, kv);
+  if (st != PA_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(sinks) & 3u) != 0) return PA_ERR_INVALID_ARG;
   if (st != PA_OK) return st;
   if (common_prefix_len < 0 || common_prefix_len % block_size != 0) return PA_ERR_INVALID_ARG;
   if (static_cast<long long>(common_prefix_len) > static_cast<long long>(bt_stride) * block_size)
@@ -676,7 +682,7 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
                         cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
                         max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size,
                         block_size, num_blocks, softmax_scale, dev_status,
-                        static_cast<cudaStream_t>(stream), kv};
+                        static_cast<cudaStream_t>(stream), kv, sinks};
     st = check_kv_update(upd, cu, key_cache, value_cache, dtype);
     if (st != PA_OK) return st;
   }
@@ -702,7 +708,7 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
   CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
                seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
                num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
-               dev_status, static_cast<cudaStream_t>(stream), kv};
+               dev_status, static_cast<cudaStream_t>(stream), kv, sinks};
   const int box_rows = gcd_int(block_size, kKeyTile);
   CUtensorMap tmK, tmV;
   if (!encode_pool_map(&tmK, key_cache, head_size, num_kv_heads, block_size, num_blocks,
@@ -879,6 +885,42 @@ pa_status pa_cascade_fwd_fp8kv(const pa_kv_update* update, const void* q,
                       max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size, block_size,
                       num_blocks, softmax_scale, common_prefix_len, out, lse, workspace,
                       workspace_bytes, dtype, dev_status, stream, fp8_format(scales));
+}
+
+// ---------------------------------------------------------------- options
+pa_status pa_varlen_fwd_ex(const pa_kv_update* update, const void* q, int64_t q_token_stride,
+                           void* key_cache, void* value_cache, int64_t cache_block_stride,
+                           const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                           const int32_t* block_table, int bt_stride, int num_seqs, int total_q,
+                           int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                           int head_size, int block_size, int num_blocks, float softmax_scale,
+                           int causal, const pa_attn_opts* opts, void* out, float* lse,
+                           void* workspace, size_t workspace_bytes, int dtype,
+                           int32_t* dev_status, void* stream) {
+  const KvFormat kv = opts && opts->fp8 ? fp8_format(opts->fp8) : kKvBf16;
+  return varlen_impl(update, q, q_token_stride, key_cache, value_cache, cache_block_stride,
+                     cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
+                     max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size, block_size,
+                     num_blocks, softmax_scale, causal, out, lse, workspace, workspace_bytes,
+                     dtype, dev_status, stream, kv, opts ? opts->sinks : nullptr);
+}
+
+pa_status pa_cascade_fwd_ex(const pa_kv_update* update, const void* q, int64_t q_token_stride,
+                            void* key_cache, void* value_cache, int64_t cache_block_stride,
+                            const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                            const int32_t* block_table, int bt_stride, int num_seqs,
+                            int total_q, int max_seqlen_q, int max_seqlen_k, int num_heads,
+                            int num_kv_heads, int head_size, int block_size, int num_blocks,
+                            float softmax_scale, int common_prefix_len, const pa_attn_opts* opts,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            int dtype, int32_t* dev_status, void* stream) {
+  const KvFormat kv = opts && opts->fp8 ? fp8_format(opts->fp8) : kKvBf16;
+  return cascade_impl(update, q, q_token_stride, key_cache, value_cache, cache_block_stride,
+                      cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
+                      max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size, block_size,
+                      num_blocks, softmax_scale, common_prefix_len, out, lse, workspace,
+                      workspace_bytes, dtype, dev_status, stream, kv,
+                      opts ? opts->sinks : nullptr);
 }
 
 }  // extern "C"

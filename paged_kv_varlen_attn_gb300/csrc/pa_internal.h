@@ -122,6 +122,10 @@ struct AttnArgs {
   int kv_fp8;
   const float* k_scale;      // [H_kv], device
   const float* v_scale;      // [H_kv], device
+  // Attention sinks: one logit per query head (natural-log units of
+  // softmax_scale * q.k), an extra key with value zero; NULL for none. Added
+  // once per row, where the final output is written.
+  const float* sinks;
   // Launch order inside one call. The kernels after the planner are launched
   // as programmatic dependents of the kernel before them, so a grid can start
   // while its predecessor drains. pdl_first = 1 for the first kernel after the

@@ -278,3 +278,24 @@ def test_merge_n_validation(lib):
     assert call(po=FAKE + 8) == pa.PA_ERR_INVALID_ARG          # misaligned
     assert call(olse=FAKE + 4 * lsee) == pa.PA_ERR_INVALID_ARG  # out_lse inside part 1's LSE
     assert call(po=None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_ex_entry_validation(lib):
+    """The option entries: sinks must be 4-byte aligned; NULL options are the
+    plain entry; an FP8 descriptor in the options is checked like the FP8
+    entry's."""
+    a = [FAKE, 32 * 128, FAKE, FAKE, 16 * 8 * 128, FAKE, FAKE, FAKE, 4, 2, 2, 1, 64, 32, 8, 128,
+         16, 10, 0.088, 1]
+    tail = [FAKE, None, FAKE, 1 << 20, 0, None, None]
+    bad = pa.AttnOpts(FAKE + 2, None)
+    assert lib.pa_varlen_fwd_ex(None, *a, ctypes.byref(bad), *tail) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_cascade_fwd_ex(None, *a[:19], 16, ctypes.byref(bad), *tail) == \
+        pa.PA_ERR_INVALID_ARG
+    empty = list(a)
+    empty[9], empty[10] = 0, 0          # no sequences, no tokens
+    assert lib.pa_varlen_fwd_ex(None, *empty, None, *tail) == pa.PA_OK
+    fp8_d64 = list(a)
+    fp8_d64[1], fp8_d64[4], fp8_d64[15] = 32 * 64, 16 * 8 * 64, 64
+    desc = pa.KvFp8(FAKE, FAKE)
+    opts = pa.AttnOpts(None, ctypes.pointer(desc))
+    assert lib.pa_varlen_fwd_ex(None, *fp8_d64, ctypes.byref(opts), *tail) == pa.PA_ERR_UNSUPPORTED
