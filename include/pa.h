@@ -348,8 +348,11 @@ pa_status pa_varlen_fwd_noalloc(const void* q, int64_t q_token_stride, const voi
  * is IEEE float32 (correctly rounded), the result is rounded to the nearest
  * e4m3 value (ties to even) and saturates at +-448 (a NaN stays NaN).
  * Attention computes exactly the bf16 path's definition on the dequantized
- * keys and values e4m3(c) * scale[h]; q.k is formed in f16 x e4m3 products
- * with float32 accumulation, so q must lie within the f16 range (|q| < 65504).
+ * keys and values e4m3(c) * scale[h], with float32 accumulation. Items of at
+ * most 8 packed query rows (decode with GQA <= 8) take q.k on the e4m3
+ * tensor MMA, q as two e4m3 terms after a power-of-two row scale (exact for
+ * every element of at least 2^-9 of its row's largest); wider items form q.k
+ * from f16 q, so there |q| must stay below 65504.
  * Layout: the NHD pools of pa_reshape_and_cache with 1-byte elements;
  * cache_block_stride is in elements (= bytes) and a multiple of 16.
  * head_size must be 128 (PA_ERR_UNSUPPORTED otherwise). Every FP8 segment

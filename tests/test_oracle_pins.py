@@ -810,3 +810,22 @@ def test_planted_sink_in_lse_only_is_caught(monkeypatch):
     monkeypatch.setattr(P, "attend_dense", bad)
     with pytest.raises(AssertionError):
         check_sinks_merge_identity()
+
+
+def test_dcp_shard_layout():
+    """Every page of every sequence is on exactly one virtual rank, in
+    logical order, and the key counts add up (input layout only)."""
+    wl = W.random_case(51, num_seqs=6, num_heads=4, num_kv_heads=2, head_size=16,
+                       block_size=16, max_q=1, max_kv=150, decode_frac=1.0)
+    for ranks in (1, 2, 3, 5):
+        tables, lens = W.dcp_shards(wl, ranks)
+        for s in range(wl.num_seqs):
+            pages = wl.pages_of(s)
+            got = []
+            for r in range(ranks):
+                nb = (int(lens[r][s]) + wl.block_size - 1) // wl.block_size
+                row = [int(x) for x in tables[r][s, :nb]]
+                assert row == pages[r::ranks]
+                got += row
+            assert sorted(got) == sorted(pages)
+            assert sum(int(l[s]) for l in lens) == wl.kv_lens[s]
