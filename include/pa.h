@@ -25,7 +25,9 @@
  *     so they can be recorded into a CUDA graph and called from several host
  *     threads on different streams with different workspaces.
  *   - Element type: PA_BF16 (bfloat16) for Q, K, V and outputs; LSE is float32.
- *     Arithmetic accumulates in float32.
+ *     The FP8 entry points (pa_*_fp8kv, pa_reshape_and_cache_fp8, or the
+ *     fp8 option of pa_*_fwd_ex) hold K and V in the page pools as e4m3
+ *     bytes instead. Arithmetic accumulates in float32.
  *   - Strides are in ELEMENTS. Every tensor pointer must be 16-byte aligned and
  *     every stride a multiple of 8 elements (16 bytes).
  *   - Return value: PA_OK, or an error code. On any host-side error nothing is
