@@ -27,16 +27,16 @@
 //    result is deterministic.
 //  * FP8 (e4m3) pools ("FlashAttention と FlashInfer" 役割 / 境界と失敗: FP8
 //    KV cache with per-head quant scales), head size 128: a key row is one
-//    128-byte swizzled line, so a stage holds twice the keys' worth of bytes
-//    per barrier round trip. Each warp widens its own slice straight from the
-//    staged bytes into f16 MMA fragments (e4m3 -> f16 is exact), with Q in
-//    f16. For Q.K^T the head dimension is permuted -- MMA k-index
-//    16*kk + {2c, 2c+1, 2c+8, 2c+9} of lane quad c is dim 32*c + 4*kk + {0..3}
-//    in both Q and K -- so a lane's K bytes of a key are 32 contiguous bytes.
-//    For P.V the output dimension is permuted -- MMA column g of n-tile n is
-//    dim 16*g + n -- so a lane reads 16 contiguous bytes of each of its four
-//    keys and pairs them with byte permutes. k_scale folds into the softmax
-//    scale and v_scale into the final normalisation.
+//    128-byte swizzled line, so a 64-key stage is half bf16's bytes (4 stages).
+//    Decode items (<= 8 packed rows) run split_consumer_fp8_dec (Q.K^T on the
+//    e4m3 MMA). Wider items: each warp widens its slice from the staged bytes
+//    into f16 MMA fragments (exact), Q in f16. For Q.K^T the head dimension
+//    is permuted -- MMA k-index 16*kk + {2c, 2c+1, 2c+8, 2c+9} of lane quad
+//    c is dim 32*c + 4*kk + {0..3} in Q and K -- so a lane's K bytes of a
+//    key are 32 contiguous bytes. For P.V the output dimension is permuted --
+//    MMA column g of n-tile n is dim 16*g + n -- so a lane reads 16 bytes of
+//    each of its four keys and pairs them with byte permutes. k_scale folds
+//    into the softmax scale and v_scale into the final normalisation.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
