@@ -44,12 +44,27 @@ import workloads as W  # noqa: E402
 METRIC = "paged-attn decode HBM GB/s + prefill TFLOPS on 1 GB300, % of roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_SUSTAINED = 1700.0
 L2_BYTES = 129 * 1024 * 1024
 _CSRC = os.path.join(ROOT, "paged_kv_varlen_attn_gb300", "csrc")
 # Sources the split kernel's code comes from; the recorded DRAM traffic is
 # valid only while all of them are unchanged.
 SPLIT_KERNEL_SRCS = [os.path.join(_CSRC, f) for f in
                      ("attn_split.cu", "device_common.cuh", "epilogue.cuh", "pa_internal.h")]
+TC_KERNEL_SRCS = [os.path.join(_CSRC, f) for f in
+                  ("attn_tc.cu", "device_common.cuh", "epilogue.cuh", "pa_internal.h")]
+KERNEL_SRCS = {"attn_split_kernel<128>": SPLIT_KERNEL_SRCS,
+               "attn_split_kernel<128, fp8>": SPLIT_KERNEL_SRCS,
+               "attn_tc_kernel<128>": TC_KERNEL_SRCS}
+# The prefill half of the metric: tensor-core prefill sub-launches timed in
+# the default run beside the decode step (workload name -> what it is).
+PREFILL_LEGS = {
+    "long_context_70b_prefill": "long_context_70b's prefill: 4 causal seqs x 4096 queries on "
+                                "28,672 prior keys, 64/8 heads, D 128, block 128",
+    "chunked_prefill_mix_prefill": "chunked_prefill_mix's prefill chunks: 8 causal seqs x 2048 "
+                                   "queries on prior context U[0, 4096], 32/8 heads, D 128, "
+                                   "block 16",
+}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -106,11 +121,13 @@ def load_peaks():
             p = json.load(f)
         hbm = p.get("hbm_gbs") or p.get("hbm_GBs")
         bf16 = p.get("bf16_tflops")
+        sus = p.get("bf16_tflops_sustained")
         return {"hbm_gbs": float(hbm) if hbm else FALLBACK_HBM_GBS,
                 "bf16_tflops": float(bf16) if bf16 else FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": float(sus) if sus else FALLBACK_BF16_SUSTAINED,
                 "source": "measured" if hbm else "fallback"}
     return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
-            "source": "fallback"}
+            "bf16_tflops_sustained": FALLBACK_BF16_SUSTAINED, "source": "fallback"}
 
 
 def sources_sha(paths):
@@ -129,7 +146,7 @@ def load_traffic(kernel, workload):
     with open(TRAFFIC_FILE) as f:
         t = json.load(f)
     e = t.get(kernel, {}).get(workload)
-    if not e or e.get("source_sha") != sources_sha(SPLIT_KERNEL_SRCS):
+    if not e or e.get("source_sha") != sources_sha(KERNEL_SRCS[kernel]):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -317,6 +334,81 @@ def timed_flushed(fn, n, flush, stream, flush_rd):
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in evs) / n
+
+
+def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0):
+    """The prefill half of the metric on one prefill-only batch: the attention
+    call (planner + tensor-core prefill kernel) timed launch by launch with
+    CUDA events on the launching stream, SM clocks sampled over the window.
+    FLOPs are 4 * D * H per visible (query, key) pair; the fraction is taken
+    against the sustained bf16 peak (the launches run back to back for
+    longer than a second), the burst fraction is given beside it."""
+    wl = W.CONFIGS[name]()
+    T, H, D = wl.q.shape
+    counts = algorithmic_counts(wl)
+    kc, vc = wl.pool(0, device=dev), wl.pool(1, device=dev)
+    b = DeviceBatch(wl, dev)
+    pa.reshape_and_cache(b.d["k_new"], b.d["v_new"], kc, vc, b.d["slot_mapping"])
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ws = pa.alloc_workspace(pa.varlen_fwd_workspace_size(wl.num_seqs, T, wl.max_seqlen_q,
+                                                         wl.max_seqlen_k, H, wl.num_kv_heads, D,
+                                                         wl.block_size, sms), dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    # Inputs read per launch (Q, K/V pages) vs L2: flush before each launch
+    # when they would fit.
+    in_bytes = counts["kv_bytes"]["prefill"] + T * H * D * 2
+    flush = flush_rd = None
+    if in_bytes < 2 * L2_BYTES:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        flush_rd = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def attn():
+        pa.varlen_fwd(b.d["q"], kc, vc, b.d["cu_seqlens_q"], b.d["seqused_k"], b.d["block_table"],
+                      wl.max_seqlen_q, wl.max_seqlen_k, wl.softmax_scale, wl.causal, out=b.out,
+                      lse=b.lse, workspace=ws, dev_status=status)
+    for _ in range(3):
+        attn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    attn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est = e0.elapsed_time(e1)
+    n = int(min(100, max(5, min(steps, 50), min_ms / max(est, 1e-3))))
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i in range(n):
+        if flush is not None:
+            l2_flush(flush, flush_rd, i)
+        ev[i][0].record(stream)
+        attn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    assert int(status.item()) == 0, f"device status bits {int(status.item())}"
+    ms = sum(a.elapsed_time(c) for a, c in ev) / n
+    tflops = counts["flops"] / (ms * 1e-3) / 1e12
+    rec = {"workload": name, "what": PREFILL_LEGS.get(name, name),
+           "kernel": "plan + attn_tc_kernel<128>", "bound": "tensor",
+           "flops_per_launch": counts["flops"], "ms_per_launch": ms, "launches": n,
+           "tflops": tflops, "unit": "TFLOP/s",
+           "peak": peaks["bf16_tflops_sustained"], "peak_kind": "bf16 sustained",
+           "frac": tflops / peaks["bf16_tflops_sustained"],
+           "frac_burst": tflops / peaks["bf16_tflops"],
+           "traffic": load_traffic("attn_tc_kernel<128>", name),
+           "algorithmic_bytes_per_launch": counts["attn_bytes"],
+           "l2": "flushed before every launch" if flush is not None else
+                 "inputs larger than L2 (%.2f GB of Q and K/V per launch)" % (in_bytes / 1e9),
+           "timing": "CUDA events per launch on the launching stream, after 3 warm-up launches",
+           "clocks": clocks, "peak_source": peaks["source"]}
+    del kc, vc, b, ws
+    torch.cuda.empty_cache()
+    return rec
 
 
 def row_figures(pa, wl, counts, dev, stream, scatter_fn, steps):
@@ -618,10 +710,15 @@ def bench_ours(args, rank, world, local):
     # 16,384-token batch, each launch timed alone after an L2 flush.
     rows_fig = row_figures(pa, wl, counts, dev, stream, lambda: scatter(main), args.steps)
     assert int(status.item()) == 0, f"device status bits {int(status.item())}"
+    # ---- the prefill half of the metric (bf16 pools) -------------------------
+    peaks = load_peaks()
+    prefill = {}
+    if not fp8 and not args.no_prefill:
+        for name in PREFILL_LEGS:
+            prefill[name] = prefill_record(pa, name, dev, peaks, args.steps)
 
     if rank != 0:
         return
-    peaks = load_peaks()
     attn_ms_avg = attn_ms / args.steps
     config = {"workload": wl.name + ("+fp8_kv" if fp8 else ""), "num_seqs": wl.num_seqs,
               "num_heads": H,
@@ -684,7 +781,16 @@ def bench_ours(args, rank, world, local):
         for kind, r in sub.items():
             r["frac_hbm"] = r["gbs"] / peaks["hbm_gbs"]
             r["frac_bf16"] = r["tflops"] / peaks["bf16_tflops"]
+            r["frac_bf16_sustained"] = r["tflops"] / peaks["bf16_tflops_sustained"]
         line["sub_launches"] = sub
+    if prefill:
+        # The headline's second half: the long-context prefill sub-launch, with
+        # the chunked-prefill chunks beside it.
+        main_leg = prefill.pop("long_context_70b_prefill", None)
+        if main_leg is not None:
+            line["prefill"] = main_leg
+        for k, v in prefill.items():
+            line["prefill_" + k] = v
     # Our kernels per step: scatter, planner, then per attention pass the
     # split-KV kernel and/or the prefill kernel (the host launches a kernel
     # only when some segment can need it).
@@ -711,6 +817,25 @@ def bench_ours(args, rank, world, local):
     print(json.dumps(line))
 
 
+def bench_prefill_only(args, rank, world, local):
+    """Only the prefill sub-launch records (one line per leg): the command the
+    profiler captures of the prefill kernel run."""
+    import paged_kv_varlen_attn_gb300 as pa
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from paged_kv_varlen_attn_gb300 import _build
+    _build.build()
+    pa.load_library()
+    peaks = load_peaks()
+    names = [args.workload] if args.workload in PREFILL_LEGS else list(PREFILL_LEGS)
+    for name in names:
+        rec = prefill_record(pa, name, dev, peaks, args.steps, min_ms=0.0)
+        if rank == 0:
+            print(json.dumps({"prefill": rec}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -722,12 +847,18 @@ def main():
     ap.add_argument("--kv-cache", default="bf16", choices=["bf16", "fp8"],
                     help="page pool element type: bf16, or e4m3 bytes with per-KV-head scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill sub-launch records (the metric's prefill half)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prefill sub-launches (for profiler captures)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the C-ABI calls directly instead of replaying CUDA graphs")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         bench_reference(args, rank, world)
+    elif args.prefill_only:
+        bench_prefill_only(args, rank, world, local)
     else:
         bench_ours(args, rank, world, local)
     if world > 1:

@@ -54,7 +54,7 @@ typedef int pa_status;
 #define PA_OK 0
 #define PA_ERR_INVALID_ARG 1 /* null pointer, negative size, bad stride/alignment, H % H_kv != 0 */
 #define PA_ERR_BLOCK_SIZE 2  /* block_size not a positive multiple of 16, or > 1024 */
-#define PA_ERR_UNSUPPORTED 3 /* head_size not 64/128, dtype not bf16, H/H_kv not 1,2,4,8,16 */
+#define PA_ERR_UNSUPPORTED 3 /* head_size or dtype not supported (see each entry point) */
 #define PA_ERR_WORKSPACE 4   /* workspace NULL, misaligned or smaller than required */
 #define PA_ERR_CUDA 5        /* a kernel launch or a CUDA runtime query failed */
 #define PA_ERR_NOALLOC_LIMIT 6 /* problem needs more scratch than pa_varlen_fwd_noalloc's fixed buffer */
@@ -126,12 +126,15 @@ size_t pa_varlen_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
  *                  are read.
  *   max_seqlen_q, max_seqlen_k : host upper bounds of the query / key lengths
  *                  (used to size launches; no device value is read on the host).
- *   softmax_scale: multiplies q.k (commonly 1/sqrt(head_size)); must be finite
- *                  and > 0 (PA_ERR_INVALID_ARG otherwise).
+ *   softmax_scale: multiplies q.k (commonly 1/sqrt(head_size)); any finite
+ *                  value (PA_ERR_INVALID_ARG for NaN or infinity). A zero or
+ *                  negative scale runs every segment on the split-KV kernel.
  *   causal       : 0 or 1. Causal masking is bottom-right aligned: query i of a
  *                  sequence with q_len queries and kv_len keys sees keys
  *                  j <= kv_len - q_len + i (a decode query sees all keys).
- *   GQA          : query head h reads KV head h / (num_heads / num_kv_heads).
+ *   GQA          : query head h reads KV head h / (num_heads / num_kv_heads);
+ *                  any ratio (num_heads % num_kv_heads == 0). Groups of more
+ *                  than 128 heads run every segment on the split-KV kernel.
  *   out          : [total_q, num_heads, head_size] bf16, contiguous.
  *   lse          : float32 [num_heads, total_q] natural-log log-sum-exp of the
  *                  scaled logits each row saw, or NULL. A row that sees no key
@@ -319,8 +322,11 @@ pa_status pa_cascade_fwd_with_update(const pa_kv_update* update, const void* q,
  * PA_ERR_NOALLOC_LIMIT before anything is launched. The function never calls
  * cudaMalloc, cudaFree or any allocating routine.
  *  - The first call on a device looks up that buffer's device address (with
- *    the device current) and caches it; make that first call before any
- *    stream capture on the device.
+ *    the device current) and caches it with the device's current context;
+ *    make that first call before any stream capture on the device. After
+ *    cudaDeviceReset (a new context) the next call looks it up again, so
+ *    make that call before any capture too. A failed lookup returns
+ *    PA_ERR_CUDA and leaves no CUDA error pending.
  *  - Every call uses the same buffer, which keeps the previous call's
  *    contents; the kernels rewrite everything they read before reading it, so
  *    nothing needs clearing. Calls that overlap on the GPU (two streams, or

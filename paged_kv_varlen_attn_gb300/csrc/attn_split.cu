@@ -40,6 +40,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "device_common.cuh"
 #include "epilogue.cuh"
 
@@ -961,15 +963,18 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
   using C = SplitCfg<D, FP8>;
   // The shared-memory opt-in is a per-device function attribute: set it on
   // the first launch on each device (before any stream capture), not again.
-  static bool configured[kMaxDevices] = {};
+  // The flags are atomics, so first calls from several host threads are
+  // race-free (two threads may both set the attribute, which is harmless).
+  static std::atomic<bool> configured[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
+  const bool known = dev >= 0 && dev < kMaxDevices;
+  if (!known || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(attn_split_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
+    if (known) configured[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(items_bound) * static_cast<unsigned>(a.H_kv));

@@ -5,10 +5,12 @@
 // 64 packed query rows (prefill, chunked prefill with prior context, the
 // cascade prefix pass of §6.3).
 //
-// One CTA per work item: 256 packed query rows -- two 128-row Q tiles A and
-// B, each 128/G tokens x the G query heads of one KV head -- against a key
-// range, in 128-key tiles. Every K/V byte brought into shared memory serves
-// 256 rows (both Q tiles, all G heads). Three warpgroups:
+// One CTA per work item: two Q tiles A and B of packed query rows, each
+// floor(128/G) tokens x the G query heads of one KV head (128 rows when G
+// divides 128; otherwise the 128 TMEM lanes hold the whole tokens that fit
+// and the rest stay idle) -- against a key range, in 128-key tiles. Every K/V
+// byte brought into shared memory serves every row of both Q tiles (all G
+// heads). Three warpgroups:
 //   control (warps 0-3; 0 and 1 work, 2 and 3 idle), registers cut to 120;
 //   softmax A (warps 4-7) and softmax B (warps 8-11), registers raised to 192.
 // Warp roles:
@@ -48,6 +50,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "device_common.cuh"
 #include "epilogue.cuh"
 
@@ -76,7 +80,7 @@ struct TcCfg {
   static constexpr int O_COL = 256;
   static constexpr float RESCALE_LOG2 = 8.0f;
 };
-static_assert(kRowsTc == 256, "a prefill work item is two 128-row Q tiles");
+static_assert(kTcTileRows == TcCfg<128>::BM, "a Q tile spans the 128 TMEM lanes");
 
 struct TcBars {
   uint64_t q_full;
@@ -102,12 +106,13 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   using C = TcCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  const int r = quarter * 32 + lane;              // row within tile X (TMEM lane)
-  const int rl = X * C::BM + r;                   // row within the work item
+  const int r = quarter * 32 + lane;              // TMEM lane
+  const int TR = tc_tile_rows(a.G);               // rows of a Q tile (whole tokens)
+  const int rl = X * TR + r;                      // row within the work item
   const uint32_t tm_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const uint32_t s_col = X * 128, o_col = C::O_COL + X * D;   // S / P and O columns
   const int G = a.G;
-  const bool rvalid = rl < R;
+  const bool rvalid = r < TR && rl < R;
   const int pr = row0 + (rvalid ? rl : 0);
   const int ti = pr / G;
   const int tok = q_start + ti;
@@ -247,8 +252,10 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   // 16-byte granules are XOR-swizzled by row to keep the shared-memory
   // accesses free of bank conflicts.
   uint8_t* stage = smem + C::OFF_Q + X * C::Q_TILE + quarter * (C::Q_TILE / 4);
-  const int rl0 = X * C::BM + quarter * 32;          // first row of this warp in the item
+  const int rl0 = X * TR + quarter * 32;             // first row of this warp in the item
   const int64_t srow0 = slot_row(a, slot, hk, rl0);  // rows of a slot are consecutive
+  // Rows of this warp that exist: inside the tile and inside the item.
+  const int wrows = max(0, min(TR - quarter * 32, R - rl0));
 #pragma unroll 1
   for (int c = 0; c < D / 32; ++c) {
     uint32_t v[32];
@@ -269,7 +276,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = i * 4 + (lane >> 3), g = lane & 7;
-        if (rl0 + r < R)
+        if (r < wrows)
           __stcg(reinterpret_cast<float4*>(a.part_o + (srow0 + r) * D + c * 32 + g * 4),
                  *reinterpret_cast<const float4*>(stage + r * 128 + ((g ^ (r & 7)) << 4)));
       }
@@ -287,7 +294,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = i * 8 + (lane >> 2), g = lane & 3;
-        if (rl0 + r < R) {
+        if (r < wrows) {
           const int prr = row0 + rl0 + r;
           const int tr = prr / G;
           const int64_t ob = (static_cast<int64_t>(q_start + tr) * a.H + hk * G + (prr - tr * G)) * D;
@@ -327,9 +334,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const int q_start = sg.x, q_len = sg.y, kv_len = sg.z;
   const int nsplit = sp.x, slot_base = sp.y, chunk = sp.z;
   const int G = a.G;
-  const int row0 = rt * kRowsTc;
-  const int R = min(kRowsTc, q_len * G - row0);
-  const bool two = R > C::BM;   // tile B has rows
+  const int TR = tc_tile_rows(G);   // rows of a Q tile: TR / G whole tokens
+  const int row0 = rt * 2 * TR;
+  const int R = min(2 * TR, q_len * G - row0);
+  const bool two = R > TR;   // tile B has rows
   const int kb = j * chunk;
   int ke = min(kv_len, kb + chunk);
   if (a.causal) ke = min(ke, kv_len - q_len + (row0 + R - 1) / G + 1);
@@ -378,12 +386,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        // A Q box is TR / G tokens x G heads x 64 dims: TR rows of 128 B in
+        // packed-row order. Lanes TR..127 of a tile keep stale rows, which
+        // only feed their own (never written) S and O rows.
         const int token0 = q_start + row0 / G;
-        mbar_arrive_expect_tx(&bars->q_full, (two ? 2 : 1) * C::Q_TILE);
+        mbar_arrive_expect_tx(&bars->q_full, (two ? 2 : 1) * C::HALVES * TR * 128);
         for (int x = 0; x < (two ? 2 : 1); ++x)
           for (int h = 0; h < C::HALVES; ++h)
             tma_load_3d(smem + C::OFF_Q + x * C::Q_TILE + h * C::Q_HALF, &tmQ, &bars->q_full,
-                        h * 64, hk * G, token0 + x * (C::BM / G));
+                        h * 64, hk * G, token0 + x * (TR / G));
       }
       const int32_t* bt_row =
           a.bt + static_cast<int64_t>(seg) * a.bt_row_stride + a.bt_col_offset;
@@ -520,15 +531,18 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
   using C = TcCfg<D>;
   // The shared-memory opt-in is a per-device function attribute: set it on
   // the first launch on each device (before any stream capture), not again.
-  static bool configured[kMaxDevices] = {};
+  // The flags are atomics, so first calls from several host threads are
+  // race-free (two threads may both set the attribute, which is harmless).
+  static std::atomic<bool> configured[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
+  const bool known = dev >= 0 && dev < kMaxDevices;
+  if (!known || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
+    if (known) configured[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(items_bound, a.H_kv);

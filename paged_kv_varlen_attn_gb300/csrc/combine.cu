@@ -42,7 +42,7 @@ cascade_combine_kernel(const __grid_constant__ AttnArgs a0, const __grid_constan
   pdl_trigger();
   if (!live || call_aborted(a)) return;
   const int rt = gr.y;
-  const int rows_per_item = cls ? kRowsTc : kRowsSplit;
+  const int rows_per_item = cls ? tc_item_rows(a.G) : kRowsSplit;
   const int row0 = rt * rows_per_item;
   const int R = min(rows_per_item, sg.y * a.G - row0);
   combine_splits<D>(a, sp.y + rt * sp.x, sp.x, hk, R, row0, sg.x, threadIdx.x, kCombineThreads);

@@ -16,18 +16,55 @@ static __device__ __align__(256) unsigned char pa_noalloc_scratch[PA_NOALLOC_SCR
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// Per device: the context the address was looked up in, and the address.
+// cudaDeviceReset destroys the device's primary context and the module with
+// the buffer; the next call then runs in a new context and looks it up again.
+void* g_ctx[kMaxDevices] = {};
 void* g_ptr[kMaxDevices] = {};
 
+// cuCtxGetCurrent through the runtime's driver entry point (no link
+// dependency on libcuda). Returns nullptr if unavailable.
+using CtxGetCurrentFn = int (*)(void**);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 // Device address of the scratch on the current device, looked up once per
-// device with that device current. Returns nullptr on failure.
+// device and context with that device current. Returns nullptr on failure,
+// leaving no CUDA error pending.
 void* scratch_on_current_device() {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  // The context the call's kernels will run in (null before the runtime has
+  // made one current on this thread; the symbol lookup below does that).
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return nullptr;
+  void* ctx = nullptr;
+  if (get(&ctx) != 0) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ptr[dev]) {
+  if (!ctx || !g_ptr[dev] || g_ctx[dev] != ctx) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, pa_noalloc_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, pa_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();   // clear it, so a later launch check does not report it
+      g_ptr[dev] = nullptr;
+      return nullptr;
+    }
+    if (get(&ctx) != 0 || !ctx) return nullptr;
     g_ptr[dev] = p;
+    g_ctx[dev] = ctx;
   }
   return g_ptr[dev];
 }

@@ -41,12 +41,16 @@ struct PassDims {
   int sms;
   bool all_partial = false;   // every item keeps a partial-state slot (cascade prefix pass)
   bool kv_fp8 = false;        // FP8 pools: every segment runs on the split-KV kernel
+  // The prefill kernel takes the row maximum of the raw scores and scales it
+  // afterwards, which needs softmax_scale > 0; a zero or negative scale runs
+  // every segment on the split-KV kernel (which scales before the maximum).
+  bool tc_allowed = true;
 };
 
 // Which kernels a pass can need, from host-known bounds only.
 bool pass_has_tc(const PassDims& d) {
   const long long rows = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
-  return kTcAvailable && !d.kv_fp8 && rows > kTcMinRows;
+  return kTcAvailable && d.tc_allowed && !d.kv_fp8 && tc_tile_rows(d.G) > 0 && rows > kTcMinRows;
 }
 bool pass_has_split(const PassDims& d) { return !d.single || !pass_has_tc(d); }
 
@@ -58,7 +62,7 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
   L.target[1] = tc ? target_tc(d.sms, d.H_kv) : 0;
   const long long rows = static_cast<long long>(d.total_q) * d.G;
   L.items_bound[0] = sp ? L.target[0] + d.num_segs + cdiv(rows, kRowsSplit) + 1 : 0;
-  L.items_bound[1] = tc ? L.target[1] + d.num_segs + cdiv(rows, kRowsTc) + 1 : 0;
+  L.items_bound[1] = tc ? L.target[1] + d.num_segs + cdiv(rows, tc_item_rows(d.G)) + 1 : 0;
   L.slots_bound[0] = sp ? 2 * L.target[0] + 2 : 0;
   L.slots_bound[1] = tc ? 2 * L.target[1] + 2 : 0;
   if (d.all_partial) {
@@ -72,7 +76,7 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
                                                    : item_rows);
   };
   L.slot_rows[0] = clamp_rows(kRowsSplit);
-  L.slot_rows[1] = clamp_rows(kRowsTc);
+  L.slot_rows[1] = clamp_rows(tc ? tc_item_rows(d.G) : 1);
   size_t off = align_up(base);
   L.header = off;                 off = align_up(off + 64 * sizeof(int));
   L.seg = off;                    off = align_up(off + static_cast<size_t>(d.num_segs) * 16);
@@ -97,14 +101,31 @@ struct CascadeLayout {
 };
 
 CascadeLayout layout_cascade(int num_seqs, int total_q, int max_q, int G, int H, int H_kv, int D,
-                             int sms, bool kv_fp8) {
+                             int sms, bool kv_fp8, bool tc_allowed) {
   CascadeLayout C{};
-  PassDims pd{1, total_q, total_q, true, G, H, H_kv, D, sms, true, kv_fp8};
+  PassDims pd{1, total_q, total_q, true, G, H, H_kv, D, sms, true, kv_fp8, tc_allowed};
   C.prefix = layout_pass(pd, 0);
-  PassDims sd{num_seqs, total_q, max_q, false, G, H, H_kv, D, sms, true, kv_fp8};
+  PassDims sd{num_seqs, total_q, max_q, false, G, H, H_kv, D, sms, true, kv_fp8, tc_allowed};
   C.suffix = layout_pass(sd, C.prefix.end);
   C.end = C.suffix.end;
   return C;
+}
+
+// Workspace bytes reported by the size queries: enough for either kernel
+// choice (the choice also depends on the sign of softmax_scale, which the
+// queries do not take).
+size_t varlen_bytes(PassDims d) {
+  d.tc_allowed = true;
+  const size_t a = layout_pass(d, 0).end;
+  d.tc_allowed = false;
+  const size_t b = layout_pass(d, 0).end;
+  return a > b ? a : b;
+}
+size_t cascade_bytes(int num_seqs, int total_q, int max_q, int G, int H, int H_kv, int D, int sms,
+                     bool kv_fp8) {
+  const size_t a = layout_cascade(num_seqs, total_q, max_q, G, H, H_kv, D, sms, kv_fp8, true).end;
+  const size_t b = layout_cascade(num_seqs, total_q, max_q, G, H, H_kv, D, sms, kv_fp8, false).end;
+  return a > b ? a : b;
 }
 
 int query_sms(int sm_count) {
@@ -115,8 +136,6 @@ int query_sms(int sm_count) {
   return n;
 }
 
-bool pow2_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
-
 // Checks shared by the attention entry points that need no device pointer.
 pa_status check_shape(int num_seqs, int total_q, int max_seqlen_q, int max_seqlen_k, int H,
                       int H_kv, int D, int bs, int dtype) {
@@ -124,7 +143,6 @@ pa_status check_shape(int num_seqs, int total_q, int max_seqlen_q, int max_seqle
   if (H <= 0 || H_kv <= 0 || H % H_kv != 0) return PA_ERR_INVALID_ARG;
   if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
-  if (!pow2_group(H / H_kv)) return PA_ERR_UNSUPPORTED;
   if (bs <= 0 || bs % 16 != 0 || bs > 1024) return PA_ERR_BLOCK_SIZE;
   return PA_OK;
 }
@@ -158,7 +176,7 @@ pa_status check_attn_ptrs(const void* q, int64_t q_stride, const void* kc, const
       return PA_ERR_INVALID_ARG;
   }
   if (bt_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return PA_ERR_INVALID_ARG;
   return PA_OK;
 }
@@ -294,8 +312,9 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
   return a;
 }
 
-// Q viewed as (dim, head, token), boxes of 64 dims x G heads x 128/G tokens:
-// exactly the 128 packed rows of one prefill Q tile, 128-byte swizzled.
+// Q viewed as (dim, head, token), boxes of 64 dims x G heads x floor(128/G)
+// tokens: exactly the tc_tile_rows(G) packed rows of one prefill Q tile,
+// 128-byte swizzled.
 bool encode_q_map(CUtensorMap* map, const void* q, int D, int H, int total_q, int64_t q_stride,
                   int G) {
   auto fn = encode_fn();
@@ -303,6 +322,7 @@ bool encode_q_map(CUtensorMap* map, const void* q, int D, int H, int total_q, in
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(total_q > 0 ? total_q : 1)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(q_stride) * 2};
+  // G <= 128 here (wider groups never use the prefill kernel).
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kTcTileRows / G)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
@@ -423,7 +443,7 @@ const char* pa_status_string(pa_status s) {
     case PA_OK: return "PA_OK";
     case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: invalid argument";
     case PA_ERR_BLOCK_SIZE: return "PA_ERR_BLOCK_SIZE: block size must be a multiple of 16 (<= 1024)";
-    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: head size, dtype or GQA ratio not supported";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: head size or dtype not supported";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA launch or query failed";
     case PA_ERR_NOALLOC_LIMIT:
@@ -464,7 +484,7 @@ size_t pa_varlen_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
   if (sms <= 0) return 0;
   PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
              num_kv_heads, head_size, sms};
-  return layout_pass(d, 0).end;
+  return varlen_bytes(d);
 }
 
 size_t pa_cascade_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
@@ -475,9 +495,8 @@ size_t pa_cascade_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q
     return 0;
   const int sms = query_sms(sm_count);
   if (sms <= 0) return 0;
-  return layout_cascade(num_seqs, total_q, max_seqlen_q, num_heads / num_kv_heads, num_heads,
-                        num_kv_heads, head_size, sms, false)
-      .end;
+  return cascade_bytes(num_seqs, total_q, max_seqlen_q, num_heads / num_kv_heads, num_heads,
+                       num_kv_heads, head_size, sms, false);
 }
 
 // pa_varlen_fwd, optionally preceded by a K/V update of the same cache.
@@ -520,6 +539,7 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
   PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
              num_kv_heads, head_size, sms};
   d.kv_fp8 = kv.fp8;
+  d.tc_allowed = softmax_scale > 0.f;
   const PassLayout L = layout_pass(d, 0);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < L.end)
@@ -531,8 +551,9 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
       !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
                        cache_block_stride, box_rows, kv.fp8))
     return PA_ERR_CUDA;
-  CUtensorMap tmQ;
-  if (!encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride,
+  CUtensorMap tmQ{};
+  if (L.items_bound[1] > 0 &&
+      !encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride,
                     num_heads / num_kv_heads))
     return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -701,7 +722,8 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
   if (sms <= 0) return PA_ERR_CUDA;
   const int G = num_heads / num_kv_heads;
   const CascadeLayout CL = layout_cascade(num_seqs, total_q, max_seqlen_q, G, num_heads,
-                                          num_kv_heads, head_size, sms, kv.fp8);
+                                          num_kv_heads, head_size, sms, kv.fp8,
+                                          softmax_scale > 0.f);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < CL.end)
     return PA_ERR_WORKSPACE;
@@ -716,8 +738,9 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
       !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
                        cache_block_stride, box_rows, kv.fp8))
     return PA_ERR_CUDA;
-  CUtensorMap tmQ;
-  if (!encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride, G))
+  CUtensorMap tmQ{};
+  if ((CL.prefix.items_bound[1] > 0 || CL.suffix.items_bound[1] > 0) &&
+      !encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride, G))
     return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int P = common_prefix_len;
@@ -838,7 +861,7 @@ size_t pa_varlen_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_seq
   PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
              num_kv_heads, head_size, sms};
   d.kv_fp8 = true;
-  return layout_pass(d, 0).end;
+  return varlen_bytes(d);
 }
 
 size_t pa_cascade_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
@@ -849,9 +872,8 @@ size_t pa_cascade_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_se
     return 0;
   const int sms = query_sms(sm_count);
   if (sms <= 0) return 0;
-  return layout_cascade(num_seqs, total_q, max_seqlen_q, num_heads / num_kv_heads, num_heads,
-                        num_kv_heads, head_size, sms, true)
-      .end;
+  return cascade_bytes(num_seqs, total_q, max_seqlen_q, num_heads / num_kv_heads, num_heads,
+                       num_kv_heads, head_size, sms, true);
 }
 
 pa_status pa_varlen_fwd_fp8kv(const pa_kv_update* update, const void* q, int64_t q_token_stride,

@@ -20,8 +20,15 @@ constexpr int kRowsSplit = 64;     // split-KV kernel (decode and short queries)
 // split kernel's four 16-row groups; 32-row segments stay on the split kernel
 // at 5.2 TB/s).
 constexpr int kTcMinRows = 32;
-constexpr int kRowsTc = 256;       // tcgen05 prefill kernel: two 128-row Q tiles
-constexpr int kTcTileRows = 128;   // rows of one Q tile (the MMA M dimension)
+constexpr int kTcTileRows = 128;   // TMEM lanes of one prefill Q tile (the MMA M dimension)
+// A prefill Q tile holds whole tokens: the largest multiple of G packed rows
+// that fits the 128 TMEM lanes (128 rows when G divides 128; 126 for G = 3,
+// 7 or 42). A work item is two such tiles. Segments of groups wider than 128
+// heads run on the split-KV kernel (tc_tile_rows = 0).
+__host__ __device__ constexpr int tc_tile_rows(int G) {
+  return G >= 1 && G <= kTcTileRows ? (kTcTileRows / G) * G : 0;
+}
+__host__ __device__ constexpr int tc_item_rows(int G) { return 2 * tc_tile_rows(G); }
 constexpr int kKeyTile = 64;       // keys per pipeline stage / split granularity
 // Smallest KV split (keys) per class. A split-KV block spends a few
 // microseconds before its first tile arrives, about the time it takes to

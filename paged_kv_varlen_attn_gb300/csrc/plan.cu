@@ -70,7 +70,7 @@ constexpr int kPlanSmemSegs = 1024;   // segment tables kept in shared memory up
 __device__ __forceinline__ int item_bucket(int s, int rt, int j, int4 g, int chunk, int G,
                                            int causal) {
   const int cls = g.w, q_len = g.y, kv = g.z;
-  const int R = cls ? kRowsTc : kRowsSplit;
+  const int R = cls ? tc_item_rows(G) : kRowsSplit;
   const int rows = q_len * G;
   const int last_row = min(rows, (rt + 1) * R) - 1;
   const int kb = j * chunk;
@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (bad) flag_status(P.status, bad);
     const int rows = q_len * G;
     const int cls = (P.tc_enabled && rows > kTcMinRows) ? 1 : 0;
-    const int nrt = (rows + (cls ? kRowsTc : kRowsSplit) - 1) / (cls ? kRowsTc : kRowsSplit);
+    const int rpi = cls ? tc_item_rows(G) : kRowsSplit;
+    const int nrt = (rows + rpi - 1) / rpi;
     const unsigned long long w = static_cast<unsigned long long>(nrt) * static_cast<unsigned>(kv);
     if (cls) w1 += w; else w0 += w;
     const int4 g = make_int4(q_start, q_len, kv, cls);
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (s < nseg) {
       const int4 g = geo_tab[s];
       cls = g.w;
-      const int R = cls ? kRowsTc : kRowsSplit;
+      const int R = cls ? tc_item_rows(G) : kRowsSplit;
       const int nrt = (g.y * G + R - 1) / R;
       const int kv = g.z;
       const int L = cls ? chunk_max[1] : chunk_max[0];

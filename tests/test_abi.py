@@ -83,7 +83,6 @@ def _varlen(lib, **kw):
     (dict(D=96), pa.PA_ERR_UNSUPPORTED),
     (dict(D=256), pa.PA_ERR_UNSUPPORTED),
     (dict(dtype=1), pa.PA_ERR_UNSUPPORTED),
-    (dict(H=24, Hk=8), pa.PA_ERR_UNSUPPORTED),          # GQA ratio 3
     (dict(H=32, Hk=6), pa.PA_ERR_INVALID_ARG),          # H % H_kv != 0
     (dict(q=None), pa.PA_ERR_INVALID_ARG),
     (dict(out=None), pa.PA_ERR_INVALID_ARG),
@@ -93,13 +92,32 @@ def _varlen(lib, **kw):
     (dict(cbs=100), pa.PA_ERR_INVALID_ARG),
     (dict(causal=2), pa.PA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), pa.PA_ERR_INVALID_ARG),
-    (dict(scale=0.0), pa.PA_ERR_INVALID_ARG),
-    (dict(scale=-0.1), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=float("-inf")), pa.PA_ERR_INVALID_ARG),
     (dict(S=-1), pa.PA_ERR_INVALID_ARG),
     (dict(S=0, T=0), pa.PA_OK),                         # empty batch: nothing to do
 ])
 def test_varlen_host_validation(lib, kw, code):
     assert _varlen(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=24, Hk=8),       # GQA ratio 3: any H % H_kv == 0 is accepted
+    dict(H=40, Hk=8),       # ratio 5
+    dict(H=28, Hk=4),       # ratio 7
+    dict(H=200, Hk=1),      # a group wider than a 128-lane prefill tile
+    dict(scale=0.0),        # any finite softmax scale
+    dict(scale=-0.1),
+])
+def test_varlen_accepts_every_ratio_and_finite_scale(lib, kw):
+    """These pass every argument check; with no workspace the call then stops
+    at PA_ERR_WORKSPACE (or PA_ERR_CUDA on a machine without a GPU, where the
+    SM count cannot be queried) -- either way before anything is launched."""
+    qs = kw.get("H", 32) * 128   # the query row is H x D elements
+    assert _varlen(lib, ws=None, wsb=0, qs=qs, **kw) in (pa.PA_ERR_WORKSPACE, pa.PA_ERR_CUDA)
+    n = lib.pa_varlen_fwd_workspace_size(2, 2, 1, 64, kw.get("H", 32), kw.get("Hk", 8), 128, 16,
+                                         152)
+    assert n > 0 and n % 256 == 0
 
 
 def test_cascade_prefix_must_be_page_multiple(lib):
@@ -178,7 +196,7 @@ def test_update_entry_validation(lib):
     assert _varlen_upd(lib, _upd(ks=512)) == pa.PA_ERR_INVALID_ARG        # shorter than a row
     assert _varlen_upd(lib, _upd(), bs=24) == pa.PA_ERR_BLOCK_SIZE
     # attention arguments are still checked
-    assert _varlen_upd(lib, _upd(), scale=0.0) == pa.PA_ERR_INVALID_ARG
+    assert _varlen_upd(lib, _upd(), scale=float("nan")) == pa.PA_ERR_INVALID_ARG
     # nothing to do: no update and an empty batch, or an update of zero tokens
     assert _varlen_upd(lib, None, S=0, T=0) == pa.PA_OK
     assert _varlen_upd(lib, _upd(n=0), S=0, T=0) == pa.PA_OK

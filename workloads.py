@@ -330,6 +330,28 @@ def long_context_70b(seed=1005, n_decode=32, kv_len=32768, n_prefill=4, q_len=40
     return _build("long_context_70b", seed, 64, 8, 128, 128, ql, kv, g)
 
 
+def long_context_70b_prefill(seed=1015, n_prefill=4, kv_len=32768, q_len=4096):
+    """The prefill side of long_context_70b as a batch of its own: 4 causal
+    prefill seqs of 4096 queries on 28672 prior tokens, 64/8 heads, head_size
+    128, block_size 128 (the same shapes and FLOPs; its own pool of those
+    sequences' pages only, ~0.3 GB per pool)."""
+    g = torch.Generator().manual_seed(seed)
+    return _build("long_context_70b_prefill", seed, 64, 8, 128, 128, [q_len] * n_prefill,
+                  [kv_len] * n_prefill, g)
+
+
+def chunked_prefill_mix_prefill(seed=1003, n_prefill=8, chunk=2048, n_decode=56):
+    """The prefill chunks of chunked_prefill_mix as a batch of their own: the
+    same 8 chunks of 2048 causal queries with the same prior-context lengths
+    (drawn first from the same seed), 32/8 heads, head_size 128, block_size
+    16; a pool of those sequences' pages only."""
+    g = torch.Generator().manual_seed(seed)
+    ctx = _uniform_int(g, 0, 4096, n_prefill)
+    _uniform_int(g, 1024, 8192, n_decode)      # the decode lengths, drawn and dropped
+    return _build("chunked_prefill_mix_prefill", seed, 32, 8, 128, 16, [chunk] * n_prefill,
+                  [c + chunk for c in ctx], g)
+
+
 def prefill_profile(seed=1006, n_prefill=4, q_len=2048, kv_len=12288):
     """A small case of the long-context prefill shape for profiler captures:
     64/8 heads, head_size 128, block_size 128, 4 causal prefill sequences of
@@ -346,6 +368,8 @@ CONFIGS = {
     "cascade_shared_prefix": cascade_shared_prefix,
     "long_context_70b": long_context_70b,
     "prefill_profile": prefill_profile,
+    "long_context_70b_prefill": long_context_70b_prefill,
+    "chunked_prefill_mix_prefill": chunked_prefill_mix_prefill,
 }
 
 
