@@ -829,7 +829,7 @@ def bench_prefill_only(args, rank, world, local):
     _build.build()
     pa.load_library()
     peaks = load_peaks()
-    names = [args.workload] if args.workload in PREFILL_LEGS else list(PREFILL_LEGS)
+    names = list(PREFILL_LEGS) if args.workload == "decode_llama8b" else [args.workload]
     for name in names:
         rec = prefill_record(pa, name, dev, peaks, args.steps, min_ms=0.0)
         if rank == 0:

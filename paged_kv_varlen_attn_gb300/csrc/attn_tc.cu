@@ -11,8 +11,8 @@
 // and the rest stay idle) -- against a key range, in 128-key tiles. Every K/V
 // byte brought into shared memory serves every row of both Q tiles (all G
 // heads). Three warpgroups:
-//   control (warps 0-3; 0 and 1 work, 2 and 3 idle), registers cut to 120;
-//   softmax A (warps 4-7) and softmax B (warps 8-11), registers raised to 192.
+//   control (warps 0-3; 0 and 1 work, 2 and 3 idle), registers cut to 104;
+//   softmax A (warps 4-7) and softmax B (warps 8-11), registers raised to 200.
 // Warp roles:
 //   warp 0     TMA producer: both Q tiles once, then K and V page boxes
 //              (128-byte swizzle) into a ring of stages (full/empty mbarriers),
@@ -87,7 +87,7 @@ struct TcBars {
   uint64_t kv_full[8];     // [s]: K of stage s, [STAGES + s]: V of stage s
   uint64_t kv_empty[8];
   uint64_t s_full[2];      // [tile]: S = Q K^T of the current key tile is in TMEM
-  uint64_t p_full[2];      // [tile]: P of the current key tile is in TMEM
+  uint64_t p_full[2][2];   // [half][tile]: P of keys [64 half, +64) of the tile is in TMEM
   uint64_t pv_done[2];     // [tile]: O += P V of the current key tile completed
   uint64_t drain;
   uint32_t tmem_base;
@@ -96,6 +96,31 @@ struct TcBars {
   volatile int issued[2];    // K / V tiles issued by the producer
   volatile int consumed[2];  // K / V tiles whose arrival the MMA issuer observed
 };
+
+// V rows past the sequence end hold arbitrary bytes: zero them so the P V
+// product (P = 0 there) cannot pick up NaN. Tile A's warps do it for key
+// tile t before they publish the first half of its P; the MMA thread issues
+// every product on V(t) -- tile A's and tile B's -- after observing that, so
+// they all see the zeros. V(t) has its own barrier and may land after S(t):
+// wait for it first, so the copy cannot overwrite the zeros. False on
+// timeout.
+template <int D>
+__device__ __forceinline__ bool zero_v_tail(TcBars* bars, uint8_t* smem, int t, int key0,
+                                            int kv_len, int tid) {
+  using C = TcCfg<D>;
+  if (!mbar_wait(&bars->kv_full[C::STAGES + t % C::STAGES], (t / C::STAGES) & 1)) return false;
+  const int first = max(0, kv_len - key0);
+  uint8_t* vt = smem + C::OFF_KV + (t % C::STAGES) * C::STAGE + C::KV_TILE;
+  const int n16 = (C::BN - first) * C::HALVES * 8;
+  for (int idx = tid; idx < n16; idx += 128) {
+    const int rr = first + idx / (C::HALVES * 8);
+    const int rem = idx % (C::HALVES * 8);
+    *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::KV_HALF + rr * 128 + (rem & 7) * 16) =
+        make_uint4(0, 0, 0, 0);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  return true;
+}
 
 template <int D>
 __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars, uint8_t* smem,
@@ -179,47 +204,41 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
     // 64 columns of this tile's S region (key k -> column k / 2). Chunk c
     // reads S columns [32c, 32c+32) and writes P columns [16c, 16c+16), which
     // only the already-read chunks occupy.
+    // P is published in two halves (keys 0-63, then 64-127), so the tensor
+    // core multiplies the first half by V while the second is computed.
     float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < C::BN / 32; ++c) {
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
-        const float x0 = xs[c * 32 + e], x1 = xs[c * 32 + e + 1];
-        const float p0 = fast_exp2(fmaf(x0, sl2, -mu));
-        const float p1 = fast_exp2(fmaf(x1, sl2, -mu));
-        ls[e & 7] += p0;
-        ls[(e + 1) & 7] += p1;
+        // Pairs in the two-lane FMA / add: half the arithmetic instructions,
+        // the same roundings and summation order as the scalar forms. The
+        // MMA-issuing thread shares issue slots with these warps, and dense
+        // FMA streams beside it starve it (measured: a single issuing thread
+        // next to eight warps of FMA/max arithmetic issued one 128x128x16 MMA
+        // per ~220 clocks instead of 64; next to exp2-only warps, 64).
+        float y0, y1;
+        ffma2(y0, y1, xs[c * 32 + e], xs[c * 32 + e + 1], sl2, sl2, -mu, -mu);
+        const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+        fadd2(ls[e & 7], ls[(e + 1) & 7], ls[e & 7], ls[(e + 1) & 7], p0, p1);
         pk[e >> 1] = pack_bf16(p0, p1);
       }
       tmem_st16(tm_row + s_col + c * 16, pk);
+      if (c == 1) {
+        tmem_wait_st();
+        if (X == 0 && key0 + C::BN > kv_len)   // warp-uniform condition and result
+          ok = __all_sync(0xffffffffu, zero_v_tail<D>(bars, smem, t, key0, kv_len, tid));
+        if (!ok) break;
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[0][X]);
+      }
     }
+    if (!ok) break;
     l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
     tmem_wait_st();
-    // V rows past the sequence end hold arbitrary bytes: zero them so the
-    // P V product (P = 0 there) cannot pick up NaN. Tile A's warps do it
-    // before tile A's P is published; the MMA thread issues tile B's product
-    // after observing that, so it sees the zeros too.
-    if (X == 0 && key0 + C::BN > kv_len) {
-      // V(t) has its own barrier and may land after S(t): wait for it first
-      // so the copy cannot overwrite the zeros.
-      if (!mbar_wait(&bars->kv_full[C::STAGES + t % C::STAGES], (t / C::STAGES) & 1)) {
-        ok = false;
-        break;
-      }
-      const int first = max(0, kv_len - key0);
-      uint8_t* vt = smem + C::OFF_KV + (t % C::STAGES) * C::STAGE + C::KV_TILE;
-      const int n16 = (C::BN - first) * C::HALVES * 8;
-      for (int idx = tid; idx < n16; idx += 128) {
-        const int rr = first + idx / (C::HALVES * 8);
-        const int rem = idx % (C::HALVES * 8);
-        *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::KV_HALF + rr * 128 + (rem & 7) * 16) =
-            make_uint4(0, 0, 0, 0);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
     tc_fence_before();
-    mbar_arrive(&bars->p_full[X]);
+    mbar_arrive(&bars->p_full[1][X]);
   }
   if (!ok) {
     abort_call(a);
@@ -352,7 +371,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->s_full[x], 1);
-      mbar_init(&bars->p_full[x], 128);
+      mbar_init(&bars->p_full[0][x], 128);
+      mbar_init(&bars->p_full[1][x], 128);
       mbar_init(&bars->pv_done[x], 1);
     }
     mbar_init(&bars->drain, 1);
@@ -371,14 +391,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   // Register split: the block is launched with 384 x 168 registers. The
-  // control warpgroup (producer, MMA issuer, two idle warps) drops to 120 and
-  // the two softmax warpgroups rise to 192: 128*120 + 256*192 = 384*168. The
-  // MMA issuer's loop must not spill (a spilled descriptor puts local-memory
-  // latency between consecutive MMAs); a few softmax spills cost less
-  // (measured: 56/224 ran 11% slower than 120/192, 152/176 8% slower).
+  // control warpgroup (producer, MMA issuer, two idle warps) drops to 104 and
+  // the two softmax warpgroups rise to 200: 128*104 + 256*200 = 384*168
+  // (the sum must not exceed the launch's, or setmaxnreg.inc never
+  // returns). The softmax's two-lane FMAs need aligned register pairs; with
+  // 200 registers they fit (measured on the 70B prefill: 1376 TFLOP/s at
+  // 104/200 against 1202 at 120/192 with the two-lane FMA and 1348 at
+  // 120/192 without it; 88/208 spills in the issuer, 1277).
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (ntiles > 0) {
@@ -404,39 +426,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One lane issues. The tensor core starves when this thread gets few
+    // issue slots (the softmax warps' arithmetic competes for them), so the
+    // work per MMA is kept small: descriptor bases are built once and each
+    // MMA adds a constant (the descriptor of address + c is the descriptor of
+    // address plus c / 16; shared addresses stay below 2^18, so the 14-bit
+    // field cannot carry).
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = mma_idesc_bf16(C::BM, C::BN, false);
       constexpr uint32_t idesc_o = mma_idesc_bf16(C::BM, D, true);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sKV = smem_u32(smem + C::OFF_KV);
+      const uint64_t qdesc[2] = {smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024),
+                                 smem_desc_sw128(smem_u32(smem + C::OFF_Q + C::Q_TILE), 16, 1024)};
+      const uint64_t kdesc0 = smem_desc_sw128(sKV, 16, 1024);
+      const uint64_t vdesc0 = smem_desc_sw128(sKV + C::KV_TILE, C::KV_HALF, 1024);
       // S_X(t) = Q_X K(t)^T into TMEM columns [128 X, 128 X + 128).
       auto issue_s = [&](int x, int t) {
         tc_fence_after();
-        const uint32_t kbase = sKV + (t % C::STAGES) * C::STAGE;
-        const uint32_t qbase = sQ + x * C::Q_TILE;
+        const uint64_t qd = qdesc[x];
+        const uint64_t kd = kdesc0 + static_cast<uint32_t>((t % C::STAGES) * (C::STAGE >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad =
-              smem_desc_sw128(qbase + (kk >> 2) * C::Q_HALF + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd =
-              smem_desc_sw128(kbase + (kk >> 2) * C::KV_HALF + (kk & 3) * 32, 16, 1024);
-          tc_mma(tmem + x * 128, ad, bd, idesc_s, kk > 0);
+          const uint32_t off = ((kk >> 2) * C::Q_HALF + (kk & 3) * 32) >> 4;
+          const uint32_t offk = ((kk >> 2) * C::KV_HALF + (kk & 3) * 32) >> 4;
+          tc_mma(tmem + x * 128, qd + off, kd + offk, idesc_s, kk > 0);
         }
         tc_commit(&bars->s_full[x]);
       };
-      // O_X += P_X(t) V(t), P_X read from TMEM (the first 64 columns of S_X).
-      auto issue_pv = [&](int x, int t) {
+      // O_X += P_X(t) V(t) over keys [64 h, 64 h + 64), P_X read from TMEM
+      // (the first 64 columns of S_X); the second half commits pv_done.
+      auto issue_pv = [&](int x, int t, int h) {
         tc_fence_after();
-        const uint32_t vbase = sKV + (t % C::STAGES) * C::STAGE + C::KV_TILE;
+        const uint64_t vd = vdesc0 + static_cast<uint32_t>((t % C::STAGES) * (C::STAGE >> 4));
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(vbase + kk * 16 * 128, C::KV_HALF, 1024);
-          tc_mma_ts(tmem + C::O_COL + x * D, tmem + x * 128 + kk * 8, bd, idesc_o,
-                    (t > 0 || kk > 0) ? 1 : 0);
+        for (int k4 = 0; k4 < C::BN / 32; ++k4) {
+          const int kk = h * (C::BN / 32) + k4;
+          tc_mma_ts(tmem + C::O_COL + x * D, tmem + x * 128 + kk * 8, vd + ((kk * 16 * 128) >> 4),
+                    idesc_o, (t > 0 || kk > 0) ? 1 : 0);
         }
-        tc_commit(&bars->pv_done[x]);
+        if (h == 1) tc_commit(&bars->pv_done[x]);
       };
-      // Issue order per tile t: P_A V, S_A(t+1), P_B V, S_B(t+1). The
+      // Issue order per tile t: P_A V (in two halves, each as soon as the
+      // softmax publishes it), S_A(t+1), P_B V (two halves), S_B(t+1). The
       // tensor core executes one thread's MMAs in issue order, so S_X(t+1)
       // overwrites P_X(t) only after P_X(t) V has read it, and the softmax
       // of tile A moves on as soon as its own product is done instead of
@@ -455,18 +486,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       for (int t = 0; ok && t < ntiles; ++t) {
         if (bars->abort) { ok = false; break; }
         const bool more = t + 1 < ntiles;
-        if (!(ok = mbar_wait(&bars->p_full[0], t & 1))) break;
+        if (!(ok = mbar_wait(&bars->p_full[0][0], t & 1))) break;
         if (!(ok = mbar_wait(&bars->kv_full[S_ + t % S_], (t / S_) & 1))) break;
         bars->consumed[1] = t + 1;
-        issue_pv(0, t);
+        issue_pv(0, t, 0);
+        if (!(ok = mbar_wait(&bars->p_full[1][0], t & 1))) break;
+        issue_pv(0, t, 1);
         if (more) {
           if (!(ok = mbar_wait(&bars->kv_full[(t + 1) % S_], ((t + 1) / S_) & 1))) break;
           bars->consumed[0] = t + 2;
           issue_s(0, t + 1);
         }
         if (two) {
-          if (!(ok = mbar_wait(&bars->p_full[1], t & 1))) break;
-          issue_pv(1, t);
+          if (!(ok = mbar_wait(&bars->p_full[0][1], t & 1))) break;
+          issue_pv(1, t, 0);
+          if (!(ok = mbar_wait(&bars->p_full[1][1], t & 1))) break;
+          issue_pv(1, t, 1);
         }
         tc_commit(&bars->kv_empty[S_ + t % S_]);
         if (more) {
@@ -484,7 +519,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int X = (warp - 4) >> 2;   // warps 4-7: tile A, 8-11: tile B
     if (X == 0 || two)
