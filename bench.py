@@ -290,7 +290,7 @@ def run_oracle_sample(wl, max_seconds=12.0, max_seqs=None, fp8=False):
 def bench_reference(args, rank, world):
     if rank != 0:
         return
-    wl = W.CONFIGS[args.workload]()
+    wl = W.CONFIGS[args.workload](dtype=DTYPES[args.dtype])
     times = []
     total_bytes = 0
     desc = ""
@@ -336,14 +336,17 @@ def timed_flushed(fn, n, flush, stream, flush_rd):
     return sum(a.elapsed_time(b) for a, b in evs) / n
 
 
-def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0):
+DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0, dtype=torch.bfloat16):
     """The prefill half of the metric on one prefill-only batch: the attention
     call (planner + tensor-core prefill kernel) timed launch by launch with
     CUDA events on the launching stream, SM clocks sampled over the window.
     FLOPs are 4 * D * H per visible (query, key) pair; the fraction is taken
     against the sustained bf16 peak (the launches run back to back for
     longer than a second), the burst fraction is given beside it."""
-    wl = W.CONFIGS[name]()
+    wl = W.CONFIGS[name](dtype=dtype)
     T, H, D = wl.q.shape
     counts = algorithmic_counts(wl)
     kc, vc = wl.pool(0, device=dev), wl.pool(1, device=dev)
@@ -393,7 +396,7 @@ def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0):
     assert int(status.item()) == 0, f"device status bits {int(status.item())}"
     ms = sum(a.elapsed_time(c) for a, c in ev) / n
     tflops = counts["flops"] / (ms * 1e-3) / 1e12
-    rec = {"workload": name, "what": PREFILL_LEGS.get(name, name),
+    rec = {"workload": name, "what": PREFILL_LEGS.get(name, name), "dtype": str(dtype)[6:],
            "kernel": "plan + attn_tc_kernel<128>", "bound": "tensor",
            "flops_per_launch": counts["flops"], "ms_per_launch": ms, "launches": n,
            "tflops": tflops, "unit": "TFLOP/s",
@@ -471,7 +474,7 @@ class DeviceBatch:
         }
         self.d = {k: v.to(dev) for k, v in self.host.items()}
         T, H, D = wl.q.shape
-        self.out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((T, H, D), dtype=wl.q.dtype, device=dev)
         self.lse = torch.empty((H, T), dtype=torch.float32, device=dev)
         self.out_h = torch.empty_like(self.out, device="cpu").pin_memory()
         self.lse_h = torch.empty_like(self.lse, device="cpu").pin_memory()
@@ -489,7 +492,7 @@ def bench_ours(args, rank, world, local):
     barrier(world)
     pa.load_library()
 
-    wl = W.CONFIGS[args.workload]()
+    wl = W.CONFIGS[args.workload](dtype=DTYPES[args.dtype])
     cascade = wl.common_prefix_len > 0
     fp8 = args.kv_cache == "fp8"
     counts = algorithmic_counts(wl, cascade=cascade, fp8=fp8)
@@ -715,7 +718,8 @@ def bench_ours(args, rank, world, local):
     prefill = {}
     if not fp8 and not args.no_prefill:
         for name in PREFILL_LEGS:
-            prefill[name] = prefill_record(pa, name, dev, peaks, args.steps)
+            prefill[name] = prefill_record(pa, name, dev, peaks, args.steps,
+                                           dtype=DTYPES[args.dtype])
 
     if rank != 0:
         return
@@ -735,7 +739,8 @@ def bench_ours(args, rank, world, local):
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3 kv (f16 mma)" if fp8 else "bf16", "data": "synthetic",
+            "dtype": ("e4m3 kv (f16 mma), %s q/out" % args.dtype) if fp8 else args.dtype,
+            "data": "synthetic",
             "config": config}
     if fp8:
         config["kv_cache"] = ("e4m3 bytes, per-KV-head scales k %s v %s"
@@ -831,7 +836,8 @@ def bench_prefill_only(args, rank, world, local):
     peaks = load_peaks()
     names = list(PREFILL_LEGS) if args.workload == "decode_llama8b" else [args.workload]
     for name in names:
-        rec = prefill_record(pa, name, dev, peaks, args.steps, min_ms=0.0)
+        rec = prefill_record(pa, name, dev, peaks, args.steps, min_ms=0.0,
+                             dtype=DTYPES[args.dtype])
         if rank == 0:
             print(json.dumps({"prefill": rec}))
 
@@ -847,6 +853,8 @@ def main():
     ap.add_argument("--kv-cache", default="bf16", choices=["bf16", "fp8"],
                     help="page pool element type: bf16, or e4m3 bytes with per-KV-head scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", default="bf16", choices=sorted(DTYPES),
+                    help="element type of Q, the 2-byte K/V pools and the outputs")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill sub-launch records (the metric's prefill half)")
     ap.add_argument("--prefill-only", action="store_true",

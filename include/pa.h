@@ -24,10 +24,14 @@
  *     host<->device copies, never synchronize, and keep no state between calls,
  *     so they can be recorded into a CUDA graph and called from several host
  *     threads on different streams with different workspaces.
- *   - Element type: PA_BF16 (bfloat16) for Q, K, V and outputs; LSE is float32.
- *     The FP8 entry points (pa_*_fp8kv, pa_reshape_and_cache_fp8, or the
- *     fp8 option of pa_*_fwd_ex) hold K and V in the page pools as e4m3
- *     bytes instead. Arithmetic accumulates in float32.
+ *   - Element type (the dtype argument): PA_BF16 (bfloat16) or PA_F16 (IEEE
+ *     half) for Q, K, V and outputs, the same type for all of them within a
+ *     call ([FA-vLLM] §2.1 lists float16 and bfloat16 as the supported
+ *     dtypes); LSE is float32. The FP8 entry points (pa_*_fp8kv,
+ *     pa_reshape_and_cache_fp8, or the fp8 option of pa_*_fwd_ex) hold K and
+ *     V in the page pools as e4m3 bytes instead (Q, the new tokens and the
+ *     outputs keep dtype). Arithmetic accumulates in float32; P enters the
+ *     P V product in dtype (f16 over e4m3 pools).
  *   - Strides are in ELEMENTS. Every tensor pointer must be 16-byte aligned and
  *     every stride a multiple of 8 elements (16 bytes).
  *   - Return value: PA_OK, or an error code. On any host-side error nothing is
@@ -66,7 +70,8 @@ typedef int pa_status;
 #define PA_DEV_TIMEOUT 8     /* a bounded wait on a pipeline barrier gave up */
 #define PA_DEV_CASCADE 16    /* cascade precondition violated (see pa_cascade_fwd) */
 
-#define PA_BF16 0
+#define PA_BF16 0 /* bfloat16 */
+#define PA_F16 1  /* IEEE half (float16) */
 
 /* Human-readable name of a pa_status value (static string). */
 const char* pa_status_string(pa_status status);
@@ -135,7 +140,7 @@ size_t pa_varlen_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
  *   GQA          : query head h reads KV head h / (num_heads / num_kv_heads);
  *                  any ratio (num_heads % num_kv_heads == 0). Groups of more
  *                  than 128 heads run every segment on the split-KV kernel.
- *   out          : [total_q, num_heads, head_size] bf16, contiguous.
+ *   out          : [total_q, num_heads, head_size] in dtype, contiguous.
  *   lse          : float32 [num_heads, total_q] natural-log log-sum-exp of the
  *                  scaled logits each row saw, or NULL. A row that sees no key
  *                  gets out = 0 and lse = -inf.
@@ -157,7 +162,7 @@ pa_status pa_varlen_fwd(const void* q, int64_t q_token_stride, const void* key_c
  * results over disjoint key sets ([FA-vLLM] §6.3 step 3 and §8.2
  * merge_attn_states(prefix_out, suffix_out, prefix_lse, suffix_lse)).
  *
- *   prefix_out, suffix_out, out : [num_tokens, num_heads, head_size] bf16, contiguous.
+ *   prefix_out, suffix_out, out : [num_tokens, num_heads, head_size] in dtype, contiguous.
  *   prefix_lse, suffix_lse      : float32 [num_heads, num_tokens], natural log.
  *   out_lse                     : float32 [num_heads, num_tokens] or NULL.
  * With m = max(a, b), wa = e^(a-m), wb = e^(b-m):
@@ -179,17 +184,17 @@ pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out
  * on one GPU, for ranks that are virtual), and the n-part form of
  * pa_merge_attn_states.
  *
- *   parts_out : bf16; part r is [num_tokens, num_heads, head_size] contiguous
+ *   parts_out : dtype; part r is [num_tokens, num_heads, head_size] contiguous
  *               at parts_out + r * part_stride_out (elements, a multiple of 8,
  *               >= num_tokens * num_heads * head_size when num_parts > 1).
  *   parts_lse : float32; part r is [num_heads, num_tokens] at
  *               parts_lse + r * part_stride_lse (>= num_heads * num_tokens).
- *   out       : [num_tokens, num_heads, head_size] bf16; may alias a part.
+ *   out       : [num_tokens, num_heads, head_size] in dtype; may alias a part.
  *   out_lse   : float32 [num_heads, num_tokens] or NULL; must not overlap the
  *               parts' LSEs (PA_ERR_INVALID_ARG).
  * With m = max_r lse_r and w_r = e^(lse_r - m): out = sum_r w_r out_r /
  * sum_r w_r, out_lse = m + ln sum_r w_r (float32 throughout, out rounded to
- * bf16 once). A row whose LSEs are all -inf gets out = 0, out_lse = -inf.
+ * dtype once). A row whose LSEs are all -inf gets out = 0, out_lse = -inf.
  * 1 <= num_parts <= PA_MERGE_N_MAX.
  *
  * A virtual-rank decode over R ranks is R pa_varlen_fwd calls (causal = 0),
@@ -258,7 +263,7 @@ pa_status pa_use_cascade_attention(int common_prefix_len, int num_seqs, int num_
 /*
  * New tokens' K/V for the update-and-attend entry points below: the
  * arguments of pa_reshape_and_cache that are not already arguments of the
- * attention call. key / value: [num_tokens, num_kv_heads, head_size] bf16,
+ * attention call. key / value: [num_tokens, num_kv_heads, head_size] in dtype,
  * token t at key + t*key_token_stride; slot_mapping: int64 [num_tokens]
  * (slot < 0 skips the token). All device pointers, owned by the caller.
  */
@@ -352,10 +357,10 @@ pa_status pa_varlen_fwd_noalloc(const void* q, int64_t q_token_stride, const voi
  * format (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest
  * finite value 448, no infinities, S.1111.111 is NaN). A stored byte c of KV
  * head h means the value e4m3(c) * scale[h]. Writes store
- * e4m3(x / scale[h]): x is the bf16 input widened to float32, the division
+ * e4m3(x / scale[h]): x is the bf16 or f16 input widened to float32, the division
  * is IEEE float32 (correctly rounded), the result is rounded to the nearest
  * e4m3 value (ties to even) and saturates at +-448 (a NaN stays NaN).
- * Attention computes exactly the bf16 path's definition on the dequantized
+ * Attention computes exactly the 2-byte pools' definition on the dequantized
  * keys and values e4m3(c) * scale[h], with float32 accumulation. Items of at
  * most 8 packed query rows (decode with GQA <= 8) take q.k on the e4m3
  * tensor MMA, q as two e4m3 terms after a power-of-two row scale (exact for
@@ -373,7 +378,7 @@ typedef struct pa_kv_fp8 {
 
 /*
  * pa_reshape_and_cache_fp8 -- pa_reshape_and_cache into e4m3 pools: key /
- * value are bf16 rows as there (dtype = PA_BF16); each element is quantized
+ * value are bf16 or f16 rows as there (dtype); each element is quantized
  * with its KV head's scale as described above. scales must be non-NULL with
  * both pointers 4-byte aligned (PA_ERR_INVALID_ARG).
  */
@@ -397,7 +402,7 @@ size_t pa_cascade_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_se
  * pa_cascade_fwd_with_update over e4m3 pools: the optional update (NULL or
  * num_tokens = 0 for none) is quantized into the pools as by
  * pa_reshape_and_cache_fp8, then the attention reads the dequantized cache.
- * q, out and lse are as in the bf16 entry points (dtype = PA_BF16).
+ * q, out and lse are as in the other entry points (dtype PA_BF16 or PA_F16).
  */
 pa_status pa_varlen_fwd_fp8kv(const pa_kv_update* update, const void* q, int64_t q_token_stride,
                               void* key_cache, void* value_cache, int64_t cache_block_stride,
@@ -430,7 +435,7 @@ pa_status pa_cascade_fwd_fp8kv(const pa_kv_update* update, const void* q,
  *           out = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink)) and
  *           lse = ln(sum_j e^(s_j) + e^(sink)); a row with no visible key gets
  *           out = 0 and lse = sink.
- *   fp8   : NULL for bf16 pools, else the pools hold e4m3 bytes with these
+ *   fp8   : NULL for 2-byte pools (dtype), else the pools hold e4m3 bytes with these
  *           scales (as in pa_varlen_fwd_fp8kv; workspace then per
  *           pa_*_fwd_fp8kv_workspace_size).
  */

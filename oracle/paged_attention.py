@@ -14,7 +14,7 @@ Sources (web pages describing vLLM's attention backends; cited by key):
              (vllm-arch-zh.pages.dev/ja/attention/backend), section 境界と失敗.
 
 What is computed is the plain definition: every query row attends to the keys
-it may see with an exact softmax, in float64, on the bf16 input values. The
+it may see with an exact softmax, in float64, on the bf16 or f16 input values. The
 tiled online softmax of [FA-vLLM] §1.1 reaches the same numbers up to rounding
 order, so the oracle does not tile. Readings of points the pages leave open:
   * causal alignment is bottom-right: query i of a sequence with q_len

@@ -30,6 +30,7 @@ PA_DEV_BAD_SEQLEN = 4
 PA_DEV_TIMEOUT = 8
 PA_DEV_CASCADE = 16
 PA_BF16 = 0
+PA_F16 = 1
 
 EXPORTS = (
     "pa_status_string",
@@ -159,6 +160,19 @@ def _need_cuda(*ts):
             raise ValueError("all tensors must be CUDA tensors (no CPU fallback)")
 
 
+def _dtype_code(*ts):
+    """PA_BF16 or PA_F16 for tensors that must all share one 2-byte float type."""
+    dts = {t.dtype for t in ts if t is not None}
+    if len(dts) != 1:
+        raise ValueError(f"tensors must share one element type, got {sorted(map(str, dts))}")
+    dt = dts.pop()
+    if dt == torch.bfloat16:
+        return PA_BF16
+    if dt == torch.float16:
+        return PA_F16
+    raise ValueError(f"unsupported element type {dt} (bfloat16 or float16)")
+
+
 def _sm_count(device) -> int:
     return torch.cuda.get_device_properties(device).multi_processor_count
 
@@ -186,10 +200,11 @@ def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, dev_stat
     if key_cache.stride(0) != value_cache.stride(0):
         raise ValueError("key and value caches must share the page stride")
     nb, bs, hk, d = key_cache.shape
+    dtype = _dtype_code(key, value, key_cache, value_cache)
     code = lib.pa_reshape_and_cache(
         _ptr(key), _ptr(value), _row_stride(key), _row_stride(value), _ptr(key_cache),
         _ptr(value_cache), _cache_stride(key_cache), _ptr(slot_mapping), key.shape[0], hk, d, bs,
-        nb, PA_BF16, _ptr(dev_status), _stream(key.device))
+        nb, dtype, _ptr(dev_status), _stream(key.device))
     _check(code, "pa_reshape_and_cache")
 
 
@@ -245,7 +260,7 @@ def _kv_update(key, value, slot_mapping):
 
 def _attend(entry, update, q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
             max_seqlen_q, max_seqlen_k, softmax_scale, mode_arg, out, lse, return_lse,
-            workspace, dev_status, size_fn, fp8=None, sinks=None):
+            workspace, dev_status, size_fn, fp8=None, sinks=None, update_tensors=None):
     lib = load_library()
     _attn_common(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table)
     T, H, D = q.shape
@@ -253,6 +268,9 @@ def _attend(entry, update, q, key_cache, value_cache, cu_seqlens_q, seqused_k, b
     S = cu_seqlens_q.numel() - 1
     if out is None:
         out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
+    # q, out, the new tokens and (unless they hold e4m3 bytes) the pools share the type
+    pools = () if fp8 is not None else (key_cache, value_cache)
+    dtype = _dtype_code(q, out, *pools, *((update_tensors or ()) if update is not None else ()))
     if lse is None and return_lse:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     if workspace is None:
@@ -262,7 +280,7 @@ def _attend(entry, update, q, key_cache, value_cache, cu_seqlens_q, seqused_k, b
             _ptr(cu_seqlens_q), _ptr(seqused_k), _ptr(block_table), block_table.stride(0), S, T,
             int(max_seqlen_q), int(max_seqlen_k), H, hk, D, bs, nb, float(softmax_scale),
             int(mode_arg)) + ((ctypes.byref(fp8),) if fp8 is not None else ()) + (
-            _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), PA_BF16,
+            _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), dtype,
             _ptr(dev_status), _stream(q.device))
     upd = ctypes.byref(update) if update is not None else None
     if sinks is not None:
@@ -302,7 +320,8 @@ def varlen_fwd_with_update(key, value, slot_mapping, q, key_cache, value_cache, 
     return _attend("pa_varlen_fwd_with_update", _kv_update(key, value, slot_mapping), q,
                    key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
                    max_seqlen_k, softmax_scale, bool(causal), out, lse, return_lse, workspace,
-                   dev_status, varlen_fwd_workspace_size, sinks=sinks)
+                   dev_status, varlen_fwd_workspace_size, sinks=sinks,
+                   update_tensors=(key, value))
 
 
 def varlen_fwd_noalloc(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_table,
@@ -324,7 +343,8 @@ def varlen_fwd_noalloc(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block
         _ptr(q), _row_stride(q), _ptr(key_cache), _ptr(value_cache), _cache_stride(key_cache),
         _ptr(cu_seqlens_q), _ptr(seqused_k), _ptr(block_table), block_table.stride(0), S, T,
         int(max_seqlen_q), int(max_seqlen_k), H, hk, D, bs, nb, float(softmax_scale),
-        int(bool(causal)), _ptr(out), _ptr(lse), PA_BF16, _ptr(dev_status), _stream(q.device))
+        int(bool(causal)), _ptr(out), _ptr(lse), _dtype_code(q, out, key_cache, value_cache),
+        _ptr(dev_status), _stream(q.device))
     _check(code, "pa_varlen_fwd_noalloc")
     return out, lse
 
@@ -344,7 +364,8 @@ def merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse, out=None, 
         out_lse = torch.empty((H, T), dtype=torch.float32, device=prefix_out.device)
     code = lib.pa_merge_attn_states(
         _ptr(out), _ptr(out_lse), _ptr(prefix_out), _ptr(prefix_lse), _ptr(suffix_out),
-        _ptr(suffix_lse), T, H, D, PA_BF16, _stream(prefix_out.device))
+        _ptr(suffix_lse), T, H, D, _dtype_code(prefix_out, suffix_out, out),
+        _stream(prefix_out.device))
     _check(code, "pa_merge_attn_states")
     return out, out_lse
 
@@ -366,7 +387,7 @@ def merge_attn_states_n(parts_out, parts_lse, out=None, out_lse=None, return_lse
         out_lse = torch.empty((H, T), dtype=torch.float32, device=parts_out.device)
     code = lib.pa_merge_attn_states_n(
         _ptr(out), _ptr(out_lse), _ptr(parts_out), parts_out.stride(0), _ptr(parts_lse),
-        parts_lse.stride(0), n, T, H, D, PA_BF16, _stream(parts_out.device))
+        parts_lse.stride(0), n, T, H, D, _dtype_code(parts_out, out), _stream(parts_out.device))
     _check(code, "pa_merge_attn_states_n")
     return out, out_lse
 
@@ -389,7 +410,8 @@ def cascade_fwd_with_update(key, value, slot_mapping, q, key_cache, value_cache,
     return _attend("pa_cascade_fwd_with_update", _kv_update(key, value, slot_mapping), q,
                    key_cache, value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q,
                    max_seqlen_k, softmax_scale, common_prefix_len, out, lse, return_lse,
-                   workspace, dev_status, cascade_fwd_workspace_size, sinks=sinks)
+                   workspace, dev_status, cascade_fwd_workspace_size, sinks=sinks,
+                   update_tensors=(key, value))
 
 
 # ---------------------------------------------------------------------------
@@ -447,7 +469,7 @@ def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_sc
     code = lib.pa_reshape_and_cache_fp8(
         _ptr(key), _ptr(value), _row_stride(key), _row_stride(value), _ptr(key_cache),
         _ptr(value_cache), _cache_stride(key_cache), _ptr(slot_mapping), key.shape[0], hk, d, bs,
-        nb, ctypes.byref(desc), PA_BF16, _ptr(dev_status), _stream(key.device))
+        nb, ctypes.byref(desc), _dtype_code(key, value), _ptr(dev_status), _stream(key.device))
     _check(code, "pa_reshape_and_cache_fp8")
     del keep
 
@@ -464,7 +486,8 @@ def varlen_fwd_fp8kv(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_t
     res = _attend("pa_varlen_fwd_fp8kv", _kv_update(key, value, slot_mapping), q, key_cache,
                   value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q, max_seqlen_k,
                   softmax_scale, bool(causal), out, lse, return_lse, workspace, dev_status,
-                  varlen_fwd_fp8kv_workspace_size, fp8=desc, sinks=sinks)
+                  varlen_fwd_fp8kv_workspace_size, fp8=desc, sinks=sinks,
+                  update_tensors=(key, value))
     del keep
     return res
 
@@ -480,6 +503,7 @@ def cascade_fwd_fp8kv(q, key_cache, value_cache, cu_seqlens_q, seqused_k, block_
     res = _attend("pa_cascade_fwd_fp8kv", _kv_update(key, value, slot_mapping), q, key_cache,
                   value_cache, cu_seqlens_q, seqused_k, block_table, max_seqlen_q, max_seqlen_k,
                   softmax_scale, common_prefix_len, out, lse, return_lse, workspace, dev_status,
-                  cascade_fwd_fp8kv_workspace_size, fp8=desc, sinks=sinks)
+                  cascade_fwd_fp8kv_workspace_size, fp8=desc, sinks=sinks,
+                  update_tensors=(key, value))
     del keep
     return res

@@ -75,7 +75,7 @@ struct SplitShared {
 // the last CTA of the (row tile, KV head) group -- found with one atomic
 // counter, no spinning -- merges every split (and, in a cascade, the prefix
 // partials) with coalesced loads by all 128 consumer threads.
-template <int D>
+template <int D, bool F16>
 __device__ __forceinline__ void finish_group(const AttnArgs& a, SplitShared sh, int slot_base,
                                              int rt, int nsplit, int hk, int R, int row0,
                                              int q_start) {
@@ -88,7 +88,7 @@ __device__ __forceinline__ void finish_group(const AttnArgs& a, SplitShared sh, 
   asm volatile("bar.sync 2, 128;" ::: "memory");
   if (!sh.flags[1]) return;
   __threadfence();
-  combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, threadIdx.x, 128);
+  combine_splits<D, F16>(a, grp, nsplit, hk, R, row0, q_start, threadIdx.x, 128);
   if (threadIdx.x == 0) *counter = 0;   // ready for the next call
 }
 
@@ -133,12 +133,13 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* vtile, int tile_key0, int s
 // Consumers. RGN = number of 16-row groups (1, 2 or 4); 4 / RGN warps share
 // each group and split every key tile between them.
 // ---------------------------------------------------------------------------
-template <int D, int RGN, bool FP8>
+template <int D, int RGN, bool FP8, bool F16>
 __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring, SplitShared sh,
                                                int hk, int seg, int rt, int j, int q_start,
                                                int q_len, int kv_len, int kb, int ke, int ntiles,
                                                int nsplit, int slot_base) {
   using C = SplitCfg<D, FP8>;
+  using E = Elem<F16>;
   static_assert(!FP8 || D == 128, "FP8 pools: head size 128");
   constexpr int KS = 4 / RGN;       // warps per row group
   constexpr int KW = C::BN / KS;    // keys per warp per tile
@@ -190,11 +191,11 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
       const int col = FP8 ? cq * 32 + kk * 4 + (x >> 1) * 2 : kk * 16 + 2 * cq + (x >> 1) * 8;
       uint32_t v = 0;
       if (rvalid[r]) {
-        const __nv_bfloat16* p = a.q + static_cast<int64_t>(tok[r]) * a.q_stride +
-                                 static_cast<int64_t>(head[r]) * D + col;
+        const uint16_t* p = a.q + static_cast<int64_t>(tok[r]) * a.q_stride +
+                            static_cast<int64_t>(head[r]) * D + col;
         v = __ldg(reinterpret_cast<const uint32_t*>(p));
-        if constexpr (FP8) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+        if constexpr (FP8 && !F16) {   // the FP8 consumers multiply in f16
+          const float2 f = Elem<false>::unpack(v);
           v = pack_f16(f.x, f.y);
         }
       }
@@ -263,8 +264,8 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
           const int c = col + ((mat & 1) << 3);
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kbase + half * C::HALF_BYTES + sw128(key, c), b0, b1, b2, b3);
-          mma_16816(sacc[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-          mma_16816(sacc[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+          E::mma(sacc[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+          E::mma(sacc[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
         }
       }
       }
@@ -366,10 +367,10 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
       } else {
 #pragma unroll
       for (int kk = 0; kk < NT / 2; ++kk) {
-        const uint32_t pa0 = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
-        const uint32_t pa1 = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
-        const uint32_t pa2 = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-        const uint32_t pa3 = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+        const uint32_t pa0 = E::pack(sacc[2 * kk][0], sacc[2 * kk][1]);
+        const uint32_t pa1 = E::pack(sacc[2 * kk][2], sacc[2 * kk][3]);
+        const uint32_t pa2 = E::pack(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+        const uint32_t pa3 = E::pack(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
 #pragma unroll
         for (int dp = 0; dp < D / 16; ++dp) {
           const int half = dp >> 2, col = (dp & 3) * 16;
@@ -377,8 +378,8 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
           const int c = col + ((mat >> 1) << 3);
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(vbase + half * C::HALF_BYTES + sw128(key, c), b0, b1, b2, b3);
-          mma_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
-          mma_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+          E::mma(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
+          E::mma(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
         }
       }
       }
@@ -471,7 +472,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
           uint32_t pk[8];
 #pragma unroll
           for (int n = 0; n < DN; n += 2)
-            pk[n / 2] = pack_bf16(o[n][2 * r + e] * inv_l[r], o[n + 1][2 * r + e] * inv_l[r]);
+            pk[n / 2] = E::pack(o[n][2 * r + e] * inv_l[r], o[n + 1][2 * r + e] * inv_l[r]);
           uint4* dst = reinterpret_cast<uint4*>(a.out + obase + 16 * (2 * cq + e));
           dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -481,7 +482,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
       for (int n = 0; n < DN; ++n) {
         const int col = n * 8 + 2 * cq;
         *reinterpret_cast<uint32_t*>(a.out + obase + col) =
-            pack_bf16(o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]);
+            E::pack(o[n][2 * r] * inv_l[r], o[n][2 * r + 1] * inv_l[r]);
       }
       }
       if (a.lse && cq == 0) a.lse[static_cast<int64_t>(head[r]) * a.lse_stride + tok[r]] = lse_nat[r];
@@ -517,7 +518,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
       if (cq == 0) __stcg(a.part_lse + slot_row0 + rl, lse_nat[r]);
     }
   }
-  finish_group<D>(a, sh, slot_base, rt, nsplit, hk, R, row0, q_start);
+  finish_group<D, F16>(a, sh, slot_base, rt, nsplit, hk, R, row0, q_start);
 }
 
 // ---------------------------------------------------------------------------
@@ -548,6 +549,7 @@ __device__ __forceinline__ void split_consumer(const AttnArgs& a, uint8_t* ring,
 // The four warps take 16 keys each of every 64-key tile; their states are
 // merged through shared memory as in the other consumer.
 // ---------------------------------------------------------------------------
+template <bool F16>
 __device__ __forceinline__ void split_consumer_fp8_dec(const AttnArgs& a, uint8_t* ring,
                                                        SplitShared sh, int hk, int rt, int j,
                                                        int q_start, int q_len, int kv_len, int kb,
@@ -608,7 +610,7 @@ __device__ __forceinline__ void split_consumer_fp8_dec(const AttnArgs& a, uint8_
       const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uw[x]));
+        const float2 f = Elem<F16>::unpack(uw[x]);
         qf[8 * v + 2 * x] = f.x;
         qf[8 * v + 2 * x + 1] = f.y;
       }
@@ -848,13 +850,14 @@ __device__ __forceinline__ void split_consumer_fp8_dec(const AttnArgs& a, uint8_
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       if (!rvalid[e]) continue;
-      __nv_bfloat16* orow = a.out + (static_cast<int64_t>(tok[e]) * a.H + head[e]) * D + 8 * g;
+      uint16_t* orow = a.out + (static_cast<int64_t>(tok[e]) * a.H + head[e]) * D + 8 * g;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          pk[q] = pack_bf16(o[2 * q][2 * half + e] * inv_l[e], o[2 * q + 1][2 * half + e] * inv_l[e]);
+          pk[q] = Elem<F16>::pack(o[2 * q][2 * half + e] * inv_l[e],
+                                  o[2 * q + 1][2 * half + e] * inv_l[e]);
         *reinterpret_cast<uint4*>(orow + 64 * half) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       if (a.lse && g == 0) a.lse[static_cast<int64_t>(head[e]) * a.lse_stride + tok[e]] = lse_nat[e];
@@ -880,10 +883,10 @@ __device__ __forceinline__ void split_consumer_fp8_dec(const AttnArgs& a, uint8_
       if (g == 0) __stcg(a.part_lse + slot_row0 + 2 * c + e, lse_nat[e]);
     }
   }
-  finish_group<D>(a, sh, slot_base, rt, nsplit, hk, R, row0, q_start);
+  finish_group<D, F16>(a, sh, slot_base, rt, nsplit, hk, R, row0, q_start);
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool F16>
 __global__ void __launch_bounds__(SplitCfg<D, FP8>::THREADS, SplitCfg<D, FP8>::CTAS_PER_SM)
 attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ AttnArgs a) {
@@ -941,23 +944,23 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   }
   if constexpr (FP8) {
     if (R <= 8) {
-      split_consumer_fp8_dec(a, ring, sh, hk, rt, j, q_start, q_len, kv_len, kb, ke, ntiles,
+      split_consumer_fp8_dec<F16>(a, ring, sh, hk, rt, j, q_start, q_len, kv_len, kb, ke, ntiles,
                              nsplit, slot_base);
       return;
     }
   }
   if (R <= 16)
-    split_consumer<D, 1, FP8>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke,
+    split_consumer<D, 1, FP8, F16>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke,
                               ntiles, nsplit, slot_base);
   else if (R <= 32)
-    split_consumer<D, 2, FP8>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke,
+    split_consumer<D, 2, FP8, F16>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke,
                               ntiles, nsplit, slot_base);
   else
-    split_consumer<D, 4, FP8>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke,
+    split_consumer<D, 4, FP8, F16>(a, ring, sh, hk, seg, rt, j, q_start, q_len, kv_len, kb, ke,
                               ntiles, nsplit, slot_base);
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool F16>
 static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const AttnArgs& a, int items_bound, cudaStream_t st) {
   using C = SplitCfg<D, FP8>;
@@ -971,7 +974,7 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
   if (e != cudaSuccess) return e;
   const bool known = dev >= 0 && dev < kMaxDevices;
   if (!known || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(attn_split_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_split_kernel<D, FP8, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (known) configured[dev].store(true, std::memory_order_release);
@@ -986,7 +989,7 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_split_kernel<D, FP8>, tmK, tmV, a);
+  e = cudaLaunchKernelEx(&cfg, attn_split_kernel<D, FP8, F16>, tmK, tmV, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -994,9 +997,14 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
 cudaError_t launch_attn_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
                               int items_bound, cudaStream_t st) {
   if (items_bound <= 0) return cudaSuccess;
-  if (a.kv_fp8) return launch_split_d<128, true>(tmK, tmV, a, items_bound, st);
-  if (a.D == 128) return launch_split_d<128, false>(tmK, tmV, a, items_bound, st);
-  return launch_split_d<64, false>(tmK, tmV, a, items_bound, st);
+  if (a.f16) {
+    if (a.kv_fp8) return launch_split_d<128, true, true>(tmK, tmV, a, items_bound, st);
+    if (a.D == 128) return launch_split_d<128, false, true>(tmK, tmV, a, items_bound, st);
+    return launch_split_d<64, false, true>(tmK, tmV, a, items_bound, st);
+  }
+  if (a.kv_fp8) return launch_split_d<128, true, false>(tmK, tmV, a, items_bound, st);
+  if (a.D == 128) return launch_split_d<128, false, false>(tmK, tmV, a, items_bound, st);
+  return launch_split_d<64, false, false>(tmK, tmV, a, items_bound, st);
 }
 
 }  // namespace pa

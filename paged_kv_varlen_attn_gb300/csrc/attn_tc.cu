@@ -122,13 +122,14 @@ __device__ __forceinline__ bool zero_v_tail(TcBars* bars, uint8_t* smem, int t, 
   return true;
 }
 
-template <int D>
+template <int D, bool F16>
 __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars, uint8_t* smem,
                                                 uint32_t tmem, int X, int q_start, int q_len,
                                                 int kv_len, int kb, int ke, int ntiles, int row0,
                                                 int R, int hk, int nsplit, int slot_base, int rt,
                                                 int j) {
   using C = TcCfg<D>;
+  using E = Elem<F16>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
   const int r = quarter * 32 + lane;              // TMEM lane
@@ -222,7 +223,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
         ffma2(y0, y1, xs[c * 32 + e], xs[c * 32 + e + 1], sl2, sl2, -mu, -mu);
         const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
         fadd2(ls[e & 7], ls[(e + 1) & 7], ls[e & 7], ls[(e + 1) & 7], p0, p1);
-        pk[e >> 1] = pack_bf16(p0, p1);
+        pk[e >> 1] = E::pack(p0, p1);
       }
       tmem_st16(tm_row + s_col + c * 16, pk);
       if (c == 1) {
@@ -303,10 +304,10 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint4 pk;
-        pk.x = pack_bf16(__uint_as_float(v[8 * g]) * inv_l, __uint_as_float(v[8 * g + 1]) * inv_l);
-        pk.y = pack_bf16(__uint_as_float(v[8 * g + 2]) * inv_l, __uint_as_float(v[8 * g + 3]) * inv_l);
-        pk.z = pack_bf16(__uint_as_float(v[8 * g + 4]) * inv_l, __uint_as_float(v[8 * g + 5]) * inv_l);
-        pk.w = pack_bf16(__uint_as_float(v[8 * g + 6]) * inv_l, __uint_as_float(v[8 * g + 7]) * inv_l);
+        pk.x = E::pack(__uint_as_float(v[8 * g]) * inv_l, __uint_as_float(v[8 * g + 1]) * inv_l);
+        pk.y = E::pack(__uint_as_float(v[8 * g + 2]) * inv_l, __uint_as_float(v[8 * g + 3]) * inv_l);
+        pk.z = E::pack(__uint_as_float(v[8 * g + 4]) * inv_l, __uint_as_float(v[8 * g + 5]) * inv_l);
+        pk.w = E::pack(__uint_as_float(v[8 * g + 6]) * inv_l, __uint_as_float(v[8 * g + 7]) * inv_l);
         *reinterpret_cast<uint4*>(stage + lane * 64 + ((g ^ ((lane >> 1) & 3)) << 4)) = pk;
       }
       __syncwarp();
@@ -333,7 +334,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   }
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ AttnArgs a) {
@@ -433,8 +434,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // address plus c / 16; shared addresses stay below 2^18, so the 14-bit
     // field cannot carry).
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idesc_s = mma_idesc_bf16(C::BM, C::BN, false);
-      constexpr uint32_t idesc_o = mma_idesc_bf16(C::BM, D, true);
+      constexpr uint32_t idesc_s = mma_idesc(C::BM, C::BN, false, Elem<F16>::kTcFormat);
+      constexpr uint32_t idesc_o = mma_idesc(C::BM, D, true, Elem<F16>::kTcFormat);
       const uint32_t sKV = smem_u32(smem + C::OFF_KV);
       const uint64_t qdesc[2] = {smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024),
                                  smem_desc_sw128(smem_u32(smem + C::OFF_Q + C::Q_TILE), 16, 1024)};
@@ -523,7 +524,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // ------------------------------------------------------------ softmax
     const int X = (warp - 4) >> 2;   // warps 4-7: tile A, 8-11: tile B
     if (X == 0 || two)
-      tc_softmax_tile<D>(a, bars, smem, tmem, X, q_start, q_len, kv_len, kb, ke, ntiles, row0,
+      tc_softmax_tile<D, F16>(a, bars, smem, tmem, X, q_start, q_len, kv_len, kb, ke, ntiles, row0,
                          R, hk, nsplit, slot_base, rt, j);
     if (nsplit > 1 && !a.partials_only) {
       // Both warpgroups (256 threads) take part, active tile or not.
@@ -536,7 +537,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (bars->last) {
         __threadfence();
-        combine_splits<D>(a, grp, nsplit, hk, R, row0, q_start, tid, 256);
+        combine_splits<D, F16>(a, grp, nsplit, hk, R, row0, q_start, tid, 256);
         if (tid == 0) *counter = 0;
       }
     }
@@ -559,7 +560,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   }
 }
 
-template <int D>
+template <int D, bool F16>
 static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const CUtensorMap& tmQ, const AttnArgs& a, int items_bound,
                                cudaStream_t st) {
@@ -574,7 +575,7 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
   if (e != cudaSuccess) return e;
   const bool known = dev >= 0 && dev < kMaxDevices;
   if (!known || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (known) configured[dev].store(true, std::memory_order_release);
@@ -589,7 +590,7 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, tmK, tmV, tmQ, a);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, F16>, tmK, tmV, tmQ, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -597,8 +598,12 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
 cudaError_t launch_attn_tc(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
                            const AttnArgs& a, int items_bound, cudaStream_t st) {
   if (items_bound <= 0) return cudaSuccess;
-  if (a.D == 128) return launch_tc_d<128>(tmK, tmV, tmQ, a, items_bound, st);
-  return launch_tc_d<64>(tmK, tmV, tmQ, a, items_bound, st);
+  if (a.f16) {
+    if (a.D == 128) return launch_tc_d<128, true>(tmK, tmV, tmQ, a, items_bound, st);
+    return launch_tc_d<64, true>(tmK, tmV, tmQ, a, items_bound, st);
+  }
+  if (a.D == 128) return launch_tc_d<128, false>(tmK, tmV, tmQ, a, items_bound, st);
+  return launch_tc_d<64, false>(tmK, tmV, tmQ, a, items_bound, st);
 }
 
 }  // namespace pa

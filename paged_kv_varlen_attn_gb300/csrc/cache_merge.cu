@@ -103,23 +103,25 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
 // ---------------------------------------------------------------------------
 // Scatter into an FP8 (e4m3) cache ("FlashAttention と FlashInfer" 役割 and
 // 境界と失敗: FP8 KV cache with per-head quant scales). Same warp-per-token
-// walk as above; a lane reads 8 bf16 values (16 bytes) of one head, divides
+// walk as above; a lane reads 8 bf16 or f16 values (16 bytes) of one head, divides
 // them by that KV head's scale (IEEE float division, correctly rounded) and
 // writes the 8 e4m3 bytes (round to nearest even, saturating at +-448).
 // ---------------------------------------------------------------------------
+template <bool F16>
 __device__ __forceinline__ uint2 quantize8(uint4 x, float s) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+  const uint32_t h[4] = {x.x, x.y, x.z, x.w};
   uint32_t w[2];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
-    const float2 a = __bfloat1622float2(h[2 * k]);
-    const float2 b = __bfloat1622float2(h[2 * k + 1]);
+    const float2 a = Elem<F16>::unpack(h[2 * k]);
+    const float2 b = Elem<F16>::unpack(h[2 * k + 1]);
     w[k] = f32x2_to_e4m3x2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)) |
            (f32x2_to_e4m3x2(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)) << 16);
   }
   return make_uint2(w[0], w[1]);
 }
 
+template <bool F16>
 __global__ void __launch_bounds__(kScatterThreads)
 reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
                              int64_t kstride_v, int64_t vstride_v, uint2* __restrict__ kc,
@@ -160,8 +162,8 @@ reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restr
         const int i = v0 + u * 32;
         if (i < vpt) {
           const int h = i / vph;
-          kdst[i] = quantize8(kv[u], __ldg(k_scale + h));
-          vdst[i] = quantize8(vv[u], __ldg(v_scale + h));
+          kdst[i] = quantize8<F16>(kv[u], __ldg(k_scale + h));
+          vdst[i] = quantize8<F16>(vv[u], __ldg(v_scale + h));
         }
       }
     }
@@ -173,7 +175,8 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int
                                          int64_t block_stride, const int64_t* slots,
                                          int num_tokens, int H_kv, int D, int bs, int num_blocks,
                                          const float* k_scale, const float* v_scale,
-                                         int32_t* status, cudaStream_t st, int sms, bool pdl) {
+                                         int32_t* status, cudaStream_t st, int sms, bool pdl,
+                                         int f16) {
   if (num_tokens == 0) return cudaSuccess;
   const int vpt = H_kv * D / 8;
   const int64_t want = (static_cast<int64_t>(num_tokens) + kScatterWarps - 1) / kScatterWarps;
@@ -189,7 +192,8 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(
-      &cfg, reshape_and_cache_fp8_kernel, static_cast<const uint4*>(key),
+      &cfg, f16 ? reshape_and_cache_fp8_kernel<true> : reshape_and_cache_fp8_kernel<false>,
+      static_cast<const uint4*>(key),
       static_cast<const uint4*>(value), kstride / 8, vstride / 8, static_cast<uint2*>(kc),
       static_cast<uint2*>(vc), block_stride / 8, slots, num_tokens, vpt, D / 8, bs,
       static_cast<int64_t>(num_blocks) * bs, k_scale, v_scale, status);
@@ -205,16 +209,19 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int
 // ---------------------------------------------------------------------------
 constexpr int kMergeThreads = 256;
 
-__device__ __forceinline__ void bf16x8_to_float(const uint4& v, float (&f)[8]) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+// 8 bf16 or f16 values of a 16-byte vector as floats.
+template <bool F16>
+__device__ __forceinline__ void x8_to_float(const uint4& v, float (&f)[8]) {
+  const uint32_t h[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float2 x = __bfloat1622float2(h[i]);
+    const float2 x = Elem<F16>::unpack(h[i]);
     f[2 * i] = x.x;
     f[2 * i + 1] = x.y;
   }
 }
 
+template <bool F16>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_attn_states_kernel(uint4* out, float* out_lse, const uint4* __restrict__ a,
                          const float* __restrict__ alse, const uint4* __restrict__ b,
@@ -241,12 +248,13 @@ merge_attn_states_kernel(uint4* out, float* out_lse, const uint4* __restrict__ a
       const float inv = 1.0f / (wa + wb);
       const float ca = wa * inv, cb = wb * inv;
       float fa[8], fb[8];
-      bf16x8_to_float(__ldcs(a + idx), fa);
-      bf16x8_to_float(__ldcs(b + idx), fb);
+      x8_to_float<F16>(__ldcs(a + idx), fa);
+      x8_to_float<F16>(__ldcs(b + idx), fb);
       uint32_t* r = reinterpret_cast<uint32_t*>(&res);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        r[i] = pack_bf16(ca * fa[2 * i] + cb * fb[2 * i], ca * fa[2 * i + 1] + cb * fb[2 * i + 1]);
+        r[i] = Elem<F16>::pack(ca * fa[2 * i] + cb * fb[2 * i],
+                               ca * fa[2 * i + 1] + cb * fb[2 * i + 1]);
       lse_out = m + fast_log2(wa + wb) * kLn2;
     }
     out[idx] = res;
@@ -256,14 +264,14 @@ merge_attn_states_kernel(uint4* out, float* out_lse, const uint4* __restrict__ a
 
 cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* alse,
                          const void* b, const float* blse, int T, int H, int D, cudaStream_t st,
-                         int sms) {
+                         int sms, int f16) {
   if (T == 0) return cudaSuccess;
   const int vpr = D / 8;
   const int64_t total = static_cast<int64_t>(T) * H * vpr;
   const int64_t want = (total + kMergeThreads - 1) / kMergeThreads;
   const int64_t cap = static_cast<int64_t>(sms) * 8;
   const int grid = static_cast<int>(want < cap ? want : cap);
-  merge_attn_states_kernel<<<grid, kMergeThreads, 0, st>>>(
+  (f16 ? merge_attn_states_kernel<true> : merge_attn_states_kernel<false>)<<<grid, kMergeThreads, 0, st>>>(
       static_cast<uint4*>(out), out_lse, static_cast<const uint4*>(a), alse,
       static_cast<const uint4*>(b), blse, T, H, vpr);
   return cudaGetLastError();
@@ -280,6 +288,7 @@ cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* 
 // ---------------------------------------------------------------------------
 constexpr int kBatchN = 4;
 
+template <bool F16>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_attn_states_n_kernel(uint4* out, float* out_lse, const uint4* __restrict__ parts,
                            int64_t pstride_v, const float* __restrict__ plse, int64_t lstride,
@@ -314,7 +323,7 @@ merge_attn_states_n_kernel(uint4* out, float* out_lse, const uint4* __restrict__
         for (int u = 0; u < kBatchN; ++u) {
           if (r0 + u >= n) continue;
           float f[8];
-          bf16x8_to_float(v[u], f);
+          x8_to_float<F16>(v[u], f);
           sw += w[u];
 #pragma unroll
           for (int i = 0; i < 8; ++i) acc[i] += w[u] * f[i];
@@ -323,7 +332,7 @@ merge_attn_states_n_kernel(uint4* out, float* out_lse, const uint4* __restrict__
       const float inv = 1.0f / sw;
       uint32_t* rr = reinterpret_cast<uint32_t*>(&res);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) rr[i] = pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+      for (int i = 0; i < 4; ++i) rr[i] = Elem<F16>::pack(acc[2 * i] * inv, acc[2 * i + 1] * inv);
       lse_out = m + fast_log2(sw) * kLn2;
     }
     out[idx] = res;
@@ -333,14 +342,14 @@ merge_attn_states_n_kernel(uint4* out, float* out_lse, const uint4* __restrict__
 
 cudaError_t launch_merge_n(void* out, float* out_lse, const void* parts, int64_t part_stride,
                            const float* parts_lse, int64_t lse_stride, int n, int T, int H, int D,
-                           cudaStream_t st, int sms) {
+                           cudaStream_t st, int sms, int f16) {
   if (T == 0) return cudaSuccess;
   const int vpr = D / 8;
   const int64_t total = static_cast<int64_t>(T) * H * vpr;
   const int64_t want = (total + kMergeThreads - 1) / kMergeThreads;
   const int64_t cap = static_cast<int64_t>(sms) * 8;
   const int grid = static_cast<int>(want < cap ? want : cap);
-  merge_attn_states_n_kernel<<<grid, kMergeThreads, 0, st>>>(
+  (f16 ? merge_attn_states_n_kernel<true> : merge_attn_states_n_kernel<false>)<<<grid, kMergeThreads, 0, st>>>(
       static_cast<uint4*>(out), out_lse, static_cast<const uint4*>(parts), part_stride / 8,
       parts_lse, lse_stride, n, T, H, vpr);
   return cudaGetLastError();

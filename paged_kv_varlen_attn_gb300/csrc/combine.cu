@@ -17,7 +17,7 @@ constexpr int kCombineThreads = 256;
 
 // One block per (row group of the suffix pass, KV head). Blocks [0, gb0)
 // take class 0 groups, the rest class 1 groups.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kCombineThreads)
 cascade_combine_kernel(const __grid_constant__ AttnArgs a0, const __grid_constant__ AttnArgs a1,
                        int gb0) {
@@ -45,10 +45,11 @@ cascade_combine_kernel(const __grid_constant__ AttnArgs a0, const __grid_constan
   const int rows_per_item = cls ? tc_item_rows(a.G) : kRowsSplit;
   const int row0 = rt * rows_per_item;
   const int R = min(rows_per_item, sg.y * a.G - row0);
-  combine_splits<D>(a, sp.y + rt * sp.x, sp.x, hk, R, row0, sg.x, threadIdx.x, kCombineThreads);
+  combine_splits<D, F16>(a, sp.y + rt * sp.x, sp.x, hk, R, row0, sg.x, threadIdx.x,
+                         kCombineThreads);
 }
 
-template <int D>
+template <int D, bool F16>
 static cudaError_t launch_combine_d(const AttnArgs& a0, const AttnArgs& a1, int gb0, int gb1,
                                     cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
@@ -61,7 +62,7 @@ static cudaError_t launch_combine_d(const AttnArgs& a0, const AttnArgs& a1, int 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, cascade_combine_kernel<D>, a0, a1, gb0);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, cascade_combine_kernel<D, F16>, a0, a1, gb0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -69,8 +70,12 @@ static cudaError_t launch_combine_d(const AttnArgs& a0, const AttnArgs& a1, int 
 cudaError_t launch_cascade_combine(const AttnArgs& a0, const AttnArgs& a1, int gb0, int gb1,
                                    cudaStream_t st) {
   if (gb0 + gb1 <= 0) return cudaSuccess;
-  if (a0.D == 128) return launch_combine_d<128>(a0, a1, gb0, gb1, st);
-  return launch_combine_d<64>(a0, a1, gb0, gb1, st);
+  if (a0.f16) {
+    if (a0.D == 128) return launch_combine_d<128, true>(a0, a1, gb0, gb1, st);
+    return launch_combine_d<64, true>(a0, a1, gb0, gb1, st);
+  }
+  if (a0.D == 128) return launch_combine_d<128, false>(a0, a1, gb0, gb1, st);
+  return launch_combine_d<64, false>(a0, a1, gb0, gb1, st);
 }
 
 }  // namespace pa

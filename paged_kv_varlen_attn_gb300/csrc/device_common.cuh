@@ -190,6 +190,36 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
+// Element type of Q, the bf16/f16 K/V pools and the outputs: bfloat16
+// (F16 = false) or IEEE half (F16 = true). Both are 2-byte types moved as raw
+// bits; the kernels differ only in the MMA operand type and the conversions.
+template <bool F16>
+struct Elem;
+template <>
+struct Elem<false> {
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16(lo, hi); }
+  static __device__ __forceinline__ float2 unpack(uint32_t v) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+  }
+  static __device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1) {
+    mma_16816(d, a0, a1, a2, a3, b0, b1);
+  }
+  static constexpr uint32_t kTcFormat = 1;   // tcgen05 kind::f16 operand format: bf16
+};
+template <>
+struct Elem<true> {
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16(lo, hi); }
+  static __device__ __forceinline__ float2 unpack(uint32_t v) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+  }
+  static __device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1) {
+    mma_16816_f16(d, a0, a1, a2, a3, b0, b1);
+  }
+  static constexpr uint32_t kTcFormat = 0;   // tcgen05 kind::f16 operand format: f16
+};
+
 // Two-lane float32 arithmetic (sm_100 and later): one instruction computes a
 // pair, each lane rounded exactly as the scalar fmaf / add would be.
 __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0,
@@ -322,11 +352,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D: D format
-// (bits 4-5) = 1, A format (7-9) = 1, B format (10-12) = 1, A K-major, B
-// K-major or MN-major (bit 16), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t mma_idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+// Instruction descriptor for kind::f16 with fp32 D: D format (bits 4-5) = 1,
+// A format (7-9) and B format (10-12) = fmt (1 bf16, 0 f16; A and B of one
+// MMA always share the type), A K-major, B K-major or MN-major (bit 16),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, bool b_mn_major, uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 

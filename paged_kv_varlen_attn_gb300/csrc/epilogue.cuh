@@ -64,9 +64,11 @@ __device__ __forceinline__ void merge_states(float& mx, float& sw, float (&o)[4]
   }
 }
 
-// Write 4 final values of a row as bf16.
+// Write 4 final values of a row in the output's element type.
+template <bool F16>
 __device__ __forceinline__ void store4(const AttnArgs& a, int64_t obase, const float (&v)[4]) {
-  *reinterpret_cast<uint2*>(a.out + obase) = make_uint2(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]));
+  using E = Elem<F16>;
+  *reinterpret_cast<uint2*>(a.out + obase) = make_uint2(E::pack(v[0], v[1]), E::pack(v[2], v[3]));
 }
 
 // Partial-state slot of (group slot `slot`, KV head hk, row rl).
@@ -79,7 +81,7 @@ __device__ __forceinline__ int64_t slot_row(const AttnArgs& a, int slot, int hk,
 // states of the same rows -- and writes the final output. Threads tid in
 // [0, nthreads) share the work, 4 columns each. The merge is associative and
 // its order is fixed, so results are deterministic.
-template <int D>
+template <int D, bool F16>
 __device__ void combine_splits(const AttnArgs& a, int grp, int nsplit, int hk, int R, int row0,
                                int q_start, int tid, int nthreads) {
   constexpr int C4 = D / 4;
@@ -129,7 +131,7 @@ __device__ void combine_splits(const AttnArgs& a, int grp, int nsplit, int hk, i
       for (int x = 0; x < 4; ++x) acc[x] = 0.f;
     }
     const int64_t obase = (static_cast<int64_t>(tk) * a.H + hh) * D + c4 * 4;
-    store4(a, obase, acc);
+    store4<F16>(a, obase, acc);
     if (a.lse && c4 == 0) a.lse[static_cast<int64_t>(hh) * a.lse_stride + tk] = lse_r;
   }
 }

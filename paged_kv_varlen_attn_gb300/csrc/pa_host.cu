@@ -141,7 +141,7 @@ pa_status check_shape(int num_seqs, int total_q, int max_seqlen_q, int max_seqle
                       int H_kv, int D, int bs, int dtype) {
   if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return PA_ERR_INVALID_ARG;
   if (H <= 0 || H_kv <= 0 || H % H_kv != 0) return PA_ERR_INVALID_ARG;
-  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
   if (bs <= 0 || bs % 16 != 0 || bs > 1024) return PA_ERR_BLOCK_SIZE;
   return PA_OK;
@@ -202,7 +202,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // box_rows rows x 1 page. Coordinates past the pool (a page id == num_blocks)
 // read as zeros.
 bool encode_pool_map(CUtensorMap* map, const void* base, int D, int H_kv, int bs, int num_blocks,
-                     int64_t block_stride, int box_rows, bool fp8 = false) {
+                     int64_t block_stride, int box_rows, bool fp8, bool f16) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t esz = fp8 ? 1 : 2;
@@ -215,7 +215,10 @@ bool encode_pool_map(CUtensorMap* map, const void* base, int D, int H_kv, int bs
   cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), 1, static_cast<cuuint32_t>(box_rows),
                        1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+  const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                : f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(map, ty, 4,
                   const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -246,6 +249,7 @@ struct CommonAttn {
   cudaStream_t st;
   KvFormat kv;
   const float* sinks;   // [H] or NULL
+  int dtype;            // PA_BF16 or PA_F16: q, out and the 2-byte pools
 };
 
 PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int single, int single_kv,
@@ -282,7 +286,7 @@ PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int si
 AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt_row_stride,
                    int bt_col_offset, int causal, void* out, float* lse) {
   AttnArgs a{};
-  a.q = static_cast<const __nv_bfloat16*>(c.q);
+  a.q = static_cast<const uint16_t*>(c.q);
   a.q_stride = c.q_stride;
   a.bt = c.bt;
   a.bt_row_stride = bt_row_stride;
@@ -295,7 +299,8 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
   a.num_blocks = c.num_blocks;
   a.scale_log2 = c.scale * 1.4426950408889634f;
   a.causal = causal;
-  a.out = static_cast<__nv_bfloat16*>(out);
+  a.out = static_cast<uint16_t*>(out);
+  a.f16 = c.dtype == PA_F16 ? 1 : 0;
   a.lse = lse;
   a.lse_stride = c.total_q;
   a.header = reinterpret_cast<const int*>(ws + L.header);
@@ -316,7 +321,7 @@ AttnArgs make_attn(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int bt
 // tokens: exactly the tc_tile_rows(G) packed rows of one prefill Q tile,
 // 128-byte swizzled.
 bool encode_q_map(CUtensorMap* map, const void* q, int D, int H, int total_q, int64_t q_stride,
-                  int G) {
+                  int G, bool f16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
@@ -325,7 +330,8 @@ bool encode_q_map(CUtensorMap* map, const void* q, int D, int H, int total_q, in
   // G <= 128 here (wider groups never use the prefill kernel).
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kTcTileRows / G)};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+  CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(q), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -373,7 +379,7 @@ pa_status check_update(const void* key, const void* value, int64_t key_token_str
                        int num_kv_heads, int head_size, int block_size, int num_blocks,
                        int dtype, const KvFormat& kv = kKvBf16) {
   if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
-  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_UNSUPPORTED;
   if (head_size != 64 && head_size != 128) return PA_ERR_UNSUPPORTED;
   if (kv.fp8 && head_size != 128) return PA_ERR_UNSUPPORTED;
   if (block_size <= 0 || block_size % 16 != 0 || block_size > 1024) return PA_ERR_BLOCK_SIZE;
@@ -400,11 +406,11 @@ cudaError_t launch_scatter(const void* key, const void* value, int64_t kstride, 
                            void* kc, void* vc, int64_t block_stride, const int64_t* slots,
                            int num_tokens, int H_kv, int D, int bs, int num_blocks,
                            const KvFormat& kv, int32_t* status, cudaStream_t st, int sms,
-                           bool pdl) {
+                           bool pdl, int dtype) {
   if (kv.fp8)
     return launch_reshape_and_cache_fp8(key, value, kstride, vstride, kc, vc, block_stride, slots,
                                         num_tokens, H_kv, D, bs, num_blocks, kv.k_scale,
-                                        kv.v_scale, status, st, sms, pdl);
+                                        kv.v_scale, status, st, sms, pdl, dtype == PA_F16);
   return launch_reshape_and_cache(key, value, kstride, vstride, kc, vc, block_stride, slots,
                                   num_tokens, H_kv, D, bs, num_blocks, status, st, sms, pdl);
 }
@@ -426,7 +432,7 @@ pa_status launch_kv_update(const pa_kv_update* u, const CommonAttn& c, void* key
   if (!u || u->num_tokens == 0) return PA_OK;
   return launch_scatter(u->key, u->value, u->key_token_stride, u->value_token_stride, key_cache,
                         value_cache, c.block_stride, u->slot_mapping, u->num_tokens, c.H_kv, c.D,
-                        c.bs, c.num_blocks, c.kv, c.status, c.st, sms, true) == cudaSuccess
+                        c.bs, c.num_blocks, c.kv, c.status, c.st, sms, true, c.dtype) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }
@@ -520,7 +526,7 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
   CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
                seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
                num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
-               dev_status, static_cast<cudaStream_t>(stream), kv, sinks};
+               dev_status, static_cast<cudaStream_t>(stream), kv, sinks, dtype};
   st = check_kv_update(upd, c, key_cache, value_cache, dtype);
   if (st != PA_OK) return st;
   if (num_seqs == 0 || total_q == 0) {   // nothing to attend: the update alone
@@ -530,7 +536,7 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
     return launch_scatter(upd->key, upd->value, upd->key_token_stride, upd->value_token_stride,
                           key_cache, value_cache, cache_block_stride, upd->slot_mapping,
                           upd->num_tokens, num_kv_heads, head_size, block_size, num_blocks, kv,
-                          dev_status, c.st, sms, false) == cudaSuccess
+                          dev_status, c.st, sms, false, dtype) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
   }
@@ -547,14 +553,14 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
   const int box_rows = gcd_int(block_size, kKeyTile);
   CUtensorMap tmK, tmV;
   if (!encode_pool_map(&tmK, key_cache, head_size, num_kv_heads, block_size, num_blocks,
-                       cache_block_stride, box_rows, kv.fp8) ||
+                       cache_block_stride, box_rows, kv.fp8, dtype == PA_F16) ||
       !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
-                       cache_block_stride, box_rows, kv.fp8))
+                       cache_block_stride, box_rows, kv.fp8, dtype == PA_F16))
     return PA_ERR_CUDA;
   CUtensorMap tmQ{};
   if (L.items_bound[1] > 0 &&
       !encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride,
-                    num_heads / num_kv_heads))
+                    num_heads / num_kv_heads, dtype == PA_F16))
     return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const long long cap = static_cast<long long>(bt_stride) * block_size;
@@ -627,7 +633,7 @@ pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out
                                const float* suffix_lse, int num_tokens, int num_heads,
                                int head_size, int dtype, void* stream) {
   if (num_tokens < 0 || num_heads <= 0) return PA_ERR_INVALID_ARG;
-  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_UNSUPPORTED;
   if (head_size <= 0 || head_size % 8 != 0 || head_size > 256) return PA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PA_OK;
   if (!out || !prefix_out || !suffix_out || !prefix_lse || !suffix_lse) return PA_ERR_INVALID_ARG;
@@ -640,7 +646,7 @@ pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out
   if (sms <= 0) return PA_ERR_CUDA;
   cudaError_t e = launch_merge(out, out_lse, prefix_out, prefix_lse, suffix_out, suffix_lse,
                                num_tokens, num_heads, head_size,
-                               static_cast<cudaStream_t>(stream), sms);
+                               static_cast<cudaStream_t>(stream), sms, dtype == PA_F16);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -650,7 +656,7 @@ pa_status pa_merge_attn_states_n(void* out, float* out_lse, const void* parts_ou
                                  int num_heads, int head_size, int dtype, void* stream) {
   if (num_parts < 1 || num_parts > PA_MERGE_N_MAX || num_tokens < 0 || num_heads <= 0)
     return PA_ERR_INVALID_ARG;
-  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_UNSUPPORTED;
   if (head_size <= 0 || head_size % 8 != 0 || head_size > 256) return PA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PA_OK;
   if (!out || !parts_out || !parts_lse) return PA_ERR_INVALID_ARG;
@@ -671,7 +677,7 @@ pa_status pa_merge_attn_states_n(void* out, float* out_lse, const void* parts_ou
   if (sms <= 0) return PA_ERR_CUDA;
   cudaError_t e = launch_merge_n(out, out_lse, parts_out, part_stride_out, parts_lse,
                                  part_stride_lse, num_parts, num_tokens, num_heads, head_size,
-                                 static_cast<cudaStream_t>(stream), sms);
+                                 static_cast<cudaStream_t>(stream), sms, dtype == PA_F16);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -703,7 +709,7 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
                         cu_seqlens_q, seqused_k, block_table, bt_stride, num_seqs, total_q,
                         max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_size,
                         block_size, num_blocks, softmax_scale, dev_status,
-                        static_cast<cudaStream_t>(stream), kv, sinks};
+                        static_cast<cudaStream_t>(stream), kv, sinks, dtype};
     st = check_kv_update(upd, cu, key_cache, value_cache, dtype);
     if (st != PA_OK) return st;
   }
@@ -714,7 +720,7 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
     return launch_scatter(upd->key, upd->value, upd->key_token_stride, upd->value_token_stride,
                           key_cache, value_cache, cache_block_stride, upd->slot_mapping,
                           upd->num_tokens, num_kv_heads, head_size, block_size, num_blocks, kv,
-                          dev_status, static_cast<cudaStream_t>(stream), sms, false) == cudaSuccess
+                          dev_status, static_cast<cudaStream_t>(stream), sms, false, dtype) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
   }
@@ -730,17 +736,17 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
   CommonAttn c{q, q_token_stride, key_cache, value_cache, cache_block_stride, cu_seqlens_q,
                seqused_k, block_table, bt_stride, num_seqs, total_q, max_seqlen_q, max_seqlen_k,
                num_heads, num_kv_heads, head_size, block_size, num_blocks, softmax_scale,
-               dev_status, static_cast<cudaStream_t>(stream), kv, sinks};
+               dev_status, static_cast<cudaStream_t>(stream), kv, sinks, dtype};
   const int box_rows = gcd_int(block_size, kKeyTile);
   CUtensorMap tmK, tmV;
   if (!encode_pool_map(&tmK, key_cache, head_size, num_kv_heads, block_size, num_blocks,
-                       cache_block_stride, box_rows, kv.fp8) ||
+                       cache_block_stride, box_rows, kv.fp8, dtype == PA_F16) ||
       !encode_pool_map(&tmV, value_cache, head_size, num_kv_heads, block_size, num_blocks,
-                       cache_block_stride, box_rows, kv.fp8))
+                       cache_block_stride, box_rows, kv.fp8, dtype == PA_F16))
     return PA_ERR_CUDA;
   CUtensorMap tmQ{};
   if ((CL.prefix.items_bound[1] > 0 || CL.suffix.items_bound[1] > 0) &&
-      !encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride, G))
+      !encode_q_map(&tmQ, q, head_size, num_heads, total_q, q_token_stride, G, dtype == PA_F16))
     return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int P = common_prefix_len;
@@ -845,7 +851,7 @@ pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, int64_t k
   return launch_scatter(key, value, key_token_stride, value_token_stride, key_cache, value_cache,
                         cache_block_stride, slot_mapping, num_tokens, num_kv_heads, head_size,
                         block_size, num_blocks, kv, dev_status, static_cast<cudaStream_t>(stream),
-                        sms, false) == cudaSuccess
+                        sms, false, dtype) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }

@@ -88,7 +88,7 @@ struct PlanPasses {
 
 // Arguments of the attention kernels (both classes).
 struct AttnArgs {
-  const __nv_bfloat16* q;
+  const uint16_t* q;         // bf16 or f16 elements (raw bits; see f16)
   int64_t q_stride;          // elements between tokens
   const int32_t* bt;         // block_table
   int bt_row_stride;         // 0 for the cascade prefix pass (row 0 only)
@@ -96,7 +96,8 @@ struct AttnArgs {
   int H, H_kv, G, D, bs, num_blocks;
   float scale_log2;          // softmax_scale * log2(e)
   int causal;
-  __nv_bfloat16* out;        // [T, H, D] bf16 (final) or NULL
+  uint16_t* out;             // [T, H, D] bf16 or f16 (final) or NULL
+  int f16;                   // element type of q, out and the 2-byte pools: 0 bf16, 1 f16
   float* lse;                // [H, lse_stride] natural log or NULL
   int lse_stride;            // = total_q
   // Cascade. Both passes run with partials_only = 1: every work item writes
@@ -151,20 +152,23 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
                                      bool pdl);
 // The same scatter into e4m3 pools (kc, vc, block_stride in bytes): each
 // value is stored as e4m3(x / scale[kv head]).
+// key / value are bf16 (f16 = 0) or f16 (f16 = 1).
 cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int64_t kstride,
                                          int64_t vstride, void* kc, void* vc,
                                          int64_t block_stride, const int64_t* slots,
                                          int num_tokens, int H_kv, int D, int bs, int num_blocks,
                                          const float* k_scale, const float* v_scale,
-                                         int32_t* status, cudaStream_t st, int sms, bool pdl);
+                                         int32_t* status, cudaStream_t st, int sms, bool pdl,
+                                         int f16);
+// Merges of bf16 (f16 = 0) or f16 (f16 = 1) states.
 cudaError_t launch_merge(void* out, float* out_lse, const void* a, const float* alse,
                          const void* b, const float* blse, int T, int H, int D, cudaStream_t st,
-                         int sms);
+                         int sms, int f16);
 // n-state merge: part r's out at parts + r * part_stride (elements), its
 // LSE at parts_lse + r * lse_stride.
 cudaError_t launch_merge_n(void* out, float* out_lse, const void* parts, int64_t part_stride,
                            const float* parts_lse, int64_t lse_stride, int n, int T, int H, int D,
-                           cudaStream_t st, int sms);
+                           cudaStream_t st, int sms, int f16);
 cudaError_t launch_plan(const PlanPasses& passes, int npasses, cudaStream_t st);
 cudaError_t launch_attn_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
                               int items_bound, cudaStream_t st);

@@ -82,7 +82,7 @@ def _varlen(lib, **kw):
     (dict(bs=2048), pa.PA_ERR_BLOCK_SIZE),
     (dict(D=96), pa.PA_ERR_UNSUPPORTED),
     (dict(D=256), pa.PA_ERR_UNSUPPORTED),
-    (dict(dtype=1), pa.PA_ERR_UNSUPPORTED),
+    (dict(dtype=2), pa.PA_ERR_UNSUPPORTED),             # neither bf16 (0) nor f16 (1)
     (dict(H=32, Hk=6), pa.PA_ERR_INVALID_ARG),          # H % H_kv != 0
     (dict(q=None), pa.PA_ERR_INVALID_ARG),
     (dict(out=None), pa.PA_ERR_INVALID_ARG),
@@ -139,7 +139,7 @@ def test_reshape_and_cache_host_validation(lib):
         return f(*a)
     assert call(11, 24) == pa.PA_ERR_BLOCK_SIZE      # the pages' "multiple of 16" rule
     assert call(10, 80) == pa.PA_ERR_UNSUPPORTED     # head size
-    assert call(13, 1) == pa.PA_ERR_UNSUPPORTED      # dtype
+    assert call(13, 2) == pa.PA_ERR_UNSUPPORTED      # dtype: neither bf16 nor f16
     assert call(0, None) == pa.PA_ERR_INVALID_ARG
     assert call(7, FAKE + 4) == pa.PA_ERR_INVALID_ARG   # int64 slots misaligned
     assert call(2, 512) == pa.PA_ERR_INVALID_ARG     # token stride shorter than a row
@@ -154,7 +154,7 @@ def test_merge_host_validation(lib):
         a = list(base)
         a[i] = v
         return f(*a)
-    assert call(9, 1) == pa.PA_ERR_UNSUPPORTED
+    assert call(9, 2) == pa.PA_ERR_UNSUPPORTED
     assert call(2, None) == pa.PA_ERR_INVALID_ARG
     assert call(1, FAKE + 0x2000) == pa.PA_ERR_INVALID_ARG   # out_lse aliases prefix_lse
     assert call(6, 0) == pa.PA_OK

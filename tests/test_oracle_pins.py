@@ -829,3 +829,41 @@ def test_dcp_shard_layout():
                 got += row
             assert sorted(got) == sorted(pages)
             assert sum(int(l[s]) for l in lens) == wl.kv_lens[s]
+
+
+# ---------------------------------------------------------------- f16 inputs
+def check_f16_values_read_exactly():
+    """f16 keeps 10 fraction bits, bf16 7: 1 + 2^-10, 3 + 2^-9 and
+    1 - 2^-11 are f16 values bf16 cannot hold. One sequence with one key: the
+    output is that key's value row exactly and the LSE is scale * q.k, both
+    from the f16 values themselves ("FlashAttention 在 vLLM 中的实现分析"
+    §2.1 lists float16 beside bfloat16)."""
+    D, bs = 8, 16
+    qv, kv, vv = 3 + 2 ** -9, 1 - 2 ** -11, 1 + 2 ** -10
+    q = torch.full((1, 1, D), qv, dtype=torch.float16)
+    kc = torch.zeros((1, bs, 1, D), dtype=torch.float16)
+    vc = torch.zeros((1, bs, 1, D), dtype=torch.float16)
+    kc[0, 0, 0] = kv
+    vc[0, 0, 0] = vv
+    for t, x in ((q, qv), (kc[0, 0], kv), (vc[0, 0], vv)):
+        assert float(t.flatten()[0]) == x                      # exact in f16
+    assert float(torch.tensor(vv).to(torch.bfloat16)) != vv    # not in bf16
+    o, l = oracle.varlen_attention(q, kc, vc, torch.tensor([0, 1], dtype=torch.int32),
+                                   torch.tensor([1], dtype=torch.int32),
+                                   torch.tensor([[0]], dtype=torch.int32), 0.25, True)
+    assert o.dtype == F64 and bool((o[0, 0] == vv).all())
+    assert float(l[0, 0]) == 0.25 * D * qv * kv               # exact: a dyadic product
+
+
+def test_f16_inputs_are_read_as_f16_values():
+    check_f16_values_read_exactly()
+
+
+def test_planted_bf16_rounding_of_f16_inputs_is_caught(monkeypatch):
+    orig = P.attend_dense
+
+    def bad(q, k, v, *args, **kw):
+        r = lambda x: x.to(torch.bfloat16).to(F64)
+        return orig(r(q), r(k), r(v), *args, **kw)
+    monkeypatch.setattr(P, "attend_dense", bad)
+    assert _fails(check_f16_values_read_exactly)

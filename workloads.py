@@ -18,8 +18,9 @@ Recipe (every workload):
     pool; unused block_table entries hold INT32_MAX;
   * the new tokens of sequence s are its last q_len[s] positions, and their
     slot is (physical page) * block_size + (position % block_size);
-  * all values are drawn in fp32 and rounded to bf16; both the oracle and the
-    GPU path consume the same bf16 values.
+  * all values are drawn in fp32 and rounded to the workload's element type
+    (bf16 by default, or f16); both the oracle and the GPU path consume the
+    same rounded values.
   * FP8 (e4m3) pools: the prior context of KV head h is the same N(0,1) pages
     divided by the pool's scale for h (kv_scales) and cast by torch to
     float8_e4m3fn (bytes kept as uint8), after clamping to +-448 -- synthetic
@@ -72,6 +73,7 @@ class Workload:
     v_new: torch.Tensor                # bf16 [T_new, H_kv, D]
     common_prefix_len: int = 0
     meta: dict = field(default_factory=dict)
+    dtype: torch.dtype = torch.bfloat16      # element type of Q, K/V pools and new tokens
 
     # ---- derived metadata -------------------------------------------------
     @property
@@ -110,16 +112,16 @@ class Workload:
         return (self.num_blocks + PAGES_PER_CHUNK - 1) // PAGES_PER_CHUNK
 
     def pool_chunk(self, which: int, chunk: int) -> torch.Tensor:
-        """bf16 pages [chunk*64, chunk*64+64) of the K (which=0) or V (which=1) pool."""
+        """Pages [chunk*64, chunk*64+64) of the K (which=0) or V (which=1) pool."""
         first = chunk * PAGES_PER_CHUNK
         n = min(PAGES_PER_CHUNK, self.num_blocks - first)
         g = torch.Generator().manual_seed(derived_seed(self.seed, 1 + which, chunk))
         x = torch.randn((n,) + self.page_shape, generator=g, dtype=torch.float32)
-        return x.to(torch.bfloat16)
+        return x.to(self.dtype)
 
     def pool(self, which: int, device="cpu", threads: int = 8) -> torch.Tensor:
         """The whole K or V pool [num_blocks, block_size, H_kv, D] before the scatter."""
-        out = torch.empty((self.num_blocks,) + self.page_shape, dtype=torch.bfloat16,
+        out = torch.empty((self.num_blocks,) + self.page_shape, dtype=self.dtype,
                           device=device)
 
         def fill(c):
@@ -206,7 +208,7 @@ class Workload:
             slot_mapping=self.slot_mapping[q_rows].clone(),
             q=self.q[q_rows].clone(), k_new=self.k_new[q_rows].clone(),
             v_new=self.v_new[q_rows].clone(),
-            common_prefix_len=self.common_prefix_len, meta=dict(self.meta))
+            common_prefix_len=self.common_prefix_len, meta=dict(self.meta), dtype=self.dtype)
 
 
 def dcp_shards(wl: "Workload", ranks: int):
@@ -234,7 +236,8 @@ def dcp_shards(wl: "Workload", ranks: int):
 
 
 def _build(name, seed, H, H_kv, D, bs, q_lens, kv_lens, g, causal=True, scale=None,
-           num_blocks=None, shared_prefix_pages=0, pool_slack=1.1, meta=None):
+           num_blocks=None, shared_prefix_pages=0, pool_slack=1.1, meta=None,
+           dtype=torch.bfloat16):
     """Lay out pages, draw Q and new K/V. ``g`` has already drawn the lengths."""
     S = len(q_lens)
     assert all(0 <= q <= k for q, k in zip(q_lens, kv_lens)), "new tokens lie inside the KV"
@@ -257,9 +260,9 @@ def _build(name, seed, H, H_kv, D, bs, q_lens, kv_lens, g, causal=True, scale=No
         bt[s, n_sh:n_sh + n_pr] = perm[cursor:cursor + n_pr]
         cursor += n_pr
     T = sum(q_lens)
-    q = torch.randn((T, H, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    k_new = torch.randn((T, H_kv, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    v_new = torch.randn((T, H_kv, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    q = torch.randn((T, H, D), generator=g, dtype=torch.float32).to(dtype)
+    k_new = torch.randn((T, H_kv, D), generator=g, dtype=torch.float32).to(dtype)
+    v_new = torch.randn((T, H_kv, D), generator=g, dtype=torch.float32).to(dtype)
     slots = []
     for s in range(S):
         for pos in range(kv_lens[s] - q_lens[s], kv_lens[s]):
@@ -271,7 +274,7 @@ def _build(name, seed, H, H_kv, D, bs, q_lens, kv_lens, g, causal=True, scale=No
                     causal=causal, q_lens=list(q_lens), kv_lens=list(kv_lens),
                     block_table=bt, slot_mapping=slot_mapping, q=q, k_new=k_new,
                     v_new=v_new, common_prefix_len=shared_prefix_pages * bs,
-                    meta=meta or {})
+                    meta=meta or {}, dtype=dtype)
 
 
 def _uniform_int(g, lo, hi, n):
@@ -279,7 +282,7 @@ def _uniform_int(g, lo, hi, n):
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
 
 
-def tiny_mixed(seed=1001):
+def tiny_mixed(seed=1001, dtype=torch.bfloat16):
     """4 seqs, 4 query / 2 KV heads, head_size 64, block_size 16, pool of 64 pages.
     KV lens {17, 33, 64, 100}; seqs 0-1 decode (one query), seqs 2-3 causal
     prefill with query length equal to KV length."""
@@ -287,18 +290,18 @@ def tiny_mixed(seed=1001):
     kv = [17, 33, 64, 100]
     ql = [1, 1, 64, 100]
     return _build("tiny_mixed", seed, 4, 2, 64, 16, ql, kv, g, num_blocks=64,
-                  scale=1.0 / 8.0)
+                  scale=1.0 / 8.0, dtype=dtype)
 
 
-def decode_llama8b(seed=1002, num_seqs=64):
+def decode_llama8b(seed=1002, num_seqs=64, dtype=torch.bfloat16):
     """64 decode seqs x 1 query token, 32/8 heads, head_size 128, block_size 16,
     KV lens uniform on [512, 8192], pool = total pages + 10%."""
     g = torch.Generator().manual_seed(seed)
     kv = _uniform_int(g, 512, 8192, num_seqs)
-    return _build("decode_llama8b", seed, 32, 8, 128, 16, [1] * num_seqs, kv, g)
+    return _build("decode_llama8b", seed, 32, 8, 128, 16, [1] * num_seqs, kv, g, dtype=dtype)
 
 
-def chunked_prefill_mix(seed=1003, n_prefill=8, chunk=2048, n_decode=56):
+def chunked_prefill_mix(seed=1003, n_prefill=8, chunk=2048, n_decode=56, dtype=torch.bfloat16):
     """8 causal prefill chunks of 2048 tokens with prior context uniform on
     [0, 4096], then 56 decode seqs with KV uniform on [1024, 8192]; 32/8 heads,
     head_size 128, block_size 16."""
@@ -307,10 +310,10 @@ def chunked_prefill_mix(seed=1003, n_prefill=8, chunk=2048, n_decode=56):
     dec = _uniform_int(g, 1024, 8192, n_decode)
     ql = [chunk] * n_prefill + [1] * n_decode
     kv = [c + chunk for c in ctx] + dec
-    return _build("chunked_prefill_mix", seed, 32, 8, 128, 16, ql, kv, g)
+    return _build("chunked_prefill_mix", seed, 32, 8, 128, 16, ql, kv, g, dtype=dtype)
 
 
-def cascade_shared_prefix(seed=1004, num_seqs=64, prefix=2048):
+def cascade_shared_prefix(seed=1004, num_seqs=64, prefix=2048, dtype=torch.bfloat16):
     """64 requests sharing a 2048-token prefix (128 pages of 16, the same first
     128 block_table entries in every row), each with one query token and a
     private suffix uniform on [64, 512] tokens; 32/8 heads, head_size 128."""
@@ -318,29 +321,29 @@ def cascade_shared_prefix(seed=1004, num_seqs=64, prefix=2048):
     suf = _uniform_int(g, 64, 512, num_seqs)
     kv = [prefix + s for s in suf]
     return _build("cascade_shared_prefix", seed, 32, 8, 128, 16, [1] * num_seqs, kv, g,
-                  shared_prefix_pages=prefix // 16)
+                  shared_prefix_pages=prefix // 16, dtype=dtype)
 
 
-def long_context_70b(seed=1005, n_decode=32, kv_len=32768, n_prefill=4, q_len=4096):
+def long_context_70b(seed=1005, n_decode=32, kv_len=32768, n_prefill=4, q_len=4096, dtype=torch.bfloat16):
     """64/8 heads (GQA 8), head_size 128, block_size 128: 32 decode seqs at KV
     32768, then 4 causal prefill seqs of 4096 tokens on 28672 prior tokens."""
     g = torch.Generator().manual_seed(seed)
     ql = [1] * n_decode + [q_len] * n_prefill
     kv = [kv_len] * (n_decode + n_prefill)
-    return _build("long_context_70b", seed, 64, 8, 128, 128, ql, kv, g)
+    return _build("long_context_70b", seed, 64, 8, 128, 128, ql, kv, g, dtype=dtype)
 
 
-def long_context_70b_prefill(seed=1015, n_prefill=4, kv_len=32768, q_len=4096):
+def long_context_70b_prefill(seed=1015, n_prefill=4, kv_len=32768, q_len=4096, dtype=torch.bfloat16):
     """The prefill side of long_context_70b as a batch of its own: 4 causal
     prefill seqs of 4096 queries on 28672 prior tokens, 64/8 heads, head_size
     128, block_size 128 (the same shapes and FLOPs; its own pool of those
     sequences' pages only, ~0.3 GB per pool)."""
     g = torch.Generator().manual_seed(seed)
     return _build("long_context_70b_prefill", seed, 64, 8, 128, 128, [q_len] * n_prefill,
-                  [kv_len] * n_prefill, g)
+                  [kv_len] * n_prefill, g, dtype=dtype)
 
 
-def chunked_prefill_mix_prefill(seed=1003, n_prefill=8, chunk=2048, n_decode=56):
+def chunked_prefill_mix_prefill(seed=1003, n_prefill=8, chunk=2048, n_decode=56, dtype=torch.bfloat16):
     """The prefill chunks of chunked_prefill_mix as a batch of their own: the
     same 8 chunks of 2048 causal queries with the same prior-context lengths
     (drawn first from the same seed), 32/8 heads, head_size 128, block_size
@@ -349,16 +352,16 @@ def chunked_prefill_mix_prefill(seed=1003, n_prefill=8, chunk=2048, n_decode=56)
     ctx = _uniform_int(g, 0, 4096, n_prefill)
     _uniform_int(g, 1024, 8192, n_decode)      # the decode lengths, drawn and dropped
     return _build("chunked_prefill_mix_prefill", seed, 32, 8, 128, 16, [chunk] * n_prefill,
-                  [c + chunk for c in ctx], g)
+                  [c + chunk for c in ctx], g, dtype=dtype)
 
 
-def prefill_profile(seed=1006, n_prefill=4, q_len=2048, kv_len=12288):
+def prefill_profile(seed=1006, n_prefill=4, q_len=2048, kv_len=12288, dtype=torch.bfloat16):
     """A small case of the long-context prefill shape for profiler captures:
     64/8 heads, head_size 128, block_size 128, 4 causal prefill sequences of
     2048 queries on 10240 prior tokens (pool ~220 MB, larger than L2)."""
     g = torch.Generator().manual_seed(seed)
     return _build("prefill_profile", seed, 64, 8, 128, 128, [q_len] * n_prefill,
-                  [kv_len] * n_prefill, g)
+                  [kv_len] * n_prefill, g, dtype=dtype)
 
 
 CONFIGS = {
@@ -375,7 +378,7 @@ CONFIGS = {
 
 def random_case(seed, num_seqs=3, num_heads=4, num_kv_heads=2, head_size=64,
                 block_size=16, max_q=40, max_kv=120, causal=True, decode_frac=0.3,
-                empty_ok=False, slack=1.5):
+                empty_ok=False, slack=1.5, dtype=torch.bfloat16):
     """A small random batch: lengths, pages and values all from ``seed``."""
     g = torch.Generator().manual_seed(seed)
     ql, kv = [], []
@@ -390,4 +393,4 @@ def random_case(seed, num_seqs=3, num_heads=4, num_kv_heads=2, head_size=64,
         ql.append(q)
         kv.append(k)
     return _build(f"random_{seed}", seed, num_heads, num_kv_heads, head_size, block_size,
-                  ql, kv, g, causal=causal, pool_slack=slack)
+                  ql, kv, g, causal=causal, pool_slack=slack, dtype=dtype)
