@@ -997,6 +997,7 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
 cudaError_t launch_attn_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
                               int items_bound, cudaStream_t st) {
   if (items_bound <= 0) return cudaSuccess;
+  if (a.D > kMaxHeadSplit) return cudaErrorInvalidValue;   // planned on the prefill kernel only
   if (a.f16) {
     if (a.kv_fp8) return launch_split_d<128, true, true>(tmK, tmV, a, items_bound, st);
     if (a.D == 128) return launch_split_d<128, false, true>(tmK, tmV, a, items_bound, st);

@@ -57,30 +57,35 @@
 
 namespace pa {
 
+// Head sizes 64 and 128: two Q tiles per CTA and 128-key K/V tiles. Head
+// size 256: one Q tile (its O takes 256 TMEM columns) and 64-key K/V tiles,
+// so that two ring stages fit beside the 64 KB Q tile.
 template <int D>
 struct TcCfg {
   static constexpr int BM = 128;         // rows per Q tile (TMEM lanes)
-  static constexpr int TILES = 2;        // Q tiles per CTA
-  static constexpr int BN = 128;         // keys per K/V tile
+  static constexpr int TILES = tc_tiles(D);   // Q tiles per CTA
+  static constexpr int BN = D > 128 ? 64 : 128;   // keys per K/V tile
   static constexpr int HALVES = D / 64;
   static constexpr int Q_HALF = BM * 128;
   static constexpr int Q_TILE = HALVES * Q_HALF;
   static constexpr int KV_HALF = BN * 128;
   static constexpr int KV_TILE = HALVES * KV_HALF;
   static constexpr int STAGE = 2 * KV_TILE;
-  static constexpr int STAGES = D == 128 ? 2 : 4;
+  static constexpr int STAGES = D == 64 ? 4 : 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = TILES * Q_TILE;
   static constexpr int OFF_BAR = OFF_KV + STAGES * STAGE;
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
   static constexpr int THREADS = 384;   // 3 warpgroups: control, softmax A, softmax B
   static constexpr int TMEM_COLS = 512;
-  // TMEM columns: S of tile X at X*128 (P of tile X as bf16 pairs in its
-  // first 64 columns); O of tile X at 256 + X*D.
+  // TMEM columns: S of tile X at X*128 (P of tile X as bf16 or f16 pairs in
+  // its first BN / 2 columns); O of tile X at 256 + X*D.
   static constexpr int O_COL = 256;
   static constexpr float RESCALE_LOG2 = 8.0f;
 };
 static_assert(kTcTileRows == TcCfg<128>::BM, "a Q tile spans the 128 TMEM lanes");
+static_assert(TcCfg<256>::SMEM_BYTES <= 227 * 1024, "head size 256 fits shared memory");
+static_assert(TcCfg<256>::O_COL + 256 <= TcCfg<256>::TMEM_COLS, "head size 256 fits TMEM");
 
 struct TcBars {
   uint64_t q_full;
@@ -226,7 +231,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
         pk[e >> 1] = E::pack(p0, p1);
       }
       tmem_st16(tm_row + s_col + c * 16, pk);
-      if (c == 1) {
+      if (c == C::BN / 64 - 1) {   // the first half of the tile's keys
         tmem_wait_st();
         if (X == 0 && key0 + C::BN > kv_len)   // warp-uniform condition and result
           ok = __all_sync(0xffffffffu, zero_v_tail<D>(bars, smem, t, key0, kv_len, tid));
@@ -355,8 +360,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const int nsplit = sp.x, slot_base = sp.y, chunk = sp.z;
   const int G = a.G;
   const int TR = tc_tile_rows(G);   // rows of a Q tile: TR / G whole tokens
-  const int row0 = rt * 2 * TR;
-  const int R = min(2 * TR, q_len * G - row0);
+  const int row0 = rt * C::TILES * TR;
+  const int R = min(C::TILES * TR, q_len * G - row0);
   const bool two = R > TR;   // tile B has rows
   const int kb = j * chunk;
   int ke = min(kv_len, kb + chunk);
@@ -599,9 +604,11 @@ cudaError_t launch_attn_tc(const CUtensorMap& tmK, const CUtensorMap& tmV, const
                            const AttnArgs& a, int items_bound, cudaStream_t st) {
   if (items_bound <= 0) return cudaSuccess;
   if (a.f16) {
+    if (a.D == 256) return launch_tc_d<256, true>(tmK, tmV, tmQ, a, items_bound, st);
     if (a.D == 128) return launch_tc_d<128, true>(tmK, tmV, tmQ, a, items_bound, st);
     return launch_tc_d<64, true>(tmK, tmV, tmQ, a, items_bound, st);
   }
+  if (a.D == 256) return launch_tc_d<256, false>(tmK, tmV, tmQ, a, items_bound, st);
   if (a.D == 128) return launch_tc_d<128, false>(tmK, tmV, tmQ, a, items_bound, st);
   return launch_tc_d<64, false>(tmK, tmV, tmQ, a, items_bound, st);
 }

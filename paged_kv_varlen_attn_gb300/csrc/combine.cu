@@ -42,7 +42,7 @@ cascade_combine_kernel(const __grid_constant__ AttnArgs a0, const __grid_constan
   pdl_trigger();
   if (!live || call_aborted(a)) return;
   const int rt = gr.y;
-  const int rows_per_item = cls ? tc_item_rows(a.G) : kRowsSplit;
+  const int rows_per_item = cls ? tc_item_rows(a.G, D) : kRowsSplit;
   const int row0 = rt * rows_per_item;
   const int R = min(rows_per_item, sg.y * a.G - row0);
   combine_splits<D, F16>(a, sp.y + rt * sp.x, sp.x, hk, R, row0, sg.x, threadIdx.x,
@@ -71,9 +71,11 @@ cudaError_t launch_cascade_combine(const AttnArgs& a0, const AttnArgs& a1, int g
                                    cudaStream_t st) {
   if (gb0 + gb1 <= 0) return cudaSuccess;
   if (a0.f16) {
+    if (a0.D == 256) return launch_combine_d<256, true>(a0, a1, gb0, gb1, st);
     if (a0.D == 128) return launch_combine_d<128, true>(a0, a1, gb0, gb1, st);
     return launch_combine_d<64, true>(a0, a1, gb0, gb1, st);
   }
+  if (a0.D == 256) return launch_combine_d<256, false>(a0, a1, gb0, gb1, st);
   if (a0.D == 128) return launch_combine_d<128, false>(a0, a1, gb0, gb1, st);
   return launch_combine_d<64, false>(a0, a1, gb0, gb1, st);
 }

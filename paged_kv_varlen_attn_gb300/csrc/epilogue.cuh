@@ -92,7 +92,7 @@ __device__ void combine_splits(const AttnArgs& a, int grp, int nsplit, int hk, i
     const int4 g0 = a.mp_seg[0];
     const int4 s0 = a.mp_segsplit[0];
     p_cls = g0.w;
-    p_rows = p_cls ? tc_item_rows(G) : kRowsSplit;
+    p_rows = p_cls ? tc_item_rows(G, D) : kRowsSplit;
     p_nsp = s0.x;
     p_base = s0.y;
   }

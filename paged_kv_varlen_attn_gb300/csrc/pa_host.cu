@@ -48,11 +48,17 @@ struct PassDims {
 };
 
 // Which kernels a pass can need, from host-known bounds only.
+// Packed rows above which a segment takes the prefill kernel: every segment
+// at head sizes the split-KV kernel does not take.
+int tc_min_rows(int D) { return D > kMaxHeadSplit ? 0 : kTcMinRows; }
 bool pass_has_tc(const PassDims& d) {
   const long long rows = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
-  return kTcAvailable && d.tc_allowed && !d.kv_fp8 && tc_tile_rows(d.G) > 0 && rows > kTcMinRows;
+  return kTcAvailable && d.tc_allowed && !d.kv_fp8 && tc_tile_rows(d.G) > 0 &&
+         rows > tc_min_rows(d.D);
 }
-bool pass_has_split(const PassDims& d) { return !d.single || !pass_has_tc(d); }
+bool pass_has_split(const PassDims& d) {
+  return d.D <= kMaxHeadSplit && (!d.single || !pass_has_tc(d));
+}
 
 // Workspace layout of one pass starting at byte offset `base`.
 PassLayout layout_pass(const PassDims& d, size_t base) {
@@ -62,7 +68,7 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
   L.target[1] = tc ? target_tc(d.sms, d.H_kv) : 0;
   const long long rows = static_cast<long long>(d.total_q) * d.G;
   L.items_bound[0] = sp ? L.target[0] + d.num_segs + cdiv(rows, kRowsSplit) + 1 : 0;
-  L.items_bound[1] = tc ? L.target[1] + d.num_segs + cdiv(rows, tc_item_rows(d.G)) + 1 : 0;
+  L.items_bound[1] = tc ? L.target[1] + d.num_segs + cdiv(rows, tc_item_rows(d.G, d.D)) + 1 : 0;
   L.slots_bound[0] = sp ? 2 * L.target[0] + 2 : 0;
   L.slots_bound[1] = tc ? 2 * L.target[1] + 2 : 0;
   if (d.all_partial) {
@@ -76,7 +82,7 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
                                                    : item_rows);
   };
   L.slot_rows[0] = clamp_rows(kRowsSplit);
-  L.slot_rows[1] = clamp_rows(tc ? tc_item_rows(d.G) : 1);
+  L.slot_rows[1] = clamp_rows(tc ? tc_item_rows(d.G, d.D) : 1);
   size_t off = align_up(base);
   L.header = off;                 off = align_up(off + 64 * sizeof(int));
   L.seg = off;                    off = align_up(off + static_cast<size_t>(d.num_segs) * 16);
@@ -142,7 +148,7 @@ pa_status check_shape(int num_seqs, int total_q, int max_seqlen_q, int max_seqle
   if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return PA_ERR_INVALID_ARG;
   if (H <= 0 || H_kv <= 0 || H % H_kv != 0) return PA_ERR_INVALID_ARG;
   if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_UNSUPPORTED;
-  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return PA_ERR_UNSUPPORTED;
   if (bs <= 0 || bs % 16 != 0 || bs > 1024) return PA_ERR_BLOCK_SIZE;
   return PA_OK;
 }
@@ -177,6 +183,10 @@ pa_status check_attn_ptrs(const void* q, int64_t q_stride, const void* kc, const
   }
   if (bt_stride < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  // Head size 256 runs on the prefill kernel only, which needs a positive
+  // scale and groups of at most 128 heads.
+  if (D > kMaxHeadSplit && (!(scale > 0.f) || tc_tile_rows(H / H_kv) == 0))
+    return PA_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return PA_ERR_INVALID_ARG;
   return PA_OK;
 }
@@ -267,7 +277,9 @@ PlanArgs make_plan(const CommonAttn& c, uint8_t* ws, const PassLayout& L, int si
   p.max_k = c.max_k;
   p.G = c.H / c.H_kv;
   p.H_kv = c.H_kv;
+  p.D = c.D;
   p.tc_enabled = L.items_bound[1] > 0 ? 1 : 0;
+  p.tc_min_rows = tc_min_rows(c.D);
   p.causal = causal;
   p.target0 = L.target[0];
   p.target1 = L.target[1];
@@ -380,7 +392,7 @@ pa_status check_update(const void* key, const void* value, int64_t key_token_str
                        int dtype, const KvFormat& kv = kKvBf16) {
   if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
   if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_UNSUPPORTED;
-  if (head_size != 64 && head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (head_size != 64 && head_size != 128 && head_size != 256) return PA_ERR_UNSUPPORTED;
   if (kv.fp8 && head_size != 128) return PA_ERR_UNSUPPORTED;
   if (block_size <= 0 || block_size % 16 != 0 || block_size > 1024) return PA_ERR_BLOCK_SIZE;
   if (num_tokens == 0) return PA_OK;

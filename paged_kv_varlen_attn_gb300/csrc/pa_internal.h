@@ -23,12 +23,19 @@ constexpr int kTcMinRows = 32;
 constexpr int kTcTileRows = 128;   // TMEM lanes of one prefill Q tile (the MMA M dimension)
 // A prefill Q tile holds whole tokens: the largest multiple of G packed rows
 // that fits the 128 TMEM lanes (128 rows when G divides 128; 126 for G = 3,
-// 7 or 42). A work item is two such tiles. Segments of groups wider than 128
-// heads run on the split-KV kernel (tc_tile_rows = 0).
+// 7 or 42). A work item is two such tiles, or one at head size 256 (its O
+// alone takes 256 of the 512 TMEM columns). Segments of groups wider than
+// 128 heads run on the split-KV kernel (tc_tile_rows = 0).
 __host__ __device__ constexpr int tc_tile_rows(int G) {
   return G >= 1 && G <= kTcTileRows ? (kTcTileRows / G) * G : 0;
 }
-__host__ __device__ constexpr int tc_item_rows(int G) { return 2 * tc_tile_rows(G); }
+__host__ __device__ constexpr int tc_tiles(int D) { return D > 128 ? 1 : 2; }
+__host__ __device__ constexpr int tc_item_rows(int G, int D) {
+  return tc_tiles(D) * tc_tile_rows(G);
+}
+// Head size 256 runs every segment on the tensor-core kernel (the split-KV
+// kernel's register tiles are sized for head sizes up to 128).
+constexpr int kMaxHeadSplit = 128;
 constexpr int kKeyTile = 64;       // keys per pipeline stage / split granularity
 // Smallest KV split (keys) per class. A split-KV block spends a few
 // microseconds before its first tile arrives, about the time it takes to
@@ -70,7 +77,9 @@ struct PlanArgs {
   int kv_len_cap;        // keys addressable through a block_table row
   int max_q, max_k;      // host bounds (for the BAD_SEQLEN check)
   int G, H_kv;
+  int D;                 // head size (sets the prefill kernel's rows per item)
   int tc_enabled;
+  int tc_min_rows;       // segments with more packed rows take the prefill kernel
   int causal;
   int target0, target1;
   int items_bound0, items_bound1, slots_bound0, slots_bound1;

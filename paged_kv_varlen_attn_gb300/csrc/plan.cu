@@ -67,10 +67,10 @@ constexpr int kPlanSmemSegs = 1024;   // segment tables kept in shared memory up
 
 // Size bucket of work item (segment s, row tile rt, split j): the number of
 // 64-key tiles the attention kernel will process for it (capped).
-__device__ __forceinline__ int item_bucket(int s, int rt, int j, int4 g, int chunk, int G,
+__device__ __forceinline__ int item_bucket(int s, int rt, int j, int4 g, int chunk, int G, int D,
                                            int causal) {
   const int cls = g.w, q_len = g.y, kv = g.z;
-  const int R = cls ? tc_item_rows(G) : kRowsSplit;
+  const int R = cls ? tc_item_rows(G, D) : kRowsSplit;
   const int rows = q_len * G;
   const int last_row = min(rows, (rt + 1) * R) - 1;
   const int kb = j * chunk;
@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (P.check_cascade && q_len > kv) bad |= PA_DEV_CASCADE;
     if (bad) flag_status(P.status, bad);
     const int rows = q_len * G;
-    const int cls = (P.tc_enabled && rows > kTcMinRows) ? 1 : 0;
-    const int rpi = cls ? tc_item_rows(G) : kRowsSplit;
+    const int cls = (P.tc_enabled && rows > P.tc_min_rows) ? 1 : 0;
+    const int rpi = cls ? tc_item_rows(G, P.D) : kRowsSplit;
     const int nrt = (rows + rpi - 1) / rpi;
     const unsigned long long w = static_cast<unsigned long long>(nrt) * static_cast<unsigned>(kv);
     if (cls) w1 += w; else w0 += w;
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (s < nseg) {
       const int4 g = geo_tab[s];
       cls = g.w;
-      const int R = cls ? tc_item_rows(G) : kRowsSplit;
+      const int R = cls ? tc_item_rows(G, P.D) : kRowsSplit;
       const int nrt = (g.y * G + R - 1) / R;
       const int kv = g.z;
       const int L = cls ? chunk_max[1] : chunk_max[0];
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const int4 g = geo_tab[s];
     const int local = idx - sp.w;
     const int rt = local / sp.x, j = local - rt * sp.x;
-    atomicAdd(&hist[g.w][item_bucket(s, rt, j, g, sp.z, G, P.causal)], 1);
+    atomicAdd(&hist[g.w][item_bucket(s, rt, j, g, sp.z, G, P.D, P.causal)], 1);
     if (j == 0 && (sp.x > 1 || P.partials_only)) {
       const int grp = sp.y + rt * sp.x;
       const int sbound = g.w ? P.slots_bound1 : P.slots_bound0;
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const int local = idx - sp.w;
     const int rt = local / sp.x, j = local - rt * sp.x;
     const int cls = g.w;
-    const int pos = atomicAdd(&hist[cls][item_bucket(s, rt, j, g, sp.z, G, P.causal)], 1);
+    const int pos = atomicAdd(&hist[cls][item_bucket(s, rt, j, g, sp.z, G, P.D, P.causal)], 1);
     if (pos < (cls ? P.items_bound1 : P.items_bound0))
       (cls ? items1 : items0)[pos] = make_int4(s, rt, j, 0);
   }

@@ -81,7 +81,11 @@ def _varlen(lib, **kw):
     (dict(bs=0), pa.PA_ERR_BLOCK_SIZE),
     (dict(bs=2048), pa.PA_ERR_BLOCK_SIZE),
     (dict(D=96), pa.PA_ERR_UNSUPPORTED),
-    (dict(D=256), pa.PA_ERR_UNSUPPORTED),
+    (dict(D=512), pa.PA_ERR_UNSUPPORTED),
+    (dict(D=256, qs=32 * 256, cbs=16 * 8 * 256, scale=-0.1),
+     pa.PA_ERR_UNSUPPORTED),                            # D 256 runs on the prefill kernel only,
+    (dict(D=256, H=200, Hk=1, qs=200 * 256, cbs=16 * 256),
+     pa.PA_ERR_UNSUPPORTED),                            # which needs scale > 0 and G <= 128
     (dict(dtype=2), pa.PA_ERR_UNSUPPORTED),             # neither bf16 (0) nor f16 (1)
     (dict(H=32, Hk=6), pa.PA_ERR_INVALID_ARG),          # H % H_kv != 0
     (dict(q=None), pa.PA_ERR_INVALID_ARG),
@@ -108,14 +112,18 @@ def test_varlen_host_validation(lib, kw, code):
     dict(H=200, Hk=1),      # a group wider than a 128-lane prefill tile
     dict(scale=0.0),        # any finite softmax scale
     dict(scale=-0.1),
+    dict(D=256),            # head sizes 64, 128 and 256
+    dict(D=256, H=24, Hk=8),
 ])
 def test_varlen_accepts_every_ratio_and_finite_scale(lib, kw):
     """These pass every argument check; with no workspace the call then stops
     at PA_ERR_WORKSPACE (or PA_ERR_CUDA on a machine without a GPU, where the
     SM count cannot be queried) -- either way before anything is launched."""
-    qs = kw.get("H", 32) * 128   # the query row is H x D elements
-    assert _varlen(lib, ws=None, wsb=0, qs=qs, **kw) in (pa.PA_ERR_WORKSPACE, pa.PA_ERR_CUDA)
-    n = lib.pa_varlen_fwd_workspace_size(2, 2, 1, 64, kw.get("H", 32), kw.get("Hk", 8), 128, 16,
+    D = kw.get("D", 128)
+    qs = kw.get("H", 32) * D     # the query row is H x D elements
+    assert _varlen(lib, ws=None, wsb=0, qs=qs, cbs=16 * kw.get("Hk", 8) * D, **kw) in (
+        pa.PA_ERR_WORKSPACE, pa.PA_ERR_CUDA)
+    n = lib.pa_varlen_fwd_workspace_size(2, 2, 1, 64, kw.get("H", 32), kw.get("Hk", 8), D, 16,
                                          152)
     assert n > 0 and n % 256 == 0
 
