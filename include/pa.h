@@ -365,11 +365,13 @@ pa_status pa_varlen_fwd_noalloc(const void* q, int64_t q_token_stride, const voi
  * most 8 packed query rows (decode with GQA <= 8) take q.k on the e4m3
  * tensor MMA, q as two e4m3 terms after a power-of-two row scale (exact for
  * every element of at least 2^-9 of its row's largest); wider items form q.k
- * from f16 q, so there |q| must stay below 65504.
+ * from f16 q, so there |q| must stay below 65504. Segments of more than 32
+ * packed query rows (prefill) run on the tensor-core kernel, which widens
+ * each e4m3 K/V tile to f16 in shared memory (exact) and multiplies it with
+ * f16 q and f16 P; shorter ones (decode) on the split-KV kernel.
  * Layout: the NHD pools of pa_reshape_and_cache with 1-byte elements;
  * cache_block_stride is in elements (= bytes) and a multiple of 16.
- * head_size must be 128 (PA_ERR_UNSUPPORTED otherwise). Every FP8 segment
- * runs on the split-KV kernel (warp-level MMA), including long prefills.
+ * head_size must be 128 (PA_ERR_UNSUPPORTED otherwise).
  */
 typedef struct pa_kv_fp8 {
   const float* k_scale; /* device float32 [num_kv_heads], finite and > 0 (not checked) */

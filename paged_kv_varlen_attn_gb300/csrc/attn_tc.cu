@@ -83,6 +83,30 @@ struct TcCfg {
   static constexpr int O_COL = 256;
   static constexpr float RESCALE_LOG2 = 8.0f;
 };
+// FP8 (e4m3) pools, head size 128: the e4m3 K/V tiles land by TMA in a ring
+// of their own; two control warps widen each tile (exactly) to f16 into K and
+// V tiles laid out as the bf16 kernel's TMA tiles, where the same kind::f16
+// MMAs read them (Q is f16 too, P is f16). Shared memory: Q 64 KB, one
+// widened K tile (32 KB), two widened V tiles (64 KB: V(t + 1) is widened
+// while the P V products of tile t still read V(t)), two e4m3 stages of
+// 32 KB: 224 KB. Measured on the 70B prefill: one K and one V buffer with
+// two e4m3 stages 668 TFLOP/s (before the widening loop's addressing was
+// hoisted), two of each with one stage 820, this layout 831, two K and one V
+// 621.
+struct TcFp8 {
+  using C = TcCfg<128>;
+  static constexpr int KBUF = 1, VBUF = 2;                // widened K / V buffers
+  static constexpr int OFF_KW = C::TILES * C::Q_TILE;     // widened K tiles
+  static constexpr int OFF_VW = OFF_KW + KBUF * C::KV_TILE;   // widened V tiles
+  static constexpr int OFF_R8 = OFF_VW + VBUF * C::KV_TILE;   // e4m3 ring
+  static constexpr int TILE8 = C::BN * 128;               // 128 keys x 128 bytes
+  static constexpr int STAGE8 = 2 * TILE8;
+  static constexpr int STAGES8 = 2;                       // e4m3 ring stages
+  static constexpr int OFF_BAR = OFF_R8 + STAGES8 * STAGE8;
+  static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
+  static constexpr int CONV_THREADS = 64;                 // warps 2 and 3
+};
+static_assert(TcFp8::SMEM_BYTES <= 227 * 1024, "the FP8 layout fits shared memory");
 static_assert(kTcTileRows == TcCfg<128>::BM, "a Q tile spans the 128 TMEM lanes");
 static_assert(TcCfg<256>::SMEM_BYTES <= 227 * 1024, "head size 256 fits shared memory");
 static_assert(TcCfg<256>::O_COL + 256 <= TcCfg<256>::TMEM_COLS, "head size 256 fits TMEM");
@@ -95,6 +119,10 @@ struct TcBars {
   uint64_t p_full[2][2];   // [half][tile]: P of keys [64 half, +64) of the tile is in TMEM
   uint64_t pv_done[2];     // [tile]: O += P V of the current key tile completed
   uint64_t drain;
+  // FP8 pools: Q converted to f16; [buffer]: widened K / V tile ready (64
+  // converter arrivals), widened K / V buffer free again (MMA commit).
+  // Buffer b of K holds tiles b, b + KBUF, ... (phase t / KBUF); V likewise.
+  uint64_t q_conv, kw_full[2], kw_free[2], vw_full[2], vw_free[2];
   uint32_t tmem_base;
   volatile int abort;
   volatile int last;
@@ -127,7 +155,57 @@ __device__ __forceinline__ bool zero_v_tail(TcBars* bars, uint8_t* smem, int t, 
   return true;
 }
 
-template <int D, bool F16>
+// Widen an e4m3 K or V tile (BN keys x 128 bytes, TMA 128-byte swizzle:
+// 16-byte chunk j of row r at r*128 + ((j ^ r%8) << 4)) to f16 in the layout
+// of a bf16 TMA tile (two halves of BN rows x 128 bytes; 8-element chunk c
+// of row r at r*128 + ((c ^ r%8) << 4)). Every e4m3 value is exact in f16.
+// Rows from zero_from on are written as zeros (keys past the sequence end:
+// their bytes are arbitrary and P = 0 there must not meet a NaN).
+__device__ __forceinline__ void widen_e4m3_tile(const uint8_t* src, uint8_t* dst, int ct,
+                                                int zero_from) {
+  using C = TcCfg<128>;
+  static_assert(TcFp8::CONV_THREADS % 8 == 0, "a thread keeps one chunk column");
+  // Thread ct takes chunk column jj = ct % 8 of rows ct / 8, ct / 8 + 8, ...;
+  // rows 8 apart share their swizzle phase, so every address below is a
+  // per-thread base plus a multiple of 8 rows.
+  const int jj = ct & 7, r0 = ct >> 3;
+  const int s_sw = (jj ^ (r0 & 7)) << 4;                     // e4m3 chunk jj
+  const int c0 = 2 * (jj & 3);                               // f16 chunks c0, c0 + 1
+  const int d_lo = ((c0 ^ (r0 & 7)) << 4), d_hi = (((c0 + 1) ^ (r0 & 7)) << 4);
+  const uint8_t* sp = src + r0 * 128 + s_sw;
+  uint8_t* dp = dst + (jj >> 2) * C::KV_HALF + r0 * 128;
+  constexpr int kStep = TcFp8::CONV_THREADS / 8;             // rows between a thread's chunks
+#pragma unroll 4
+  for (int r = r0; r < C::BN; r += kStep, sp += kStep * 128, dp += kStep * 128) {
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    if (r < zero_from) {
+      const uint4 w = *reinterpret_cast<const uint4*>(sp);
+      lo = make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
+                      e4m3x2_to_f16x2(w.y >> 16));
+      hi = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
+                      e4m3x2_to_f16x2(w.w >> 16));
+    }
+    *reinterpret_cast<uint4*>(dp + d_lo) = lo;
+    *reinterpret_cast<uint4*>(dp + d_hi) = hi;
+  }
+}
+
+// bf16 Q tiles to f16 in place (same layout; exact for |q| in f16's normal
+// range, which the FP8 path requires of q).
+__device__ __forceinline__ void q_bf16_to_f16(uint8_t* q, int bytes, int ct) {
+  for (int i = ct * 16; i < bytes; i += TcFp8::CONV_THREADS * 16) {
+    uint4 w = *reinterpret_cast<const uint4*>(q + i);
+    uint32_t* x = &w.x;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = Elem<false>::unpack(x[k]);
+      x[k] = pack_f16(f.x, f.y);
+    }
+    *reinterpret_cast<uint4*>(q + i) = w;
+  }
+}
+
+template <int D, bool F16, bool FP8>
 __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars, uint8_t* smem,
                                                 uint32_t tmem, int X, int q_start, int q_len,
                                                 int kv_len, int kb, int ke, int ntiles, int row0,
@@ -150,7 +228,9 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   const int head = hk * G + (pr - ti * G);
   // Last key this row may see (bottom-right causal), or the last key.
   const int lim = !rvalid ? -1 : (a.causal ? kv_len - q_len + ti : kv_len - 1);
-  const float sl2 = a.scale_log2;
+  // FP8 pools: scores use the stored codes, so k_scale joins the softmax
+  // scale and v_scale the final normalisation.
+  const float sl2 = FP8 ? a.scale_log2 * __ldg(a.k_scale + hk) : a.scale_log2;
   const int tid = threadIdx.x - 128 - X * 128;     // 0..127 within the warpgroup
   float m_use = -INFINITY, l = 0.f;
   bool ok = true;
@@ -228,12 +308,12 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
         ffma2(y0, y1, xs[c * 32 + e], xs[c * 32 + e + 1], sl2, sl2, -mu, -mu);
         const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
         fadd2(ls[e & 7], ls[(e + 1) & 7], ls[e & 7], ls[(e + 1) & 7], p0, p1);
-        pk[e >> 1] = E::pack(p0, p1);
+        pk[e >> 1] = Elem<F16 || FP8>::pack(p0, p1);   // P has the MMA's operand type
       }
       tmem_st16(tm_row + s_col + c * 16, pk);
       if (c == C::BN / 64 - 1) {   // the first half of the tile's keys
         tmem_wait_st();
-        if (X == 0 && key0 + C::BN > kv_len)   // warp-uniform condition and result
+        if (!FP8 && X == 0 && key0 + C::BN > kv_len)   // warp-uniform condition and result
           ok = __all_sync(0xffffffffu, zero_v_tail<D>(bars, smem, t, key0, kv_len, tid));
         if (!ok) break;
         tc_fence_before();
@@ -265,7 +345,7 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   float mf = m_use, lf = ok ? l : 0.f, of = 1.f;
   if (a.sinks && !partial && rvalid) of = add_sink(mf, lf, __ldg(a.sinks + head) * kLog2e);
   const bool any = ok && lf > 0.f;
-  const float inv_l = any ? of / lf : 0.f;
+  const float inv_l = any ? (FP8 ? __ldg(a.v_scale + hk) : 1.f) * of / lf : 0.f;
   float lse_nat = any ? (mf + fast_log2(lf)) * kLn2 : -INFINITY;
   const int slot = slot_base + rt * nsplit + j;
   const int64_t srow = slot_row(a, slot, hk, rl);
@@ -339,15 +419,16 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   }
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool FP8>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ AttnArgs a) {
   using C = TcCfg<D>;
+  static_assert(!FP8 || D == 128, "FP8 pools: head size 128");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  TcBars* bars = reinterpret_cast<TcBars*>(smem + C::OFF_BAR);
+  TcBars* bars = reinterpret_cast<TcBars*>(smem + (FP8 ? TcFp8::OFF_BAR : C::OFF_BAR));
 
   pdl_enter(a.pdl_first);
   if (static_cast<int>(blockIdx.x) >= a.header[1] || call_aborted(a)) return;
@@ -373,7 +454,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < 2 * C::STAGES; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      // FP8: the converter warps free an e4m3 stage once they widened it.
+      mbar_init(&bars->kv_empty[s], FP8 ? TcFp8::CONV_THREADS : 1);
+    }
+    mbar_init(&bars->q_conv, TcFp8::CONV_THREADS);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->kw_full[b], TcFp8::CONV_THREADS);
+      mbar_init(&bars->vw_full[b], TcFp8::CONV_THREADS);
+      mbar_init(&bars->kw_free[b], 1);
+      mbar_init(&bars->vw_free[b], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->s_full[x], 1);
@@ -426,9 +515,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       }
       const int32_t* bt_row =
           a.bt + static_cast<int64_t>(seg) * a.bt_row_stride + a.bt_col_offset;
-      produce_kv<C::BN, C::HALVES, C::STAGES, true>(&tmK, &tmV, a, smem + C::OFF_KV, bars->kv_full,
-                                              bars->kv_empty, &bars->abort, bars->issued,
-                                              bt_row, hk, kb, kv_len, ntiles, lane);
+      if constexpr (FP8) {
+        static_assert(2 * TcFp8::STAGES8 <= 8, "the ring barrier arrays hold 8");
+        produce_kv<C::BN, 1, TcFp8::STAGES8, true>(&tmK, &tmV, a, smem + TcFp8::OFF_R8,
+                                                   bars->kv_full, bars->kv_empty, &bars->abort,
+                                                   bars->issued, bt_row, hk, kb, kv_len, ntiles,
+                                                   lane);
+      } else {
+        produce_kv<C::BN, C::HALVES, C::STAGES, true>(&tmK, &tmV, a, smem + C::OFF_KV,
+                                                      bars->kv_full, bars->kv_empty, &bars->abort,
+                                                      bars->issued, bt_row, hk, kb, kv_len,
+                                                      ntiles, lane);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -439,18 +537,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // address plus c / 16; shared addresses stay below 2^18, so the 14-bit
     // field cannot carry).
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idesc_s = mma_idesc(C::BM, C::BN, false, Elem<F16>::kTcFormat);
-      constexpr uint32_t idesc_o = mma_idesc(C::BM, D, true, Elem<F16>::kTcFormat);
-      const uint32_t sKV = smem_u32(smem + C::OFF_KV);
+      // Operand type: the activations' (bf16 or f16), or f16 over FP8 pools.
+      constexpr uint32_t fmt = Elem<F16 || FP8>::kTcFormat;
+      constexpr uint32_t idesc_s = mma_idesc(C::BM, C::BN, false, fmt);
+      constexpr uint32_t idesc_o = mma_idesc(C::BM, D, true, fmt);
+      // K / V operands: the ring stage (2-byte pools) or the widened tiles
+      // (FP8 pools: one K and one V buffer, stage offset 0).
+      const uint32_t sKV = smem_u32(smem + (FP8 ? TcFp8::OFF_KW : C::OFF_KV));
+      // tile t uses ring stage t % STAGES (2-byte pools) or widened K buffer
+      // t % KBUF and V buffer t % VBUF (FP8 pools).
+      constexpr int kStageBytes = FP8 ? C::KV_TILE : C::STAGE;
       const uint64_t qdesc[2] = {smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024),
                                  smem_desc_sw128(smem_u32(smem + C::OFF_Q + C::Q_TILE), 16, 1024)};
       const uint64_t kdesc0 = smem_desc_sw128(sKV, 16, 1024);
-      const uint64_t vdesc0 = smem_desc_sw128(sKV + C::KV_TILE, C::KV_HALF, 1024);
+      const uint64_t vdesc0 = smem_desc_sw128(sKV + (FP8 ? TcFp8::OFF_VW - TcFp8::OFF_KW
+                                                        : C::KV_TILE),
+                                              C::KV_HALF, 1024);
       // S_X(t) = Q_X K(t)^T into TMEM columns [128 X, 128 X + 128).
       auto issue_s = [&](int x, int t) {
         tc_fence_after();
         const uint64_t qd = qdesc[x];
-        const uint64_t kd = kdesc0 + static_cast<uint32_t>((t % C::STAGES) * (C::STAGE >> 4));
+        constexpr int kBufs = FP8 ? TcFp8::KBUF : C::STAGES;
+        const uint64_t kd = kdesc0 + static_cast<uint32_t>((t % kBufs) * (kStageBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::Q_HALF + (kk & 3) * 32) >> 4;
@@ -463,7 +571,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       // (the first 64 columns of S_X); the second half commits pv_done.
       auto issue_pv = [&](int x, int t, int h) {
         tc_fence_after();
-        const uint64_t vd = vdesc0 + static_cast<uint32_t>((t % C::STAGES) * (C::STAGE >> 4));
+        constexpr int vBufs = FP8 ? TcFp8::VBUF : C::STAGES;
+        const uint64_t vd = vdesc0 + static_cast<uint32_t>((t % vBufs) * (kStageBytes >> 4));
 #pragma unroll
         for (int k4 = 0; k4 < C::BN / 32; ++k4) {
           const int kk = h * (C::BN / 32) + k4;
@@ -481,26 +590,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       // P_X(t) V, so O_X is final when the softmax sees S_X(t+1). K and V
       // have their own ring barriers: K(t) is released once both S(t) are
       // done, so its stage refills while V(t) is still in use.
+      // FP8 pools: K(t) / V(t) are ready when the converter warps have
+      // widened them (kw_full / vw_full, phase t); the widened buffers are
+      // released by commits after the last S / P V that reads them (kw_free /
+      // vw_free), and the converters free the e4m3 ring stages themselves.
       constexpr int S_ = C::STAGES;
-      bool ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->kv_full[0], 0);
+      auto k_ready = [&](int t) {
+        if constexpr (FP8)
+          return mbar_wait(&bars->kw_full[t % TcFp8::KBUF], (t / TcFp8::KBUF) & 1);
+        if (!mbar_wait(&bars->kv_full[t % S_], (t / S_) & 1)) return false;
+        bars->consumed[0] = t + 1;
+        return true;
+      };
+      auto v_ready = [&](int t) {
+        if constexpr (FP8)
+          return mbar_wait(&bars->vw_full[t % TcFp8::VBUF], (t / TcFp8::VBUF) & 1);
+        if (!mbar_wait(&bars->kv_full[S_ + t % S_], (t / S_) & 1)) return false;
+        bars->consumed[1] = t + 1;
+        return true;
+      };
+      auto k_release = [&](int t) {
+        tc_commit(FP8 ? &bars->kw_free[t % TcFp8::KBUF] : &bars->kv_empty[t % S_]);
+      };
+      auto v_release = [&](int t) {
+        tc_commit(FP8 ? &bars->vw_free[t % TcFp8::VBUF] : &bars->kv_empty[S_ + t % S_]);
+      };
+      bool ok = mbar_wait(FP8 && !F16 ? &bars->q_conv : &bars->q_full, 0) && k_ready(0);
       if (ok) {
-        bars->consumed[0] = 1;
         issue_s(0, 0);
         if (two) issue_s(1, 0);
-        tc_commit(&bars->kv_empty[0]);
+        k_release(0);
       }
       for (int t = 0; ok && t < ntiles; ++t) {
         if (bars->abort) { ok = false; break; }
         const bool more = t + 1 < ntiles;
         if (!(ok = mbar_wait(&bars->p_full[0][0], t & 1))) break;
-        if (!(ok = mbar_wait(&bars->kv_full[S_ + t % S_], (t / S_) & 1))) break;
-        bars->consumed[1] = t + 1;
+        if (!(ok = v_ready(t))) break;
         issue_pv(0, t, 0);
         if (!(ok = mbar_wait(&bars->p_full[1][0], t & 1))) break;
         issue_pv(0, t, 1);
         if (more) {
-          if (!(ok = mbar_wait(&bars->kv_full[(t + 1) % S_], ((t + 1) / S_) & 1))) break;
-          bars->consumed[0] = t + 2;
+          if (!(ok = k_ready(t + 1))) break;
           issue_s(0, t + 1);
         }
         if (two) {
@@ -509,10 +639,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           if (!(ok = mbar_wait(&bars->p_full[1][1], t & 1))) break;
           issue_pv(1, t, 1);
         }
-        tc_commit(&bars->kv_empty[S_ + t % S_]);
+        v_release(t);
         if (more) {
           if (two) issue_s(1, t + 1);
-          tc_commit(&bars->kv_empty[(t + 1) % S_]);
+          k_release(t + 1);
         }
       }
       if (!ok) {
@@ -523,13 +653,56 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       tc_commit(&bars->drain);
       mbar_wait(&bars->drain, 0);
     }
+  } else if (FP8 && ntiles > 0) {
+    // ------------------------------------------------------------ converters
+    // Warps 2 and 3 (FP8 pools): Q to f16 once (bf16 activations), then per
+    // key tile t widen the e4m3 K(t) into the K buffer once the S products
+    // of tile t - 1 have read it, and V(t) (rows past the sequence end as
+    // zeros) into the V buffer once the P V products of tile t - 1 have;
+    // each e4m3 ring stage is freed as soon as it is widened.
+    const int ct = threadIdx.x - 64;   // 0 .. 63
+    constexpr int S8 = TcFp8::STAGES8;
+    bool ok = true;
+    if constexpr (!F16) {
+      ok = mbar_wait(&bars->q_full, 0);
+      if (ok) {
+        q_bf16_to_f16(smem + C::OFF_Q, (two ? 2 : 1) * C::Q_TILE, ct);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&bars->q_conv);
+      }
+    }
+    for (int t = 0; ok && t < ntiles; ++t) {
+      if (bars->abort) { ok = false; break; }
+      const uint8_t* k8 = smem + TcFp8::OFF_R8 + (t % S8) * TcFp8::STAGE8;
+      if (!(ok = mbar_wait(&bars->kv_full[t % S8], (t / S8) & 1))) break;
+      if (ct == 0) bars->consumed[0] = t + 1;
+      // buffer t % 2 last held tile t - 2
+      constexpr int KB = TcFp8::KBUF, VB = TcFp8::VBUF;
+      if (t >= KB && !(ok = mbar_wait(&bars->kw_free[t % KB], ((t / KB) - 1) & 1))) break;
+      widen_e4m3_tile(k8, smem + TcFp8::OFF_KW + (t % KB) * C::KV_TILE, ct, C::BN);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&bars->kw_full[t % KB]);
+      mbar_arrive(&bars->kv_empty[t % S8]);
+      if (!(ok = mbar_wait(&bars->kv_full[S8 + t % S8], (t / S8) & 1))) break;
+      if (ct == 0) bars->consumed[1] = t + 1;
+      if (t >= VB && !(ok = mbar_wait(&bars->vw_free[t % VB], ((t / VB) - 1) & 1))) break;
+      widen_e4m3_tile(k8 + TcFp8::TILE8, smem + TcFp8::OFF_VW + (t % VB) * C::KV_TILE, ct,
+                      kv_len - (kb + t * C::BN));
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&bars->vw_full[t % VB]);
+      mbar_arrive(&bars->kv_empty[S8 + t % S8]);
+    }
+    if (!ok) {
+      abort_call(a);
+      bars->abort = 1;
+    }
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int X = (warp - 4) >> 2;   // warps 4-7: tile A, 8-11: tile B
     if (X == 0 || two)
-      tc_softmax_tile<D, F16>(a, bars, smem, tmem, X, q_start, q_len, kv_len, kb, ke, ntiles, row0,
+      tc_softmax_tile<D, F16, FP8>(a, bars, smem, tmem, X, q_start, q_len, kv_len, kb, ke, ntiles, row0,
                          R, hk, nsplit, slot_base, rt, j);
     if (nsplit > 1 && !a.partials_only) {
       // Both warpgroups (256 threads) take part, active tile or not.
@@ -555,8 +728,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // After an abort, wait (bounded) for the copies still in flight.
     if (ntiles > 0) mbar_wait(&bars->q_full, 0);
     for (int p = 0; p < 2; ++p)
-      for (int t = bars->consumed[p]; t < bars->issued[p]; ++t)
-        if (!mbar_wait(&bars->kv_full[p * C::STAGES + t % C::STAGES], (t / C::STAGES) & 1)) break;
+      for (int t = bars->consumed[p]; t < bars->issued[p]; ++t) {
+        constexpr int STG = FP8 ? TcFp8::STAGES8 : C::STAGES;   // ring stages
+        if (!mbar_wait(&bars->kv_full[p * STG + t % STG], (t / STG) & 1)) break;
+      }
   }
   __syncthreads();
   if (warp == 1) {
@@ -565,7 +740,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   }
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool FP8 = false>
 static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const CUtensorMap& tmQ, const AttnArgs& a, int items_bound,
                                cudaStream_t st) {
@@ -580,22 +755,23 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
   if (e != cudaSuccess) return e;
   const bool known = dev >= 0 && dev < kMaxDevices;
   if (!known || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(attn_tc_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES);
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, F16, FP8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             FP8 ? TcFp8::SMEM_BYTES : C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (known) configured[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(items_bound, a.H_kv);
   cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.dynamicSmemBytes = FP8 ? TcFp8::SMEM_BYTES : C::SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, F16>, tmK, tmV, tmQ, a);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, F16, FP8>, tmK, tmV, tmQ, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -603,6 +779,10 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
 cudaError_t launch_attn_tc(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
                            const AttnArgs& a, int items_bound, cudaStream_t st) {
   if (items_bound <= 0) return cudaSuccess;
+  if (a.kv_fp8) {   // head size 128 (checked on the host)
+    if (a.f16) return launch_tc_d<128, true, true>(tmK, tmV, tmQ, a, items_bound, st);
+    return launch_tc_d<128, false, true>(tmK, tmV, tmQ, a, items_bound, st);
+  }
   if (a.f16) {
     if (a.D == 256) return launch_tc_d<256, true>(tmK, tmV, tmQ, a, items_bound, st);
     if (a.D == 128) return launch_tc_d<128, true>(tmK, tmV, tmQ, a, items_bound, st);

@@ -40,7 +40,7 @@ struct PassDims {
   int G, H, H_kv, D;
   int sms;
   bool all_partial = false;   // every item keeps a partial-state slot (cascade prefix pass)
-  bool kv_fp8 = false;        // FP8 pools: every segment runs on the split-KV kernel
+  bool kv_fp8 = false;        // FP8 pools (head size 128; the prefill kernel widens them)
   // The prefill kernel takes the row maximum of the raw scores and scales it
   // afterwards, which needs softmax_scale > 0; a zero or negative scale runs
   // every segment on the split-KV kernel (which scales before the maximum).
@@ -53,8 +53,7 @@ struct PassDims {
 int tc_min_rows(int D) { return D > kMaxHeadSplit ? 0 : kTcMinRows; }
 bool pass_has_tc(const PassDims& d) {
   const long long rows = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
-  return kTcAvailable && d.tc_allowed && !d.kv_fp8 && tc_tile_rows(d.G) > 0 &&
-         rows > tc_min_rows(d.D);
+  return kTcAvailable && d.tc_allowed && tc_tile_rows(d.G) > 0 && rows > tc_min_rows(d.D);
 }
 bool pass_has_split(const PassDims& d) {
   return d.D <= kMaxHeadSplit && (!d.single || !pass_has_tc(d));

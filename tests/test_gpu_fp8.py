@@ -129,6 +129,13 @@ CASES = [
     (215, 7, 32, 8, 128, 33, 1500, True, 0.5),   # page 128, ragged
     (216, 5, 16, 16, 48, 20, 200, True, 0.3),    # page 48 (boxes of 16 rows)
     (219, 4, 32, 2, 16, 1, 700, True, 1.0),      # decode, GQA 16: 16-row items
+    # prefill segments (more than 32 packed rows): the tensor-core kernel
+    # with the e4m3 tiles widened to f16 in shared memory
+    (231, 2, 8, 2, 16, 300, 1100, True, 0.0),    # several Q tiles, prior context
+    (232, 3, 32, 8, 128, 200, 3000, True, 0.0),  # long keys: KV splits, page 128
+    (233, 2, 24, 8, 16, 150, 400, True, 0.0),    # G = 3: 126-row tiles
+    (234, 3, 16, 2, 32, 100, 300, False, 0.0),   # non-causal
+    (235, 4, 8, 1, 48, 70, 260, True, 0.3),      # G = 8, page 48, with decode rows
 ]
 
 
@@ -226,3 +233,40 @@ def test_fp8_decode_llama8b_sampled():
         b2, r2 = divmod(int(slots[i]), bs)
         assert torch.equal(kc[b, r].cpu(), kc_s[b2, r2])
         assert torch.equal(vc[b, r].cpu(), vc_s[b2, r2])
+
+
+def test_fp8_long_context_prefill_sampled():
+    """The 70B prefill shape (4 causal x 4096 queries on 28,672 prior keys,
+    64/8 heads, page 128) on e4m3 pools: the tensor-core kernel over widened
+    tiles, checked on sampled rows of every sequence (first, last, tile
+    boundaries and seeded random rows)."""
+    wl = W.long_context_70b_prefill()
+    out, lse, kc, vc = run_fp8(wl)
+    seqs = list(range(wl.num_seqs))
+    pages = sorted({p for s in seqs for p in wl.pages_of(s)})
+    remap = {p: i for i, p in enumerate(pages)}
+    kp, vp = wl.fp8_pool_pages(0, pages), wl.fp8_pool_pages(1, pages)
+    kc_s = torch.stack([kp[p] for p in pages])
+    vc_s = torch.stack([vp[p] for p in pages])
+    bt = torch.full_like(wl.block_table, W.INT32_MAX)
+    for s in seqs:
+        ps = wl.pages_of(s)
+        bt[s, :len(ps)] = torch.tensor([remap[p] for p in ps], dtype=torch.int32)
+    bs = wl.block_size
+    slots = torch.tensor([remap[int(x) // bs] * bs + int(x) % bs for x in wl.slot_mapping],
+                         dtype=torch.int64)
+    oracle.reshape_and_cache_e4m3(wl.k_new, wl.v_new, slots, kc_s, vc_s, wl.kv_scales(0),
+                                  wl.kv_scales(1))
+    g = torch.Generator().manual_seed(17)
+    rows = {}
+    for s in seqs:
+        n = wl.q_lens[s]
+        pick = {0, 15, 16, 127, 128, n // 2, n - 1} | set(int(x) for x in
+                                                         torch.randint(0, n, (12,), generator=g))
+        rows[s] = sorted(pick)
+    ref_o, ref_l = oracle.varlen_attention_e4m3(wl.q, kc_s, vc_s, wl.cu_seqlens_q, wl.seqused_k,
+                                                bt, wl.softmax_scale, True, wl.kv_scales(0),
+                                                wl.kv_scales(1), rows=rows)
+    cu = wl.cu_seqlens_q.tolist()
+    tokens = torch.tensor([cu[s] + r for s in seqs for r in rows[s]])
+    assert_close(out, lse, ref_o[tokens], ref_l[:, tokens], tokens=tokens)
