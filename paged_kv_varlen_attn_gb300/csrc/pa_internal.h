@@ -80,6 +80,7 @@ struct PlanArgs {
   int D;                 // head size (sets the prefill kernel's rows per item)
   int tc_enabled;
   int tc_min_rows;       // segments with more packed rows take the prefill kernel
+  int min_chunk_tc;      // smallest KV split of the prefill kernel's items (keys)
   int causal;
   int target0, target1;
   int items_bound0, items_bound1, slots_bound0, slots_bound1;

@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (W == 0) L = 0;
     else if (W < 0xffffffffull - tg) L = (static_cast<unsigned>(W) + tg - 1) / tg;
     else L = (W + tg - 1) / tg;
-    const int min_chunk = c ? kMinChunkTc : kMinChunkSplit;
+    const int min_chunk = c ? P.min_chunk_tc : kMinChunkSplit;
     if (L < static_cast<unsigned long long>(min_chunk)) L = min_chunk;
     L = (L + kKeyTile - 1) / kKeyTile * kKeyTile;
     if (L > 0x40000000ull) L = 0x40000000ull;
