@@ -104,21 +104,49 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t
 // Scatter into an FP8 (e4m3) cache ("FlashAttention と FlashInfer" 役割 and
 // 境界と失敗: FP8 KV cache with per-head quant scales). Same warp-per-token
 // walk as above; a lane reads 8 bf16 or f16 values (16 bytes) of one head, divides
-// them by that KV head's scale (IEEE float division, correctly rounded) and
-// writes the 8 e4m3 bytes (round to nearest even, saturating at +-448).
+// them by that KV head's scale (the IEEE float32 quotient, correctly rounded)
+// and writes the 8 e4m3 bytes (round to nearest even, saturating at +-448).
 // ---------------------------------------------------------------------------
+// x / s correctly rounded to float32 wherever the quotient decides an e4m3
+// code, from y = RN(1/s): q0 = RN(x y), the remainder r = x - q0 s (exact,
+// one FMA) and q = RN(q0 + r y). By Markstein's theorem (y within half an
+// ulp of 1/s and q0 within one ulp of x/s make RN(q0 + r y) the correctly
+// rounded quotient, as long as r neither underflows nor the quotient
+// overflows), q is RN(x/s). Exact quotients (r = 0, which keeps the sign of
+// a zero) and |q0| >= 512, infinities and NaN take q0: every quotient of at
+// least 464 saturates to the same code. With 2^-32 <= |s| <= 2^32 the
+// reciprocal is normal and every quotient of at least 2^-11 (below that the
+// code is a signed zero either way) has a normal, hence exact, remainder;
+// other scales take the IEEE division. Three instructions per element
+// instead of a division.
+__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
+  const float q0 = x * y;
+  const float r = fmaf(-q0, s, x);
+  return (r == 0.f || !(fabsf(q0) < 512.f)) ? q0 : fmaf(r, y, q0);
+}
+
 template <bool F16>
 __device__ __forceinline__ uint2 quantize8(uint4 x, float s) {
   const uint32_t h[4] = {x.x, x.y, x.z, x.w};
-  uint32_t w[2];
+  float v[8];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float2 a = Elem<F16>::unpack(h[2 * k]);
-    const float2 b = Elem<F16>::unpack(h[2 * k + 1]);
-    w[k] = f32x2_to_e4m3x2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)) |
-           (f32x2_to_e4m3x2(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)) << 16);
+  for (int k = 0; k < 4; ++k) {
+    const float2 a = Elem<F16>::unpack(h[k]);
+    v[2 * k] = a.x;
+    v[2 * k + 1] = a.y;
   }
-  return make_uint2(w[0], w[1]);
+  const float as = fabsf(s);
+  if (as >= 0x1p-32f && as <= 0x1p32f) {
+    const float y = __frcp_rn(s);   // correctly rounded reciprocal
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = div_by_scale(v[k], s, y);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __fdiv_rn(v[k], s);
+  }
+  const uint32_t w0 = f32x2_to_e4m3x2(v[0], v[1]) | (f32x2_to_e4m3x2(v[2], v[3]) << 16);
+  const uint32_t w1 = f32x2_to_e4m3x2(v[4], v[5]) | (f32x2_to_e4m3x2(v[6], v[7]) << 16);
+  return make_uint2(w0, w1);
 }
 
 template <bool F16>

@@ -101,6 +101,40 @@ def test_fp8_scatter_bit_exact(seed, bs, Hk):
                                                  kc_ref[b, r, 0, 5].item(), 0x4A]
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_fp8_scatter_every_value(dtype):
+    """Every bf16 (or f16) value -- zeros, subnormals, infinities and NaNs
+    included -- divided by each of 8 KV-head scales: the edges of the range
+    the kernel divides by reciprocal and correction (2^-32, 2^32), scales
+    outside it (2^-40, 2^40, which divide) and ordinary ones. Bit-exact."""
+    Hk, D, bs = 8, 128, 16
+    T = 65536 // D
+    every = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(dtype)
+    g = torch.Generator().manual_seed(241)
+    k_new = torch.stack([every[torch.randperm(65536, generator=g)].reshape(T, D)
+                         for _ in range(Hk)], dim=1)
+    v_new = torch.stack([every[torch.randperm(65536, generator=g)].reshape(T, D)
+                         for _ in range(Hk)], dim=1)
+    ks = [2.0 ** -32, 2.0 ** 32, 2.0 ** -40, 2.0 ** 40, 0.0123, 1 / 3, 3.7 / 448, 1.0]
+    vs = [0.021, 2.0 ** 40, 1 / 7, 2.0 ** -32, 2.0 ** 32, 2.0 ** -40, 0.5, 255.0]
+    ks = [float(torch.tensor(x, dtype=torch.float32)) for x in ks]
+    vs = [float(torch.tensor(x, dtype=torch.float32)) for x in vs]
+    nb = T // bs + 2
+    slots = torch.randperm(nb * bs, generator=g)[:T].to(torch.int64)
+    kc_ref = torch.zeros((nb, bs, Hk, D), dtype=torch.uint8)
+    vc_ref = kc_ref.clone()
+    oracle.reshape_and_cache_e4m3(k_new, v_new, slots, kc_ref, vc_ref, ks, vs)
+    kc, vc = torch.zeros_like(kc_ref, device=DEV), torch.zeros_like(vc_ref, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa.reshape_and_cache_fp8(k_new.to(DEV), v_new.to(DEV), kc, vc, slots.to(DEV),
+                             torch.tensor(ks, device=DEV), torch.tensor(vs, device=DEV),
+                             dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(kc.cpu(), kc_ref)
+    assert torch.equal(vc.cpu(), vc_ref)
+
+
 def test_fp8_scatter_scalar_scale_and_bad_slot():
     wl = W.random_case(205, num_seqs=3, num_heads=8, num_kv_heads=4, head_size=128,
                        block_size=16, max_q=20, max_kv=60)
