@@ -3,10 +3,10 @@
 The e4m3 code of a new K/V value is that of the IEEE float32 quotient
 x / scale ("FlashAttention と FlashInfer" 境界と失敗: per-head quantization
 scales). The scatter kernel does not divide: from the correctly rounded
-reciprocal y = RN(1/s) it forms q0 = RN(x y), the remainder r = RN(s * -q0 + x)
+reciprocal y = RN(1/s) it forms q0 = RN(x y), the remainder r = RN(q0 * -s + x)
 and q = RN(r y + q0) (Markstein's correction step, P. Markstein, "Computation
 of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
-Dev. 34(1), 1990), keeping q0 where r = 0 or |q0| >= 512, for scales of
+Dev. 34(1), 1990), keeping q0 where q0 = 0 or |q0| >= 512, for scales of
 magnitude 2^-32 .. 2^32 (other scales divide). These tests replay those steps
 in float32 with an exactly rounded FMA and compare, for every bf16 and every
 f16 value and a spread of scales, the quotient bit for bit wherever it can
@@ -43,9 +43,9 @@ def fast_quotient(x, s):
     with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
         y = F32(F32(1.0) / s)                       # RN(1/s)
         q0 = x * y                                  # RN(x y)
-        r = fma32(-q0, np.full_like(x, s), x)
+        r = fma32(q0, np.full_like(x, -s), x)
         corrected = fma32(r, np.full_like(x, y), q0)
-        keep = (r == 0) | ~(np.abs(q0) < 512)
+        keep = (q0 == 0) | ~(np.abs(q0) < 512)
         return np.where(keep, q0, corrected), q0
 
 
