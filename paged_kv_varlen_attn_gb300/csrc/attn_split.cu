@@ -750,6 +750,12 @@ __device__ __forceinline__ void split_consumer_fp8_dec(const AttnArgs& a, uint8_
         va[x] = *reinterpret_cast<const uint2*>(row + (((g >> 1) ^ (key & 7)) << 4));
         vb[x] = *reinterpret_cast<const uint2*>(row + (((4 + (g >> 1)) ^ (key & 7)) << 4));
       }
+      // This warp's reads of the stage are done: release it before the P V
+      // products (123.1 us against 124.0 us on the Llama-8B decode batch;
+      // releasing it before any arithmetic, with every fragment loaded
+      // first, measured 135.7 us).
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[s]);
 #pragma unroll
       for (int w = 0; w < 2; ++w) {
         const uint32_t a01 = w ? va[0].y : va[0].x, a01b = w ? va[1].y : va[1].x;
@@ -769,9 +775,10 @@ __device__ __forceinline__ void split_consumer_fp8_dec(const AttnArgs& a, uint8_
         mma_16816_f16(o[4 * w + 3], e4m3x2_to_f16x2(hi_a01 >> 16), e4m3x2_to_f16x2(hi_b01 >> 16),
                       e4m3x2_to_f16x2(hi_a23 >> 16), e4m3x2_to_f16x2(hi_b23 >> 16), pb0, pb1);
       }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[s]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.empty[s]);
     if (sh.flags[0]) break;
   }
   // Row sums over the eight lanes of each column (the key halves).
