@@ -71,8 +71,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 # ---------------------------------------------------------------------------
 def is_prefill(wl, s, fp8=False):
     """Segments with more than 32 packed query rows run on the tensor-core
-    kernel (bf16 pools; FP8 pools run every segment on the split-KV kernel,
-    but such segments are still counted as the compute-heavy prefill side)."""
+    kernel (for FP8 pools too, over tiles widened to f16)."""
     return wl.q_lens[s] * (wl.num_heads // wl.num_kv_heads) > 32
 
 
@@ -339,23 +338,32 @@ def timed_flushed(fn, n, flush, stream, flush_rd):
 DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
 
 
-def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0, dtype=torch.bfloat16):
+def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0, dtype=torch.bfloat16, fp8=False):
     """The prefill half of the metric on one prefill-only batch: the attention
     call (planner + tensor-core prefill kernel) timed launch by launch with
     CUDA events on the launching stream, SM clocks sampled over the window.
     FLOPs are 4 * D * H per visible (query, key) pair; the fraction is taken
     against the sustained bf16 peak (the launches run back to back for
-    longer than a second), the burst fraction is given beside it."""
+    longer than a second), the burst fraction is given beside it. With fp8
+    the pools hold e4m3 bytes (the kernel widens them to f16 and multiplies
+    at the 16-bit rate, so the same peak applies)."""
     wl = W.CONFIGS[name](dtype=dtype)
     T, H, D = wl.q.shape
-    counts = algorithmic_counts(wl)
-    kc, vc = wl.pool(0, device=dev), wl.pool(1, device=dev)
+    counts = algorithmic_counts(wl, fp8=fp8)
     b = DeviceBatch(wl, dev)
-    pa.reshape_and_cache(b.d["k_new"], b.d["v_new"], kc, vc, b.d["slot_mapping"])
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    ws = pa.alloc_workspace(pa.varlen_fwd_workspace_size(wl.num_seqs, T, wl.max_seqlen_q,
-                                                         wl.max_seqlen_k, H, wl.num_kv_heads, D,
-                                                         wl.block_size, sms), dev)
+    if fp8:
+        kc, vc = wl.fp8_pool(0, dev), wl.fp8_pool(1, dev)
+        ksc = torch.tensor(wl.kv_scales(0), device=dev)
+        vsc = torch.tensor(wl.kv_scales(1), device=dev)
+        pa.reshape_and_cache_fp8(b.d["k_new"], b.d["v_new"], kc, vc, b.d["slot_mapping"], ksc, vsc)
+        size_fn = pa.varlen_fwd_fp8kv_workspace_size
+    else:
+        kc, vc = wl.pool(0, device=dev), wl.pool(1, device=dev)
+        pa.reshape_and_cache(b.d["k_new"], b.d["v_new"], kc, vc, b.d["slot_mapping"])
+        size_fn = pa.varlen_fwd_workspace_size
+    ws = pa.alloc_workspace(size_fn(wl.num_seqs, T, wl.max_seqlen_q, wl.max_seqlen_k, H,
+                                    wl.num_kv_heads, D, wl.block_size, sms), dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     # Inputs read per launch (Q, K/V pages) vs L2: flush before each launch
@@ -367,9 +375,15 @@ def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0, dtype=torch.bfloat
         flush_rd = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def attn():
-        pa.varlen_fwd(b.d["q"], kc, vc, b.d["cu_seqlens_q"], b.d["seqused_k"], b.d["block_table"],
-                      wl.max_seqlen_q, wl.max_seqlen_k, wl.softmax_scale, wl.causal, out=b.out,
-                      lse=b.lse, workspace=ws, dev_status=status)
+        if fp8:
+            pa.varlen_fwd_fp8kv(b.d["q"], kc, vc, b.d["cu_seqlens_q"], b.d["seqused_k"],
+                                b.d["block_table"], wl.max_seqlen_q, wl.max_seqlen_k,
+                                wl.softmax_scale, wl.causal, ksc, vsc, out=b.out, lse=b.lse,
+                                workspace=ws, dev_status=status)
+        else:
+            pa.varlen_fwd(b.d["q"], kc, vc, b.d["cu_seqlens_q"], b.d["seqused_k"],
+                          b.d["block_table"], wl.max_seqlen_q, wl.max_seqlen_k, wl.softmax_scale,
+                          wl.causal, out=b.out, lse=b.lse, workspace=ws, dev_status=status)
     for _ in range(3):
         attn()
     torch.cuda.synchronize()
@@ -396,14 +410,15 @@ def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0, dtype=torch.bfloat
     assert int(status.item()) == 0, f"device status bits {int(status.item())}"
     ms = sum(a.elapsed_time(c) for a, c in ev) / n
     tflops = counts["flops"] / (ms * 1e-3) / 1e12
-    rec = {"workload": name, "what": PREFILL_LEGS.get(name, name), "dtype": str(dtype)[6:],
-           "kernel": "plan + attn_tc_kernel<128>", "bound": "tensor",
+    rec = {"workload": name + ("+fp8_kv" if fp8 else ""), "what": PREFILL_LEGS.get(name, name),
+           "dtype": str(dtype)[6:] + (", e4m3 kv widened to f16" if fp8 else ""),
+           "kernel": "plan + attn_tc_kernel<128%s>" % (", fp8" if fp8 else ""), "bound": "tensor",
            "flops_per_launch": counts["flops"], "ms_per_launch": ms, "launches": n,
            "tflops": tflops, "unit": "TFLOP/s",
            "peak": peaks["bf16_tflops_sustained"], "peak_kind": "bf16 sustained",
            "frac": tflops / peaks["bf16_tflops_sustained"],
            "frac_burst": tflops / peaks["bf16_tflops"],
-           "traffic": load_traffic("attn_tc_kernel<128>", name),
+           "traffic": None if fp8 else load_traffic("attn_tc_kernel<128>", name),
            "algorithmic_bytes_per_launch": counts["attn_bytes"],
            "l2": "flushed before every launch" if flush is not None else
                  "inputs larger than L2 (%.2f GB of Q and K/V per launch)" % (in_bytes / 1e9),
@@ -713,13 +728,13 @@ def bench_ours(args, rank, world, local):
     # 16,384-token batch, each launch timed alone after an L2 flush.
     rows_fig = row_figures(pa, wl, counts, dev, stream, lambda: scatter(main), args.steps)
     assert int(status.item()) == 0, f"device status bits {int(status.item())}"
-    # ---- the prefill half of the metric (bf16 pools) -------------------------
+    # ---- the prefill half of the metric (same pool format) -------------------
     peaks = load_peaks()
     prefill = {}
-    if not fp8 and not args.no_prefill:
+    if not args.no_prefill:
         for name in PREFILL_LEGS:
             prefill[name] = prefill_record(pa, name, dev, peaks, args.steps,
-                                           dtype=DTYPES[args.dtype])
+                                           dtype=DTYPES[args.dtype], fp8=fp8)
 
     if rank != 0:
         return
@@ -757,8 +772,9 @@ def bench_ours(args, rank, world, local):
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
         ach = counts["flops"] / (attn_ms_avg * 1e-3) / 1e12
         line["roofline"] = {"bound": "tensor",
-                            "kernel": ("plan + attn_split_kernel<128, fp8> (every segment)" if fp8
-                                       else "plan + attn_tc_kernel<128> + attn_split_kernel<128>"),
+                            "kernel": ("plan + attn_tc_kernel<128, fp8> + attn_split_kernel<128, fp8>"
+                                       if fp8 else
+                                       "plan + attn_tc_kernel<128> + attn_split_kernel<128>"),
                             "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                             "frac": ach / peaks["bf16_tflops"], "traffic": None,
                             "peak_source": peaks["source"], "attn_ms_per_launch": attn_ms_avg}
@@ -767,11 +783,10 @@ def bench_ours(args, rank, world, local):
         line["e2e"] = {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
         kname = "attn_split_kernel<128, fp8>" if fp8 else "attn_split_kernel<128>"
+        tname = "attn_tc_kernel<128, fp8>" if fp8 else "attn_tc_kernel<128>"
         line["roofline"] = {"bound": "hbm",
-                            "kernel": ("plan + attn_tc_kernel<128> (prefix) + attn_split_kernel<128> "
-                                       "(suffix) + cascade_combine_kernel<128>" if cascade and not fp8
-                                       else "plan + %s (both passes) + cascade_combine_kernel<128>"
-                                       % kname if cascade else
+                            "kernel": ("plan + %s (prefix) + %s (suffix) + cascade_combine_kernel<128>"
+                                       % (tname, kname) if cascade else
                                        "plan + %s (+ split combine)" % kname),
                             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": achieved / peaks["hbm_gbs"],
@@ -800,7 +815,7 @@ def bench_ours(args, rank, world, local):
     # split-KV kernel and/or the prefill kernel (the host launches a kernel
     # only when some segment can need it).
     G = H // wl.num_kv_heads
-    tc_rows = (lambda rows: False) if fp8 else (lambda rows: rows > 32)
+    tc_rows = lambda rows: rows > 32   # the prefill kernel takes wider segments
     if cascade:
         # scatter, planner, prefix pass (prefill kernel for more than 32
         # packed rows, else split-KV), suffix pass (split-KV and/or prefill
@@ -837,7 +852,7 @@ def bench_prefill_only(args, rank, world, local):
     names = list(PREFILL_LEGS) if args.workload == "decode_llama8b" else [args.workload]
     for name in names:
         rec = prefill_record(pa, name, dev, peaks, args.steps, min_ms=0.0,
-                             dtype=DTYPES[args.dtype])
+                             dtype=DTYPES[args.dtype], fp8=args.kv_cache == "fp8")
         if rank == 0:
             print(json.dumps({"prefill": rec}))
 
