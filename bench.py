@@ -55,7 +55,8 @@ TC_KERNEL_SRCS = [os.path.join(_CSRC, f) for f in
                   ("attn_tc.cu", "device_common.cuh", "epilogue.cuh", "pa_internal.h")]
 KERNEL_SRCS = {"attn_split_kernel<128>": SPLIT_KERNEL_SRCS,
                "attn_split_kernel<128, fp8>": SPLIT_KERNEL_SRCS,
-               "attn_tc_kernel<128>": TC_KERNEL_SRCS}
+               "attn_tc_kernel<128>": TC_KERNEL_SRCS,
+               "attn_tc_kernel<128, fp8>": TC_KERNEL_SRCS}
 # The prefill half of the metric: tensor-core prefill sub-launches timed in
 # the default run beside the decode step (workload name -> what it is).
 PREFILL_LEGS = {
@@ -418,7 +419,8 @@ def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0, dtype=torch.bfloat
            "peak": peaks["bf16_tflops_sustained"], "peak_kind": "bf16 sustained",
            "frac": tflops / peaks["bf16_tflops_sustained"],
            "frac_burst": tflops / peaks["bf16_tflops"],
-           "traffic": None if fp8 else load_traffic("attn_tc_kernel<128>", name),
+           "traffic": load_traffic("attn_tc_kernel<128%s>" % (", fp8" if fp8 else ""),
+                                   name + ("+fp8_kv" if fp8 else "")),
            "algorithmic_bytes_per_launch": counts["attn_bytes"],
            "l2": "flushed before every launch" if flush is not None else
                  "inputs larger than L2 (%.2f GB of Q and K/V per launch)" % (in_bytes / 1e9),
