@@ -83,26 +83,27 @@ struct TcCfg {
   static constexpr int O_COL = 256;
   static constexpr float RESCALE_LOG2 = 8.0f;
 };
-// FP8 (e4m3) pools, head size 128: the e4m3 K/V tiles land by TMA in a ring
-// of their own; two control warps widen each tile (exactly) to f16 into K and
-// V tiles laid out as the bf16 kernel's TMA tiles, where the same kind::f16
-// MMAs read them (Q is f16 too, P is f16). Shared memory: Q 64 KB, one
-// widened K tile (32 KB), two widened V tiles (64 KB: V(t + 1) is widened
-// while the P V products of tile t still read V(t)), two e4m3 stages of
-// 32 KB: 224 KB. Measured on the 70B prefill: one K and one V buffer with
-// two e4m3 stages 668 TFLOP/s (before the widening loop's addressing was
-// hoisted), two of each with one stage 820, this layout 831, two K and one V
-// 621.
+// FP8 (e4m3) pools, head size 128. S = Q K^T runs on the e4m3 tensor MMA
+// (kind::f8f6f4) straight from the TMA-staged key bytes, with Q taken as two
+// e4m3 terms Qh + Ql after a power-of-two row scale (split in place, in the Q
+// tiles' own shared memory, by two converter warps); P V stays on kind::f16:
+// the converter warps widen each e4m3 V tile (exactly) into f16 tiles laid
+// out as the 2-byte kernel's TMA tiles. Shared memory: Q 64 KB (Qh and Ql of
+// tile X in its two 16 KB halves after the split), two widened V buffers
+// (64 KB: V(t + 1) is widened while the P V products of tile t still read
+// V(t)), two e4m3 stages of 32 KB, 1 KB of row scales. Measured on the 70B
+// prefill with the keys widened too (one K buffer): 831 TFLOP/s; without
+// widening the keys the converters' work halves.
 struct TcFp8 {
   using C = TcCfg<128>;
-  static constexpr int KBUF = 1, VBUF = 2;                // widened K / V buffers
-  static constexpr int OFF_KW = C::TILES * C::Q_TILE;     // widened K tiles
-  static constexpr int OFF_VW = OFF_KW + KBUF * C::KV_TILE;   // widened V tiles
+  static constexpr int VBUF = 2;                          // widened V buffers
+  static constexpr int OFF_VW = C::TILES * C::Q_TILE;     // widened V tiles
   static constexpr int OFF_R8 = OFF_VW + VBUF * C::KV_TILE;   // e4m3 ring
   static constexpr int TILE8 = C::BN * 128;               // 128 keys x 128 bytes
   static constexpr int STAGE8 = 2 * TILE8;
   static constexpr int STAGES8 = 2;                       // e4m3 ring stages
-  static constexpr int OFF_BAR = OFF_R8 + STAGES8 * STAGE8;
+  static constexpr int OFF_RS = OFF_R8 + STAGES8 * STAGE8;   // float[TILES * BM]: 2^-k per row
+  static constexpr int OFF_BAR = OFF_RS + C::TILES * C::BM * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
   static constexpr int CONV_THREADS = 64;                 // warps 2 and 3
 };
@@ -119,10 +120,10 @@ struct TcBars {
   uint64_t p_full[2][2];   // [half][tile]: P of keys [64 half, +64) of the tile is in TMEM
   uint64_t pv_done[2];     // [tile]: O += P V of the current key tile completed
   uint64_t drain;
-  // FP8 pools: Q converted to f16; [buffer]: widened K / V tile ready (64
-  // converter arrivals), widened K / V buffer free again (MMA commit).
-  // Buffer b of K holds tiles b, b + KBUF, ... (phase t / KBUF); V likewise.
-  uint64_t q_conv, kw_full[2], kw_free[2], vw_full[2], vw_free[2];
+  // FP8 pools: Q split into e4m3 terms (64 converter arrivals); [buffer]:
+  // widened V tile ready (64 arrivals), widened V buffer free again (MMA
+  // commit). Buffer b holds tiles b, b + VBUF, ... (phase t / VBUF).
+  uint64_t q_conv, vw_full[2], vw_free[2];
   uint32_t tmem_base;
   volatile int abort;
   volatile int last;
@@ -190,18 +191,72 @@ __device__ __forceinline__ void widen_e4m3_tile(const uint8_t* src, uint8_t* dst
   }
 }
 
-// bf16 Q tiles to f16 in place (same layout; exact for |q| in f16's normal
-// range, which the FP8 path requires of q).
-__device__ __forceinline__ void q_bf16_to_f16(uint8_t* q, int bytes, int ct) {
-  for (int i = ct * 16; i < bytes; i += TcFp8::CONV_THREADS * 16) {
-    uint4 w = *reinterpret_cast<const uint4*>(q + i);
-    uint32_t* x = &w.x;
+// Split the Q tiles in place into e4m3 terms for the kind::f8f6f4 S product.
+// Row r of tile X holds dims 0..63 in half 0 and 64..127 in half 1 (2-byte
+// elements, 128-byte swizzled rows: 16-byte chunk c at r*128 + ((c ^ r%8) << 4)).
+// With 2^k putting the row's largest |q| in [128, 256) (k = 126 for a zero
+// or subnormal maximum), q 2^k = Qh + Ql with Qh = e4m3(q 2^k) and
+// Ql = e4m3(q 2^k - Qh); Qh's 128 bytes (dims in order) replace half 0 and
+// Ql's replace half 1, in the same swizzled layout, which is the K-major
+// e4m3 operand layout; 2^-k goes to rs[X*128 + r]. Thread ct takes rows ct
+// and ct + 64 of each tile. Half 1 is read whole before any write; chunk c
+// of half 0 is overwritten only after dims 8c..8c+7 were read.
+template <bool F16>
+__device__ __forceinline__ void q_split_e4m3(uint8_t* q, float* rs, int tiles, int ct) {
+  using C = TcCfg<128>;
+  for (int x = 0; x < tiles; ++x) {
+    for (int r = ct; r < C::BM; r += TcFp8::CONV_THREADS) {
+      uint8_t* h0 = q + x * C::Q_TILE + r * 128;
+      uint8_t* h1 = h0 + C::Q_HALF;
+      const int sw = r & 7;
+      uint4 hi[8];
+      float amax = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = Elem<false>::unpack(x[k]);
-      x[k] = pack_f16(f.x, f.y);
+      for (int c = 0; c < 8; ++c) {
+        hi[c] = *reinterpret_cast<const uint4*>(h1 + ((c ^ sw) << 4));
+        const uint4 lo = *reinterpret_cast<const uint4*>(h0 + ((c ^ sw) << 4));
+        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi[c].x, hi[c].y, hi[c].z, hi[c].w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float2 f = Elem<F16>::unpack(w[k]);
+          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+      const int ebits = (__float_as_int(amax) >> 23) & 0xFF;
+      const int kexp = max(-126, min(126, ebits == 0 ? 126 : 134 - ebits));
+      const float up = __int_as_float((127 + kexp) << 23);
+      rs[x * C::BM + r] = __int_as_float((127 - kexp) << 23);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {   // dims 16c .. 16c + 15
+        uint4 a, b;
+        if (c < 4) {
+          a = *reinterpret_cast<const uint4*>(h0 + (((2 * c) ^ sw) << 4));
+          b = *reinterpret_cast<const uint4*>(h0 + (((2 * c + 1) ^ sw) << 4));
+        } else {
+          a = hi[2 * c - 8];
+          b = hi[2 * c - 7];
+        }
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t qh[4], ql[4];
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+          uint32_t hh = 0, ll = 0;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float2 f = Elem<F16>::unpack(w[k + e]);
+            const float y0 = f.x * up, y1 = f.y * up;
+            const uint32_t hb = f32x2_to_e4m3x2(y0, y1);
+            const float2 hv = Elem<true>::unpack(e4m3x2_to_f16x2(hb));
+            hh |= hb << (16 * e);
+            ll |= f32x2_to_e4m3x2(y0 - hv.x, y1 - hv.y) << (16 * e);
+          }
+          qh[k / 2] = hh;
+          ql[k / 2] = ll;
+        }
+        *reinterpret_cast<uint4*>(h0 + ((c ^ sw) << 4)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+        *reinterpret_cast<uint4*>(h1 + ((c ^ sw) << 4)) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+      }
     }
-    *reinterpret_cast<uint4*>(q + i) = w;
   }
 }
 
@@ -230,11 +285,19 @@ __device__ __forceinline__ void tc_softmax_tile(const AttnArgs& a, TcBars* bars,
   const int lim = !rvalid ? -1 : (a.causal ? kv_len - q_len + ti : kv_len - 1);
   // FP8 pools: scores use the stored codes, so k_scale joins the softmax
   // scale and v_scale the final normalisation.
-  const float sl2 = FP8 ? a.scale_log2 * __ldg(a.k_scale + hk) : a.scale_log2;
+  float sl2 = FP8 ? a.scale_log2 * __ldg(a.k_scale + hk) : a.scale_log2;
   const int tid = threadIdx.x - 128 - X * 128;     // 0..127 within the warpgroup
   float m_use = -INFINITY, l = 0.f;
   bool ok = true;
-  for (int t = 0; t < ntiles; ++t) {
+  if constexpr (FP8) {
+    // S holds q 2^k . k for the row's power of two 2^k (Q entered the e4m3
+    // products as two e4m3 terms): 2^-k joins the softmax scale.
+    if (ntiles > 0) {
+      ok = mbar_wait(&bars->q_conv, 0);
+      sl2 *= reinterpret_cast<const float*>(smem + TcFp8::OFF_RS)[X * C::BM + r];
+    }
+  }
+  for (int t = 0; ok && t < ntiles; ++t) {
     if (!mbar_wait(&bars->s_full[X], t & 1)) { ok = false; break; }
     tc_fence_after();
     const int key0 = kb + t * C::BN;
@@ -454,15 +517,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < 2 * C::STAGES; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      // FP8: the converter warps free an e4m3 stage once they widened it.
-      mbar_init(&bars->kv_empty[s], FP8 ? TcFp8::CONV_THREADS : 1);
+      // FP8: an e4m3 K stage is freed by the commit after its S products, a
+      // V stage by the converter warps once they widened it.
+      mbar_init(&bars->kv_empty[s], FP8 && s >= C::STAGES ? TcFp8::CONV_THREADS : 1);
     }
     if constexpr (FP8) {
+      static_assert(TcFp8::STAGES8 == C::STAGES, "the e4m3 ring has the 2-byte ring's stages");
       mbar_init(&bars->q_conv, TcFp8::CONV_THREADS);
       for (int b = 0; b < 2; ++b) {
-        mbar_init(&bars->kw_full[b], TcFp8::CONV_THREADS);
         mbar_init(&bars->vw_full[b], TcFp8::CONV_THREADS);
-        mbar_init(&bars->kw_free[b], 1);
         mbar_init(&bars->vw_free[b], 1);
       }
     }
@@ -539,65 +602,62 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // address plus c / 16; shared addresses stay below 2^18, so the 14-bit
     // field cannot carry).
     if (lane == 0 && ntiles > 0) {
-      // Operand type: the activations' (bf16 or f16), or f16 over FP8 pools.
-      constexpr uint32_t fmt = Elem<F16 || FP8>::kTcFormat;
-      constexpr uint32_t idesc_s = mma_idesc(C::BM, C::BN, false, fmt);
-      constexpr uint32_t idesc_o = mma_idesc(C::BM, D, true, fmt);
-      // K / V operands: ring stage t % STAGES (2-byte pools), or the widened
-      // K buffer t % KBUF and V buffer t % VBUF (FP8 pools).
-      constexpr int kBufs = FP8 ? TcFp8::KBUF : C::STAGES;
-      constexpr int vBufs = FP8 ? TcFp8::VBUF : C::STAGES;
-      constexpr int kStep = (FP8 ? C::KV_TILE : C::STAGE) >> 4;   // descriptor step per buffer
-      const uint32_t sK = smem_u32(smem + (FP8 ? TcFp8::OFF_KW : C::OFF_KV));
-      const uint32_t sV = FP8 ? smem_u32(smem + TcFp8::OFF_VW) : sK + C::KV_TILE;
-      const uint64_t qdesc[2] = {smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024),
-                                 smem_desc_sw128(smem_u32(smem + C::OFF_Q + C::Q_TILE), 16, 1024)};
-      const uint64_t kdesc0 = smem_desc_sw128(sK, 16, 1024);
-      const uint64_t vdesc0 = smem_desc_sw128(sV, C::KV_HALF, 1024);
-      // S_X(t) = Q_X K(t)^T into TMEM columns [128 X, 128 X + 128).
-      auto issue_s = [&](int x, int t) {
-        tc_fence_after();
-        const uint64_t qd = qdesc[x];
-        const uint64_t kd = kdesc0 + static_cast<uint32_t>((t % kBufs) * kStep);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * C::Q_HALF + (kk & 3) * 32) >> 4;
-          const uint32_t offk = ((kk >> 2) * C::KV_HALF + (kk & 3) * 32) >> 4;
-          tc_mma(tmem + x * 128, qd + off, kd + offk, idesc_s, kk > 0);
-        }
-        tc_commit(&bars->s_full[x]);
-      };
-      // O_X += P_X(t) V(t) over keys [64 h, 64 h + 64), P_X read from TMEM
-      // (the first 64 columns of S_X); the second half commits pv_done.
-      auto issue_pv = [&](int x, int t, int h) {
-        tc_fence_after();
-        const uint64_t vd = vdesc0 + static_cast<uint32_t>((t % vBufs) * kStep);
-#pragma unroll
-        for (int k4 = 0; k4 < C::BN / 32; ++k4) {
-          const int kk = h * (C::BN / 32) + k4;
-          tc_mma_ts(tmem + C::O_COL + x * D, tmem + x * 128 + kk * 8, vd + ((kk * 16 * 128) >> 4),
-                    idesc_o, (t > 0 || kk > 0) ? 1 : 0);
-        }
-        if (h == 1) tc_commit(&bars->pv_done[x]);
-      };
-      // Issue order per tile t: P_A V (in two halves, each as soon as the
-      // softmax publishes it), S_A(t+1), P_B V (two halves), S_B(t+1). The
-      // tensor core executes one thread's MMAs in issue order, so S_X(t+1)
-      // overwrites P_X(t) only after P_X(t) V has read it, and the softmax
-      // of tile A moves on as soon as its own product is done instead of
-      // waiting for tile B's softmax. The commit after S_X(t+1) also covers
-      // P_X(t) V, so O_X is final when the softmax sees S_X(t+1). K and V
-      // have their own barriers: K(t) is released once both S(t) are done,
-      // so its buffer refills while V(t) is still in use.
-      //
-      // 2-byte pools wait on the TMA ring and release its stages; FP8 pools
-      // wait for the converter warps' widened tiles (kw_full / vw_full) and
-      // release the widened buffers (kw_free / vw_free). The two loops are
-      // written out separately: the issuing thread is the bottleneck, and a
-      // single loop with shared wait / release helpers measured 14% slower
-      // on the 70B prefill (1185 against 1378 TFLOP/s).
       bool ok;
       if constexpr (!FP8) {
+        // Operand type: the activations' (bf16 or f16).
+        constexpr uint32_t fmt = Elem<F16>::kTcFormat;
+        constexpr uint32_t idesc_s = mma_idesc(C::BM, C::BN, false, fmt);
+        constexpr uint32_t idesc_o = mma_idesc(C::BM, D, true, fmt);
+        // K / V operands: ring stage t % STAGES.
+        constexpr int kBufs = C::STAGES;
+        constexpr int vBufs = C::STAGES;
+        constexpr int kStep = C::STAGE >> 4;   // descriptor step per stage
+        const uint32_t sK = smem_u32(smem + C::OFF_KV);
+        const uint32_t sV = sK + C::KV_TILE;
+        const uint64_t qdesc[2] = {smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024),
+                                   smem_desc_sw128(smem_u32(smem + C::OFF_Q + C::Q_TILE), 16, 1024)};
+        const uint64_t kdesc0 = smem_desc_sw128(sK, 16, 1024);
+        const uint64_t vdesc0 = smem_desc_sw128(sV, C::KV_HALF, 1024);
+        // S_X(t) = Q_X K(t)^T into TMEM columns [128 X, 128 X + 128).
+        auto issue_s = [&](int x, int t) {
+          tc_fence_after();
+          const uint64_t qd = qdesc[x];
+          const uint64_t kd = kdesc0 + static_cast<uint32_t>((t % kBufs) * kStep);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * C::Q_HALF + (kk & 3) * 32) >> 4;
+            const uint32_t offk = ((kk >> 2) * C::KV_HALF + (kk & 3) * 32) >> 4;
+            tc_mma(tmem + x * 128, qd + off, kd + offk, idesc_s, kk > 0);
+          }
+          tc_commit(&bars->s_full[x]);
+        };
+        // O_X += P_X(t) V(t) over keys [64 h, 64 h + 64), P_X read from TMEM
+        // (the first 64 columns of S_X); the second half commits pv_done.
+        auto issue_pv = [&](int x, int t, int h) {
+          tc_fence_after();
+          const uint64_t vd = vdesc0 + static_cast<uint32_t>((t % vBufs) * kStep);
+#pragma unroll
+          for (int k4 = 0; k4 < C::BN / 32; ++k4) {
+            const int kk = h * (C::BN / 32) + k4;
+            tc_mma_ts(tmem + C::O_COL + x * D, tmem + x * 128 + kk * 8, vd + ((kk * 16 * 128) >> 4),
+                      idesc_o, (t > 0 || kk > 0) ? 1 : 0);
+          }
+          if (h == 1) tc_commit(&bars->pv_done[x]);
+        };
+        // Issue order per tile t: P_A V (in two halves, each as soon as the
+        // softmax publishes it), S_A(t+1), P_B V (two halves), S_B(t+1). The
+        // tensor core executes one thread's MMAs in issue order, so S_X(t+1)
+        // overwrites P_X(t) only after P_X(t) V has read it, and the softmax
+        // of tile A moves on as soon as its own product is done instead of
+        // waiting for tile B's softmax. The commit after S_X(t+1) also covers
+        // P_X(t) V, so O_X is final when the softmax sees S_X(t+1). K and V
+        // have their own barriers: K(t) is released once both S(t) are done,
+        // so its buffer refills while V(t) is still in use.
+        //
+        // The 2-byte and FP8 paths are written out separately: the issuing
+        // thread is the bottleneck, and a single loop with shared wait /
+        // release helpers measured 14% slower on the 70B prefill (1185
+        // against 1378 TFLOP/s).
         constexpr int S_ = C::STAGES;
         ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->kv_full[0], 0);
         if (ok) {
@@ -633,13 +693,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           }
         }
       } else {
-        constexpr int KB = TcFp8::KBUF, VB = TcFp8::VBUF;
-        ok = mbar_wait(F16 ? &bars->q_full : &bars->q_conv, 0) &&
-             mbar_wait(&bars->kw_full[0], 0);
+        // FP8 pools: S_X(t) = Qh_X K(t)^T + Ql_X K(t)^T on kind::f8f6f4, K
+        // straight from the e4m3 ring stage (128-byte swizzled rows, 32 bytes
+        // of K per MMA); Qh_X and Ql_X are the two halves of Q tile X after
+        // the converter warps' split. P V on kind::f16 from the widened V
+        // buffers. The ring's K stage is released by the commit after both
+        // tiles' S products; V stages by the converter warps.
+        constexpr uint32_t idesc_s8 = mma_idesc(C::BM, C::BN, false, 0);   // e4m3 x e4m3
+        constexpr uint32_t idesc_o = mma_idesc(C::BM, D, true, Elem<true>::kTcFormat);
+        constexpr int VB = TcFp8::VBUF, S8 = TcFp8::STAGES8;
+        const uint64_t qhdesc[2] = {smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024),
+                                    smem_desc_sw128(smem_u32(smem + C::OFF_Q + C::Q_TILE), 16, 1024)};
+        const uint64_t k8desc0 = smem_desc_sw128(smem_u32(smem + TcFp8::OFF_R8), 16, 1024);
+        const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + TcFp8::OFF_VW), C::KV_HALF, 1024);
+        auto issue_s = [&](int x, int t) {
+          tc_fence_after();
+          const uint64_t qh = qhdesc[x], ql = qhdesc[x] + (C::Q_HALF >> 4);
+          const uint64_t kd = k8desc0 + static_cast<uint32_t>((t % S8) * (TcFp8::STAGE8 >> 4));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f8(tmem + x * 128, qh + kk * 2, kd + kk * 2, idesc_s8, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f8(tmem + x * 128, ql + kk * 2, kd + kk * 2, idesc_s8, 1);
+          tc_commit(&bars->s_full[x]);
+        };
+        auto issue_pv = [&](int x, int t, int h) {
+          tc_fence_after();
+          const uint64_t vd = vdesc0 + static_cast<uint32_t>((t % VB) * (C::KV_TILE >> 4));
+#pragma unroll
+          for (int k4 = 0; k4 < C::BN / 32; ++k4) {
+            const int kk = h * (C::BN / 32) + k4;
+            tc_mma_ts(tmem + C::O_COL + x * D, tmem + x * 128 + kk * 8,
+                      vd + ((kk * 16 * 128) >> 4), idesc_o, (t > 0 || kk > 0) ? 1 : 0);
+          }
+          if (h == 1) tc_commit(&bars->pv_done[x]);
+        };
+        ok = mbar_wait(&bars->q_conv, 0) && mbar_wait(&bars->kv_full[0], 0);
         if (ok) {
+          bars->consumed[0] = 1;
           issue_s(0, 0);
           if (two) issue_s(1, 0);
-          tc_commit(&bars->kw_free[0]);
+          tc_commit(&bars->kv_empty[0]);
         }
         for (int t = 0; ok && t < ntiles; ++t) {
           if (bars->abort) { ok = false; break; }
@@ -650,7 +745,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           if (!(ok = mbar_wait(&bars->p_full[1][0], t & 1))) break;
           issue_pv(0, t, 1);
           if (more) {
-            if (!(ok = mbar_wait(&bars->kw_full[(t + 1) % KB], ((t + 1) / KB) & 1))) break;
+            if (!(ok = mbar_wait(&bars->kv_full[(t + 1) % S8], ((t + 1) / S8) & 1))) break;
+            bars->consumed[0] = t + 2;
             issue_s(0, t + 1);
           }
           if (two) {
@@ -662,7 +758,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           tc_commit(&bars->vw_free[t % VB]);
           if (more) {
             if (two) issue_s(1, t + 1);
-            tc_commit(&bars->kw_free[(t + 1) % KB]);
+            tc_commit(&bars->kv_empty[(t + 1) % S8]);
           }
         }
       }
@@ -676,38 +772,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
   } else if (FP8 && ntiles > 0) {
     // ------------------------------------------------------------ converters
-    // Warps 2 and 3 (FP8 pools): Q to f16 once (bf16 activations), then per
-    // key tile t widen the e4m3 K(t) into the K buffer once the S products
-    // of tile t - 1 have read it, and V(t) (rows past the sequence end as
-    // zeros) into the V buffer once the P V products of tile t - 1 have;
-    // each e4m3 ring stage is freed as soon as it is widened.
+    // Warps 2 and 3 (FP8 pools): split the Q tiles into e4m3 terms once,
+    // then per key tile t widen the e4m3 V(t) (rows past the sequence end as
+    // zeros) into V buffer t % VBUF once the P V products of tile t - VBUF
+    // have read it, and free the ring's V stage as soon as it is widened.
     const int ct = threadIdx.x - 64;   // 0 .. 63
-    constexpr int S8 = TcFp8::STAGES8;
-    bool ok = true;
-    if constexpr (!F16) {
-      ok = mbar_wait(&bars->q_full, 0);
-      if (ok) {
-        q_bf16_to_f16(smem + C::OFF_Q, (two ? 2 : 1) * C::Q_TILE, ct);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&bars->q_conv);
-      }
+    constexpr int S8 = TcFp8::STAGES8, VB = TcFp8::VBUF;
+    bool ok = mbar_wait(&bars->q_full, 0);
+    if (ok) {
+      q_split_e4m3<F16>(smem + C::OFF_Q, reinterpret_cast<float*>(smem + TcFp8::OFF_RS),
+                        two ? 2 : 1, ct);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&bars->q_conv);
     }
     for (int t = 0; ok && t < ntiles; ++t) {
       if (bars->abort) { ok = false; break; }
-      const uint8_t* k8 = smem + TcFp8::OFF_R8 + (t % S8) * TcFp8::STAGE8;
-      if (!(ok = mbar_wait(&bars->kv_full[t % S8], (t / S8) & 1))) break;
-      if (ct == 0) bars->consumed[0] = t + 1;
-      // buffer t % 2 last held tile t - 2
-      constexpr int KB = TcFp8::KBUF, VB = TcFp8::VBUF;
-      if (t >= KB && !(ok = mbar_wait(&bars->kw_free[t % KB], ((t / KB) - 1) & 1))) break;
-      widen_e4m3_tile(k8, smem + TcFp8::OFF_KW + (t % KB) * C::KV_TILE, ct, C::BN);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&bars->kw_full[t % KB]);
-      mbar_arrive(&bars->kv_empty[t % S8]);
+      const uint8_t* v8 = smem + TcFp8::OFF_R8 + (t % S8) * TcFp8::STAGE8 + TcFp8::TILE8;
       if (!(ok = mbar_wait(&bars->kv_full[S8 + t % S8], (t / S8) & 1))) break;
       if (ct == 0) bars->consumed[1] = t + 1;
       if (t >= VB && !(ok = mbar_wait(&bars->vw_free[t % VB], ((t / VB) - 1) & 1))) break;
-      widen_e4m3_tile(k8 + TcFp8::TILE8, smem + TcFp8::OFF_VW + (t % VB) * C::KV_TILE, ct,
+      widen_e4m3_tile(v8, smem + TcFp8::OFF_VW + (t % VB) * C::KV_TILE, ct,
                       kv_len - (kb + t * C::BN));
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&bars->vw_full[t % VB]);

@@ -287,6 +287,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f8f6f4 (e4m3 operands as
+// the instruction descriptor's type fields say, fp32 accumulate; 32 bytes of
+// K per instruction).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]: A read from tensor memory (row m in
 // lane m, two bf16 K-elements per 32-bit column), kind::f16.
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
@@ -352,10 +364,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor for kind::f16 with fp32 D: D format (bits 4-5) = 1,
-// A format (7-9) and B format (10-12) = fmt (1 bf16, 0 f16; A and B of one
-// MMA always share the type), A K-major, B K-major or MN-major (bit 16),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// Instruction descriptor for kind::f16 (and kind::f8f6f4) with fp32 D: D
+// format (bits 4-5) = 1, A format (7-9) and B format (10-12) = fmt (kind::f16:
+// 1 bf16, 0 f16; kind::f8f6f4: 0 e4m3; A and B of one MMA always share the
+// type here), A K-major, B K-major or MN-major (bit 16), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t mma_idesc(int M, int N, bool b_mn_major, uint32_t fmt) {
   return (1u << 4) | (fmt << 7) | (fmt << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
