@@ -210,18 +210,22 @@ __device__ __forceinline__ void q_split_e4m3(uint8_t* q, float* rs, int tiles, i
       uint8_t* h1 = h0 + C::Q_HALF;
       const int sw = r & 7;
       uint4 hi[8];
-      float amax = 0.f;
+      float part[8];   // eight independent maximum chains, then a tree
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         hi[c] = *reinterpret_cast<const uint4*>(h1 + ((c ^ sw) << 4));
         const uint4 lo = *reinterpret_cast<const uint4*>(h0 + ((c ^ sw) << 4));
         const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi[c].x, hi[c].y, hi[c].z, hi[c].w};
+        float m = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const float2 f = Elem<F16>::unpack(w[k]);
-          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+          m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
         }
+        part[c] = m;
       }
+      const float amax = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                               fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
       const int ebits = (__float_as_int(amax) >> 23) & 0xFF;
       const int kexp = max(-126, min(126, ebits == 0 ? 126 : 134 - ebits));
       const float up = __int_as_float((127 + kexp) << 23);
