@@ -361,14 +361,15 @@ pa_status pa_varlen_fwd_noalloc(const void* q, int64_t q_token_stride, const voi
  * is IEEE float32 (correctly rounded), the result is rounded to the nearest
  * e4m3 value (ties to even) and saturates at +-448 (a NaN stays NaN).
  * Attention computes exactly the 2-byte pools' definition on the dequantized
- * keys and values e4m3(c) * scale[h], with float32 accumulation. Items of at
- * most 8 packed query rows (decode with GQA <= 8) take q.k on the e4m3
- * tensor MMA, q as two e4m3 terms after a power-of-two row scale (exact for
- * every element of at least 2^-9 of its row's largest); wider items form q.k
- * from f16 q, so there |q| must stay below 65504. Segments of more than 32
- * packed query rows (prefill) run on the tensor-core kernel, which widens
- * each e4m3 K/V tile to f16 in shared memory (exact) and multiplies it with
- * f16 q and f16 P; shorter ones (decode) on the split-KV kernel.
+ * keys and values e4m3(c) * scale[h], with float32 accumulation. Segments
+ * of more than 32 packed query rows (prefill) run on the tensor-core kernel:
+ * q.k on the e4m3 tensor MMA straight from the stored key bytes, p.v on the
+ * f16 MMA with each e4m3 V tile widened to f16 in shared memory (exact).
+ * Shorter segments run on the split-KV kernel: items of at most 8 packed
+ * rows (decode with GQA <= 8) take q.k on the e4m3 MMA too, wider ones form
+ * q.k from f16 q (there |q| must stay below 65504). Wherever q.k is on the
+ * e4m3 MMA, q is taken as two e4m3 terms after a power-of-two row scale
+ * (exact for every element of at least 2^-9 of its row's largest).
  * Layout: the NHD pools of pa_reshape_and_cache with 1-byte elements;
  * cache_block_stride is in elements (= bytes) and a multiple of 16.
  * head_size must be 128 (PA_ERR_UNSUPPORTED otherwise).
