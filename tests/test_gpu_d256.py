@@ -125,3 +125,19 @@ def test_d256_refusals():
                           d["seqused_k"], d["block_table"], wl.max_seqlen_q, wl.max_seqlen_k,
                           scale, True)
         assert e.value.code == pa.PA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name,seqs", [
+    ("decode_d256", {0: [0], 31: [0], 63: [0]}),
+    ("prefill_d256", {0: [0, 1, 1023, 2047], 3: [5, 2046]}),
+])
+def test_d256_bench_workloads_sampled(name, seqs):
+    """The head-size-256 workloads the bench times (16/8 heads): the full
+    batch on the GPU, sampled query rows against the oracle."""
+    wl = W.CONFIGS[name]()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse, _ = run_gpu(wl, status=status)
+    ref = oracle_sampled(wl, seqs)
+    for s, (tok, ro, rl) in ref.items():
+        assert_close(out, lse, ro, rl, tokens=tok)
+    assert int(status.item()) == 0

@@ -364,6 +364,23 @@ def prefill_profile(seed=1006, n_prefill=4, q_len=2048, kv_len=12288, dtype=torc
                   [kv_len] * n_prefill, g, dtype=dtype)
 
 
+def decode_d256(seed=1007, num_seqs=64, dtype=torch.bfloat16):
+    """A decode batch at head size 256 (Gemma-2-like heads): 64 sequences x 1
+    query, 16/8 heads, block_size 16, KV lengths uniform on [512, 4096]
+    (about 1.2 GB of K/V, as the head-size-128 decode batch)."""
+    g = torch.Generator().manual_seed(seed)
+    kv = _uniform_int(g, 512, 4096, num_seqs)
+    return _build("decode_d256", seed, 16, 8, 256, 16, [1] * num_seqs, kv, g, dtype=dtype)
+
+
+def prefill_d256(seed=1008, n_prefill=4, q_len=2048, kv_len=10240, dtype=torch.bfloat16):
+    """A prefill batch at head size 256: 4 causal sequences of 2048 queries on
+    8192 prior tokens, 16/8 heads, block_size 16."""
+    g = torch.Generator().manual_seed(seed)
+    return _build("prefill_d256", seed, 16, 8, 256, 16, [q_len] * n_prefill,
+                  [kv_len] * n_prefill, g, dtype=dtype)
+
+
 CONFIGS = {
     "tiny_mixed": tiny_mixed,
     "decode_llama8b": decode_llama8b,
@@ -373,6 +390,8 @@ CONFIGS = {
     "prefill_profile": prefill_profile,
     "long_context_70b_prefill": long_context_70b_prefill,
     "chunked_prefill_mix_prefill": chunked_prefill_mix_prefill,
+    "decode_d256": decode_d256,
+    "prefill_d256": prefill_d256,
 }
 
 
