@@ -72,7 +72,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 # ---------------------------------------------------------------------------
 def is_prefill(wl, s, fp8=False):
     """Segments with more than 32 packed query rows run on the tensor-core
-    kernel (for FP8 pools too, over tiles widened to f16)."""
+    kernel (for FP8 pools too; at head size 256 every segment does)."""
     return wl.q_lens[s] * (wl.num_heads // wl.num_kv_heads) > 32
 
 
@@ -774,7 +774,8 @@ def bench_ours(args, rank, world, local):
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
         ach = counts["flops"] / (attn_ms_avg * 1e-3) / 1e12
         line["roofline"] = {"bound": "tensor",
-                            "kernel": ("plan + attn_tc_kernel<128, fp8> + attn_split_kernel<128, fp8>"
+                            "kernel": ("plan + attn_tc_kernel<%d> (every segment)" % D if D > 128
+                                       else "plan + attn_tc_kernel<128, fp8> + attn_split_kernel<128, fp8>"
                                        if fp8 else
                                        "plan + attn_tc_kernel<128> + attn_split_kernel<128>"),
                             "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -786,9 +787,12 @@ def bench_ours(args, rank, world, local):
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
         kname = "attn_split_kernel<128, fp8>" if fp8 else "attn_split_kernel<128>"
         tname = "attn_tc_kernel<128, fp8>" if fp8 else "attn_tc_kernel<128>"
+        if D > 128:   # head size 256: every segment on the prefill kernel
+            kname = tname = "attn_tc_kernel<%d>" % D
         line["roofline"] = {"bound": "hbm",
-                            "kernel": ("plan + %s (prefix) + %s (suffix) + cascade_combine_kernel<128>"
-                                       % (tname, kname) if cascade else
+                            "kernel": ("plan + %s (prefix) + %s (suffix) + cascade_combine_kernel<%d>"
+                                       % (tname, kname, D) if cascade else
+                                       "plan + %s (every segment)" % kname if D > 128 else
                                        "plan + %s (+ split combine)" % kname),
                             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": achieved / peaks["hbm_gbs"],
@@ -817,7 +821,9 @@ def bench_ours(args, rank, world, local):
     # split-KV kernel and/or the prefill kernel (the host launches a kernel
     # only when some segment can need it).
     G = H // wl.num_kv_heads
-    tc_rows = lambda rows: rows > 32   # the prefill kernel takes wider segments
+    # The prefill kernel takes segments of more than 32 packed rows (every
+    # segment at head size 256, where the split-KV kernel is not launched).
+    tc_rows = lambda rows: rows > 32 or D > 128
     if cascade:
         # scatter, planner, prefix pass (prefill kernel for more than 32
         # packed rows, else split-KV), suffix pass (split-KV and/or prefill
@@ -825,6 +831,8 @@ def bench_ours(args, rank, world, local):
         per_step = 2 + 1 + 1 + (1 if tc_rows(wl.max_seqlen_q * G) else 0) + 1
     else:
         per_step = 3 + (1 if tc_rows(wl.max_seqlen_q * G) else 0)
+    if D > 128:
+        per_step -= 1   # no split-KV launch beside the prefill kernel
     line["gpu_launches"] = per_step * args.steps
     for r in rows_fig.values():
         r["frac_hbm"] = r["gbs"] / peaks["hbm_gbs"]
