@@ -987,7 +987,9 @@ static cudaError_t launch_split_d(const CUtensorMap& tmK, const CUtensorMap& tmV
     if (known) configured[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(items_bound) * static_cast<unsigned>(a.H_kv));
+  // One block per (item, KV head), and one more that has no item (the block
+  // that waits for the predecessor grid; see pdl_enter).
+  cfg.gridDim = dim3(static_cast<unsigned>(items_bound) * static_cast<unsigned>(a.H_kv) + 1u);
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;

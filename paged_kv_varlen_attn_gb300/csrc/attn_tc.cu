@@ -871,7 +871,9 @@ static cudaError_t launch_tc_d(const CUtensorMap& tmK, const CUtensorMap& tmV,
     if (known) configured[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(items_bound, a.H_kv);
+  // One column of blocks past the last item: the last block, which waits for
+  // the predecessor grid (see pdl_enter), then has no item to delay.
+  cfg.gridDim = dim3(items_bound + 1, a.H_kv);
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = FP8 ? TcFp8::SMEM_BYTES : C::SMEM_BYTES;
   cfg.stream = st;

@@ -32,8 +32,9 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
                          int64_t num_slots, int32_t* status) {
   // Launched after the planner inside an update-and-attend call (a no-op
   // otherwise): its inputs predate the planner, so only the last block waits
-  // for it, which keeps the grids completing in launch order.
-  pdl_enter(0);
+  // for it, after its own rows, which keeps the grids completing in launch
+  // order without delaying any row.
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kScatterWarps;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kScatterWarps + (threadIdx.x >> 5);
@@ -70,6 +71,7 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
       }
     }
   }
+  pdl_leave();
 }
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, int64_t kstride,
@@ -185,7 +187,7 @@ reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restr
                              int vph, int bs, int64_t num_slots,
                              const float* __restrict__ k_scale,
                              const float* __restrict__ v_scale, int32_t* status) {
-  pdl_enter(0);
+  pdl_trigger();   // the planner: as in reshape_and_cache_kernel
   const int lane = threadIdx.x & 31;
   const int vsh = __ffs(vph) - 1;   // log2(D / 8)
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kScatterWarps;
@@ -236,6 +238,7 @@ reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restr
       }
     }
   }
+  pdl_leave();
 }
 
 cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int64_t kstride,

@@ -13,7 +13,12 @@
 
 namespace pa {
 
+// Threads of a block: 256 when the suffix pass has prefill-kernel groups (up
+// to 256 rows each), else 128 -- a decode group of G rows has G * D / 4
+// four-column units, 128 at G = 4 and D = 128, and the smaller blocks fit
+// six to an SM instead of three (one wave for 64 sequences x 8 KV heads).
 constexpr int kCombineThreads = 256;
+constexpr int kCombineThreadsSmall = 128;
 
 // One block per (row group of the suffix pass, KV head). Blocks [0, gb0)
 // take class 0 groups, the rest class 1 groups.
@@ -21,20 +26,23 @@ template <int D, bool F16>
 __global__ void __launch_bounds__(kCombineThreads)
 cascade_combine_kernel(const __grid_constant__ AttnArgs a0, const __grid_constant__ AttnArgs a1,
                        int gb0) {
-  // The plan is complete when this grid starts (the kernels before it
-  // started only after their own wait on the planner), so the group is read
-  // before the wait; the partial states are read after it.
+  // The plan is complete when this grid starts (the first attention kernel
+  // of the call lets its successors start only after each of its blocks has
+  // waited for the plan), so the group and the prefix pass's records are
+  // read before the wait; the partial states are read after it.
   int g = static_cast<int>(blockIdx.x);
   const int cls = g >= gb0 ? 1 : 0;
   if (cls) g -= gb0;
   const AttnArgs& a = cls ? a1 : a0;
   const int hk = blockIdx.y;
   const bool live = g < a.header[4 + cls];
-  int4 gr = make_int4(0, 0, 0, 0), sg = gr, sp = gr;
+  int4 gr = make_int4(0, 0, 0, 0), sg = gr, sp = gr, pseg = gr, psplit = gr;
   if (live) {
     gr = a.groups[g];
     sg = a.seg[gr.x];
     sp = a.segsplit[gr.x];
+    pseg = a.mp_seg[0];
+    psplit = a.mp_segsplit[0];
   }
   // Launched as a dependent of the last attention kernel of the call: once
   // the wait returns, every kernel of the call before this one has completed.
@@ -46,7 +54,7 @@ cascade_combine_kernel(const __grid_constant__ AttnArgs a0, const __grid_constan
   const int row0 = rt * rows_per_item;
   const int R = min(rows_per_item, sg.y * a.G - row0);
   combine_splits<D, F16>(a, sp.y + rt * sp.x, sp.x, hk, R, row0, sg.x, threadIdx.x,
-                         kCombineThreads);
+                         static_cast<int>(blockDim.x), pseg, psplit);
 }
 
 template <int D, bool F16>
@@ -54,7 +62,7 @@ static cudaError_t launch_combine_d(const AttnArgs& a0, const AttnArgs& a1, int 
                                     cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(gb0 + gb1), static_cast<unsigned>(a0.H_kv));
-  cfg.blockDim = dim3(kCombineThreads);
+  cfg.blockDim = dim3(gb1 > 0 ? kCombineThreads : kCombineThreadsSmall);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

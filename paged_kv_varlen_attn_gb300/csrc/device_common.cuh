@@ -387,14 +387,30 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-// Entry of an attention kernel: the first kernel after the planner waits in
-// every block (it reads the plan next); a later kernel waits only in its last
-// block, so that it cannot complete before its predecessor. Then the next
-// kernel of the call may be scheduled.
+__device__ __forceinline__ bool pdl_last_block() {
+  return blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1;
+}
+// Entry of an attention kernel. The first kernel after the planner waits in
+// every block (it reads the plan next) and only then lets the next kernel of
+// the call be scheduled, so every later kernel starts with the plan complete.
+// A later kernel lets its successor be scheduled at once and waits only in
+// its last block, so that it cannot complete before its predecessor; the
+// launchers size the grids one block past the last work item, so that this
+// block has no work for the wait to delay.
 __device__ __forceinline__ void pdl_enter(int pdl_first) {
-  const bool last = blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1;
-  if (pdl_first || last) pdl_wait();
-  pdl_trigger();
+  if (pdl_first) {
+    pdl_wait();
+    pdl_trigger();
+  } else {
+    pdl_trigger();
+    if (pdl_last_block()) pdl_wait();
+  }
+}
+// Exit of a kernel whose work does not depend on its predecessor (the K/V
+// scatter): its last block waits at the end, after its own work, so that the
+// grid still completes after its predecessor.
+__device__ __forceinline__ void pdl_leave() {
+  if (pdl_last_block()) pdl_wait();
 }
 
 // Fold a sink of logit s2 (base-2 units) into a row's final state kept as

@@ -81,20 +81,22 @@ __device__ __forceinline__ int64_t slot_row(const AttnArgs& a, int slot, int hk,
 // states of the same rows -- and writes the final output. Threads tid in
 // [0, nthreads) share the work, 4 columns each. The merge is associative and
 // its order is fixed, so results are deterministic.
+// In a cascade (a.merge_parts), pseg / psplit are the prefix pass's segment
+// and split records (its one segment), read by the caller.
 template <int D, bool F16>
 __device__ void combine_splits(const AttnArgs& a, int grp, int nsplit, int hk, int R, int row0,
-                               int q_start, int tid, int nthreads) {
+                               int q_start, int tid, int nthreads,
+                               int4 pseg = make_int4(0, 0, 0, 0),
+                               int4 psplit = make_int4(0, 0, 0, 0)) {
   constexpr int C4 = D / 4;
   const int G = a.G;
   // Prefix pass geometry (cascade): one segment holding every query token.
   int p_nsp = 0, p_base = 0, p_rows = 1, p_cls = 0;
   if (a.merge_parts) {
-    const int4 g0 = a.mp_seg[0];
-    const int4 s0 = a.mp_segsplit[0];
-    p_cls = g0.w;
+    p_cls = pseg.w;
     p_rows = p_cls ? tc_item_rows(G, D) : kRowsSplit;
-    p_nsp = s0.x;
-    p_base = s0.y;
+    p_nsp = psplit.x;
+    p_base = psplit.y;
   }
   const int64_t own_step = static_cast<int64_t>(a.H_kv) * a.slot_rows;
   for (int idx = tid; idx < R * C4; idx += nthreads) {

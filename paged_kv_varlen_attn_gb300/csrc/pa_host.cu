@@ -45,6 +45,7 @@ struct PassDims {
   // afterwards, which needs softmax_scale > 0; a zero or negative scale runs
   // every segment on the split-KV kernel (which scales before the maximum).
   bool tc_allowed = true;
+  int max_kv = 0x7fffffff;    // host bound of a segment's key count
 };
 
 // Which kernels a pass can need, from host-known bounds only.
@@ -68,6 +69,25 @@ PassLayout layout_pass(const PassDims& d, size_t base) {
   const long long rows = static_cast<long long>(d.total_q) * d.G;
   L.items_bound[0] = sp ? L.target[0] + d.num_segs + cdiv(rows, kRowsSplit) + 1 : 0;
   L.items_bound[1] = tc ? L.target[1] + d.num_segs + cdiv(rows, tc_item_rows(d.G, d.D)) + 1 : 0;
+  // A second bound from the key lengths: a segment splits into at most
+  // ceil(max_kv / smallest chunk) items per row tile. Where the keys are
+  // short (decode suffixes of a cascade, a prefix of a few thousand keys) it
+  // is far below the first, so the launches carry fewer blocks that find no
+  // item and return (blocks are dispatched in index order, and a dependent
+  // launch starts only once every block of its predecessor has started).
+  auto by_keys = [&](int rpi, int min_chunk) {
+    const long long seg_rows = static_cast<long long>(d.single ? d.total_q : d.max_q) * d.G;
+    long long nrt = static_cast<long long>(d.num_segs) * cdiv(seg_rows, rpi);
+    const long long nrt2 = d.num_segs + static_cast<long long>(cdiv(rows, rpi));
+    if (nrt2 < nrt) nrt = nrt2;
+    const long long nsp = d.max_kv > 0 ? cdiv(d.max_kv, min_chunk) : 1;
+    const long long b = nrt * nsp;
+    return static_cast<int>(b < 1 ? 1 : (b > 0x7fffffffLL ? 0x7fffffffLL : b));
+  };
+  if (sp && by_keys(kRowsSplit, kMinChunkSplit) < L.items_bound[0])
+    L.items_bound[0] = by_keys(kRowsSplit, kMinChunkSplit);
+  if (tc && by_keys(tc_item_rows(d.G, d.D), kMinChunkTc) < L.items_bound[1])
+    L.items_bound[1] = by_keys(tc_item_rows(d.G, d.D), kMinChunkTc);
   L.slots_bound[0] = sp ? 2 * L.target[0] + 2 : 0;
   L.slots_bound[1] = tc ? 2 * L.target[1] + 2 : 0;
   if (d.all_partial) {
@@ -105,12 +125,17 @@ struct CascadeLayout {
   size_t end;
 };
 
-CascadeLayout layout_cascade(int num_seqs, int total_q, int max_q, int G, int H, int H_kv, int D,
-                             int sms, bool kv_fp8, bool tc_allowed) {
+// prefix_len < 0 (the size queries, which do not take it): the bound of
+// either pass's keys is max_k, which covers every prefix length.
+CascadeLayout layout_cascade(int num_seqs, int total_q, int max_q, int max_k, int prefix_len,
+                             int G, int H, int H_kv, int D, int sms, bool kv_fp8,
+                             bool tc_allowed) {
   CascadeLayout C{};
   PassDims pd{1, total_q, total_q, true, G, H, H_kv, D, sms, true, kv_fp8, tc_allowed};
+  pd.max_kv = prefix_len < 0 ? max_k : prefix_len;
   C.prefix = layout_pass(pd, 0);
   PassDims sd{num_seqs, total_q, max_q, false, G, H, H_kv, D, sms, true, kv_fp8, tc_allowed};
+  sd.max_kv = prefix_len < 0 ? max_k : (max_k > prefix_len ? max_k - prefix_len : 0);
   C.suffix = layout_pass(sd, C.prefix.end);
   C.end = C.suffix.end;
   return C;
@@ -126,10 +151,12 @@ size_t varlen_bytes(PassDims d) {
   const size_t b = layout_pass(d, 0).end;
   return a > b ? a : b;
 }
-size_t cascade_bytes(int num_seqs, int total_q, int max_q, int G, int H, int H_kv, int D, int sms,
-                     bool kv_fp8) {
-  const size_t a = layout_cascade(num_seqs, total_q, max_q, G, H, H_kv, D, sms, kv_fp8, true).end;
-  const size_t b = layout_cascade(num_seqs, total_q, max_q, G, H, H_kv, D, sms, kv_fp8, false).end;
+size_t cascade_bytes(int num_seqs, int total_q, int max_q, int max_k, int G, int H, int H_kv,
+                     int D, int sms, bool kv_fp8) {
+  const size_t a =
+      layout_cascade(num_seqs, total_q, max_q, max_k, -1, G, H, H_kv, D, sms, kv_fp8, true).end;
+  const size_t b =
+      layout_cascade(num_seqs, total_q, max_q, max_k, -1, G, H, H_kv, D, sms, kv_fp8, false).end;
   return a > b ? a : b;
 }
 
@@ -502,6 +529,7 @@ size_t pa_varlen_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
   if (sms <= 0) return 0;
   PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
              num_kv_heads, head_size, sms};
+  d.max_kv = max_seqlen_k;
   return varlen_bytes(d);
 }
 
@@ -513,8 +541,8 @@ size_t pa_cascade_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q
     return 0;
   const int sms = query_sms(sm_count);
   if (sms <= 0) return 0;
-  return cascade_bytes(num_seqs, total_q, max_seqlen_q, num_heads / num_kv_heads, num_heads,
-                       num_kv_heads, head_size, sms, false);
+  return cascade_bytes(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads / num_kv_heads,
+                       num_heads, num_kv_heads, head_size, sms, false);
 }
 
 // pa_varlen_fwd, optionally preceded by a K/V update of the same cache.
@@ -556,6 +584,7 @@ static pa_status varlen_impl(const pa_kv_update* upd, const void* q, int64_t q_t
   if (sms <= 0) return PA_ERR_CUDA;
   PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
              num_kv_heads, head_size, sms};
+  d.max_kv = max_seqlen_k;
   d.kv_fp8 = kv.fp8;
   d.tc_allowed = softmax_scale > 0.f;
   const PassLayout L = layout_pass(d, 0);
@@ -739,9 +768,9 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
   const int sms = query_sms(0);
   if (sms <= 0) return PA_ERR_CUDA;
   const int G = num_heads / num_kv_heads;
-  const CascadeLayout CL = layout_cascade(num_seqs, total_q, max_seqlen_q, G, num_heads,
-                                          num_kv_heads, head_size, sms, kv.fp8,
-                                          softmax_scale > 0.f);
+  const CascadeLayout CL = layout_cascade(num_seqs, total_q, max_seqlen_q, max_seqlen_k,
+                                          common_prefix_len, G, num_heads, num_kv_heads,
+                                          head_size, sms, kv.fp8, softmax_scale > 0.f);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < CL.end)
     return PA_ERR_WORKSPACE;
@@ -768,12 +797,14 @@ static pa_status cascade_impl(const pa_kv_update* upd, const void* q, int64_t q_
   // Pass A: all queries, one non-causal segment, row 0's first P keys; every
   // work item leaves its partial state in its slot.
   pp.p[0] = make_plan(c, ws, CL.prefix, 1, P, 0, P, 0, 0, 1);
-  // The prefix pass's items hold every query row of a KV head; splitting its
-  // keys finer than 512 adds more partial states (each row's full fp32 O) to
-  // write and merge than parallelism gains (measured on 64 decode requests
-  // sharing 2048 tokens: 49.1 us per step with 256-key chunks, 46.0 with
-  // 512, 53.3 with 1024).
-  pp.p[0].min_chunk_tc = 2 * kMinChunkTc;
+  // The prefix pass's items hold every query row of a KV head, and the two
+  // passes run side by side. Over 2-byte pools the suffix pass is the longer
+  // and finer prefix chunks only take SMs from it; over e4m3 pools the suffix
+  // streams half the bytes and the prefix pass is the longer one. Measured on
+  // 64 decode requests sharing 2048 tokens (graph step): 2-byte pools 48.2 us
+  // with 512-key chunks, 52.4 with 256; e4m3 pools 50.3 with 512, 46.2 with
+  // 256.
+  pp.p[0].min_chunk_tc = kv.fp8 ? kMinChunkTc : 2 * kMinChunkTc;
   // Pass B: each sequence, causal, its own keys from position P on; each final
   // row is merged with pass A's partial states of the same row.
   pp.p[1] = make_plan(c, ws, CL.suffix, 0, 0, P,
@@ -884,6 +915,7 @@ size_t pa_varlen_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_seq
   if (sms <= 0) return 0;
   PassDims d{num_seqs, total_q, max_seqlen_q, false, num_heads / num_kv_heads, num_heads,
              num_kv_heads, head_size, sms};
+  d.max_kv = max_seqlen_k;
   d.kv_fp8 = true;
   return varlen_bytes(d);
 }
@@ -896,8 +928,8 @@ size_t pa_cascade_fwd_fp8kv_workspace_size(int num_seqs, int total_q, int max_se
     return 0;
   const int sms = query_sms(sm_count);
   if (sms <= 0) return 0;
-  return cascade_bytes(num_seqs, total_q, max_seqlen_q, num_heads / num_kv_heads, num_heads,
-                       num_kv_heads, head_size, sms, true);
+  return cascade_bytes(num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads / num_kv_heads,
+                       num_heads, num_kv_heads, head_size, sms, true);
 }
 
 pa_status pa_varlen_fwd_fp8kv(const pa_kv_update* update, const void* q, int64_t q_token_stride,
