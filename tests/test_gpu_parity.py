@@ -224,6 +224,45 @@ def test_bad_page_is_flagged_not_read():
     assert bool(torch.isfinite(out.float()).all())
 
 
+def test_key_bound_sizes_launches_not_results():
+    """The caller's key bound only sizes the launches and the workspace; the
+    plan follows the lengths themselves. A bound four times too large gives
+    bitwise the same outputs, for a cascade over decode suffixes and for a
+    decode batch."""
+    for wl, cascade in ((W.cascade_shared_prefix(num_seqs=16), True),
+                        (W.decode_llama8b(num_seqs=8), False)):
+        d = to_dev(wl, DEV)
+        pa.reshape_and_cache(d["k_new"], d["v_new"], d["key_cache"], d["value_cache"],
+                             d["slot_mapping"])
+        res = []
+        for max_k in (wl.max_seqlen_k, 4 * wl.max_seqlen_k):
+            args = (d["q"], d["key_cache"], d["value_cache"], d["cu_seqlens_q"], d["seqused_k"],
+                    d["block_table"], max(wl.max_seqlen_q, 1), max_k, wl.softmax_scale)
+            status = torch.zeros(1, dtype=torch.int32, device=DEV)
+            if cascade:
+                res.append(pa.cascade_fwd(*args, wl.common_prefix_len, dev_status=status))
+            else:
+                res.append(pa.varlen_fwd(*args, True, dev_status=status))
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+        assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+
+
+def test_keys_above_bound_are_flagged():
+    """A sequence with more keys than the caller's bound is a caller error
+    the planner reports (PA_DEV_BAD_SEQLEN); the block table it reads stays
+    within its rows."""
+    wl = W.random_case(52, num_seqs=4, num_heads=4, num_kv_heads=2, head_size=64,
+                       block_size=16, max_q=1, max_kv=100, decode_frac=1.0)
+    d = to_dev(wl, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa.varlen_fwd(d["q"], d["key_cache"], d["value_cache"], d["cu_seqlens_q"], d["seqused_k"],
+                  d["block_table"], max(wl.max_seqlen_q, 1), wl.max_seqlen_k - 1,
+                  wl.softmax_scale, True, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & pa.PA_DEV_BAD_SEQLEN
+
+
 def test_workspace_too_small_is_rejected():
     wl = W.tiny_mixed()
     d = to_dev(wl, DEV)
