@@ -251,7 +251,11 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, int
   if (num_tokens == 0) return cudaSuccess;
   const int vpt = H_kv * D / 8;
   const int64_t want = (static_cast<int64_t>(num_tokens) + kScatterWarps - 1) / kScatterWarps;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  // One wave: the kernel keeps three CTAs per SM (its launch bounds), and
+  // warps stride over the tokens. Measured with L2 flushed: 4,110 tokens
+  // 12.3-12.5 us against 14.2 with eight CTAs per SM (2.7 waves); 16,440
+  // tokens 24.2-24.5 against 24.6-25.9.
+  const int64_t cap = static_cast<int64_t>(sms) * 3;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
   cfg.blockDim = dim3(kScatterThreads);
