@@ -422,7 +422,12 @@ cudaError_t launch_merge_n(void* out, float* out_lse, const void* parts, int64_t
   const int vpr = D / 8;
   const int64_t total = static_cast<int64_t>(T) * H * vpr;
   const int64_t want = (total + kMergeThreads - 1) / kMergeThreads;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  // One wave: four CTAs per SM fit (64 registers a thread), and threads
+  // stride over the vectors. Measured on 4 parts x 16,384 tokens x 32 heads:
+  // 122.7 us against 125.0 with eight per SM (two waves), 145 with six.
+  // (Requesting the first batch of vectors before the LSEs took 80
+  // registers; held to 64 for four CTAs per SM it measured 137 us.)
+  const int64_t cap = static_cast<int64_t>(sms) * 4;
   const int grid = static_cast<int>(want < cap ? want : cap);
   (f16 ? merge_attn_states_n_kernel<true> : merge_attn_states_n_kernel<false>)<<<grid, kMergeThreads, 0, st>>>(
       static_cast<uint4*>(out), out_lse, static_cast<const uint4*>(parts), part_stride / 8,
