@@ -180,7 +180,7 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.05)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -204,6 +204,16 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def hold(step, batch, seconds):
+    """Replay `step` on `batch` (untimed) for about `seconds` of wall time."""
+    import torch
+    t0 = time.time()
+    while time.time() - t0 < seconds:
+        for _ in range(16):
+            step(batch)
+        torch.cuda.synchronize()
 
 
 # ---------------------------------------------------------------------------
@@ -397,7 +407,7 @@ def prefill_record(pa, name, dev, peaks, steps, min_ms=600.0, dtype=torch.bfloat
     n = int(min(100, max(5, min(steps, 50), min_ms / max(est, 1e-3))))
     sampler = ClockSampler(dev.index or 0)
     sampler.start()
-    time.sleep(0.3)
+    hold(lambda _b: attn(), None, 0.3)   # the clock record under this launch's load
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n)]
     for i in range(n):
@@ -635,7 +645,11 @@ def bench_ours(args, rank, world, local):
     flush_rd = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if cascade else None
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.3)
+    # The timed region lasts a few milliseconds, shorter than the sampling
+    # period, so the GPU is held at this workload's load (untimed replays of
+    # the step) for ~0.4 s before it and ~0.2 s after it: the clock record is
+    # then the clocks this workload runs at, not those of an idle GPU.
+    hold(step, main, 0.4)
     barrier(world)
     torch.cuda.synchronize()
     t_begin = torch.cuda.Event(enable_timing=True)
@@ -673,6 +687,7 @@ def bench_ours(args, rank, world, local):
             attention_only()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
+    hold(step, main, 0.2)
     barrier(world)
     clocks = sampler.stop()
     attn_ms = sum(x.elapsed_time(y) for x, y in ev)
