@@ -130,7 +130,9 @@ size_t pa_varlen_fwd_workspace_size(int num_seqs, int total_q, int max_seqlen_q,
  *                  Only entries j / block_size < ceil(seqused_k[s] / block_size)
  *                  are read.
  *   max_seqlen_q, max_seqlen_k : host upper bounds of the query / key lengths
- *                  (used to size launches; no device value is read on the host).
+ *                  (used to size launches and the workspace; no device value is
+ *                  read on the host). A looser bound gives the same results;
+ *                  a sequence above it sets PA_DEV_BAD_SEQLEN.
  *   softmax_scale: multiplies q.k (commonly 1/sqrt(head_size)); any finite
  *                  value (PA_ERR_INVALID_ARG for NaN or infinity). A zero or
  *                  negative scale runs every segment on the split-KV kernel.
