@@ -82,3 +82,23 @@ def test_clock_record_parsing():
     r = s.stop()
     assert r == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
                  "samples": 3}
+
+
+def test_committed_traffic_records_name_their_captures():
+    """Every committed DRAM-traffic record names the summary under profiles/
+    that gives its ncu command, and keys a kernel and a workload the bench
+    knows."""
+    import json
+    import os
+    import workloads as W
+    with open(bench.TRAFFIC_FILE) as f:
+        t = json.load(f)
+    for kernel, recs in t.items():
+        assert kernel in bench.KERNEL_SRCS
+        for workload, e in recs.items():
+            assert workload.split("+")[0] in W.CONFIGS
+            path = os.path.join(bench.ROOT, e["capture"])
+            assert os.path.isfile(path) and e["capture"].startswith("profiles/")
+            with open(path) as f:
+                assert "ncu " in f.read()
+            assert e["dram_bytes_per_launch"] == e["dram_bytes_read"] + e["dram_bytes_write"]
