@@ -231,6 +231,24 @@ def test_fp8_cascade_parity(seed, S, H, Hk, P, qmax, smax):
     assert int(status.item()) == 0
 
 
+def test_fp8_cascade_shared_prefix_config():
+    """The cascade bench workload (64 requests sharing a 2048-token prefix,
+    32/8 heads, page 16) on e4m3 pools, every row against the oracle: the
+    prefix pass in 256-key chunks on the tensor-core kernel (Q as two e4m3
+    terms), the suffix pass on the split kernel, then the combine."""
+    wl = W.cascade_shared_prefix()
+    kc_ref, vc_ref = oracle_fp8_pools(wl)
+    kd = oracle.dequantize_e4m3(kc_ref, wl.kv_scales(0))
+    vd = oracle.dequantize_e4m3(vc_ref, wl.kv_scales(1))
+    ref_o, ref_l = oracle.cascade_attention(wl.q, kd, vd, wl.cu_seqlens_q, wl.seqused_k,
+                                            wl.block_table, wl.softmax_scale,
+                                            wl.common_prefix_len)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse, _, _ = run_fp8(wl, cascade=True, status=status)
+    assert_close(out, lse, ref_o, ref_l)
+    assert int(status.item()) == 0
+
+
 def test_fp8_decode_llama8b_sampled():
     """The full-size decode batch (64 sequences, KV 512-8192, 32/8 heads) on
     e4m3 pools, checked on sampled sequences (the oracle regenerates only
