@@ -248,6 +248,47 @@ def test_key_bound_sizes_launches_not_results():
         assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
 
 
+def test_back_to_back_calls_share_a_workspace():
+    """Calls queued on one stream with one workspace and no host sync between
+    them: each call's planner is launched normally, so it starts only once the
+    previous call's kernels (chained by programmatic dependent launch inside
+    the call) have all completed. A decode batch, a cascade and a mixed batch
+    in a row give bitwise the outputs of the same calls made one at a time."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    wls = [(W.decode_llama8b(num_seqs=8), False),
+           (W.cascade_shared_prefix(num_seqs=8), True),
+           (W.random_case(53, num_seqs=5, num_heads=8, num_kv_heads=2, head_size=128,
+                          block_size=16, max_q=70, max_kv=300, decode_frac=0.4), False)]
+    calls, need = [], 0
+    for wl, cascade in wls:
+        d = to_dev(wl, DEV)
+        pa.reshape_and_cache(d["k_new"], d["v_new"], d["key_cache"], d["value_cache"],
+                             d["slot_mapping"])
+        T, H, D = wl.q.shape
+        size = (pa.cascade_fwd_workspace_size if cascade else pa.varlen_fwd_workspace_size)(
+            wl.num_seqs, T, max(wl.max_seqlen_q, 1), wl.max_seqlen_k, H, wl.num_kv_heads, D,
+            wl.block_size, sms)
+        need = max(need, size)
+        calls.append((wl, cascade, d))
+    ws = pa.alloc_workspace(need, DEV)
+
+    def call(wl, cascade, d):
+        args = (d["q"], d["key_cache"], d["value_cache"], d["cu_seqlens_q"], d["seqused_k"],
+                d["block_table"], max(wl.max_seqlen_q, 1), wl.max_seqlen_k, wl.softmax_scale)
+        if cascade:
+            return pa.cascade_fwd(*args, wl.common_prefix_len, workspace=ws)
+        return pa.varlen_fwd(*args, wl.causal, workspace=ws)
+
+    alone = []
+    for c in calls:
+        alone.append(call(*c))
+        torch.cuda.synchronize()
+    queued = [call(*c) for c in calls]
+    torch.cuda.synchronize()
+    for (o1, l1), (o2, l2) in zip(alone, queued):
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_keys_above_bound_are_flagged():
     """A sequence with more keys than the caller's bound is a caller error
     the planner reports (PA_DEV_BAD_SEQLEN); the block table it reads stays
